@@ -1,0 +1,461 @@
+// api.cu -- the C ABI of include/moe.h: argument validation, workspace
+// carve-up, and the launch sequence of each call on the caller's stream.
+//
+// moe_layer_forward enqueues, all on one stream and chained by programmatic
+// dependent launch (no host synchronisation anywhere):
+//   1. router GEMV                       (many CTAs)
+//   2. top-k + align + work plan         (one CTA; top-k fused for T <= 128,
+//                                         a separate warp-per-token kernel above)
+//   3. gate_up + SwiGLU                  (persistent, bulk-copy pipeline)
+//   4. down                              (persistent, bulk-copy pipeline)
+//   5. combine + shared-expert gate      (one CTA per token)
+// The shared expert rides in stages 3-4 as one more work expert, so its weight
+// stream overlaps the routed experts' ("veloGB10", Kernel work: shared-expert
+// work overlapped with the MoE step; small kernels -- the expert routing --
+// folded into their neighbours).
+#include <atomic>
+#include <mutex>
+#include <unordered_map>
+#include <utility>
+
+#include "../../include/moe.h"
+#include "launch.h"
+
+namespace moe {
+
+namespace {
+
+std::atomic<uint64_t> g_launches{0};
+
+constexpr int kMaxDevices = 64;
+constexpr int kFusedTopkMaxT = 128;
+constexpr size_t kAlign = 256;
+
+struct DeviceInfo {
+  bool init = false;
+  int sms = 0;
+  int smem_optin = 0;
+};
+DeviceInfo g_dev[kMaxDevices];
+std::mutex g_mu;
+
+bool device_info(DeviceInfo* out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return false;
+  std::lock_guard<std::mutex> lk(g_mu);
+  DeviceInfo& di = g_dev[dev];
+  if (!di.init) {
+    if (cudaDeviceGetAttribute(&di.sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+      return false;
+    if (cudaDeviceGetAttribute(&di.smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) !=
+        cudaSuccess)
+      return false;
+    di.init = true;
+  }
+  *out = di;
+  return true;
+}
+
+// Shared-memory budget of the persistent GEMV kernels.  Fixed (not read from
+// the device) so that the stage plan, hence the unit counts, depend only on the
+// dims; 227 KB is the per-CTA opt-in maximum of sm_100-class GPUs.
+constexpr int kGemvSmemBudget = 227 * 1024 - 1024;
+
+struct Layout {
+  size_t header, plan, work, logits, ids, w, sorted, blocks, npp, offs, h, hs, y, ys, total;
+  int64_t cap;
+};
+
+size_t carve(size_t* cursor, size_t bytes) {
+  const size_t at = *cursor;
+  *cursor += (bytes + kAlign - 1) / kAlign * kAlign;
+  return at;
+}
+
+Layout layout_of(const moe_dims_t& dm) {
+  Layout L;
+  const int64_t S = (int64_t)dm.T * dm.top_k;
+  L.cap = S + (int64_t)dm.E * (dm.block_size - 1);
+  size_t c = 0;
+  L.header = carve(&c, kAlign);
+  L.plan = carve(&c, sizeof(Plan));
+  L.work = carve(&c, sizeof(WorkExpert) * (size_t)(dm.E + 1));
+  L.logits = carve(&c, sizeof(float) * (size_t)dm.T * dm.E);
+  L.ids = carve(&c, sizeof(int32_t) * (size_t)S);
+  L.w = carve(&c, sizeof(float) * (size_t)S);
+  L.sorted = carve(&c, sizeof(int32_t) * (size_t)L.cap);
+  L.blocks = carve(&c, sizeof(int32_t) * (size_t)(L.cap / dm.block_size + 1));
+  L.npp = carve(&c, sizeof(int32_t));
+  L.offs = carve(&c, sizeof(int32_t) * (size_t)(dm.E + 1));
+  L.h = carve(&c, sizeof(float) * (size_t)L.cap * dm.I);
+  L.hs = carve(&c, sizeof(float) * (size_t)dm.T * dm.I_shared);
+  L.y = carve(&c, sizeof(float) * (size_t)S * dm.d);
+  L.ys = carve(&c, sizeof(float) * (size_t)dm.T * dm.d);
+  L.total = c;
+  return L;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+moe_status_t check_dims(const moe_dims_t* dm) {
+  if (dm == nullptr) return MOE_ERR_INVALID_ARG;
+  const moe_dims_t& d = *dm;
+  if (d.T < 0 || d.d <= 0 || d.E <= 0 || d.top_k <= 0 || d.I <= 0 || d.I_shared < 0 ||
+      d.block_size <= 0)
+    return MOE_ERR_INVALID_ARG;
+  if (d.renormalize != 0 && d.renormalize != 1) return MOE_ERR_INVALID_ARG;
+  if (d.T > 65536 || d.d < 8 || d.d > 8192 || d.d % 8 != 0) return MOE_ERR_UNSUPPORTED;
+  if (d.E > 1024 || d.top_k > d.E || d.top_k > 16) return MOE_ERR_UNSUPPORTED;
+  if (d.I < 8 || d.I > 4096 || d.I % 8 != 0) return MOE_ERR_UNSUPPORTED;
+  if (d.I_shared != 0 && (d.I_shared < 8 || d.I_shared > 4096 || d.I_shared % 8 != 0))
+    return MOE_ERR_UNSUPPORTED;
+  if (d.block_size > 1024) return MOE_ERR_UNSUPPORTED;
+  if (d.weight_format == MOE_WEIGHTS_BF16) return MOE_OK;
+  if (d.weight_format == MOE_WEIGHTS_INT4_G32) {
+    if (d.group_size != 32 || d.d % 256 != 0 || d.I % 256 != 0) return MOE_ERR_UNSUPPORTED;
+    return MOE_OK;
+  }
+  return MOE_ERR_UNSUPPORTED;
+}
+
+moe_status_t check_ws(const moe_dims_t& dm, void* ws, size_t ws_bytes, Layout* L) {
+  *L = layout_of(dm);
+  if (ws == nullptr || (reinterpret_cast<uintptr_t>(ws) % kAlign) != 0) return MOE_ERR_WORKSPACE;
+  if (ws_bytes < L->total) return MOE_ERR_WORKSPACE;
+  return MOE_OK;
+}
+
+template <typename T>
+T* at(void* ws, size_t off) {
+  return reinterpret_cast<T*>(static_cast<uint8_t*>(ws) + off);
+}
+
+moe_status_t cuda_status(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA; }
+
+moe_status_t check_weights(const moe_dims_t& dm, const moe_expert_weights_t* ex,
+                           const moe_shared_weights_t* sh) {
+  if (ex == nullptr || ex->gate_up == nullptr || ex->down == nullptr) return MOE_ERR_INVALID_ARG;
+  if (!aligned16(ex->gate_up) || !aligned16(ex->down)) return MOE_ERR_INVALID_ARG;
+  if (dm.weight_format == MOE_WEIGHTS_INT4_G32) {
+    if (ex->gate_up_scales == nullptr || ex->down_scales == nullptr) return MOE_ERR_INVALID_ARG;
+    if (!aligned16(ex->gate_up_scales) || !aligned16(ex->down_scales)) return MOE_ERR_INVALID_ARG;
+  }
+  if ((sh != nullptr) != (dm.I_shared > 0)) return MOE_ERR_INVALID_ARG;
+  if (sh != nullptr) {
+    if (sh->gate_up == nullptr || sh->down == nullptr || sh->gate_w == nullptr)
+      return MOE_ERR_INVALID_ARG;
+    if (!aligned16(sh->gate_up) || !aligned16(sh->down) || !aligned16(sh->gate_w))
+      return MOE_ERR_INVALID_ARG;
+  }
+  return MOE_OK;
+}
+
+struct ExpertPlan {
+  GemvShape gu, dn;
+  PlanParams pp;
+};
+
+moe_status_t expert_plan(const moe_dims_t& dm, void* ws, const Layout& L, ExpertPlan* ep) {
+  const int fmt = dm.weight_format;
+  ep->gu = gate_up_shape(fmt, dm.d, dm.I, dm.I_shared, kGemvSmemBudget);
+  ep->dn = down_shape(fmt, dm.d, dm.I, dm.I_shared, kGemvSmemBudget);
+  if (ep->gu.n_stages < 2 || ep->dn.n_stages < 2) return MOE_ERR_UNSUPPORTED;
+  PlanParams& pp = ep->pp;
+  pp.work = at<WorkExpert>(ws, L.work);
+  pp.plan = at<Plan>(ws, L.plan);
+  pp.tiles_gu = (int)ceil_div(dm.I, ep->gu.rg);
+  pp.tiles_dn = (int)ceil_div(dm.d, ep->dn.rg);
+  pp.tiles_gu_shared = dm.I_shared > 0 ? (int)ceil_div(dm.I_shared, ep->gu.rg_shared) : 0;
+  pp.tiles_dn_shared = dm.I_shared > 0 ? (int)ceil_div(dm.d, ep->dn.rg_shared) : 0;
+  pp.xt_gu = ep->gu.xt;
+  pp.xt_dn = ep->dn.xt;
+  return MOE_OK;
+}
+
+ExpertArgs expert_args(const moe_dims_t& dm, const moe_expert_weights_t* ex,
+                       const moe_shared_weights_t* sh) {
+  ExpertArgs a;
+  a.fmt = dm.weight_format;
+  a.gate_up = ex->gate_up;
+  a.gate_up_scales = static_cast<const uint16_t*>(ex->gate_up_scales);
+  a.down = ex->down;
+  a.down_scales = static_cast<const uint16_t*>(ex->down_scales);
+  a.s_gate_up = sh ? static_cast<const uint16_t*>(sh->gate_up) : nullptr;
+  a.s_down = sh ? static_cast<const uint16_t*>(sh->down) : nullptr;
+  a.T = dm.T;
+  a.d = dm.d;
+  a.E = dm.E;
+  a.k = dm.top_k;
+  a.I = dm.I;
+  a.Is = sh ? dm.I_shared : 0;
+  return a;
+}
+
+moe_status_t record(void* const* events, int which, cudaStream_t st) {
+  if (events && events[which] &&
+      cudaEventRecord(static_cast<cudaEvent_t>(events[which]), st) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  return MOE_OK;
+}
+
+// Stages 3-5 given a plan already in the workspace.
+moe_status_t run_experts(const moe_dims_t& dm, const void* x, const float* topk_w,
+                         const int32_t* sorted_ids, const moe_expert_weights_t* ex,
+                         const moe_shared_weights_t* sh, void* out, void* ws, const Layout& L,
+                         const ExpertPlan& ep, int sms, cudaStream_t st, void* const* events) {
+  const LaunchCfg next{st, true};
+  int* status = at<int>(ws, L.header);
+  const ExpertArgs a = expert_args(dm, ex, sh);
+  float* h = at<float>(ws, L.h);
+  float* hs = at<float>(ws, L.hs);
+  float* y = at<float>(ws, L.y);
+  float* ys = at<float>(ws, L.ys);
+  moe_status_t s;
+  if (launch_gate_up(next, a, ep.gu, static_cast<const uint16_t*>(x), sorted_ids, ep.pp.plan,
+                     ep.pp.work, h, hs, status, sms) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  if ((s = record(events, MOE_EV_GATE_UP, st)) != MOE_OK) return s;
+  if (launch_down(next, a, ep.dn, sorted_ids, ep.pp.plan, ep.pp.work, h, hs, y, ys, status,
+                  sms) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  if ((s = record(events, MOE_EV_DOWN, st)) != MOE_OK) return s;
+  if (launch_combine(next, dm.T, dm.d, dm.top_k, topk_w, y, sh ? ys : nullptr,
+                     static_cast<const uint16_t*>(x),
+                     sh ? static_cast<const uint16_t*>(sh->gate_w) : nullptr,
+                     static_cast<uint16_t*>(out)) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  return MOE_OK;
+}
+
+moe_status_t layer_forward(const moe_dims_t* dims, const void* x, const void* router_w,
+                           const moe_expert_weights_t* ex, const moe_shared_weights_t* sh,
+                           void* out, int32_t* ids_out, float* w_out, void* ws, size_t ws_bytes,
+                           void* stream, void* const* events) {
+  moe_status_t s = check_dims(dims);
+  if (s != MOE_OK) return s;
+  const moe_dims_t dm = *dims;
+  if (x == nullptr || router_w == nullptr || out == nullptr) return MOE_ERR_INVALID_ARG;
+  if (!aligned16(x) || !aligned16(router_w) || !aligned16(out)) return MOE_ERR_INVALID_ARG;
+  if ((ids_out && !aligned16(ids_out)) || (w_out && !aligned16(w_out))) return MOE_ERR_INVALID_ARG;
+  if ((s = check_weights(dm, ex, sh)) != MOE_OK) return s;
+  Layout L;
+  if ((s = check_ws(dm, ws, ws_bytes, &L)) != MOE_OK) return s;
+  ExpertPlan ep;
+  if ((s = expert_plan(dm, ws, L, &ep)) != MOE_OK) return s;
+  if (dm.T == 0) return MOE_OK;
+  DeviceInfo di;
+  if (!device_info(&di)) return MOE_ERR_CUDA;
+
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const LaunchCfg first{st, false}, next{st, true};
+  int* status = at<int>(ws, L.header);
+  float* logits = at<float>(ws, L.logits);
+  int32_t* ids = at<int32_t>(ws, L.ids);
+  float* w = at<float>(ws, L.w);
+  int32_t* sorted = at<int32_t>(ws, L.sorted);
+
+  if ((s = record(events, MOE_EV_BEGIN, st)) != MOE_OK) return s;
+  if (launch_router_logits(first, static_cast<const uint16_t*>(x),
+                           static_cast<const uint16_t*>(router_w), logits, dm.T, dm.d, dm.E,
+                           di.sms) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  const bool fused = dm.T <= kFusedTopkMaxT;
+  if (!fused && launch_topk(next, logits, dm.T, dm.E, dm.top_k, dm.renormalize, ids, w, ids_out,
+                            w_out) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  if (launch_align(next, fused ? logits : nullptr, dm.T, dm.E, dm.top_k, dm.renormalize, ids, w,
+                   fused ? ids_out : nullptr, fused ? w_out : nullptr, dm.block_size, sorted,
+                   at<int32_t>(ws, L.blocks), at<int32_t>(ws, L.npp), at<int32_t>(ws, L.offs),
+                   ep.pp, status) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  if ((s = record(events, MOE_EV_ROUTED, st)) != MOE_OK) return s;
+  if ((s = run_experts(dm, x, w, sorted, ex, sh, out, ws, L, ep, di.sms, st, events)) != MOE_OK)
+    return s;
+  return record(events, MOE_EV_END, st);
+}
+
+}  // namespace
+
+void count_launch() { g_launches.fetch_add(1, std::memory_order_relaxed); }
+
+cudaError_t launch_kernel(const LaunchCfg& c, const void* fn, dim3 grid, dim3 block, size_t smem,
+                          void** args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = c.stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = c.pdl ? 1 : 0;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  count_launch();
+  return cudaLaunchKernelExC(&cfg, fn, args);
+}
+
+cudaError_t ensure_smem(const void* fn, int bytes) {
+  if (bytes <= 48 * 1024) return cudaSuccess;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  static std::unordered_map<const void*, int> set_to[kMaxDevices];
+  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lk(g_mu);
+  auto it = set_to[dev].find(fn);
+  if (it != set_to[dev].end() && it->second >= bytes) return cudaSuccess;
+  e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e == cudaSuccess) set_to[dev][fn] = bytes;
+  return e;
+}
+
+}  // namespace moe
+
+using namespace moe;
+
+extern "C" {
+
+const char* moe_status_string(moe_status_t status) {
+  switch (status) {
+    case MOE_OK: return "MOE_OK";
+    case MOE_ERR_INVALID_ARG: return "MOE_ERR_INVALID_ARG: null pointer, misalignment or bad value";
+    case MOE_ERR_UNSUPPORTED: return "MOE_ERR_UNSUPPORTED: dims outside the supported limits";
+    case MOE_ERR_WORKSPACE: return "MOE_ERR_WORKSPACE: workspace missing, misaligned or too small";
+    case MOE_ERR_CUDA: return "MOE_ERR_CUDA: a CUDA call or kernel launch failed";
+    case MOE_ERR_DEVICE_CHECK: return "MOE_ERR_DEVICE_CHECK: a kernel saw an out-of-range index";
+    case MOE_ERR_TIMEOUT: return "MOE_ERR_TIMEOUT: a kernel's bounded pipeline wait ran out";
+  }
+  return "MOE_ERR_UNKNOWN";
+}
+
+moe_status_t moe_workspace_bytes(const moe_dims_t* dims, size_t* bytes) {
+  if (bytes == nullptr) return MOE_ERR_INVALID_ARG;
+  *bytes = 0;
+  moe_status_t s = check_dims(dims);
+  if (s != MOE_OK) return s;
+  *bytes = layout_of(*dims).total;
+  return MOE_OK;
+}
+
+moe_status_t moe_workspace_init(void* workspace, size_t workspace_bytes, void* stream) {
+  if (workspace == nullptr || (reinterpret_cast<uintptr_t>(workspace) % kAlign) != 0 ||
+      workspace_bytes < kAlign)
+    return MOE_ERR_WORKSPACE;
+  return cuda_status(cudaMemsetAsync(workspace, 0, kAlign, static_cast<cudaStream_t>(stream)));
+}
+
+moe_status_t moe_route(const moe_dims_t* dims, const void* x, const void* router_w,
+                       int32_t* topk_ids, float* topk_weights, void* workspace,
+                       size_t workspace_bytes, void* stream) {
+  moe_status_t s = check_dims(dims);
+  if (s != MOE_OK) return s;
+  const moe_dims_t dm = *dims;
+  if (!x || !router_w || !topk_ids || !topk_weights) return MOE_ERR_INVALID_ARG;
+  if (!aligned16(x) || !aligned16(router_w) || !aligned16(topk_ids) || !aligned16(topk_weights))
+    return MOE_ERR_INVALID_ARG;
+  Layout L;
+  if ((s = check_ws(dm, workspace, workspace_bytes, &L)) != MOE_OK) return s;
+  if (dm.T == 0) return MOE_OK;
+  DeviceInfo di;
+  if (!device_info(&di)) return MOE_ERR_CUDA;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  float* logits = at<float>(workspace, L.logits);
+  if (launch_router_logits(LaunchCfg{st, false}, static_cast<const uint16_t*>(x),
+                           static_cast<const uint16_t*>(router_w), logits, dm.T, dm.d, dm.E,
+                           di.sms) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  return cuda_status(launch_topk(LaunchCfg{st, true}, logits, dm.T, dm.E, dm.top_k,
+                                 dm.renormalize, topk_ids, topk_weights, nullptr, nullptr));
+}
+
+moe_status_t moe_align_block_size(const moe_dims_t* dims, const int32_t* topk_ids,
+                                  int32_t* sorted_ids, int32_t* block_expert_ids,
+                                  int32_t* num_post_pad, int32_t* expert_offsets, void* workspace,
+                                  size_t workspace_bytes, void* stream) {
+  moe_status_t s = check_dims(dims);
+  if (s != MOE_OK) return s;
+  const moe_dims_t dm = *dims;
+  if (!topk_ids || !sorted_ids || !block_expert_ids || !num_post_pad || !expert_offsets)
+    return MOE_ERR_INVALID_ARG;
+  if (!aligned16(topk_ids) || !aligned16(sorted_ids) || !aligned16(block_expert_ids) ||
+      !aligned16(num_post_pad) || !aligned16(expert_offsets))
+    return MOE_ERR_INVALID_ARG;
+  Layout L;
+  if ((s = check_ws(dm, workspace, workspace_bytes, &L)) != MOE_OK) return s;
+  PlanParams none = {};
+  return cuda_status(launch_align(LaunchCfg{static_cast<cudaStream_t>(stream), false}, nullptr,
+                                  dm.T, dm.E, dm.top_k, dm.renormalize,
+                                  const_cast<int32_t*>(topk_ids), nullptr, nullptr, nullptr,
+                                  dm.block_size, sorted_ids, block_expert_ids, num_post_pad,
+                                  expert_offsets, none, at<int>(workspace, L.header)));
+}
+
+moe_status_t moe_expert_forward(const moe_dims_t* dims, const void* x, const float* topk_weights,
+                                const int32_t* sorted_ids, const int32_t* block_expert_ids,
+                                const int32_t* num_post_pad, const int32_t* expert_offsets,
+                                const moe_expert_weights_t* experts,
+                                const moe_shared_weights_t* shared, void* out, void* workspace,
+                                size_t workspace_bytes, void* stream) {
+  moe_status_t s = check_dims(dims);
+  if (s != MOE_OK) return s;
+  const moe_dims_t dm = *dims;
+  if (!x || !topk_weights || !sorted_ids || !block_expert_ids || !num_post_pad ||
+      !expert_offsets || !out)
+    return MOE_ERR_INVALID_ARG;
+  if (!aligned16(x) || !aligned16(topk_weights) || !aligned16(sorted_ids) ||
+      !aligned16(num_post_pad) || !aligned16(expert_offsets) || !aligned16(out))
+    return MOE_ERR_INVALID_ARG;
+  if ((s = check_weights(dm, experts, shared)) != MOE_OK) return s;
+  Layout L;
+  if ((s = check_ws(dm, workspace, workspace_bytes, &L)) != MOE_OK) return s;
+  ExpertPlan ep;
+  if ((s = expert_plan(dm, workspace, L, &ep)) != MOE_OK) return s;
+  if (dm.T == 0) return MOE_OK;
+  DeviceInfo di;
+  if (!device_info(&di)) return MOE_ERR_CUDA;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (launch_plan(LaunchCfg{st, false}, dm.T, dm.E, dm.top_k, dm.block_size, sorted_ids,
+                  num_post_pad, expert_offsets, ep.pp, at<int>(workspace, L.header)) !=
+      cudaSuccess)
+    return MOE_ERR_CUDA;
+  return run_experts(dm, x, topk_weights, sorted_ids, experts, shared, out, workspace, L, ep,
+                     di.sms, st, nullptr);
+}
+
+moe_status_t moe_layer_forward(const moe_dims_t* dims, const void* x, const void* router_w,
+                               const moe_expert_weights_t* experts,
+                               const moe_shared_weights_t* shared, void* out,
+                               int32_t* topk_ids_out, float* topk_weights_out, void* workspace,
+                               size_t workspace_bytes, void* stream) {
+  return layer_forward(dims, x, router_w, experts, shared, out, topk_ids_out, topk_weights_out,
+                       workspace, workspace_bytes, stream, nullptr);
+}
+
+moe_status_t moe_layer_forward_timed(const moe_dims_t* dims, const void* x, const void* router_w,
+                                     const moe_expert_weights_t* experts,
+                                     const moe_shared_weights_t* shared, void* out,
+                                     int32_t* topk_ids_out, float* topk_weights_out,
+                                     void* workspace, size_t workspace_bytes, void* stream,
+                                     void* const* events) {
+  if (events == nullptr) return MOE_ERR_INVALID_ARG;
+  return layer_forward(dims, x, router_w, experts, shared, out, topk_ids_out, topk_weights_out,
+                       workspace, workspace_bytes, stream, events);
+}
+
+moe_status_t moe_read_device_status(void* workspace, int32_t* code, void* stream) {
+  if (workspace == nullptr || code == nullptr ||
+      (reinterpret_cast<uintptr_t>(workspace) % kAlign) != 0)
+    return MOE_ERR_INVALID_ARG;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  int32_t v = 0;
+  if (cudaMemcpyAsync(&v, workspace, sizeof v, cudaMemcpyDeviceToHost, st) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  if (cudaStreamSynchronize(st) != cudaSuccess) return MOE_ERR_CUDA;
+  *code = v;
+  if (v != 0 && cudaMemsetAsync(workspace, 0, sizeof v, st) != cudaSuccess) return MOE_ERR_CUDA;
+  return MOE_OK;
+}
+
+uint64_t moe_kernel_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
+
+}  // extern "C"

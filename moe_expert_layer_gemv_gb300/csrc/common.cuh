@@ -1,0 +1,140 @@
+// common.cuh -- device helpers shared by the sm_103a kernels of the MoE layer:
+// bf16 unpacking, warp reductions, mbarrier / bulk-copy (TMA) pipeline
+// primitives with bounded waits, programmatic dependent launch, and the work
+// plan records shared by host and device.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace moe {
+
+// ---------------------------------------------------------------- status codes
+// Same values as moe_status_t in include/moe.h.
+constexpr int kStatusOk = 0;
+constexpr int kStatusDeviceCheck = 5;
+constexpr int kStatusTimeout = 6;
+
+// A pipeline wait gives up after this many try_wait polls (each poll may itself
+// suspend for a hardware-defined time), records kStatusTimeout and returns.
+constexpr uint32_t kSpinLimit = 1u << 22;
+
+// ---------------------------------------------------------------- plan layout
+// One entry per "work expert": every touched routed expert in ascending id,
+// then (if present) the shared expert.  Built on the device after align.
+struct WorkExpert {
+  int32_t expert;      // routed expert id, or -1 for the shared expert
+  int32_t n_tok;       // tokens routed to it (T for the shared expert)
+  int32_t pos;         // first sorted position of its slots (h row base)
+  int32_t unit_gu;     // first gate_up work unit
+  int32_t unit_dn;     // first down work unit
+  int32_t pad_[3];
+};
+
+struct Plan {
+  int32_t n_work;      // number of WorkExpert entries
+  int32_t units_gu;    // total gate_up units
+  int32_t units_dn;    // total down units
+  int32_t num_post_pad;
+  int32_t pad_[4];
+};
+
+// ---------------------------------------------------------------- bf16 / math
+__device__ __forceinline__ float bf16lo(uint32_t v) { return __uint_as_float(v << 16); }
+__device__ __forceinline__ float bf16hi(uint32_t v) { return __uint_as_float(v & 0xffff0000u); }
+
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+
+__device__ __forceinline__ float silu(float g) { return g / (1.0f + expf(-g)); }
+__device__ __forceinline__ float sigmoid(float z) { return 1.0f / (1.0f + expf(-z)); }
+
+__device__ __forceinline__ void record_status(int* status, int code) {
+  if (status) atomicCAS(status, kStatusOk, code);
+}
+
+// ---------------------------------------------------------------- PDL
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+// ---------------------------------------------------------------- mbarrier
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count)
+               : "memory");
+}
+
+__device__ __forceinline__ void fence_barrier_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)),
+               "r"(bytes)
+               : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// Bounded wait for phase `parity` of `bar`.  Returns false (after recording
+// kStatusTimeout) if the phase did not complete within kSpinLimit polls.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, int* status) {
+  for (uint32_t i = 0; i < kSpinLimit; ++i)
+    if (mbar_try_wait(bar, parity)) return true;
+  record_status(status, kStatusTimeout);
+  return false;
+}
+
+// ---------------------------------------------------------------- bulk copy
+// L2 policies: evict-first for data read once (expert weights), evict-last for
+// small data many CTAs re-read (activations).
+__device__ __forceinline__ uint64_t policy_evict_first() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+__device__ __forceinline__ uint64_t policy_evict_last() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+
+// Global -> shared bulk copy (non-tensor TMA).  dst, src 16-byte aligned; bytes
+// a multiple of 16.  Completion is signalled on `bar` as transaction bytes.
+__device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar,
+                                         uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+      " [%0], [%1], %2, [%3], %4;" ::"r"(smem_u32(dst)),
+      "l"(src), "r"(bytes), "r"(smem_u32(bar)), "l"(policy)
+      : "memory");
+}
+
+// ---------------------------------------------------------------- misc
+__host__ __device__ constexpr int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
+__host__ __device__ constexpr int64_t round_up(int64_t a, int64_t b) { return ceil_div(a, b) * b; }
+
+}  // namespace moe

@@ -1,0 +1,102 @@
+// launch.h -- host-side launchers of the MoE layer's kernels (internal to the
+// library; the public surface is include/moe.h).  Each launcher enqueues one
+// kernel on `stream` and returns the cudaError_t of the launch.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "common.cuh"
+
+namespace moe {
+
+// Counts every kernel this library enqueues (moe_kernel_launch_count).
+void count_launch();
+
+// Launch attributes: programmatic dependent launch on/off.
+struct LaunchCfg {
+  cudaStream_t stream;
+  bool pdl;  // allow this kernel to start before its predecessor finishes
+};
+
+// cudaLaunchKernelExC with the PDL attribute of `c`; counts the launch.
+cudaError_t launch_kernel(const LaunchCfg& c, const void* fn, dim3 grid, dim3 block, size_t smem,
+                          void** args);
+
+// Sets a kernel's dynamic shared-memory limit once per (device, kernel).
+cudaError_t ensure_smem(const void* fn, int bytes);
+
+// ------------------------------------------------------------------ routing
+// logits[t][e] = x[t] . wr[e] (fp32 accumulate).
+cudaError_t launch_router_logits(const LaunchCfg& c, const uint16_t* x, const uint16_t* wr,
+                                 float* logits, int T, int d, int E, int sms);
+
+// Per token: softmax over E, top-k (ties -> lower id), (re)normalised weights.
+cudaError_t launch_topk(const LaunchCfg& c, const float* logits, int T, int E, int k,
+                        int renormalize, int32_t* ids, float* w, int32_t* ids_copy,
+                        float* w_copy);
+
+// Parameters of the work plan built after align (see Plan / WorkExpert).
+struct PlanParams {
+  WorkExpert* work;      // [E + 1]
+  Plan* plan;
+  int tiles_gu;          // gate_up tiles per routed expert
+  int tiles_dn;          // down tiles per routed expert
+  int tiles_gu_shared;   // 0 = no shared expert
+  int tiles_dn_shared;
+  int xt_gu;             // tokens per gate_up unit
+  int xt_dn;             // tokens per down unit
+};
+
+// Single-CTA align: optional fused top-k (logits != nullptr), the
+// moe_align_block_size layout, and optionally the work plan (pp.work != nullptr).
+cudaError_t launch_align(const LaunchCfg& c, const float* logits, int T, int E, int k,
+                         int renormalize, int32_t* ids, float* w, int32_t* ids_copy,
+                         float* w_copy, int B, int32_t* sorted_ids, int32_t* block_ids,
+                         int32_t* num_post_pad, int32_t* expert_offsets, const PlanParams& pp,
+                         int* status);
+
+// Work plan from an existing align layout (moe_expert_forward path).
+cudaError_t launch_plan(const LaunchCfg& c, int T, int E, int k, int B,
+                        const int32_t* sorted_ids, const int32_t* num_post_pad,
+                        const int32_t* expert_offsets, const PlanParams& pp, int* status);
+
+// ------------------------------------------------------------------ experts
+struct GemvShape {
+  int rg;        // gate_up: (gate, up) row pairs per tile  | down: rows per tile (routed)
+  int rg_shared; // same for the shared expert
+  int xt;        // tokens per unit
+  int stage_bytes;
+  int n_stages;
+};
+
+struct ExpertArgs {
+  int fmt;                  // 0 bf16, 1 int4 (routed experts)
+  const void* gate_up;      // routed
+  const uint16_t* gate_up_scales;
+  const void* down;
+  const uint16_t* down_scales;
+  const uint16_t* s_gate_up;  // shared (bf16), may be null
+  const uint16_t* s_down;
+  int T, d, E, k, I, Is;
+};
+
+cudaError_t launch_gate_up(const LaunchCfg& c, const ExpertArgs& a, const GemvShape& g,
+                           const uint16_t* x, const int32_t* sorted_ids, const Plan* plan,
+                           const WorkExpert* work, float* h, float* hs, int* status, int grid);
+
+cudaError_t launch_down(const LaunchCfg& c, const ExpertArgs& a, const GemvShape& g,
+                        const int32_t* sorted_ids, const Plan* plan, const WorkExpert* work,
+                        const float* h, const float* hs, float* y, float* ys, int* status,
+                        int grid);
+
+// out[t] = sum_j w[t][j] y[t*k+j] + sigmoid(x[t].w_sg) ys[t]   (bf16, RNE)
+cudaError_t launch_combine(const LaunchCfg& c, int T, int d, int k, const float* w,
+                           const float* y, const float* ys, const uint16_t* x,
+                           const uint16_t* w_sg, uint16_t* out);
+
+// Host-side tile/stage choices for the two GEMV stages.
+GemvShape gate_up_shape(int fmt, int d, int I, int Is, int smem_budget);
+GemvShape down_shape(int fmt, int d, int I, int Is, int smem_budget);
+
+}  // namespace moe
