@@ -1,0 +1,381 @@
+"""Benchmark of the MoE expert layer on GB300.
+
+One step = one whole layer (router, top-k, align, gate_up+SwiGLU, down, combine,
+shared expert) over one batch of seeded synthetic tokens.  Default workload: the
+speculative-verify layer, T=8 tokens (1 target + 7 draft positions), d=2048,
+E=256 routed experts, top-8 renormalised, I=512, shared expert I=512, bf16.
+
+Prints one JSON line (rank 0).  `value` = tokens/s of the whole job with inputs
+resident in HBM; `e2e` = the same through the C ABI with the step's x copied from
+pinned host memory and out copied back inside the timed region.
+
+L2: the 129 MB L2 is not allowed to serve weights across steps: steps rotate
+over several device copies of the full weight set (together well over 2x L2),
+and over several token batches.
+
+--impl reference times the fp64 CPU oracle (the only reference there is: the
+source pages publish no code for this layer) on the same workload, metric and
+unit, on the host cores.
+"""
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "MoE layer tokens/s & achieved HBM GB/s (T=8 verify) vs roofline; prefill TFLOP/s"
+UNIT = "tokens/s"
+
+
+def parse():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=200)
+    p.add_argument("--warmup", type=int, default=20)
+    p.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
+    p.add_argument("--workload", default="verify_t8")
+    p.add_argument("--copies", type=int, default=0, help="weight copies to rotate (0 = auto)")
+    p.add_argument("--batches", type=int, default=8, help="token batches to rotate")
+    p.add_argument("--cpu-seconds", type=float, default=10.0)
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    return p.parse_args()
+
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def measured_peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return json.load(f), "measured"
+    except OSError:
+        return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}, "fallback"
+
+
+# --------------------------------------------------------------------------- clocks
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled during the timed region."""
+
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.Q}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except OSError:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.t.join(timeout=2)
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            f = [x.strip() for x in ln.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx = float(f[2])
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": mx,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# --------------------------------------------------------------------------- byte model
+def algorithmic(shape, ids_list):
+    """Per-step algorithmic bytes (whole layer and gate_up stage) and flops,
+    averaged over the token batches' actual routing.  Touched experts only; no
+    padding, no intermediates beyond the stage's own inputs/outputs."""
+    s = shape
+    if s.fmt == "int4":
+        gu_e = 2 * s.I * (s.d // 2 + s.d // s.group * 2)
+        dn_e = s.d * (s.I // 2 + s.I // s.group * 2)
+    else:
+        gu_e = 2 * s.I * s.d * 2
+        dn_e = s.d * s.I * 2
+    sh_gu = 2 * s.Is * s.d * 2
+    sh_dn = s.d * s.Is * 2
+    router = s.E * s.d * 2
+    x = s.T * s.d * 2
+    out = s.T * s.d * 2
+    layer_b, gu_b, touched = [], [], []
+    for ids in ids_list:
+        n = len(set(ids.reshape(-1).tolist()))
+        touched.append(n)
+        layer_b.append(n * (gu_e + dn_e) + sh_gu + sh_dn + (s.d * 2 if s.Is else 0) + router + x + out)
+        gu_b.append(n * gu_e + sh_gu + x)
+    flops = 2 * s.T * s.k * 3 * s.I * s.d + 2 * s.T * 3 * s.Is * s.d + 2 * s.T * s.E * s.d
+    return {"layer_bytes": statistics.mean(layer_b), "gate_up_bytes": statistics.mean(gu_b),
+            "touched": statistics.mean(touched), "flops": flops}
+
+
+def kernel_traffic(src_name, workload):
+    """ncu dram bytes per launch for the dominant kernel, if recorded for the
+    current source of that kernel (profiles/<kernel>_<workload>.json)."""
+    prof = os.path.join(ROOT, "profiles", f"gate_up_{workload}.json")
+    src = os.path.join(ROOT, "moe_expert_layer_gemv_gb300", "csrc", src_name)
+    try:
+        rec = json.load(open(prof))
+        h = hashlib.sha256(open(src, "rb").read()).hexdigest()
+        if rec.get("source_sha256") == h:
+            return rec.get("dram_bytes_per_launch")
+    except (OSError, ValueError):
+        pass
+    return None
+
+
+# --------------------------------------------------------------------------- CPU oracle
+def oracle_tokens_per_s(inp, seconds, nthreads=0):
+    """Time the fp64 oracle on whole batches of the workload until `seconds`."""
+    import oracle
+    from moe_expert_layer_gemv_gb300 import inputs as I
+
+    s = inp["shape"]
+    fmt = oracle.BF16 if s.fmt == "bf16" else oracle.INT4
+    conv = I.bits if s.fmt == "bf16" else (lambda t: t.numpy())
+    ex = {"format": fmt, "group": s.group, "gate_up": conv(inp["gate_up"]), "down": conv(inp["down"]),
+          "gate_up_scales": None if inp["gate_up_scales"] is None else I.bits(inp["gate_up_scales"]),
+          "down_scales": None if inp["down_scales"] is None else I.bits(inp["down_scales"])}
+    sh = None
+    if s.Is:
+        sh = {"gate_up": I.bits(inp["shared_gate_up"]), "down": I.bits(inp["shared_down"]),
+              "gate_w": I.bits(inp["w_sg"])}
+    dims = {"T": s.T, "d": s.d, "E": s.E, "k": s.k, "I": s.I, "Is": s.Is,
+            "renormalize": int(s.renormalize)}
+    xb, rb = I.bits(inp["x"]), I.bits(inp["router_w"])
+    tokens, t0 = 0, time.perf_counter()
+    while True:
+        oracle.layer(xb, rb, ex, sh, dims, nthreads=nthreads)
+        tokens += s.T
+        el = time.perf_counter() - t0
+        if el >= seconds:
+            break
+    threads = nthreads if nthreads > 0 else oracle.max_threads()
+    return tokens / el, threads, tokens, el
+
+
+def run_reference(args, shape):
+    """The reference arm: the fp64 CPU oracle on the host cores."""
+    from moe_expert_layer_gemv_gb300 import inputs as I
+    import oracle
+
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return
+    inp = I.make_inputs(shape, seed=0)
+    for _ in range(args.warmup):
+        oracle_tokens_per_s(inp, 0.0)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        oracle_tokens_per_s(inp, 0.0)
+    el = time.perf_counter() - t0
+    v = args.steps * shape.T / el
+    cores = oracle.max_threads()
+    line = {"impl": "reference", "metric": METRIC, "value": v, "unit": UNIT, "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": el / args.steps * 1e3,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "config": {"workload": shape.name, "T": shape.T, "d": shape.d,
+                                            "E": shape.E, "top_k": shape.k, "I": shape.I,
+                                            "I_shared": shape.Is, "weights": shape.fmt},
+            "cpu_baseline": {"value": v, "unit": UNIT, "cores": cores, "kind": "oracle",
+                             "sample": f"{args.steps} full steps of {shape.T} tokens, fp64, "
+                                       f"OpenMP over tokens"},
+            "e2e": {"value": v, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+# --------------------------------------------------------------------------- GPU arm
+def main():
+    args = parse()
+    from moe_expert_layer_gemv_gb300 import inputs as I
+
+    shape = I.shape(args.workload)
+    if args.impl == "reference":
+        run_reference(args, shape)
+        return
+
+    import numpy as np
+    import torch
+    import torch.distributed as dist
+
+    from moe_expert_layer_gemv_gb300 import abi, build
+    from moe_expert_layer_gemv_gb300.layer import MoeLayer
+
+    rank, world, local = dist_env()
+    if world > 1:
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    build.build()
+    abi.load()
+
+    # CPU baseline first (before heavy GPU allocations), rank 0 only, N=1 only.
+    cpu = None
+    inp0 = I.make_inputs(shape, seed=0)
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        v, threads, ntok, el = oracle_tokens_per_s(inp0, args.cpu_seconds)
+        cpu = {"value": v, "unit": UNIT, "cores": threads, "kind": "oracle",
+               "sample": f"{ntok // shape.T} whole steps ({ntok} tokens) of the {shape.name} "
+                         f"workload, {el:.1f} s, fp64 OpenMP over tokens"}
+
+    # Device state: weight copies rotated across steps, token batches rotated.
+    props = torch.cuda.get_device_properties(dev)
+    l2 = getattr(props, "L2_cache_size", 0) or 0
+    layer0 = MoeLayer(inp0, dev)
+    w_bytes = sum(t.numel() * t.element_size() for t in
+                  [layer0.router_w, layer0.gate_up, layer0.down] +
+                  [t for t in [layer0.gate_up_scales, layer0.down_scales] if t is not None] +
+                  ([layer0.s_gate_up, layer0.s_down, layer0.w_sg] if shape.Is else []))
+    ncopy = args.copies or max(2, math.ceil(4 * max(l2, 128 << 20) / w_bytes))
+    layers = [layer0] + [MoeLayer(inp0, dev) for _ in range(ncopy - 1)]
+    xs = [I.make_x(shape, seed=100 + b).to(dev) for b in range(args.batches)]
+    outs = [torch.empty((shape.T, shape.d), dtype=torch.bfloat16, device=dev) for _ in xs]
+    ids_dev = [torch.empty((shape.T, shape.k), dtype=torch.int32, device=dev) for _ in xs]
+    for b, x in enumerate(xs):
+        layers[0].forward(x, outs[b], topk_ids=ids_dev[b])
+    torch.cuda.synchronize()
+    ids_host = [t.cpu().numpy() for t in ids_dev]
+    alg = algorithmic(shape, ids_host)
+
+    def step(i, stream=None):
+        b = i % len(xs)
+        layers[i % ncopy].forward(xs[b], outs[b], stream=stream)
+
+    for i in range(args.warmup):
+        step(i)
+    torch.cuda.synchronize()
+
+    # ---- timed region A: the layer, inputs resident in HBM
+    clocks = ClockSampler(local)
+    clocks.start()
+    time.sleep(0.3)
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    launches0 = abi.moe_kernel_launch_count()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    ev0.record()
+    for i in range(args.steps):
+        step(i)
+    ev1.record()
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    gpu_launches = abi.moe_kernel_launch_count() - launches0
+    ms = ev0.elapsed_time(ev1) / args.steps
+
+    # ---- timed region B: same steps with per-stage events (kernel durations)
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(abi.MOE_EV_COUNT)]
+           for _ in range(args.steps)]
+    torch.cuda.synchronize()
+    for i in range(args.steps):
+        b = i % len(xs)
+        layers[i % ncopy].forward_timed(xs[b], outs[b], evs[i])
+    torch.cuda.synchronize()
+    stage_names = ["route_align", "gate_up", "down", "combine"]
+    stage_ms = {n: statistics.mean(e[j].elapsed_time(e[j + 1]) for e in evs)
+                for j, n in enumerate(stage_names)}
+    ms_timed = statistics.mean(e[0].elapsed_time(e[-1]) for e in evs)
+
+    # ---- timed region C: end to end from pinned host memory
+    x_host = [x.cpu().pin_memory() for x in xs]
+    out_host = [torch.empty((shape.T, shape.d), dtype=torch.bfloat16).pin_memory() for _ in xs]
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t_wall = time.perf_counter()
+    e0.record()
+    for i in range(args.steps):
+        b = i % len(xs)
+        xs[b].copy_(x_host[b], non_blocking=True)
+        layers[i % ncopy].forward(xs[b], outs[b])
+        out_host[b].copy_(outs[b], non_blocking=True)
+    e1.record()
+    torch.cuda.synchronize()
+    t_wall = time.perf_counter() - t_wall
+    ms_e2e = e0.elapsed_time(e1) / args.steps
+    clk = clocks.stop()
+
+    if world > 1:
+        t = torch.tensor([ms, ms_e2e], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms, ms_e2e = t.tolist()
+
+    peaks, peak_kind = measured_peaks()
+    gu_ms = stage_ms["gate_up"]
+    achieved = alg["gate_up_bytes"] / (gu_ms * 1e-3) / 1e9
+    traffic = kernel_traffic("expert_gemv.cu", shape.name)
+    if rank == 0:
+        tok_s = world * shape.T / (ms * 1e-3)
+        line = {
+            "metric": METRIC, "value": tok_s, "unit": UNIT, "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic",
+            "config": {"workload": shape.name, "T": shape.T, "d": shape.d, "E": shape.E,
+                       "top_k": shape.k, "I": shape.I, "I_shared": shape.Is, "weights": shape.fmt,
+                       "parallelism": f"replicas{world}" if world > 1 else "single",
+                       "l2": f"rotate {ncopy} device copies of all weights "
+                             f"({ncopy * w_bytes / 1e9:.2f} GB) and {len(xs)} token batches"},
+            "layer_us": ms * 1e3,
+            "layer_hbm_gbs": alg["layer_bytes"] / (ms * 1e-3) / 1e9,
+            "layer_roofline_frac": alg["layer_bytes"] / (ms * 1e-3) / 1e9 / peaks["hbm_gbs"],
+            "touched_experts": alg["touched"],
+            "stage_us": {k: v * 1e3 for k, v in stage_ms.items()},
+            "timed_pass_us": ms_timed * 1e3,
+            "roofline": {"kernel": "gate_up_kernel", "bound": "hbm", "achieved": achieved,
+                         "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                         "frac": achieved / peaks["hbm_gbs"], "traffic": traffic,
+                         "algorithmic_bytes": alg["gate_up_bytes"], "peak_source": peak_kind},
+            "cpu_baseline": cpu,
+            "e2e": {"value": world * shape.T / (ms_e2e * 1e-3), "unit": UNIT,
+                    "h2d_bytes_per_step": shape.T * shape.d * 2,
+                    "d2h_bytes_per_step": shape.T * shape.d * 2,
+                    "wall_value": args.steps * world * shape.T / t_wall},
+            "gpu_launches": gpu_launches,
+            "clocks": clk,
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -36,6 +36,9 @@
  *     bad access and returns; read it with moe_read_device_status().
  *   - bf16 values are IEEE binary32 truncated to their top 16 bits; the output
  *     is rounded to nearest even.
+ *   - T == 0: moe_route, moe_expert_forward and moe_layer_forward return MOE_OK
+ *     without inspecting any pointer and launch nothing; moe_align_block_size
+ *     writes the empty layout (all offsets 0, num_post_pad 0).
  *
  * Limits (MOE_ERR_UNSUPPORTED otherwise): 0 <= T <= 65536, 8 <= d <= 8192 with
  * d % 8 == 0, 1 <= E <= 1024, 1 <= top_k <= min(E, 16), 8 <= I <= 4096 with

@@ -234,6 +234,7 @@ moe_status_t layer_forward(const moe_dims_t* dims, const void* x, const void* ro
   moe_status_t s = check_dims(dims);
   if (s != MOE_OK) return s;
   const moe_dims_t dm = *dims;
+  if (dm.T == 0) return MOE_OK;  // no tokens: nothing read, written or launched
   if (x == nullptr || router_w == nullptr || out == nullptr) return MOE_ERR_INVALID_ARG;
   if (!aligned16(x) || !aligned16(router_w) || !aligned16(out)) return MOE_ERR_INVALID_ARG;
   if ((ids_out && !aligned16(ids_out)) || (w_out && !aligned16(w_out))) return MOE_ERR_INVALID_ARG;
@@ -350,6 +351,7 @@ moe_status_t moe_route(const moe_dims_t* dims, const void* x, const void* router
   moe_status_t s = check_dims(dims);
   if (s != MOE_OK) return s;
   const moe_dims_t dm = *dims;
+  if (dm.T == 0) return MOE_OK;
   if (!x || !router_w || !topk_ids || !topk_weights) return MOE_ERR_INVALID_ARG;
   if (!aligned16(x) || !aligned16(router_w) || !aligned16(topk_ids) || !aligned16(topk_weights))
     return MOE_ERR_INVALID_ARG;
@@ -375,9 +377,10 @@ moe_status_t moe_align_block_size(const moe_dims_t* dims, const int32_t* topk_id
   moe_status_t s = check_dims(dims);
   if (s != MOE_OK) return s;
   const moe_dims_t dm = *dims;
-  if (!topk_ids || !sorted_ids || !block_expert_ids || !num_post_pad || !expert_offsets)
+  if (!topk_ids && dm.T > 0) return MOE_ERR_INVALID_ARG;
+  if (!sorted_ids || !block_expert_ids || !num_post_pad || !expert_offsets)
     return MOE_ERR_INVALID_ARG;
-  if (!aligned16(topk_ids) || !aligned16(sorted_ids) || !aligned16(block_expert_ids) ||
+  if ((topk_ids && !aligned16(topk_ids)) || !aligned16(sorted_ids) || !aligned16(block_expert_ids) ||
       !aligned16(num_post_pad) || !aligned16(expert_offsets))
     return MOE_ERR_INVALID_ARG;
   Layout L;
@@ -399,6 +402,7 @@ moe_status_t moe_expert_forward(const moe_dims_t* dims, const void* x, const flo
   moe_status_t s = check_dims(dims);
   if (s != MOE_OK) return s;
   const moe_dims_t dm = *dims;
+  if (dm.T == 0) return MOE_OK;
   if (!x || !topk_weights || !sorted_ids || !block_expert_ids || !num_post_pad ||
       !expert_offsets || !out)
     return MOE_ERR_INVALID_ARG;

@@ -359,8 +359,9 @@ __global__ void __launch_bounds__(kAlignThreads)
   const int e = threadIdx.x;
   if (e < E) {
     const int o = expert_offsets[e], o1 = expert_offsets[e + 1];
+    const int cap = S + E * (B - 1);
     int c = o1 - o;
-    if (o < 0 || c < 0 || c % B != 0) {
+    if (o < 0 || c < 0 || c % B != 0 || o1 > cap) {
       record_status(status, kStatusDeviceCheck);
       c = 0;
     }

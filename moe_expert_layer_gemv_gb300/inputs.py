@@ -124,6 +124,13 @@ def make_inputs(s: LayerShape, seed: int = 0) -> dict:
     return out
 
 
+def make_x(s: LayerShape, seed: int) -> torch.Tensor:
+    """Only the token batch of make_inputs(s, seed) (x is its first draw)."""
+    g = torch.Generator(device="cpu")
+    g.manual_seed(seed)
+    return torch.randn((s.T, s.d), generator=g, dtype=torch.float32).to(torch.bfloat16)
+
+
 def bits(t: torch.Tensor):
     """Raw bit pattern of a bf16 CPU tensor as a numpy uint16 array."""
     return t.contiguous().view(torch.int16).numpy().view("uint16")

@@ -1,0 +1,71 @@
+"""Shared helpers of the test suite: feeding the same seeded inputs to the CUDA
+path (through the C ABI) and to the fp64 oracle, and the parity criteria.
+
+Parity criteria (the layer's stated pass bar):
+  * expert ids, and the aligned sort/pad layout, bit-exact on every token whose
+    oracle k-th vs (k+1)-th router-logit margin exceeds 1e-4; near-tie tokens
+    are counted separately, their GPU choice must still be a valid top-k within
+    the margin, and the oracle output is recomputed with the GPU's ids;
+  * output rel-L2 error <= 5e-3 and max-abs error <= 2e-2 * rms(out) against
+    the fp64 oracle, for the bf16 output.
+"""
+import numpy as np
+import torch
+
+import oracle
+from moe_expert_layer_gemv_gb300 import inputs as I
+
+NEAR_TIE = 1e-4
+REL_L2_TOL = 5e-3
+MAX_ABS_TOL = 2e-2  # times rms(oracle out)
+WEIGHT_RTOL = 2e-5  # fp32 softmax weights vs fp64
+
+
+def oracle_args(inp):
+    s = inp["shape"]
+    fmt = oracle.BF16 if s.fmt == "bf16" else oracle.INT4
+    conv = I.bits if s.fmt == "bf16" else (lambda t: t.numpy())
+    ex = {"format": fmt, "group": s.group, "gate_up": conv(inp["gate_up"]), "down": conv(inp["down"]),
+          "gate_up_scales": None if inp["gate_up_scales"] is None else I.bits(inp["gate_up_scales"]),
+          "down_scales": None if inp["down_scales"] is None else I.bits(inp["down_scales"])}
+    sh = None
+    if s.Is > 0:
+        sh = {"gate_up": I.bits(inp["shared_gate_up"]), "down": I.bits(inp["shared_down"]),
+              "gate_w": I.bits(inp["w_sg"])}
+    dims = {"T": s.T, "d": s.d, "E": s.E, "k": s.k, "I": s.I, "Is": s.Is,
+            "renormalize": int(s.renormalize)}
+    return I.bits(inp["x"]), I.bits(inp["router_w"]), ex, sh, dims
+
+
+def bf16_to_f64(t: torch.Tensor) -> np.ndarray:
+    return t.detach().to("cpu").to(torch.float64).numpy()
+
+
+def compare_out(gpu_out, ref_out):
+    """Returns (rel_l2, max_abs / rms) and asserts the pass bar."""
+    g = np.asarray(gpu_out, np.float64)
+    r = np.asarray(ref_out, np.float64)
+    assert g.shape == r.shape
+    assert np.all(np.isfinite(g))
+    rms = float(np.sqrt(np.mean(r * r)))
+    rel = float(np.linalg.norm(g - r) / max(np.linalg.norm(r), 1e-300))
+    mx = float(np.abs(g - r).max() / max(rms, 1e-300)) if g.size else 0.0
+    assert rel <= REL_L2_TOL, f"rel-L2 {rel:.3e} > {REL_L2_TOL}"
+    assert mx <= MAX_ABS_TOL, f"max-abs/rms {mx:.3e} > {MAX_ABS_TOL}"
+    return rel, mx
+
+
+def check_routing(gpu_ids, gpu_w, ref, logits64=None):
+    """ids bit-exact off near-ties; near-ties must be valid; weights close.
+    `ref` is an oracle.layer result for the same tokens (own routing)."""
+    ids = np.asarray(gpu_ids)
+    margin = ref["margin"]
+    far = margin > NEAR_TIE
+    mism = np.any(ids != ref["ids"], axis=1)
+    assert not np.any(mism & far), f"ids differ on {int(np.sum(mism & far))} tokens with margin > 1e-4"
+    for t in np.nonzero(mism)[0]:
+        assert len(set(ids[t].tolist())) == ids.shape[1]
+        if logits64 is not None:
+            kth = np.sort(logits64[t])[::-1][ids.shape[1] - 1]
+            assert np.all(logits64[t][ids[t]] >= kth - NEAR_TIE)
+    return int(np.sum(~far)), int(np.sum(mism))

@@ -1,0 +1,121 @@
+"""CPU tier of the C ABI: the library builds for sm_103a, loads without a GPU,
+exports every entry point include/moe.h declares, and rejects bad arguments on
+the host before launching anything (no CUDA call is reached by these cases)."""
+import ctypes as C
+import os
+import re
+
+import pytest
+
+from moe_expert_layer_gemv_gb300 import abi, build
+from moe_expert_layer_gemv_gb300 import inputs as I
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build.build()
+    return abi.load()
+
+
+def declared_functions():
+    text = open(os.path.join(ROOT, "include", "moe.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"^\s*(?:const\s+)?\w+\**\s+\**(moe_\w+)\s*\(", text, flags=re.M)))
+
+
+def test_header_declares_the_abi():
+    names = declared_functions()
+    assert set(names) == set(abi.EXPORTS), names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+        assert C.cast(getattr(lib, name), C.c_void_p).value
+
+
+def test_status_strings(lib):
+    for code in range(7):
+        assert abi.moe_status_string(code).startswith("MOE_")
+    assert abi.moe_status_string(99) == "MOE_ERR_UNKNOWN"
+
+
+def test_workspace_bytes_and_dims_validation(lib):
+    d8 = abi.dims_of(I.shape("verify_t8"))
+    n8 = abi.moe_workspace_bytes(d8)
+    n64 = abi.moe_workspace_bytes(abi.dims_of(I.shape("verify_t64")))
+    assert 0 < n8 < n64
+    assert n8 % 256 == 0
+    bad = [abi.make_dims(8, 2047, 256, 8, 512),        # d % 8
+           abi.make_dims(8, 2048, 2048, 8, 512),       # E > 1024
+           abi.make_dims(8, 2048, 8, 9, 512),          # k > E
+           abi.make_dims(8, 2048, 64, 17, 512),        # k > 16
+           abi.make_dims(8, 2048, 64, 8, 100),         # I % 8
+           abi.make_dims(8, 2048, 64, 8, 512, weight_format=1, group_size=64),  # int4 group
+           abi.make_dims(8, 2048 + 8, 64, 8, 512, weight_format=1),  # int4 needs d % 256
+           abi.make_dims(8, 2048, 64, 8, 512, block_size=2048)]
+    for dm in bad:
+        with pytest.raises(abi.MoeError) as e:
+            abi.moe_workspace_bytes(dm)
+        assert e.value.status == abi.MOE_ERR_UNSUPPORTED
+    with pytest.raises(abi.MoeError) as e:
+        abi.moe_workspace_bytes(abi.make_dims(-1, 2048, 64, 8, 512))
+    assert e.value.status == abi.MOE_ERR_INVALID_ARG
+    n = C.c_size_t(7)
+    assert lib.moe_workspace_bytes(None, C.byref(n)) == abi.MOE_ERR_INVALID_ARG and n.value == 0
+
+
+FAKE = 1 << 40  # an aligned, never-dereferenced address: these calls stop before any launch
+
+
+def _layer(lib, dims, ws=FAKE, ws_bytes=1 << 40, x=FAKE, shared=True, out=FAKE, ex=None):
+    ex = ex or abi.moe_expert_weights_t(FAKE, None, FAKE, None)
+    sh = abi.moe_shared_weights_t(FAKE, FAKE, FAKE) if shared else None
+    return lib.moe_layer_forward(C.byref(dims), x, FAKE, C.byref(ex),
+                                 C.byref(sh) if sh is not None else None, out, None, None, ws,
+                                 ws_bytes, None)
+
+
+def test_layer_forward_host_side_rejections(lib):
+    dims = abi.dims_of(I.shape("verify_t8"))
+    need = abi.moe_workspace_bytes(dims)
+    assert _layer(lib, dims, x=None) == abi.MOE_ERR_INVALID_ARG
+    assert _layer(lib, dims, x=FAKE + 2) == abi.MOE_ERR_INVALID_ARG          # misaligned
+    assert _layer(lib, dims, out=None) == abi.MOE_ERR_INVALID_ARG
+    assert _layer(lib, dims, shared=False) == abi.MOE_ERR_INVALID_ARG         # I_shared > 0
+    assert _layer(lib, dims, ws=None) == abi.MOE_ERR_WORKSPACE
+    assert _layer(lib, dims, ws=FAKE + 16) == abi.MOE_ERR_WORKSPACE           # not 256-aligned
+    assert _layer(lib, dims, ws_bytes=need - 1) == abi.MOE_ERR_WORKSPACE
+    assert _layer(lib, dims, ex=abi.moe_expert_weights_t(FAKE, None, None, None)) == \
+        abi.MOE_ERR_INVALID_ARG
+    d4 = abi.dims_of(I.shape("int4_t32"))
+    assert _layer(lib, d4, ex=abi.moe_expert_weights_t(FAKE, None, FAKE, None)) == \
+        abi.MOE_ERR_INVALID_ARG                                                # scales missing
+    assert lib.moe_layer_forward(None, FAKE, FAKE, None, None, FAKE, None, None, FAKE, 1, None) == \
+        abi.MOE_ERR_INVALID_ARG
+    assert lib.moe_layer_forward_timed(C.byref(dims), FAKE, FAKE, None, None, FAKE, None, None,
+                                       FAKE, need, None, None) == abi.MOE_ERR_INVALID_ARG
+
+
+def test_stage_calls_host_side_rejections(lib):
+    dims = abi.dims_of(I.shape("verify_t8"))
+    need = abi.moe_workspace_bytes(dims)
+    assert lib.moe_route(C.byref(dims), FAKE, FAKE, None, FAKE, FAKE, need, None) == \
+        abi.MOE_ERR_INVALID_ARG
+    assert lib.moe_route(C.byref(dims), FAKE, FAKE, FAKE, FAKE, FAKE, need - 256, None) == \
+        abi.MOE_ERR_WORKSPACE
+    assert lib.moe_align_block_size(C.byref(dims), FAKE, FAKE, FAKE, None, FAKE, FAKE, need,
+                                    None) == abi.MOE_ERR_INVALID_ARG
+    ex = abi.moe_expert_weights_t(FAKE, None, FAKE, None)
+    sh = abi.moe_shared_weights_t(FAKE, FAKE, FAKE)
+    assert lib.moe_expert_forward(C.byref(dims), FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, C.byref(ex),
+                                  C.byref(sh), FAKE, FAKE, 16, None) == abi.MOE_ERR_WORKSPACE
+    assert lib.moe_workspace_init(None, 1024, None) == abi.MOE_ERR_WORKSPACE
+    code = C.c_int32(0)
+    assert lib.moe_read_device_status(None, C.byref(code), None) == abi.MOE_ERR_INVALID_ARG
+
+
+def test_launch_counter_starts_at_zero_without_launches(lib):
+    assert abi.moe_kernel_launch_count() == 0

@@ -1,0 +1,243 @@
+"""GPU parity of the CUDA path (called through the C ABI) against the fp64
+oracle on the same seeded inputs: the whole layer on every workload shape,
+each stage on its own, and the edge cases (T=1, T=0, ties, k=E, one expert
+holding all tokens, several align block sizes, ragged tiles, bad ids)."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from moe_expert_layer_gemv_gb300 import abi, build
+from moe_expert_layer_gemv_gb300 import inputs as I
+from moe_expert_layer_gemv_gb300.layer import MoeLayer
+
+from _common import NEAR_TIE, WEIGHT_RTOL, bf16_to_f64, check_routing, compare_out, oracle_args
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    if not torch.cuda.is_available():
+        pytest.skip("needs a CUDA GPU")
+    build.build()
+    abi.load()
+
+
+def run_layer(inp):
+    s = inp["shape"]
+    layer = MoeLayer(inp, "cuda")
+    x = inp["x"].cuda()
+    ids = torch.empty((s.T, s.k), dtype=torch.int32, device="cuda")
+    w = torch.empty((s.T, s.k), dtype=torch.float32, device="cuda")
+    out = layer.forward(x, topk_ids=ids, topk_weights=w)
+    torch.cuda.synchronize()
+    assert layer.device_status() == abi.MOE_OK
+    return layer, out, ids.cpu().numpy(), w.cpu().numpy()
+
+
+def logits64(inp):
+    return (inp["x"].to(torch.float64) @ inp["router_w"].to(torch.float64).T).numpy()
+
+
+def layer_parity(inp, tokens=None):
+    """Full-layer check.  tokens: None = all; else a sample (large T)."""
+    s = inp["shape"]
+    layer, out, ids, w = run_layer(inp)
+    args = oracle_args(inp)
+    tl = None if tokens is None else np.asarray(tokens, np.int32)
+    ref = oracle.layer(*args, tokens=tl)
+    sel = slice(None) if tl is None else tl
+    L64 = logits64(inp)[sel]
+    n_near, n_mism = check_routing(ids[sel], w[sel], ref, L64)
+    # outputs against the oracle fed the GPU's routing (covers near-ties)
+    ov = oracle.layer(*args, ids_override=ids, tokens=tl)
+    np.testing.assert_allclose(w[sel], ov["w"], rtol=WEIGHT_RTOL, atol=1e-7)
+    rel, mx = compare_out(bf16_to_f64(out)[sel], ov["out"])
+    return {"rel": rel, "max": mx, "near": n_near, "mism": n_mism, "layer": layer, "ids": ids}
+
+
+@pytest.mark.parametrize("name,seed", [("tiny", 0), ("tiny", 1), ("tiny", 2),
+                                       ("verify_t8", 0), ("verify_t8", 1), ("verify_t8", 2),
+                                       ("verify_t64", 0), ("verify_t64_skew", 0),
+                                       ("int4_t32", 0), ("int4_t32", 1)])
+def test_layer_parity_workloads(name, seed):
+    r = layer_parity(I.make_inputs(I.shape(name), seed))
+    print(f"{name} seed {seed}: rel-L2 {r['rel']:.2e} max/rms {r['max']:.2e} "
+          f"near-ties {r['near']} mismatched {r['mism']}")
+
+
+def test_layer_parity_prefill_sampled():
+    s = I.shape("prefill_t4096")
+    inp = I.make_inputs(s, 0)
+    rng = np.random.default_rng(0)
+    tokens = np.sort(rng.choice(s.T, size=48, replace=False))
+    tokens[0], tokens[-1] = 0, s.T - 1
+    r = layer_parity(inp, tokens)
+    # whole-layer property at full size: the align layout of the GPU's ids
+    ids = r["ids"]
+    ref = oracle.align(ids.reshape(-1), s.E, s.block)
+    assert ref["counts"].sum() == s.T * s.k
+    print(f"prefill sampled: rel-L2 {r['rel']:.2e} max/rms {r['max']:.2e}")
+
+
+@pytest.mark.parametrize("over,seed", [
+    ({"T": 5, "d": 264, "E": 12, "k": 3, "I": 40, "Is": 24}, 3),     # ragged everything
+    ({"T": 1}, 4),                                                   # single token
+    ({"T": 33, "d": 1032, "E": 70, "k": 5, "I": 200, "Is": 56, "block": 64}, 5),
+    ({"T": 17, "d": 512, "E": 8, "k": 8, "I": 64, "Is": 0}, 6),      # k == E
+    ({"T": 130, "d": 256, "E": 32, "k": 4, "I": 72, "Is": 40, "block": 128}, 7),  # T > fused top-k
+])
+def test_layer_parity_ragged_and_edges(over, seed):
+    layer_parity(I.make_inputs(I.shape("verify_t8", **over), seed))
+
+
+def test_layer_int4_ragged():
+    layer_parity(I.make_inputs(I.shape("int4_t32", T=7, d=512, E=20, k=4, I=256, Is=72), 9))
+
+
+def test_zero_router_ties_pick_lowest_ids():
+    inp = I.make_inputs(I.shape("verify_t8", T=6, d=256, E=16, k=4, I=32, Is=16), 1)
+    inp["router_w"] = torch.zeros_like(inp["router_w"])
+    layer, out, ids, w = run_layer(inp)
+    assert ids.tolist() == [[0, 1, 2, 3]] * 6
+    assert np.all(w == np.float32(0.25))
+    ov = oracle.layer(*oracle_args(inp), ids_override=ids)
+    compare_out(bf16_to_f64(out), ov["out"])
+
+
+def test_one_expert_holds_every_token():
+    # x > 0 and router row 3 = +1, others 0: every token's top-1 is expert 3.
+    s = I.shape("verify_t8", T=64, d=256, E=8, k=1, I=48, Is=24)
+    inp = I.make_inputs(s, 2)
+    inp["x"] = inp["x"].abs()
+    wr = torch.zeros((s.E, s.d), dtype=torch.bfloat16)
+    wr[3] = 1.0
+    inp["router_w"] = wr
+    layer, out, ids, w = run_layer(inp)
+    assert np.all(ids == 3) and np.all(w == 1.0)
+    ov = oracle.layer(*oracle_args(inp), ids_override=ids)
+    compare_out(bf16_to_f64(out), ov["out"])
+
+
+def test_empty_batch_launches_nothing():
+    s = I.shape("verify_t8", T=0)
+    inp = I.make_inputs(s, 0)
+    layer = MoeLayer(inp, "cuda")
+    before = abi.moe_kernel_launch_count()
+    out = torch.full((0, s.d), 7.0, dtype=torch.bfloat16, device="cuda")
+    layer.forward(torch.empty((0, s.d), dtype=torch.bfloat16, device="cuda"), out=out)
+    assert abi.moe_kernel_launch_count() == before
+
+
+# ----------------------------------------------------------------------------- stage tests
+
+
+def _stage_tensors(s):
+    S = s.T * s.k
+    cap = S + s.E * (s.block - 1)
+    dev = "cuda"
+    return {"ids": torch.empty((s.T, s.k), dtype=torch.int32, device=dev),
+            "w": torch.empty((s.T, s.k), dtype=torch.float32, device=dev),
+            "sorted": torch.full((cap,), -1, dtype=torch.int32, device=dev),
+            "blocks": torch.full((cap // s.block + 1,), -1, dtype=torch.int32, device=dev),
+            "npp": torch.zeros((1,), dtype=torch.int32, device=dev),
+            "offs": torch.zeros((s.E + 1,), dtype=torch.int32, device=dev)}
+
+
+@pytest.mark.parametrize("name", ["tiny", "verify_t8", "verify_t64", "int4_t32"])
+def test_stage_route(name):
+    s = I.shape(name)
+    inp = I.make_inputs(s, 0)
+    dims = abi.dims_of(s)
+    ws = abi.alloc_workspace(dims)
+    t = _stage_tensors(s)
+    abi.moe_route(dims, inp["x"].cuda(), inp["router_w"].cuda(), t["ids"], t["w"], ws)
+    torch.cuda.synchronize()
+    L = logits64(inp)
+    ids_ref, w_ref, margin, _ = oracle.topk(L, s.k, s.renormalize)
+    ids = t["ids"].cpu().numpy()
+    far = margin > NEAR_TIE
+    assert np.array_equal(ids[far], ids_ref[far])
+    w_ov = oracle.weights_for_ids(L, ids, s.renormalize)
+    np.testing.assert_allclose(t["w"].cpu().numpy(), w_ov, rtol=WEIGHT_RTOL, atol=1e-7)
+
+
+@pytest.mark.parametrize("T,E,k,B,seed", [(4, 8, 2, 16, 0), (8, 256, 8, 16, 1), (64, 256, 8, 16, 2),
+                                          (4096, 256, 8, 128, 3), (32, 512, 10, 16, 4),
+                                          (37, 5, 3, 1, 5), (300, 17, 4, 64, 6), (1, 1024, 16, 16, 7)])
+def test_stage_align_bit_exact(T, E, k, B, seed):
+    s = I.LayerShape(T=T, d=64, E=E, k=k, I=16, block=B)
+    rng = np.random.default_rng(seed)
+    ids_np = np.stack([rng.choice(E, size=k, replace=False) for _ in range(T)]).astype(np.int32)
+    dims = abi.dims_of(s)
+    ws = abi.alloc_workspace(dims)
+    t = _stage_tensors(s)
+    ids = torch.from_numpy(ids_np).cuda()
+    abi.moe_align_block_size(dims, ids, t["sorted"], t["blocks"], t["npp"], t["offs"], ws)
+    torch.cuda.synchronize()
+    ref = oracle.align(ids_np.reshape(-1), E, B)
+    n = int(t["npp"].item())
+    assert n == ref["num_post_pad"]
+    assert np.array_equal(t["sorted"].cpu().numpy()[:n], ref["sorted_ids"])
+    assert np.array_equal(t["blocks"].cpu().numpy()[: n // B], ref["block_expert_ids"])
+    assert np.array_equal(t["offs"].cpu().numpy(), ref["expert_offsets"])
+    assert abi.moe_read_device_status(ws) == abi.MOE_OK
+
+
+def test_stage_align_rejects_out_of_range_ids_without_fault():
+    s = I.LayerShape(T=4, d=64, E=8, k=2, I=16, block=4)
+    dims = abi.dims_of(s)
+    ws = abi.alloc_workspace(dims)
+    t = _stage_tensors(s)
+    ids = torch.tensor([[0, 1], [2, 13], [-1, 3], [4, 5]], dtype=torch.int32, device="cuda")
+    abi.moe_align_block_size(dims, ids, t["sorted"], t["blocks"], t["npp"], t["offs"], ws)
+    assert abi.moe_read_device_status(ws) == abi.MOE_ERR_DEVICE_CHECK
+    assert abi.moe_read_device_status(ws) == abi.MOE_OK  # read clears it
+
+
+@pytest.mark.parametrize("name", ["tiny", "verify_t8", "int4_t32"])
+def test_stage_expert_forward_from_oracle_routing(name):
+    """moe_expert_forward fed the oracle's routing and align layout."""
+    s = I.shape(name)
+    inp = I.make_inputs(s, 1)
+    args = oracle_args(inp)
+    ref = oracle.layer(*args)
+    al = oracle.align(ref["ids"].reshape(-1), s.E, s.block)
+    layer = MoeLayer(inp, "cuda")
+    t = _stage_tensors(s)
+    n = al["num_post_pad"]
+    t["sorted"][:n] = torch.from_numpy(al["sorted_ids"]).cuda()
+    t["blocks"][: n // s.block] = torch.from_numpy(al["block_expert_ids"]).cuda()
+    t["npp"][0] = n
+    t["offs"].copy_(torch.from_numpy(al["expert_offsets"]))
+    w = torch.from_numpy(ref["w"].astype(np.float32)).cuda()
+    out = layer.new_out()
+    abi.moe_expert_forward(layer.dims, inp["x"].cuda(), w, t["sorted"], t["blocks"], t["npp"],
+                           t["offs"], layer.experts, layer.shared, out, layer.ws)
+    torch.cuda.synchronize()
+    assert layer.device_status() == abi.MOE_OK
+    compare_out(bf16_to_f64(out), ref["out"])
+
+
+def test_repeat_calls_are_bitwise_deterministic():
+    inp = I.make_inputs(I.shape("verify_t64_skew"), 0)
+    layer = MoeLayer(inp, "cuda")
+    x = inp["x"].cuda()
+    a = layer.forward(x).clone()
+    for _ in range(3):
+        b = layer.forward(x)
+        assert torch.equal(a, b)
+
+
+def test_timed_entry_point_matches_and_records_events():
+    inp = I.make_inputs(I.shape("verify_t8"), 0)
+    layer = MoeLayer(inp, "cuda")
+    x = inp["x"].cuda()
+    a = layer.forward(x).clone()
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(abi.MOE_EV_COUNT)]
+    b = layer.forward_timed(x, layer.new_out(), ev)
+    torch.cuda.synchronize()
+    assert torch.equal(a, b)
+    times = [ev[i].elapsed_time(ev[i + 1]) for i in range(abi.MOE_EV_COUNT - 1)]
+    assert all(t >= 0 for t in times)
