@@ -191,6 +191,37 @@ moe_status_t moe_layer_forward_timed(const moe_dims_t* dims, const void* x, cons
                                      void* workspace, size_t workspace_bytes, void* stream,
                                      void* const* events);
 
+/* Size of the library-owned scratch array used by moe_layer_forward_static. */
+#define MOE_STATIC_SCRATCH_BYTES (32u << 20)
+
+/* moe_layer_forward for callers that cannot allocate device memory.  The
+ * source pages have no counterpart to this call; it exists for code that may
+ * not call cudaMalloc (a caller whose allocator hands out only model tensors, a
+ * serving loop that forbids allocation after start-up, a host embedding this
+ * library without a caching allocator) and so cannot supply a workspace.
+ * Inputs and outputs are still the caller's device buffers, as for
+ * moe_layer_forward; the scratch lives in one static device array of
+ * MOE_STATIC_SCRATCH_BYTES (32 MiB) inside this library, held by every GPU
+ * that loads it until the process exits.  This call allocates nothing.
+ *   - Dims whose workspace (moe_workspace_bytes) exceeds the array are rejected
+ *     with MOE_ERR_WORKSPACE before anything is launched.  Every decode-sized
+ *     layer of the workloads here fits; a T=4096 prefill layer does not.
+ *   - The first call on a device looks up the array's device address
+ *     (cudaGetSymbolAddress) with that device current; make that first call
+ *     before any stream capture.
+ *   - All calls share the one array and each call overwrites it (the status
+ *     word is cleared at the start of every call).  Calls that overlap on the
+ *     GPU -- on two streams, or from two threads -- race on it and give wrong
+ *     results: order them on one stream.
+ *   - device_status_out (optional device int32, may be NULL) receives this
+ *     call's device status word (MOE_OK or the device-detected error) at the
+ *     end of the call, in stream order. */
+moe_status_t moe_layer_forward_static(const moe_dims_t* dims, const void* x, const void* router_w,
+                                      const moe_expert_weights_t* experts,
+                                      const moe_shared_weights_t* shared, void* out,
+                                      int32_t* topk_ids_out, float* topk_weights_out,
+                                      int32_t* device_status_out, void* stream);
+
 /* Read (and clear) the workspace's device status word.  Synchronises `stream`.
  * *code is MOE_OK or the first device-detected error since the last read. */
 moe_status_t moe_read_device_status(void* workspace, int32_t* code, void* stream);

@@ -21,7 +21,9 @@ MOE_EV_BEGIN, MOE_EV_ROUTED, MOE_EV_GATE_UP, MOE_EV_DOWN, MOE_EV_END, MOE_EV_COU
 # Every extern "C" symbol include/moe.h declares.
 EXPORTS = ("moe_status_string", "moe_workspace_bytes", "moe_workspace_init", "moe_route",
            "moe_align_block_size", "moe_expert_forward", "moe_layer_forward",
-           "moe_layer_forward_timed", "moe_read_device_status", "moe_kernel_launch_count")
+           "moe_layer_forward_timed", "moe_layer_forward_static", "moe_read_device_status",
+           "moe_kernel_launch_count")
+MOE_STATIC_SCRATCH_BYTES = 32 << 20
 
 
 class MoeError(RuntimeError):
@@ -70,6 +72,8 @@ def load():
     L.moe_layer_forward.argtypes = [_D, _P, _P, C.POINTER(moe_expert_weights_t),
                                     C.POINTER(moe_shared_weights_t), _P, _P, _P, _P, C.c_size_t, _P]
     L.moe_layer_forward_timed.argtypes = L.moe_layer_forward.argtypes + [C.POINTER(C.c_void_p)]
+    L.moe_layer_forward_static.argtypes = [_D, _P, _P, C.POINTER(moe_expert_weights_t),
+                                           C.POINTER(moe_shared_weights_t), _P, _P, _P, _P, _P]
     L.moe_read_device_status.argtypes = [_P, C.POINTER(C.c_int32), _P]
     L.moe_kernel_launch_count.argtypes = []
     L.moe_kernel_launch_count.restype = C.c_uint64
@@ -188,6 +192,17 @@ def moe_layer_forward_timed(dims, x, router_w, experts, shared, out, topk_ids_ou
                                           sh, _ptr(out), _ptr(topk_ids_out), _ptr(topk_weights_out),
                                           _ptr(ws), ws.numel(), _stream(stream), arr),
            "moe_layer_forward_timed")
+
+
+def moe_layer_forward_static(dims, x, router_w, experts, shared, out, topk_ids_out=None,
+                             topk_weights_out=None, device_status_out=None, stream=None):
+    """The layer with the library's own static scratch: no workspace argument,
+    nothing allocated (for callers that may not allocate device memory)."""
+    sh = C.byref(shared) if shared is not None else None
+    _check(load().moe_layer_forward_static(C.byref(dims), _ptr(x), _ptr(router_w), C.byref(experts),
+                                           sh, _ptr(out), _ptr(topk_ids_out),
+                                           _ptr(topk_weights_out), _ptr(device_status_out),
+                                           _stream(stream)), "moe_layer_forward_static")
 
 
 def moe_read_device_status(ws, stream=None) -> int:
