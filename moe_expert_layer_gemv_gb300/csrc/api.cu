@@ -62,7 +62,7 @@ bool device_info(DeviceInfo* out) {
 constexpr int kGemvSmemBudget = 227 * 1024 - 1024;
 
 struct Layout {
-  size_t header, plan, work, logits, ids, w, sorted, blocks, npp, offs, h, hs, y, ys, total;
+  size_t header, plan, work, cta, logits, ids, w, sorted, blocks, npp, offs, h, hs, y, ys, total;
   int64_t cap;
 };
 
@@ -80,6 +80,7 @@ Layout layout_of(const moe_dims_t& dm) {
   L.header = carve(&c, kAlign);
   L.plan = carve(&c, sizeof(Plan));
   L.work = carve(&c, sizeof(WorkExpert) * (size_t)(dm.E + 1));
+  L.cta = carve(&c, sizeof(int32_t) * 2 * (size_t)kMaxGrid);
   L.logits = carve(&c, sizeof(float) * (size_t)dm.T * dm.E);
   L.ids = carve(&c, sizeof(int32_t) * (size_t)S);
   L.w = carve(&c, sizeof(float) * (size_t)S);
@@ -155,7 +156,8 @@ struct ExpertPlan {
   PlanParams pp;
 };
 
-moe_status_t expert_plan(const moe_dims_t& dm, void* ws, const Layout& L, ExpertPlan* ep) {
+moe_status_t expert_plan(const moe_dims_t& dm, void* ws, const Layout& L, int sms,
+                         ExpertPlan* ep) {
   const int fmt = dm.weight_format;
   ep->gu = gate_up_shape(fmt, dm.d, dm.I, dm.I_shared, kGemvSmemBudget);
   ep->dn = down_shape(fmt, dm.d, dm.I, dm.I_shared, kGemvSmemBudget);
@@ -169,6 +171,9 @@ moe_status_t expert_plan(const moe_dims_t& dm, void* ws, const Layout& L, Expert
   pp.tiles_dn_shared = dm.I_shared > 0 ? (int)ceil_div(dm.d, ep->dn.rg_shared) : 0;
   pp.xt_gu = ep->gu.xt;
   pp.xt_dn = ep->dn.xt;
+  pp.grid = sms < kMaxGrid ? sms : kMaxGrid;
+  pp.cta_first_gu = at<int32_t>(ws, L.cta);
+  pp.cta_first_dn = at<int32_t>(ws, L.cta) + kMaxGrid;
   return MOE_OK;
 }
 
@@ -202,7 +207,7 @@ moe_status_t record(void* const* events, int which, cudaStream_t st) {
 moe_status_t run_experts(const moe_dims_t& dm, const void* x, const float* topk_w,
                          const int32_t* sorted_ids, const moe_expert_weights_t* ex,
                          const moe_shared_weights_t* sh, void* out, void* ws, const Layout& L,
-                         const ExpertPlan& ep, int sms, cudaStream_t st, void* const* events) {
+                         const ExpertPlan& ep, cudaStream_t st, void* const* events) {
   const LaunchCfg next{st, true};
   int* status = at<int>(ws, L.header);
   const ExpertArgs a = expert_args(dm, ex, sh);
@@ -212,11 +217,11 @@ moe_status_t run_experts(const moe_dims_t& dm, const void* x, const float* topk_
   float* ys = at<float>(ws, L.ys);
   moe_status_t s;
   if (launch_gate_up(next, a, ep.gu, static_cast<const uint16_t*>(x), sorted_ids, ep.pp.plan,
-                     ep.pp.work, h, hs, status, sms) != cudaSuccess)
+                     ep.pp.work, ep.pp.cta_first_gu, h, hs, status, ep.pp.grid) != cudaSuccess)
     return MOE_ERR_CUDA;
   if ((s = record(events, MOE_EV_GATE_UP, st)) != MOE_OK) return s;
-  if (launch_down(next, a, ep.dn, sorted_ids, ep.pp.plan, ep.pp.work, h, hs, y, ys, status,
-                  sms) != cudaSuccess)
+  if (launch_down(next, a, ep.dn, sorted_ids, ep.pp.plan, ep.pp.work, ep.pp.cta_first_dn, h, hs, y,
+                  ys, status, ep.pp.grid) != cudaSuccess)
     return MOE_ERR_CUDA;
   if ((s = record(events, MOE_EV_DOWN, st)) != MOE_OK) return s;
   if (launch_combine(next, dm.T, dm.d, dm.top_k, topk_w, y, sh ? ys : nullptr,
@@ -241,11 +246,10 @@ moe_status_t layer_forward(const moe_dims_t* dims, const void* x, const void* ro
   if ((s = check_weights(dm, ex, sh)) != MOE_OK) return s;
   Layout L;
   if ((s = check_ws(dm, ws, ws_bytes, &L)) != MOE_OK) return s;
-  ExpertPlan ep;
-  if ((s = expert_plan(dm, ws, L, &ep)) != MOE_OK) return s;
-  if (dm.T == 0) return MOE_OK;
   DeviceInfo di;
   if (!device_info(&di)) return MOE_ERR_CUDA;
+  ExpertPlan ep;
+  if ((s = expert_plan(dm, ws, L, di.sms, &ep)) != MOE_OK) return s;
 
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   const LaunchCfg first{st, false}, next{st, true};
@@ -270,7 +274,7 @@ moe_status_t layer_forward(const moe_dims_t* dims, const void* x, const void* ro
                    ep.pp, status) != cudaSuccess)
     return MOE_ERR_CUDA;
   if ((s = record(events, MOE_EV_ROUTED, st)) != MOE_OK) return s;
-  if ((s = run_experts(dm, x, w, sorted, ex, sh, out, ws, L, ep, di.sms, st, events)) != MOE_OK)
+  if ((s = run_experts(dm, x, w, sorted, ex, sh, out, ws, L, ep, st, events)) != MOE_OK)
     return s;
   return record(events, MOE_EV_END, st);
 }
@@ -412,18 +416,17 @@ moe_status_t moe_expert_forward(const moe_dims_t* dims, const void* x, const flo
   if ((s = check_weights(dm, experts, shared)) != MOE_OK) return s;
   Layout L;
   if ((s = check_ws(dm, workspace, workspace_bytes, &L)) != MOE_OK) return s;
-  ExpertPlan ep;
-  if ((s = expert_plan(dm, workspace, L, &ep)) != MOE_OK) return s;
-  if (dm.T == 0) return MOE_OK;
   DeviceInfo di;
   if (!device_info(&di)) return MOE_ERR_CUDA;
+  ExpertPlan ep;
+  if ((s = expert_plan(dm, workspace, L, di.sms, &ep)) != MOE_OK) return s;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   if (launch_plan(LaunchCfg{st, false}, dm.T, dm.E, dm.top_k, dm.block_size, sorted_ids,
                   num_post_pad, expert_offsets, ep.pp, at<int>(workspace, L.header)) !=
       cudaSuccess)
     return MOE_ERR_CUDA;
-  return run_experts(dm, x, topk_weights, sorted_ids, experts, shared, out, workspace, L, ep,
-                     di.sms, st, nullptr);
+  return run_experts(dm, x, topk_weights, sorted_ids, experts, shared, out, workspace, L, ep, st,
+                     nullptr);
 }
 
 moe_status_t moe_layer_forward(const moe_dims_t* dims, const void* x, const void* router_w,

@@ -12,9 +12,10 @@ namespace moe {
 
 namespace {
 
-constexpr int kThreads = 256;
+constexpr int kThreads = 64;
+constexpr int kCols = kThreads * 8;  // output columns per CTA
 
-// grid = T; each thread writes 8 consecutive outputs per step.
+// grid = (T, ceil(d / kCols)); each thread writes 8 consecutive outputs.
 __global__ void __launch_bounds__(kThreads)
     combine_kernel(int d, int k, const float* __restrict__ w, const float* __restrict__ y,
                    const float* __restrict__ ys, const uint16_t* __restrict__ x,
@@ -48,10 +49,12 @@ __global__ void __launch_bounds__(kThreads)
     gate = sigmoid(z);
   }
   const float* wt = w + (size_t)t * k;
-  for (int c = threadIdx.x * 8; c < d; c += kThreads * 8) {
+  for (int c = blockIdx.y * kCols + threadIdx.x * 8; c < min(d, (int)(blockIdx.y + 1) * kCols);
+       c += kThreads * 8) {
     float acc[8];
 #pragma unroll
     for (int q = 0; q < 8; ++q) acc[q] = 0.f;
+#pragma unroll 4
     for (int j = 0; j < k; ++j) {
       const float wj = wt[j];
       const float4* yr = reinterpret_cast<const float4*>(y + ((size_t)t * k + j) * d + c);
@@ -95,7 +98,8 @@ cudaError_t launch_combine(const LaunchCfg& c, int T, int d, int k, const float*
                            const uint16_t* w_sg, uint16_t* out) {
   if (T == 0) return cudaSuccess;
   void* args[] = {&d, &k, &w, &y, &ys, &x, &w_sg, &out};
-  return launch_kernel(c, (const void*)combine_kernel, dim3(T), dim3(kThreads), 0, args);
+  return launch_kernel(c, (const void*)combine_kernel, dim3(T, (unsigned)ceil_div(d, kCols)),
+                       dim3(kThreads), 0, args);
 }
 
 }  // namespace moe

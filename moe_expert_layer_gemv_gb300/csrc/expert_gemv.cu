@@ -6,7 +6,9 @@
 // persistent grid).
 //
 // Structure (both stages): a persistent grid, one CTA per SM.  Work is cut into
-// units = (work expert, row tile, token group); unit u goes to CTA u mod grid.
+// units = (work expert, token group, row tile); each CTA takes one contiguous
+// range of units (its first work expert is precomputed by the plan), so
+// consecutive units mostly share an expert and a token group.
 // Warp 8 is a producer: one bulk copy (cp.async.bulk, the non-tensor TMA) per
 // weight block and per activation row lands a unit in a shared-memory ring
 // stage and completes its mbarrier by transaction bytes.  Warps 0-7 consume:
@@ -36,6 +38,7 @@ struct GuArgs {
   const int32_t* sorted_ids;
   const Plan* plan;
   const WorkExpert* work;
+  const int32_t* cta_first;  // [grid] first work expert of each CTA's range
   float* h;   // [num_post_pad][I]
   float* hs;  // [T][Is]
   int* status;
@@ -50,6 +53,7 @@ struct DnArgs {
   const int32_t* sorted_ids;
   const Plan* plan;
   const WorkExpert* work;
+  const int32_t* cta_first;
   const float* h;
   const float* hs;
   float* y;   // [T*k][d]
@@ -59,11 +63,27 @@ struct DnArgs {
   int rd, rds, xt, stage_bytes, n_stages;
 };
 
-// Advance the work-expert cursor `i` to the entry holding unit u.
+// Walks the work experts along a CTA's contiguous unit range.  Units of one
+// work expert are numbered group-major: unit = grp * tiles + tile, so
+// consecutive units share a token group (same activation rows).
 template <bool kDown>
-__device__ __forceinline__ void locate(const WorkExpert* work, int n_work, int u, int& i) {
-  while (i + 1 < n_work && (kDown ? work[i + 1].unit_dn : work[i + 1].unit_gu) <= u) ++i;
-}
+struct UnitCursor {
+  const WorkExpert* work;
+  int n_work, tiles_r, tiles_s, xt;
+  int i, ubeg, uend, tiles, groups;
+  WorkExpert we;
+  __device__ __forceinline__ void load(int idx) {
+    i = idx;
+    we = work[idx];
+    tiles = we.expert < 0 ? tiles_s : tiles_r;
+    groups = (int)ceil_div(we.n_tok, xt);
+    ubeg = kDown ? we.unit_dn : we.unit_gu;
+    uend = ubeg + tiles * groups;
+  }
+  __device__ __forceinline__ void seek(int u) {
+    while (u >= uend && i + 1 < n_work) load(i + 1);
+  }
+};
 
 __device__ __forceinline__ float dot8(uint4 w, uint4 xv, float acc) {
   acc = fmaf(bf16lo(w.x), bf16lo(xv.x), acc);
@@ -153,24 +173,29 @@ __global__ void __launch_bounds__(kThreads, 1) gate_up_kernel(const GuArgs a) {
   // Routed row bytes (codes only, for int4) and int4 scale bytes per row.
   const int rowb = kFmt ? d / 2 : d * 2;
   const int srowb = kFmt ? d / 16 : 0;
+  const int u_begin = unit_begin(blockIdx.x, plan.units_gu, gridDim.x);
+  const int u_end = unit_begin(blockIdx.x + 1, plan.units_gu, gridDim.x);
+  UnitCursor<false> cur;
+  cur.work = a.work;
+  cur.n_work = plan.n_work;
+  cur.tiles_r = (int)ceil_div(a.I, a.rg);
+  cur.tiles_s = a.Is > 0 ? (int)ceil_div(a.Is, a.rgs) : 1;
+  cur.xt = xt;
+  if (u_begin < u_end) cur.load(a.cta_first[blockIdx.x]);
 
   if (warp == kConsumerWarps) {
     // ------------------------------------------------------------ producer
     const uint64_t pol_w = policy_evict_first();
     const uint64_t pol_x = policy_evict_last();
-    int i = 0, j = 0;
+    int j = 0;
     bool ok = true;
-    for (int u = blockIdx.x; u < plan.units_gu; u += gridDim.x, ++j) {
+    int tok = 0, tok_i = -1, tok_g = -1;  // lane 4+m: token of member m of the cached group
+    for (int u = u_begin; u < u_end; ++u, ++j) {
       const int s = j % NS, use = j / NS;
-      if (use > 0 && !mbar_wait(&empty[s], (uint32_t)((use - 1) & 1), a.status)) {
-        ok = false;
-        break;
-      }
-      locate<false>(a.work, plan.n_work, u, i);
-      const WorkExpert we = a.work[i];
-      const int groups = (int)ceil_div(we.n_tok, xt);
-      const int local = u - we.unit_gu;
-      const int tile = local / groups, grp = local % groups;
+      cur.seek(u);
+      const WorkExpert& we = cur.we;
+      const int local = u - cur.ubeg;
+      const int grp = local / cur.tiles, tile = local - grp * cur.tiles;
       const bool shared = we.expert < 0;
       const int RG = shared ? a.rgs : a.rg;
       const int Iw = shared ? a.Is : a.I;
@@ -178,6 +203,27 @@ __global__ void __launch_bounds__(kThreads, 1) gate_up_kernel(const GuArgs a) {
       const int nr = min(RG, Iw - r0);
       const int g0 = grp * xt;
       const int nt = min(xt, we.n_tok - g0);
+      // Token rows of this group: looked up once per (work expert, group).
+      if (cur.i != tok_i || grp != tok_g) {
+        tok_i = cur.i;
+        tok_g = grp;
+        tok = 0;
+        if (lane >= 4 && lane < 4 + nt) {
+          tok = g0 + lane - 4;
+          if (!shared) {
+            const int slot = a.sorted_ids[we.pos + g0 + lane - 4];
+            tok = slot / a.k;
+            if (slot < 0 || tok >= a.T) {
+              record_status(a.status, kStatusDeviceCheck);
+              tok = 0;
+            }
+          }
+        }
+      }
+      if (use > 0 && !mbar_wait(&empty[s], (uint32_t)((use - 1) & 1), a.status)) {
+        ok = false;
+        break;
+      }
       uint8_t* st = stages + (size_t)s * a.stage_bytes;
       const int rb = shared ? d * 2 : rowb;
       const int sb = shared ? 0 : srowb;
@@ -198,34 +244,21 @@ __global__ void __launch_bounds__(kThreads, 1) gate_up_kernel(const GuArgs a) {
                    pol_w);
       }
       const int xoff = 2 * RG * (rb + sb);
-      if (lane >= 4 && lane < 4 + nt) {
-        const int m = g0 + lane - 4;
-        int t = m;
-        if (!shared) {
-          const int slot = a.sorted_ids[we.pos + m];
-          t = slot / a.k;
-          if (slot < 0 || t >= a.T) {
-            record_status(a.status, kStatusDeviceCheck);
-            t = 0;
-          }
-        }
-        bulk_g2s(st + xoff + (lane - 4) * d * 2, a.x + (size_t)t * d, d * 2, &full[s], pol_x);
-      }
+      if (lane >= 4 && lane < 4 + nt)
+        bulk_g2s(st + xoff + (lane - 4) * d * 2, a.x + (size_t)tok * d, d * 2, &full[s], pol_x);
     }
     if (!ok) drain_stages(full, j, NS, a.status);
     return;
   }
 
   // -------------------------------------------------------------- consumers
-  int i = 0, j = 0;
-  for (int u = blockIdx.x; u < plan.units_gu; u += gridDim.x, ++j) {
+  int j = 0;
+  for (int u = u_begin; u < u_end; ++u, ++j) {
     const int s = j % NS, use = j / NS;
-    if (!mbar_wait(&full[s], (uint32_t)(use & 1), a.status)) break;
-    locate<false>(a.work, plan.n_work, u, i);
-    const WorkExpert we = a.work[i];
-    const int groups = (int)ceil_div(we.n_tok, xt);
-    const int local = u - we.unit_gu;
-    const int tile = local / groups, grp = local % groups;
+    cur.seek(u);
+    const WorkExpert& we = cur.we;
+    const int local = u - cur.ubeg;
+    const int grp = local / cur.tiles, tile = local - grp * cur.tiles;
     const bool shared = we.expert < 0;
     const int RG = shared ? a.rgs : a.rg;
     const int Iw = shared ? a.Is : a.I;
@@ -233,6 +266,7 @@ __global__ void __launch_bounds__(kThreads, 1) gate_up_kernel(const GuArgs a) {
     const int nr = min(RG, Iw - r0);
     const int g0 = grp * xt;
     const int nt = min(xt, we.n_tok - g0);
+    if (!mbar_wait(&full[s], (uint32_t)(use & 1), a.status)) break;
     const uint8_t* st = stages + (size_t)s * a.stage_bytes;
     const int rb = shared ? d * 2 : rowb;
     const int sb = shared ? 0 : srowb;
@@ -335,23 +369,27 @@ __global__ void __launch_bounds__(kThreads, 1) down_kernel(const DnArgs a) {
   const int xt = a.xt;
   const int rowb = kFmt ? a.I / 2 : a.I * 2;
   const int srowb = kFmt ? a.I / 16 : 0;
+  const int u_begin = unit_begin(blockIdx.x, plan.units_dn, gridDim.x);
+  const int u_end = unit_begin(blockIdx.x + 1, plan.units_dn, gridDim.x);
+  UnitCursor<true> cur;
+  cur.work = a.work;
+  cur.n_work = plan.n_work;
+  cur.tiles_r = (int)ceil_div(a.d, a.rd);
+  cur.tiles_s = a.Is > 0 ? (int)ceil_div(a.d, a.rds) : 1;
+  cur.xt = xt;
+  if (u_begin < u_end) cur.load(a.cta_first[blockIdx.x]);
 
   if (warp == kConsumerWarps) {
     const uint64_t pol_w = policy_evict_first();
     const uint64_t pol_h = policy_evict_last();  // h rows are re-read by every row tile
-    int i = 0, j = 0;
+    int j = 0;
     bool ok = true;
-    for (int u = blockIdx.x; u < plan.units_dn; u += gridDim.x, ++j) {
+    for (int u = u_begin; u < u_end; ++u, ++j) {
       const int s = j % NS, use = j / NS;
-      if (use > 0 && !mbar_wait(&empty[s], (uint32_t)((use - 1) & 1), a.status)) {
-        ok = false;
-        break;
-      }
-      locate<true>(a.work, plan.n_work, u, i);
-      const WorkExpert we = a.work[i];
-      const int groups = (int)ceil_div(we.n_tok, xt);
-      const int local = u - we.unit_dn;
-      const int tile = local / groups, grp = local % groups;
+      cur.seek(u);
+      const WorkExpert& we = cur.we;
+      const int local = u - cur.ubeg;
+      const int grp = local / cur.tiles, tile = local - grp * cur.tiles;
       const bool shared = we.expert < 0;
       const int RD = shared ? a.rds : a.rd;
       const int Iw = shared ? a.Is : a.I;
@@ -359,6 +397,10 @@ __global__ void __launch_bounds__(kThreads, 1) down_kernel(const DnArgs a) {
       const int nr = min(RD, a.d - r0);
       const int g0 = grp * xt;
       const int nt = min(xt, we.n_tok - g0);
+      if (use > 0 && !mbar_wait(&empty[s], (uint32_t)((use - 1) & 1), a.status)) {
+        ok = false;
+        break;
+      }
       uint8_t* st = stages + (size_t)s * a.stage_bytes;
       const int rb = shared ? Iw * 2 : rowb;
       const int sb = shared ? 0 : srowb;
@@ -384,15 +426,14 @@ __global__ void __launch_bounds__(kThreads, 1) down_kernel(const DnArgs a) {
   }
 
   const int sub = lane >> 3, sl = lane & 7;  // row within the warp's quad, lane in row
-  int i = 0, j = 0;
-  for (int u = blockIdx.x; u < plan.units_dn; u += gridDim.x, ++j) {
+  int j = 0;
+  int slot_of_lane = 0, slot_i = -1, slot_g = -1;  // slot id of token sl of the cached group
+  for (int u = u_begin; u < u_end; ++u, ++j) {
     const int s = j % NS, use = j / NS;
-    if (!mbar_wait(&full[s], (uint32_t)(use & 1), a.status)) break;
-    locate<true>(a.work, plan.n_work, u, i);
-    const WorkExpert we = a.work[i];
-    const int groups = (int)ceil_div(we.n_tok, xt);
-    const int local = u - we.unit_dn;
-    const int tile = local / groups, grp = local % groups;
+    cur.seek(u);
+    const WorkExpert& we = cur.we;
+    const int local = u - cur.ubeg;
+    const int grp = local / cur.tiles, tile = local - grp * cur.tiles;
     const bool shared = we.expert < 0;
     const int RD = shared ? a.rds : a.rd;
     const int Iw = shared ? a.Is : a.I;
@@ -400,14 +441,16 @@ __global__ void __launch_bounds__(kThreads, 1) down_kernel(const DnArgs a) {
     const int nr = min(RD, a.d - r0);
     const int g0 = grp * xt;
     const int nt = min(xt, we.n_tok - g0);
+    if (cur.i != slot_i || grp != slot_g) {
+      slot_i = cur.i;
+      slot_g = grp;
+      slot_of_lane = (!shared && sl < nt) ? a.sorted_ids[we.pos + g0 + sl] : 0;
+    }
+    if (!mbar_wait(&full[s], (uint32_t)(use & 1), a.status)) break;
     const uint8_t* st = stages + (size_t)s * a.stage_bytes;
     const int rb = shared ? Iw * 2 : rowb;
     const int sb = shared ? 0 : srowb;
     const float* hsm = reinterpret_cast<const float*>(st + RD * (rb + sb));
-
-    // Slot id of token sl of this group (routed) for the output write.
-    int slot_of_lane = 0;
-    if (!shared && sl < nt) slot_of_lane = a.sorted_ids[we.pos + g0 + sl];
 
     for (int rq = warp * 4; rq < nr; rq += kConsumerWarps * 4) {
       const int r = rq + sub;  // this lane group's row within the tile
@@ -519,8 +562,10 @@ GemvShape down_shape(int fmt, int d, int I, int Is, int smem_budget) {
 
 cudaError_t launch_gate_up(const LaunchCfg& c, const ExpertArgs& e, const GemvShape& g,
                            const uint16_t* x, const int32_t* sorted_ids, const Plan* plan,
-                           const WorkExpert* work, float* h, float* hs, int* status, int grid) {
+                           const WorkExpert* work, const int32_t* cta_first, float* h, float* hs,
+                           int* status, int grid) {
   GuArgs a;
+  a.cta_first = cta_first;
   a.gu = static_cast<const uint8_t*>(e.gate_up);
   a.gu_scales = e.gate_up_scales;
   a.sgu = reinterpret_cast<const uint8_t*>(e.s_gate_up);
@@ -551,9 +596,10 @@ cudaError_t launch_gate_up(const LaunchCfg& c, const ExpertArgs& e, const GemvSh
 
 cudaError_t launch_down(const LaunchCfg& c, const ExpertArgs& e, const GemvShape& g,
                         const int32_t* sorted_ids, const Plan* plan, const WorkExpert* work,
-                        const float* h, const float* hs, float* y, float* ys, int* status,
-                        int grid) {
+                        const int32_t* cta_first, const float* h, const float* hs, float* y,
+                        float* ys, int* status, int grid) {
   DnArgs a;
+  a.cta_first = cta_first;
   a.dn = static_cast<const uint8_t*>(e.down);
   a.dn_scales = e.down_scales;
   a.sdn = reinterpret_cast<const uint8_t*>(e.s_down);

@@ -46,6 +46,9 @@ struct PlanParams {
   int tiles_dn_shared;
   int xt_gu;             // tokens per gate_up unit
   int xt_dn;             // tokens per down unit
+  int grid;              // CTAs of the persistent expert kernels (<= kMaxGrid)
+  int32_t* cta_first_gu; // [grid] first work expert of each CTA's unit range
+  int32_t* cta_first_dn; // [grid]
 };
 
 // Single-CTA align: optional fused top-k (logits != nullptr), the
@@ -83,12 +86,13 @@ struct ExpertArgs {
 
 cudaError_t launch_gate_up(const LaunchCfg& c, const ExpertArgs& a, const GemvShape& g,
                            const uint16_t* x, const int32_t* sorted_ids, const Plan* plan,
-                           const WorkExpert* work, float* h, float* hs, int* status, int grid);
+                           const WorkExpert* work, const int32_t* cta_first, float* h, float* hs,
+                           int* status, int grid);
 
 cudaError_t launch_down(const LaunchCfg& c, const ExpertArgs& a, const GemvShape& g,
                         const int32_t* sorted_ids, const Plan* plan, const WorkExpert* work,
-                        const float* h, const float* hs, float* y, float* ys, int* status,
-                        int grid);
+                        const int32_t* cta_first, const float* h, const float* hs, float* y,
+                        float* ys, int* status, int grid);
 
 // out[t] = sum_j w[t][j] y[t*k+j] + sigmoid(x[t].w_sg) ys[t]   (bf16, RNE)
 cudaError_t launch_combine(const LaunchCfg& c, int T, int d, int k, const float* w,

@@ -197,10 +197,13 @@ __device__ int block_exclusive_scan(int v, int* scratch, int* total) {
 }
 
 // Work plan: one WorkExpert per touched routed expert (ascending id), then the
-// shared expert; gate_up / down work units counted per expert.  Called by all
-// 1024 threads; cnt/off are the per-expert counts and padded offsets.
+// shared expert; gate_up / down work units counted per expert; and for every
+// CTA of the persistent expert kernels, the work expert its unit range starts
+// in.  Called by all 1024 threads; cnt/off are per-expert counts and padded
+// offsets; tmp holds >= 2 * (E + 1) ints of shared memory.
 __device__ void build_plan(const int* cnt, const int* off, int E, int T, int num_post_pad,
-                           const PlanParams& pp, int* scratch) {
+                           const PlanParams& pp, int* scratch, int* tmp) {
+  __syncthreads();
   const int e = threadIdx.x;
   const int c = (e < E) ? cnt[e] : 0;
   const int flag = c > 0;
@@ -210,6 +213,8 @@ __device__ void build_plan(const int* cnt, const int* off, int E, int T, int num
   const int udn = flag ? pp.tiles_dn * (int)ceil_div(c, pp.xt_dn) : 0;
   const int egu = block_exclusive_scan(ugu, scratch, &tot_gu);
   const int edn = block_exclusive_scan(udn, scratch, &tot_dn);
+  int* s_gu = tmp;          // [n_work] first gate_up unit of each work expert
+  int* s_dn = tmp + E + 1;  // [n_work] first down unit
   if (flag) {
     WorkExpert we;
     we.expert = e;
@@ -219,10 +224,13 @@ __device__ void build_plan(const int* cnt, const int* off, int E, int T, int num
     we.unit_dn = edn;
     we.pad_[0] = we.pad_[1] = we.pad_[2] = 0;
     pp.work[idx] = we;
+    s_gu[idx] = egu;
+    s_dn[idx] = edn;
   }
-  if (threadIdx.x == 0) {
-    int n_work = n_routed;
-    if (pp.tiles_gu_shared > 0 && T > 0) {
+  const bool has_shared = pp.tiles_gu_shared > 0 && T > 0;
+  const int n_work = n_routed + (has_shared ? 1 : 0);
+  if (has_shared) {
+    if (threadIdx.x == 0) {
       WorkExpert we;
       we.expert = -1;
       we.n_tok = T;
@@ -230,10 +238,32 @@ __device__ void build_plan(const int* cnt, const int* off, int E, int T, int num
       we.unit_gu = tot_gu;
       we.unit_dn = tot_dn;
       we.pad_[0] = we.pad_[1] = we.pad_[2] = 0;
-      pp.work[n_work++] = we;
-      tot_gu += pp.tiles_gu_shared * (int)ceil_div(T, pp.xt_gu);
-      tot_dn += pp.tiles_dn_shared * (int)ceil_div(T, pp.xt_dn);
+      pp.work[n_routed] = we;
+      s_gu[n_routed] = tot_gu;
+      s_dn[n_routed] = tot_dn;
     }
+    tot_gu += pp.tiles_gu_shared * (int)ceil_div(T, pp.xt_gu);
+    tot_dn += pp.tiles_dn_shared * (int)ceil_div(T, pp.xt_dn);
+  }
+  __syncthreads();
+  // CTA c's range starts in the last work expert whose first unit <= its begin.
+  for (int cta = threadIdx.x; cta < pp.grid; cta += blockDim.x) {
+    const int ug = unit_begin(cta, tot_gu, pp.grid), ud = unit_begin(cta, tot_dn, pp.grid);
+    int lo = 0, hi = n_work - 1;
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (s_gu[mid] <= ug) lo = mid; else hi = mid - 1;
+    }
+    pp.cta_first_gu[cta] = n_work > 0 ? lo : 0;
+    lo = 0;
+    hi = n_work - 1;
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (s_dn[mid] <= ud) lo = mid; else hi = mid - 1;
+    }
+    pp.cta_first_dn[cta] = n_work > 0 ? lo : 0;
+  }
+  if (threadIdx.x == 0) {
     Plan p;
     p.n_work = n_work;
     p.units_gu = tot_gu;
@@ -340,7 +370,7 @@ __global__ void __launch_bounds__(kAlignThreads)
     __syncwarp();
   }
 
-  if (pp.work != nullptr) build_plan(cnt, off, E, T, total, pp, scratch);
+  if (pp.work != nullptr) build_plan(cnt, off, E, T, total, pp, scratch, hist);
 }
 
 // Plan from an existing align layout: counts recovered from the padded runs
@@ -350,9 +380,10 @@ __global__ void __launch_bounds__(kAlignThreads)
                 const int32_t* __restrict__ num_post_pad, const int32_t* __restrict__ expert_offsets,
                 PlanParams pp, int* status) {
   extern __shared__ int sm[];
-  int* cnt = sm;          // [E]
-  int* off = cnt + E;     // [E]
-  int* scratch = off + E; // [32]
+  int* cnt = sm;               // [E]
+  int* off = cnt + E;          // [E]
+  int* scratch = off + E;      // [32]
+  int* tmp = scratch + 32;     // [2 * (E + 1)]
   pdl_wait();
   pdl_trigger();
   const int S = T * k;
@@ -371,7 +402,7 @@ __global__ void __launch_bounds__(kAlignThreads)
     off[e] = o;
   }
   __syncthreads();
-  build_plan(cnt, off, E, T, *num_post_pad, pp, scratch);
+  build_plan(cnt, off, E, T, *num_post_pad, pp, scratch, tmp);
 }
 
 }  // namespace
@@ -422,7 +453,7 @@ cudaError_t launch_align(const LaunchCfg& c, const float* logits, int T, int E, 
 cudaError_t launch_plan(const LaunchCfg& c, int T, int E, int k, int B,
                         const int32_t* sorted_ids, const int32_t* num_post_pad,
                         const int32_t* expert_offsets, const PlanParams& pp, int* status) {
-  const size_t smem = (2 * (size_t)E + 32) * sizeof(int);
+  const size_t smem = (4 * (size_t)E + 34) * sizeof(int);
   PlanParams p = pp;
   void* args[] = {&T, &E, &k, &B, &sorted_ids, &num_post_pad, &expert_offsets, &p, &status};
   return launch_kernel(c, (const void*)plan_kernel, dim3(1), dim3(kAlignThreads), smem, args);
