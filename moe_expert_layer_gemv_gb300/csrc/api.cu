@@ -56,10 +56,11 @@ bool device_info(DeviceInfo* out) {
   return true;
 }
 
-// Shared-memory budget of the persistent GEMV kernels.  Fixed (not read from
-// the device) so that the stage plan, hence the unit counts, depend only on the
-// dims; 227 KB is the per-CTA opt-in maximum of sm_100-class GPUs.
-constexpr int kGemvSmemBudget = 227 * 1024 - 1024;
+// Shared-memory budget per CTA of the persistent GEMV kernels: the SM's 228 KB
+// split over kCtasPerSm CTAs, less the 1 KB the hardware reserves per CTA and a
+// little slack.  Fixed (not read from the device) so that the stage plan, hence
+// the unit counts, depend only on the dims.
+constexpr int kGemvSmemBudget = 228 * 1024 / kCtasPerSm - 1024 - 512;
 
 struct Layout {
   size_t header, plan, work, cta, logits, ids, w, sorted, blocks, npp, offs, h, hs, y, ys, total;
@@ -171,7 +172,7 @@ moe_status_t expert_plan(const moe_dims_t& dm, void* ws, const Layout& L, int sm
   pp.tiles_dn_shared = dm.I_shared > 0 ? (int)ceil_div(dm.d, ep->dn.rg_shared) : 0;
   pp.xt_gu = ep->gu.xt;
   pp.xt_dn = ep->dn.xt;
-  pp.grid = sms < kMaxGrid ? sms : kMaxGrid;
+  pp.grid = kCtasPerSm * sms < kMaxGrid ? kCtasPerSm * sms : kMaxGrid;
   pp.cta_first_gu = at<int32_t>(ws, L.cta);
   pp.cta_first_dn = at<int32_t>(ws, L.cta) + kMaxGrid;
   return MOE_OK;

@@ -15,9 +15,16 @@ constexpr int kStatusOk = 0;
 constexpr int kStatusDeviceCheck = 5;
 constexpr int kStatusTimeout = 6;
 
-// A pipeline wait gives up after this many try_wait polls (each poll may itself
-// suspend for a hardware-defined time), records kStatusTimeout and returns.
-constexpr uint32_t kSpinLimit = 1u << 22;
+// A pipeline wait gives up after kWaitLimitNs of wall time (or kSpinLimit
+// polls, whichever comes first), records kStatusTimeout and returns.
+constexpr uint64_t kWaitLimitNs = 2000000000ull;
+constexpr uint32_t kSpinLimit = 1u << 26;
+// Each poll may park the thread for up to this long (woken early when the
+// phase completes), so waiting warps do not steal issue slots.
+constexpr uint32_t kSuspendHintNs = 100000;
+
+// Persistent expert kernels run this many CTAs per SM.
+constexpr int kCtasPerSm = 2;
 
 // ---------------------------------------------------------------- plan layout
 // One entry per "work expert": every touched routed expert in ascending id,
@@ -99,19 +106,29 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   uint32_t ok;
   asm volatile(
       "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
       "selp.u32 %0, 1, 0, p;\n\t}"
       : "=r"(ok)
-      : "r"(smem_u32(bar)), "r"(parity)
+      : "r"(smem_u32(bar)), "r"(parity), "r"(kSuspendHintNs)
       : "memory");
   return ok != 0;
 }
 
+__device__ __forceinline__ uint64_t global_timer_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
 // Bounded wait for phase `parity` of `bar`.  Returns false (after recording
-// kStatusTimeout) if the phase did not complete within kSpinLimit polls.
+// kStatusTimeout) if the phase did not complete within the bounds above.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, int* status) {
-  for (uint32_t i = 0; i < kSpinLimit; ++i)
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = global_timer_ns();
+  for (uint32_t i = 1; i < kSpinLimit; ++i) {
     if (mbar_try_wait(bar, parity)) return true;
+    if ((i & 15u) == 0 && global_timer_ns() - t0 > kWaitLimitNs) break;
+  }
   record_status(status, kStatusTimeout);
   return false;
 }

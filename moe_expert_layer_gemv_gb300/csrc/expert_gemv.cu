@@ -5,15 +5,18 @@
 // the MoE step -- here the shared expert is one more work expert in the same
 // persistent grid).
 //
-// Structure (both stages): a persistent grid, one CTA per SM.  Work is cut into
-// units = (work expert, token group, row tile); each CTA takes one contiguous
-// range of units (its first work expert is precomputed by the plan), so
-// consecutive units mostly share an expert and a token group.
-// Warp 8 is a producer: one bulk copy (cp.async.bulk, the non-tensor TMA) per
-// weight block and per activation row lands a unit in a shared-memory ring
-// stage and completes its mbarrier by transaction bytes.  Warps 0-7 consume:
-// fp32 dot products out of shared memory, warp-shuffle reductions, the SwiGLU
-// (gate_up) or the per-slot output write (down), then release the stage.
+// Structure (both stages): a persistent grid of kCtasPerSm CTAs per SM.  Work
+// is cut into units = (work expert, token group, row tile); each CTA takes one
+// contiguous range of units (its first work expert is precomputed by the
+// plan), so consecutive units mostly share an expert and a token group.  The
+// last warp of a CTA is the producer: one bulk copy (cp.async.bulk, the
+// non-tensor TMA) per weight block and per activation row lands a unit in a
+// shared-memory ring stage and completes the stage's mbarrier by transaction
+// bytes.  The other warps consume: fp32 dot products out of shared memory with
+// several independent accumulators per output, warp-shuffle reductions, the
+// SwiGLU (gate_up) or the per-slot output write (down), then release the stage.
+// The number of tokens a consumer warp handles in a unit is a template
+// parameter, so the inner loops carry no per-token branches.
 // int4 weights are dequantised in registers: (nibble - 8) accumulated against
 // the activations per group of 32, times the group's bf16 scale (W4A16 routed
 // experts: "Qwen3.8 Flash-Next - GB10 UltraFast", How it works).
@@ -23,9 +26,8 @@ namespace moe {
 
 namespace {
 
-constexpr int kConsumerWarps = 8;
+constexpr int kConsumerWarps = 4;
 constexpr int kThreads = (kConsumerWarps + 1) * 32;
-constexpr int kMaxTokPerWarp = 8;  // gate_up: tokens one warp handles per unit
 constexpr int kMaxXT = 8;          // tokens per unit
 constexpr int kBarBytes = 256;     // barrier area at the start of shared memory
 constexpr int kMaxStages = 8;
@@ -38,9 +40,9 @@ struct GuArgs {
   const int32_t* sorted_ids;
   const Plan* plan;
   const WorkExpert* work;
-  const int32_t* cta_first;  // [grid] first work expert of each CTA's range
-  float* h;   // [num_post_pad][I]
-  float* hs;  // [T][Is]
+  const int32_t* cta_first;   // [grid] first work expert of each CTA's range
+  float* h;                   // [num_post_pad][I]
+  float* hs;                  // [T][Is]
   int* status;
   int T, d, I, Is, k;
   int rg, rgs, xt, stage_bytes, n_stages;
@@ -56,8 +58,8 @@ struct DnArgs {
   const int32_t* cta_first;
   const float* h;
   const float* hs;
-  float* y;   // [T*k][d]
-  float* ys;  // [T][d]
+  float* y;                   // [T*k][d]
+  float* ys;                  // [T][d]
   int* status;
   int T, d, I, Is, k;
   int rd, rds, xt, stage_bytes, n_stages;
@@ -85,16 +87,49 @@ struct UnitCursor {
   }
 };
 
-__device__ __forceinline__ float dot8(uint4 w, uint4 xv, float acc) {
-  acc = fmaf(bf16lo(w.x), bf16lo(xv.x), acc);
-  acc = fmaf(bf16hi(w.x), bf16hi(xv.x), acc);
-  acc = fmaf(bf16lo(w.y), bf16lo(xv.y), acc);
-  acc = fmaf(bf16hi(w.y), bf16hi(xv.y), acc);
-  acc = fmaf(bf16lo(w.z), bf16lo(xv.z), acc);
-  acc = fmaf(bf16hi(w.z), bf16hi(xv.z), acc);
-  acc = fmaf(bf16lo(w.w), bf16lo(xv.w), acc);
-  acc = fmaf(bf16hi(w.w), bf16hi(xv.w), acc);
-  return acc;
+// ------------------------------------------------------------------ smem loads
+__device__ __forceinline__ uint4 lds128(uint32_t addr) {
+  uint4 v;
+  asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "r"(addr));
+  return v;
+}
+__device__ __forceinline__ float4 lds128f(uint32_t addr) {
+  float4 v;
+  asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
+               : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+               : "r"(addr));
+  return v;
+}
+__device__ __forceinline__ float lds_bf16(uint32_t addr) {
+  uint16_t v;
+  asm volatile("ld.shared.u16 %0, [%1];" : "=h"(v) : "r"(addr));
+  return __uint_as_float((uint32_t)v << 16);
+}
+
+// ------------------------------------------------------------------ dot pieces
+// Two independent accumulators (even / odd elements) for 8 bf16 products.
+__device__ __forceinline__ void fma8(uint4 w, uint4 x, float& a0, float& a1) {
+  a0 = fmaf(bf16lo(w.x), bf16lo(x.x), a0);
+  a1 = fmaf(bf16hi(w.x), bf16hi(x.x), a1);
+  a0 = fmaf(bf16lo(w.y), bf16lo(x.y), a0);
+  a1 = fmaf(bf16hi(w.y), bf16hi(x.y), a1);
+  a0 = fmaf(bf16lo(w.z), bf16lo(x.z), a0);
+  a1 = fmaf(bf16hi(w.z), bf16hi(x.z), a1);
+  a0 = fmaf(bf16lo(w.w), bf16lo(x.w), a0);
+  a1 = fmaf(bf16hi(w.w), bf16hi(x.w), a1);
+}
+
+__device__ __forceinline__ void fma8f(uint4 w, float4 p, float4 q, float& a0, float& a1) {
+  a0 = fmaf(bf16lo(w.x), p.x, a0);
+  a1 = fmaf(bf16hi(w.x), p.y, a1);
+  a0 = fmaf(bf16lo(w.y), p.z, a0);
+  a1 = fmaf(bf16hi(w.y), p.w, a1);
+  a0 = fmaf(bf16lo(w.z), q.x, a0);
+  a1 = fmaf(bf16hi(w.z), q.y, a1);
+  a0 = fmaf(bf16lo(w.w), q.z, a0);
+  a1 = fmaf(bf16hi(w.w), q.w, a1);
 }
 
 // Signed int4 value (nibble - 8) as an exact float: (2^23 + nibble) - (2^23 + 8).
@@ -102,41 +137,167 @@ __device__ __forceinline__ float nib(uint32_t v, int sh) {
   return __uint_as_float(0x4b000000u | ((v >> sh) & 15u)) - 8388616.0f;
 }
 
-// sum_{e<8} (code_e - 8) * x_e for the 8 codes of word v against 8 bf16 of xv.
-__device__ __forceinline__ float dot8_int4(uint32_t v, uint4 xv, float acc) {
-  acc = fmaf(nib(v, 0), bf16lo(xv.x), acc);
-  acc = fmaf(nib(v, 4), bf16hi(xv.x), acc);
-  acc = fmaf(nib(v, 8), bf16lo(xv.y), acc);
-  acc = fmaf(nib(v, 12), bf16hi(xv.y), acc);
-  acc = fmaf(nib(v, 16), bf16lo(xv.z), acc);
-  acc = fmaf(nib(v, 20), bf16hi(xv.z), acc);
-  acc = fmaf(nib(v, 24), bf16lo(xv.w), acc);
-  acc = fmaf(nib(v, 28), bf16hi(xv.w), acc);
-  return acc;
+// The 8 codes of word v (element 2b in the low nibble of byte b) against 8 bf16.
+__device__ __forceinline__ void fma8_int4(uint32_t v, uint4 x, float& a0, float& a1) {
+  a0 = fmaf(nib(v, 0), bf16lo(x.x), a0);
+  a1 = fmaf(nib(v, 4), bf16hi(x.x), a1);
+  a0 = fmaf(nib(v, 8), bf16lo(x.y), a0);
+  a1 = fmaf(nib(v, 12), bf16hi(x.y), a1);
+  a0 = fmaf(nib(v, 16), bf16lo(x.z), a0);
+  a1 = fmaf(nib(v, 20), bf16hi(x.z), a1);
+  a0 = fmaf(nib(v, 24), bf16lo(x.w), a0);
+  a1 = fmaf(nib(v, 28), bf16hi(x.w), a1);
 }
 
-__device__ __forceinline__ float dot8_f32(uint4 w, float4 a, float4 b, float acc) {
-  acc = fmaf(bf16lo(w.x), a.x, acc);
-  acc = fmaf(bf16hi(w.x), a.y, acc);
-  acc = fmaf(bf16lo(w.y), a.z, acc);
-  acc = fmaf(bf16hi(w.y), a.w, acc);
-  acc = fmaf(bf16lo(w.z), b.x, acc);
-  acc = fmaf(bf16hi(w.z), b.y, acc);
-  acc = fmaf(bf16lo(w.w), b.z, acc);
-  acc = fmaf(bf16hi(w.w), b.w, acc);
-  return acc;
+__device__ __forceinline__ void fma8_int4f(uint32_t v, float4 p, float4 q, float& a0, float& a1) {
+  a0 = fmaf(nib(v, 0), p.x, a0);
+  a1 = fmaf(nib(v, 4), p.y, a1);
+  a0 = fmaf(nib(v, 8), p.z, a0);
+  a1 = fmaf(nib(v, 12), p.w, a1);
+  a0 = fmaf(nib(v, 16), q.x, a0);
+  a1 = fmaf(nib(v, 20), q.y, a1);
+  a0 = fmaf(nib(v, 24), q.z, a0);
+  a1 = fmaf(nib(v, 28), q.w, a1);
 }
 
-__device__ __forceinline__ float dot8_int4_f32(uint32_t v, float4 a, float4 b, float acc) {
-  acc = fmaf(nib(v, 0), a.x, acc);
-  acc = fmaf(nib(v, 4), a.y, acc);
-  acc = fmaf(nib(v, 8), a.z, acc);
-  acc = fmaf(nib(v, 12), a.w, acc);
-  acc = fmaf(nib(v, 16), b.x, acc);
-  acc = fmaf(nib(v, 20), b.y, acc);
-  acc = fmaf(nib(v, 24), b.z, acc);
-  acc = fmaf(nib(v, 28), b.w, acc);
-  return acc;
+// ------------------------------------------------------------------ gate_up math
+// One warp: gate row at wg, up row at wu (shared addresses), NT token rows at
+// xa + q * xs.  bf16 weights; 16-byte chunks strided over the lanes.  Returns
+// the per-token full dot products in every lane.
+template <int NT>
+__device__ __forceinline__ void gu_rows_bf16(uint32_t wg, uint32_t wu, uint32_t xa, uint32_t xs,
+                                             int nch, int lane, float* g, float* u) {
+  float g0[NT], g1[NT], u0[NT], u1[NT];
+#pragma unroll
+  for (int q = 0; q < NT; ++q) g0[q] = g1[q] = u0[q] = u1[q] = 0.f;
+#pragma unroll 2
+  for (int c = lane; c < nch; c += 32) {
+    const uint32_t off = (uint32_t)c * 16u;
+    const uint4 vg = lds128(wg + off), vu = lds128(wu + off);
+    uint4 xv[NT];
+#pragma unroll
+    for (int q = 0; q < NT; ++q) xv[q] = lds128(xa + q * xs + off);
+#pragma unroll
+    for (int q = 0; q < NT; ++q) {
+      fma8(vg, xv[q], g0[q], g1[q]);
+      fma8(vu, xv[q], u0[q], u1[q]);
+    }
+  }
+#pragma unroll
+  for (int q = 0; q < NT; ++q) {
+    g[q] = warp_sum(g0[q] + g1[q]);
+    u[q] = warp_sum(u0[q] + u1[q]);
+  }
+}
+
+// int4 weights: a 16-byte chunk is 32 codes = one scale group; the group's
+// bf16 scales at sg / su (one per chunk).
+template <int NT>
+__device__ __forceinline__ void gu_rows_int4(uint32_t wg, uint32_t wu, uint32_t sg, uint32_t su,
+                                             uint32_t xa, uint32_t xs, int ngroups, int lane,
+                                             float* g, float* u) {
+  float ga[NT], ua[NT];
+#pragma unroll
+  for (int q = 0; q < NT; ++q) ga[q] = ua[q] = 0.f;
+  for (int c = lane; c < ngroups; c += 32) {
+    const uint32_t off = (uint32_t)c * 16u;
+    const uint4 vg = lds128(wg + off), vu = lds128(wu + off);
+    const float fg = lds_bf16(sg + 2u * c), fu = lds_bf16(su + 2u * c);
+#pragma unroll
+    for (int q = 0; q < NT; ++q) {
+      const uint32_t xr = xa + q * xs + 4u * off;
+      const uint4 x0 = lds128(xr), x1 = lds128(xr + 16), x2 = lds128(xr + 32), x3 = lds128(xr + 48);
+      float p0 = 0.f, p1 = 0.f, r0 = 0.f, r1 = 0.f;
+      fma8_int4(vg.x, x0, p0, p1);
+      fma8_int4(vg.y, x1, p0, p1);
+      fma8_int4(vg.z, x2, p0, p1);
+      fma8_int4(vg.w, x3, p0, p1);
+      fma8_int4(vu.x, x0, r0, r1);
+      fma8_int4(vu.y, x1, r0, r1);
+      fma8_int4(vu.z, x2, r0, r1);
+      fma8_int4(vu.w, x3, r0, r1);
+      ga[q] = fmaf(fg, p0 + p1, ga[q]);
+      ua[q] = fmaf(fu, r0 + r1, ua[q]);
+    }
+  }
+#pragma unroll
+  for (int q = 0; q < NT; ++q) {
+    g[q] = warp_sum(ga[q]);
+    u[q] = warp_sum(ua[q]);
+  }
+}
+
+// One consumer warp's share of a gate_up unit: NT tokens; lane q writes token
+// q's h value at hout + q * hstride.
+template <int NT, bool kInt4>
+__device__ __forceinline__ void gu_warp(uint32_t wg, uint32_t wu, uint32_t sg, uint32_t su,
+                                        uint32_t xa, uint32_t xs, int d, int lane, float* hout,
+                                        size_t hstride) {
+  float g[NT], u[NT];
+  if (kInt4)
+    gu_rows_int4<NT>(wg, wu, sg, su, xa, xs, d / 32, lane, g, u);
+  else
+    gu_rows_bf16<NT>(wg, wu, xa, xs, d / 8, lane, g, u);
+  float gv = g[0], uv = u[0];
+#pragma unroll
+  for (int q = 1; q < NT; ++q)
+    if (lane == q) {
+      gv = g[q];
+      uv = u[q];
+    }
+  if (lane < NT) hout[(size_t)lane * hstride] = silu(gv) * uv;
+}
+
+// ------------------------------------------------------------------ down math
+// One weight row per 8-lane group.  NT tokens' h rows (fp32) at ha + q * hsb.
+// Returns, in lane sl of the group, the output of token sl for that row.
+template <int NT, bool kInt4>
+__device__ __forceinline__ float dn_row(uint32_t wr, uint32_t sr, uint32_t ha, uint32_t hsb,
+                                        int Iw, int sl) {
+  float a0[NT], a1[NT];
+#pragma unroll
+  for (int q = 0; q < NT; ++q) a0[q] = a1[q] = 0.f;
+  if (!kInt4) {
+#pragma unroll 2
+    for (int c = sl; c < Iw / 8; c += 8) {
+      const uint32_t off = (uint32_t)c * 16u;
+      const uint4 w = lds128(wr + off);
+      float4 hp[NT], hq[NT];
+#pragma unroll
+      for (int q = 0; q < NT; ++q) {
+        hp[q] = lds128f(ha + q * hsb + 2u * off);
+        hq[q] = lds128f(ha + q * hsb + 2u * off + 16u);
+      }
+#pragma unroll
+      for (int q = 0; q < NT; ++q) fma8f(w, hp[q], hq[q], a0[q], a1[q]);
+    }
+  } else {
+    for (int c = sl; c < Iw / 32; c += 8) {
+      const uint32_t off = (uint32_t)c * 16u;
+      const uint4 v = lds128(wr + off);
+      const float sc = lds_bf16(sr + 2u * c);
+#pragma unroll
+      for (int q = 0; q < NT; ++q) {
+        const uint32_t hr = ha + q * hsb + 8u * off;
+        float p0 = 0.f, p1 = 0.f;
+        fma8_int4f(v.x, lds128f(hr), lds128f(hr + 16), p0, p1);
+        fma8_int4f(v.y, lds128f(hr + 32), lds128f(hr + 48), p0, p1);
+        fma8_int4f(v.z, lds128f(hr + 64), lds128f(hr + 80), p0, p1);
+        fma8_int4f(v.w, lds128f(hr + 96), lds128f(hr + 112), p0, p1);
+        a0[q] = fmaf(sc, p0 + p1, a0[q]);
+      }
+    }
+  }
+  float mine = 0.f;
+#pragma unroll
+  for (int q = 0; q < NT; ++q) {
+    float v = a0[q] + a1[q];
+    v += __shfl_xor_sync(0xffffffffu, v, 4);
+    v += __shfl_xor_sync(0xffffffffu, v, 2);
+    v += __shfl_xor_sync(0xffffffffu, v, 1);
+    if (sl == q) mine = v;
+  }
+  return mine;
 }
 
 // Producer drain after an abort: wait (bounded) for the last fills of every
@@ -148,11 +309,12 @@ __device__ void drain_stages(uint64_t* full, int issued, int n_stages, int* stat
 
 // --------------------------------------------------------------------------- gate_up
 template <int kFmt>
-__global__ void __launch_bounds__(kThreads, 1) gate_up_kernel(const GuArgs a) {
+__global__ void __launch_bounds__(kThreads, kCtasPerSm) gate_up_kernel(const GuArgs a) {
   extern __shared__ __align__(128) uint8_t smem[];
   uint64_t* full = reinterpret_cast<uint64_t*>(smem);
   uint64_t* empty = full + kMaxStages;
   uint8_t* stages = smem + kBarBytes;
+  const uint32_t stages_sa = smem_u32(stages);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int NS = a.n_stages;
 
@@ -168,7 +330,7 @@ __global__ void __launch_bounds__(kThreads, 1) gate_up_kernel(const GuArgs a) {
   pdl_trigger();
 
   const Plan plan = *a.plan;
-  const int d = a.d, nch = d >> 3;
+  const int d = a.d;
   const int xt = a.xt;
   // Routed row bytes (codes only, for int4) and int4 scale bytes per row.
   const int rowb = kFmt ? d / 2 : d * 2;
@@ -266,91 +428,56 @@ __global__ void __launch_bounds__(kThreads, 1) gate_up_kernel(const GuArgs a) {
     const int nr = min(RG, Iw - r0);
     const int g0 = grp * xt;
     const int nt = min(xt, we.n_tok - g0);
-    if (!mbar_wait(&full[s], (uint32_t)(use & 1), a.status)) break;
-    const uint8_t* st = stages + (size_t)s * a.stage_bytes;
     const int rb = shared ? d * 2 : rowb;
     const int sb = shared ? 0 : srowb;
-    const int p = warp % RG, tsub = warp / RG, nsub = kConsumerWarps / RG;
-    const uint4* xs = reinterpret_cast<const uint4*>(st + 2 * RG * (rb + sb));
-
-    if (p < nr) {
-      float ag[kMaxTokPerWarp], au[kMaxTokPerWarp];
-#pragma unroll
-      for (int q = 0; q < kMaxTokPerWarp; ++q) ag[q] = au[q] = 0.f;
-      if (kFmt == 0 || shared) {
-        const uint4* wg = reinterpret_cast<const uint4*>(st + p * rb);
-        const uint4* wu = reinterpret_cast<const uint4*>(st + RG * rb + p * rb);
-        for (int c = lane; c < nch; c += 32) {
-          const uint4 vg = wg[c], vu = wu[c];
-#pragma unroll
-          for (int q = 0; q < kMaxTokPerWarp; ++q) {
-            const int m = tsub + q * nsub;
-            if (m < nt) {
-              const uint4 xv = xs[m * nch + c];
-              ag[q] = dot8(vg, xv, ag[q]);
-              au[q] = dot8(vu, xv, au[q]);
-            }
-          }
-        }
-      } else {
-        // int4: one 16-byte chunk = 32 codes = one scale group.
-        const uint4* cg = reinterpret_cast<const uint4*>(st + p * rb);
-        const uint4* cu = reinterpret_cast<const uint4*>(st + RG * rb + p * rb);
-        const uint16_t* sg = reinterpret_cast<const uint16_t*>(st + 2 * RG * rb + p * sb);
-        const uint16_t* su = reinterpret_cast<const uint16_t*>(st + 2 * RG * rb + RG * sb + p * sb);
-        for (int c = lane; c < d / 32; c += 32) {
-          const uint4 vg = cg[c], vu = cu[c];
-          const float fg = __uint_as_float((uint32_t)sg[c] << 16);
-          const float fu = __uint_as_float((uint32_t)su[c] << 16);
-#pragma unroll
-          for (int q = 0; q < kMaxTokPerWarp; ++q) {
-            const int m = tsub + q * nsub;
-            if (m < nt) {
-              const uint4* xr = xs + m * nch + 4 * c;
-              const uint4 x0 = xr[0], x1 = xr[1], x2 = xr[2], x3 = xr[3];
-              float pg = dot8_int4(vg.x, x0, 0.f);
-              pg = dot8_int4(vg.y, x1, pg);
-              pg = dot8_int4(vg.z, x2, pg);
-              pg = dot8_int4(vg.w, x3, pg);
-              float pu = dot8_int4(vu.x, x0, 0.f);
-              pu = dot8_int4(vu.y, x1, pu);
-              pu = dot8_int4(vu.z, x2, pu);
-              pu = dot8_int4(vu.w, x3, pu);
-              ag[q] = fmaf(fg, pg, ag[q]);
-              au[q] = fmaf(fu, pu, au[q]);
-            }
-          }
-        }
-      }
-#pragma unroll
-      for (int q = 0; q < kMaxTokPerWarp; ++q) {
-        const int m = tsub + q * nsub;
-        if (m < nt) {
-          const float g = warp_sum(ag[q]);
-          const float uu = warp_sum(au[q]);
-          if (lane == 0) {
-            const float hv = silu(g) * uu;
-            if (shared)
-              a.hs[(size_t)(g0 + m) * a.Is + r0 + p] = hv;
-            else
-              a.h[(size_t)(we.pos + g0 + m) * a.I + r0 + p] = hv;
-          }
-        }
-      }
+    // Warp -> (pair p, token subset tsub of nsub): tokens m = tsub + q * nsub.
+    const int nsub = kConsumerWarps / RG;
+    const int p = warp % RG, tsub = warp / RG;
+    const int cnt = (p < nr && nt > tsub) ? (nt - tsub + nsub - 1) / nsub : 0;
+    if (!mbar_wait(&full[s], (uint32_t)(use & 1), a.status)) break;
+    const uint32_t st = stages_sa + (uint32_t)(s * a.stage_bytes);
+    const uint32_t wg = st + p * rb, wu = st + RG * rb + p * rb;
+    const uint32_t sg = st + 2 * RG * rb + p * sb, su = sg + RG * sb;
+    const uint32_t xs = (uint32_t)(nsub * d * 2);
+    const uint32_t xa = st + 2 * RG * (rb + sb) + tsub * d * 2;
+    float* hout = shared ? a.hs + (size_t)(g0 + tsub) * a.Is + r0 + p
+                         : a.h + (size_t)(we.pos + g0 + tsub) * a.I + r0 + p;
+    const size_t hstride = (size_t)nsub * (shared ? a.Is : a.I);
+    const bool int4 = kFmt && !shared;
+#define MOE_GU_CASE(N)                                                   \
+  case N:                                                                \
+    if (int4)                                                            \
+      gu_warp<N, true>(wg, wu, sg, su, xa, xs, d, lane, hout, hstride);  \
+    else                                                                 \
+      gu_warp<N, false>(wg, wu, sg, su, xa, xs, d, lane, hout, hstride); \
+    break;
+    switch (cnt) {
+      MOE_GU_CASE(1)
+      MOE_GU_CASE(2)
+      MOE_GU_CASE(3)
+      MOE_GU_CASE(4)
+      MOE_GU_CASE(5)
+      MOE_GU_CASE(6)
+      MOE_GU_CASE(7)
+      MOE_GU_CASE(8)
+      default:
+        break;
     }
+#undef MOE_GU_CASE
     __syncwarp();
     if (lane == 0) mbar_arrive(&empty[s]);
   }
 }
 
 // --------------------------------------------------------------------------- down
-// Consumers: 8 lanes per weight row, so a warp works on 4 rows at a time.
+// Consumers: 8 lanes per weight row, 4 rows per warp pass.
 template <int kFmt>
-__global__ void __launch_bounds__(kThreads, 1) down_kernel(const DnArgs a) {
+__global__ void __launch_bounds__(kThreads, kCtasPerSm) down_kernel(const DnArgs a) {
   extern __shared__ __align__(128) uint8_t smem[];
   uint64_t* full = reinterpret_cast<uint64_t*>(smem);
   uint64_t* empty = full + kMaxStages;
   uint8_t* stages = smem + kBarBytes;
+  const uint32_t stages_sa = smem_u32(stages);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int NS = a.n_stages;
 
@@ -446,67 +573,43 @@ __global__ void __launch_bounds__(kThreads, 1) down_kernel(const DnArgs a) {
       slot_g = grp;
       slot_of_lane = (!shared && sl < nt) ? a.sorted_ids[we.pos + g0 + sl] : 0;
     }
-    if (!mbar_wait(&full[s], (uint32_t)(use & 1), a.status)) break;
-    const uint8_t* st = stages + (size_t)s * a.stage_bytes;
     const int rb = shared ? Iw * 2 : rowb;
     const int sb = shared ? 0 : srowb;
-    const float* hsm = reinterpret_cast<const float*>(st + RD * (rb + sb));
+    if (!mbar_wait(&full[s], (uint32_t)(use & 1), a.status)) break;
+    const uint32_t st = stages_sa + (uint32_t)(s * a.stage_bytes);
+    const uint32_t ha = st + RD * (rb + sb);
+    const uint32_t hsb = (uint32_t)Iw * 4u;
+    const bool int4 = kFmt && !shared;
 
     for (int rq = warp * 4; rq < nr; rq += kConsumerWarps * 4) {
-      const int r = rq + sub;  // this lane group's row within the tile
-      float acc[kMaxXT];
-#pragma unroll
-      for (int m = 0; m < kMaxXT; ++m) acc[m] = 0.f;
-      if (r < nr) {
-        if (kFmt == 0 || shared) {
-          const uint4* wr = reinterpret_cast<const uint4*>(st + r * rb);
-          for (int c = sl; c < Iw / 8; c += 8) {
-            const uint4 w = wr[c];
-#pragma unroll
-            for (int m = 0; m < kMaxXT; ++m) {
-              if (m < nt) {
-                const float4* hp = reinterpret_cast<const float4*>(hsm + (size_t)m * Iw + c * 8);
-                acc[m] = dot8_f32(w, hp[0], hp[1], acc[m]);
-              }
-            }
-          }
-        } else {
-          const uint4* cr = reinterpret_cast<const uint4*>(st + r * rb);
-          const uint16_t* sr = reinterpret_cast<const uint16_t*>(st + RD * rb + r * sb);
-          for (int c = sl; c < Iw / 32; c += 8) {
-            const uint4 v = cr[c];
-            const float sc = __uint_as_float((uint32_t)sr[c] << 16);
-#pragma unroll
-            for (int m = 0; m < kMaxXT; ++m) {
-              if (m < nt) {
-                const float4* hp = reinterpret_cast<const float4*>(hsm + (size_t)m * Iw + c * 32);
-                float pp = dot8_int4_f32(v.x, hp[0], hp[1], 0.f);
-                pp = dot8_int4_f32(v.y, hp[2], hp[3], pp);
-                pp = dot8_int4_f32(v.z, hp[4], hp[5], pp);
-                pp = dot8_int4_f32(v.w, hp[6], hp[7], pp);
-                acc[m] = fmaf(sc, pp, acc[m]);
-              }
-            }
-          }
-        }
-      }
-      // Reduce across the 8 lanes of each row; lane sl of the group owns token sl.
+      const int r = min(rq + sub, nr - 1);  // lanes past the tile recompute its last row
+      const uint32_t wr = st + r * rb, sr = st + RD * rb + r * sb;
       float mine = 0.f;
-#pragma unroll
-      for (int m = 0; m < kMaxXT; ++m) {
-        float v = acc[m];
-        v += __shfl_xor_sync(0xffffffffu, v, 4);
-        v += __shfl_xor_sync(0xffffffffu, v, 2);
-        v += __shfl_xor_sync(0xffffffffu, v, 1);
-        if (sl == m) mine = v;
+#define MOE_DN_CASE(N)                                       \
+  case N:                                                    \
+    mine = int4 ? dn_row<N, true>(wr, sr, ha, hsb, Iw, sl)   \
+                : dn_row<N, false>(wr, sr, ha, hsb, Iw, sl); \
+    break;
+      switch (nt) {
+        MOE_DN_CASE(1)
+        MOE_DN_CASE(2)
+        MOE_DN_CASE(3)
+        MOE_DN_CASE(4)
+        MOE_DN_CASE(5)
+        MOE_DN_CASE(6)
+        MOE_DN_CASE(7)
+        MOE_DN_CASE(8)
+        default:
+          break;
       }
-      if (r < nr && sl < nt) {
+#undef MOE_DN_CASE
+      if (rq + sub < nr && sl < nt) {
         if (shared) {
-          a.ys[(size_t)(g0 + sl) * a.d + r0 + r] = mine;
+          a.ys[(size_t)(g0 + sl) * a.d + r0 + rq + sub] = mine;
         } else {
           const int slot = slot_of_lane;
           if (slot >= 0 && slot < a.T * a.k)
-            a.y[(size_t)slot * a.d + r0 + r] = mine;
+            a.y[(size_t)slot * a.d + r0 + rq + sub] = mine;
           else
             record_status(a.status, kStatusDeviceCheck);
         }
@@ -524,10 +627,10 @@ GemvShape gate_up_shape(int fmt, int d, int I, int Is, int smem_budget) {
   GemvShape g;
   const int rowr = fmt ? d / 2 + d / 16 : d * 2;
   const int rows = d * 2;
-  const int target = 32 * 1024;
-  g.rg = 8;
+  const int target = 32 * 1024;  // weight bytes per stage
+  g.rg = kConsumerWarps;
   while (g.rg > 1 && 2 * g.rg * rowr > target) g.rg /= 2;
-  g.rg_shared = 8;
+  g.rg_shared = kConsumerWarps;
   while (g.rg_shared > 1 && 2 * g.rg_shared * rows > target) g.rg_shared /= 2;
   g.xt = 16 * 1024 / (d * 2);
   g.xt = g.xt < 1 ? 1 : (g.xt > kMaxXT ? kMaxXT : g.xt);
