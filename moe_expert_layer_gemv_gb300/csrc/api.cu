@@ -81,7 +81,7 @@ Layout layout_of(const moe_dims_t& dm) {
   L.header = carve(&c, kAlign);
   L.plan = carve(&c, sizeof(Plan));
   L.work = carve(&c, sizeof(WorkExpert) * (size_t)(dm.E + 1));
-  L.cta = carve(&c, sizeof(int32_t) * 2 * (size_t)kMaxGrid);
+  L.cta = carve(&c, sizeof(int32_t) * 4 * ((size_t)kMaxGrid + 1));
   L.logits = carve(&c, sizeof(float) * (size_t)dm.T * dm.E);
   L.ids = carve(&c, sizeof(int32_t) * (size_t)S);
   L.w = carve(&c, sizeof(float) * (size_t)S);
@@ -173,8 +173,8 @@ moe_status_t expert_plan(const moe_dims_t& dm, void* ws, const Layout& L, int sm
   pp.xt_gu = ep->gu.xt;
   pp.xt_dn = ep->dn.xt;
   pp.grid = kCtasPerSm * sms < kMaxGrid ? kCtasPerSm * sms : kMaxGrid;
-  pp.cta_first_gu = at<int32_t>(ws, L.cta);
-  pp.cta_first_dn = at<int32_t>(ws, L.cta) + kMaxGrid;
+  pp.cta_gu = at<int32_t>(ws, L.cta);
+  pp.cta_dn = at<int32_t>(ws, L.cta) + 2 * (kMaxGrid + 1);
   return MOE_OK;
 }
 
@@ -218,10 +218,10 @@ moe_status_t run_experts(const moe_dims_t& dm, const void* x, const float* topk_
   float* ys = at<float>(ws, L.ys);
   moe_status_t s;
   if (launch_gate_up(next, a, ep.gu, static_cast<const uint16_t*>(x), sorted_ids, ep.pp.plan,
-                     ep.pp.work, ep.pp.cta_first_gu, h, hs, status, ep.pp.grid) != cudaSuccess)
+                     ep.pp.work, ep.pp.cta_gu, h, hs, status, ep.pp.grid) != cudaSuccess)
     return MOE_ERR_CUDA;
   if ((s = record(events, MOE_EV_GATE_UP, st)) != MOE_OK) return s;
-  if (launch_down(next, a, ep.dn, sorted_ids, ep.pp.plan, ep.pp.work, ep.pp.cta_first_dn, h, hs, y,
+  if (launch_down(next, a, ep.dn, sorted_ids, ep.pp.plan, ep.pp.work, ep.pp.cta_dn, h, hs, y,
                   ys, status, ep.pp.grid) != cudaSuccess)
     return MOE_ERR_CUDA;
   if ((s = record(events, MOE_EV_DOWN, st)) != MOE_OK) return s;

@@ -38,13 +38,8 @@ struct WorkExpert {
   int32_t pad_[3];
 };
 
-// Units of the persistent expert kernels are split into contiguous ranges,
-// one per CTA: CTA c of `grid` takes [unit_begin(c), unit_begin(c + 1)).
+// The persistent expert kernels run at most this many CTAs.
 constexpr int kMaxGrid = 1024;
-__host__ __device__ __forceinline__ int unit_begin(int c, int units, int grid) {
-  const int per = units / grid, rem = units % grid;
-  return c * per + (c < rem ? c : rem);
-}
 
 struct Plan {
   int32_t n_work;      // number of WorkExpert entries

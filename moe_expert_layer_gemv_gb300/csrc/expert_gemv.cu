@@ -40,7 +40,7 @@ struct GuArgs {
   const int32_t* sorted_ids;
   const Plan* plan;
   const WorkExpert* work;
-  const int32_t* cta_first;   // [grid] first work expert of each CTA's range
+  const int32_t* cta;         // CTA unit ranges and first work experts (see PlanParams)
   float* h;                   // [num_post_pad][I]
   float* hs;                  // [T][Is]
   int* status;
@@ -55,7 +55,7 @@ struct DnArgs {
   const int32_t* sorted_ids;
   const Plan* plan;
   const WorkExpert* work;
-  const int32_t* cta_first;
+  const int32_t* cta;
   const float* h;
   const float* hs;
   float* y;                   // [T*k][d]
@@ -249,55 +249,73 @@ __device__ __forceinline__ void gu_warp(uint32_t wg, uint32_t wu, uint32_t sg, u
 }
 
 // ------------------------------------------------------------------ down math
-// One weight row per 8-lane group.  NT tokens' h rows (fp32) at ha + q * hsb.
-// Returns, in lane sl of the group, the output of token sl for that row.
+// Two weight rows (wa, wb) per 8-lane group, so every h chunk loaded from
+// shared memory serves both.  NT tokens' h rows (fp32) at ha + q * hsb.  On
+// return, lane sl of the group holds token sl's outputs for both rows.
 template <int NT, bool kInt4>
-__device__ __forceinline__ float dn_row(uint32_t wr, uint32_t sr, uint32_t ha, uint32_t hsb,
-                                        int Iw, int sl) {
-  float a0[NT], a1[NT];
+__device__ __forceinline__ void dn_rows2(uint32_t wa, uint32_t wb, uint32_t sa, uint32_t sbb,
+                                         uint32_t ha, uint32_t hsb, int Iw, int sl, float& oa,
+                                         float& ob) {
+  float a0[NT], a1[NT], b0[NT], b1[NT];
 #pragma unroll
-  for (int q = 0; q < NT; ++q) a0[q] = a1[q] = 0.f;
+  for (int q = 0; q < NT; ++q) a0[q] = a1[q] = b0[q] = b1[q] = 0.f;
   if (!kInt4) {
 #pragma unroll 2
     for (int c = sl; c < Iw / 8; c += 8) {
       const uint32_t off = (uint32_t)c * 16u;
-      const uint4 w = lds128(wr + off);
-      float4 hp[NT], hq[NT];
+      const uint4 va = lds128(wa + off), vb = lds128(wb + off);
 #pragma unroll
       for (int q = 0; q < NT; ++q) {
-        hp[q] = lds128f(ha + q * hsb + 2u * off);
-        hq[q] = lds128f(ha + q * hsb + 2u * off + 16u);
+        const float4 hp = lds128f(ha + q * hsb + 2u * off);
+        const float4 hq = lds128f(ha + q * hsb + 2u * off + 16u);
+        fma8f(va, hp, hq, a0[q], a1[q]);
+        fma8f(vb, hp, hq, b0[q], b1[q]);
       }
-#pragma unroll
-      for (int q = 0; q < NT; ++q) fma8f(w, hp[q], hq[q], a0[q], a1[q]);
     }
   } else {
     for (int c = sl; c < Iw / 32; c += 8) {
       const uint32_t off = (uint32_t)c * 16u;
-      const uint4 v = lds128(wr + off);
-      const float sc = lds_bf16(sr + 2u * c);
+      const uint4 va = lds128(wa + off), vb = lds128(wb + off);
+      const float fa = lds_bf16(sa + 2u * c), fb = lds_bf16(sbb + 2u * c);
 #pragma unroll
       for (int q = 0; q < NT; ++q) {
         const uint32_t hr = ha + q * hsb + 8u * off;
-        float p0 = 0.f, p1 = 0.f;
-        fma8_int4f(v.x, lds128f(hr), lds128f(hr + 16), p0, p1);
-        fma8_int4f(v.y, lds128f(hr + 32), lds128f(hr + 48), p0, p1);
-        fma8_int4f(v.z, lds128f(hr + 64), lds128f(hr + 80), p0, p1);
-        fma8_int4f(v.w, lds128f(hr + 96), lds128f(hr + 112), p0, p1);
-        a0[q] = fmaf(sc, p0 + p1, a0[q]);
+        float p0 = 0.f, p1 = 0.f, r0 = 0.f, r1 = 0.f;
+        float4 h0 = lds128f(hr), h1 = lds128f(hr + 16);
+        fma8_int4f(va.x, h0, h1, p0, p1);
+        fma8_int4f(vb.x, h0, h1, r0, r1);
+        h0 = lds128f(hr + 32);
+        h1 = lds128f(hr + 48);
+        fma8_int4f(va.y, h0, h1, p0, p1);
+        fma8_int4f(vb.y, h0, h1, r0, r1);
+        h0 = lds128f(hr + 64);
+        h1 = lds128f(hr + 80);
+        fma8_int4f(va.z, h0, h1, p0, p1);
+        fma8_int4f(vb.z, h0, h1, r0, r1);
+        h0 = lds128f(hr + 96);
+        h1 = lds128f(hr + 112);
+        fma8_int4f(va.w, h0, h1, p0, p1);
+        fma8_int4f(vb.w, h0, h1, r0, r1);
+        a0[q] = fmaf(fa, p0 + p1, a0[q]);
+        b0[q] = fmaf(fb, r0 + r1, b0[q]);
       }
     }
   }
-  float mine = 0.f;
+  oa = ob = 0.f;
 #pragma unroll
   for (int q = 0; q < NT; ++q) {
-    float v = a0[q] + a1[q];
-    v += __shfl_xor_sync(0xffffffffu, v, 4);
-    v += __shfl_xor_sync(0xffffffffu, v, 2);
-    v += __shfl_xor_sync(0xffffffffu, v, 1);
-    if (sl == q) mine = v;
+    float va = a0[q] + a1[q], vb = b0[q] + b1[q];
+    va += __shfl_xor_sync(0xffffffffu, va, 4);
+    vb += __shfl_xor_sync(0xffffffffu, vb, 4);
+    va += __shfl_xor_sync(0xffffffffu, va, 2);
+    vb += __shfl_xor_sync(0xffffffffu, vb, 2);
+    va += __shfl_xor_sync(0xffffffffu, va, 1);
+    vb += __shfl_xor_sync(0xffffffffu, vb, 1);
+    if (sl == q) {
+      oa = va;
+      ob = vb;
+    }
   }
-  return mine;
 }
 
 // Producer drain after an abort: wait (bounded) for the last fills of every
@@ -335,15 +353,15 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) gate_up_kernel(const GuA
   // Routed row bytes (codes only, for int4) and int4 scale bytes per row.
   const int rowb = kFmt ? d / 2 : d * 2;
   const int srowb = kFmt ? d / 16 : 0;
-  const int u_begin = unit_begin(blockIdx.x, plan.units_gu, gridDim.x);
-  const int u_end = unit_begin(blockIdx.x + 1, plan.units_gu, gridDim.x);
+  const int u_begin = a.cta[blockIdx.x];
+  const int u_end = a.cta[blockIdx.x + 1];
   UnitCursor<false> cur;
   cur.work = a.work;
   cur.n_work = plan.n_work;
   cur.tiles_r = (int)ceil_div(a.I, a.rg);
   cur.tiles_s = a.Is > 0 ? (int)ceil_div(a.Is, a.rgs) : 1;
   cur.xt = xt;
-  if (u_begin < u_end) cur.load(a.cta_first[blockIdx.x]);
+  if (u_begin < u_end) cur.load(a.cta[gridDim.x + 1 + blockIdx.x]);
 
   if (warp == kConsumerWarps) {
     // ------------------------------------------------------------ producer
@@ -470,7 +488,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) gate_up_kernel(const GuA
 }
 
 // --------------------------------------------------------------------------- down
-// Consumers: 8 lanes per weight row, 4 rows per warp pass.
+// Consumers: 8 lanes per pair of weight rows, 16 row pairs per pass of the CTA.
 template <int kFmt>
 __global__ void __launch_bounds__(kThreads, kCtasPerSm) down_kernel(const DnArgs a) {
   extern __shared__ __align__(128) uint8_t smem[];
@@ -496,15 +514,15 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) down_kernel(const DnArgs
   const int xt = a.xt;
   const int rowb = kFmt ? a.I / 2 : a.I * 2;
   const int srowb = kFmt ? a.I / 16 : 0;
-  const int u_begin = unit_begin(blockIdx.x, plan.units_dn, gridDim.x);
-  const int u_end = unit_begin(blockIdx.x + 1, plan.units_dn, gridDim.x);
+  const int u_begin = a.cta[blockIdx.x];
+  const int u_end = a.cta[blockIdx.x + 1];
   UnitCursor<true> cur;
   cur.work = a.work;
   cur.n_work = plan.n_work;
   cur.tiles_r = (int)ceil_div(a.d, a.rd);
   cur.tiles_s = a.Is > 0 ? (int)ceil_div(a.d, a.rds) : 1;
   cur.xt = xt;
-  if (u_begin < u_end) cur.load(a.cta_first[blockIdx.x]);
+  if (u_begin < u_end) cur.load(a.cta[gridDim.x + 1 + blockIdx.x]);
 
   if (warp == kConsumerWarps) {
     const uint64_t pol_w = policy_evict_first();
@@ -581,14 +599,20 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) down_kernel(const DnArgs
     const uint32_t hsb = (uint32_t)Iw * 4u;
     const bool int4 = kFmt && !shared;
 
-    for (int rq = warp * 4; rq < nr; rq += kConsumerWarps * 4) {
-      const int r = min(rq + sub, nr - 1);  // lanes past the tile recompute its last row
-      const uint32_t wr = st + r * rb, sr = st + RD * rb + r * sb;
-      float mine = 0.f;
-#define MOE_DN_CASE(N)                                       \
-  case N:                                                    \
-    mine = int4 ? dn_row<N, true>(wr, sr, ha, hsb, Iw, sl)   \
-                : dn_row<N, false>(wr, sr, ha, hsb, Iw, sl); \
+    // 8-lane group grp8 (0..15) takes rows grp8 and grp8 + 16 of each 32-row block.
+    const int grp8 = warp * 4 + sub;
+    for (int rb0 = 0; rb0 < nr; rb0 += 32) {
+      const int ra = rb0 + grp8, rbr = rb0 + grp8 + 16;
+      const int ca = min(ra, nr - 1), cb = min(rbr, nr - 1);  // clamp: recompute, not written
+      const uint32_t wa = st + ca * rb, wb = st + cb * rb;
+      const uint32_t sa = st + RD * rb + ca * sb, sbb = st + RD * rb + cb * sb;
+      float oa = 0.f, ob = 0.f;
+#define MOE_DN_CASE(N)                                                 \
+  case N:                                                              \
+    if (int4)                                                          \
+      dn_rows2<N, true>(wa, wb, sa, sbb, ha, hsb, Iw, sl, oa, ob);     \
+    else                                                               \
+      dn_rows2<N, false>(wa, wb, sa, sbb, ha, hsb, Iw, sl, oa, ob);    \
     break;
       switch (nt) {
         MOE_DN_CASE(1)
@@ -603,15 +627,20 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) down_kernel(const DnArgs
           break;
       }
 #undef MOE_DN_CASE
-      if (rq + sub < nr && sl < nt) {
+      if (sl < nt) {
         if (shared) {
-          a.ys[(size_t)(g0 + sl) * a.d + r0 + rq + sub] = mine;
+          float* yr = a.ys + (size_t)(g0 + sl) * a.d + r0;
+          if (ra < nr) yr[ra] = oa;
+          if (rbr < nr) yr[rbr] = ob;
         } else {
           const int slot = slot_of_lane;
-          if (slot >= 0 && slot < a.T * a.k)
-            a.y[(size_t)slot * a.d + r0 + rq + sub] = mine;
-          else
+          if (slot >= 0 && slot < a.T * a.k) {
+            float* yr = a.y + (size_t)slot * a.d + r0;
+            if (ra < nr) yr[ra] = oa;
+            if (rbr < nr) yr[rbr] = ob;
+          } else {
             record_status(a.status, kStatusDeviceCheck);
+          }
         }
       }
     }
@@ -665,10 +694,10 @@ GemvShape down_shape(int fmt, int d, int I, int Is, int smem_budget) {
 
 cudaError_t launch_gate_up(const LaunchCfg& c, const ExpertArgs& e, const GemvShape& g,
                            const uint16_t* x, const int32_t* sorted_ids, const Plan* plan,
-                           const WorkExpert* work, const int32_t* cta_first, float* h, float* hs,
+                           const WorkExpert* work, const int32_t* cta, float* h, float* hs,
                            int* status, int grid) {
   GuArgs a;
-  a.cta_first = cta_first;
+  a.cta = cta;
   a.gu = static_cast<const uint8_t*>(e.gate_up);
   a.gu_scales = e.gate_up_scales;
   a.sgu = reinterpret_cast<const uint8_t*>(e.s_gate_up);
@@ -699,10 +728,10 @@ cudaError_t launch_gate_up(const LaunchCfg& c, const ExpertArgs& e, const GemvSh
 
 cudaError_t launch_down(const LaunchCfg& c, const ExpertArgs& e, const GemvShape& g,
                         const int32_t* sorted_ids, const Plan* plan, const WorkExpert* work,
-                        const int32_t* cta_first, const float* h, const float* hs, float* y,
+                        const int32_t* cta, const float* h, const float* hs, float* y,
                         float* ys, int* status, int grid) {
   DnArgs a;
-  a.cta_first = cta_first;
+  a.cta = cta;
   a.dn = static_cast<const uint8_t*>(e.down);
   a.dn_scales = e.down_scales;
   a.sdn = reinterpret_cast<const uint8_t*>(e.s_down);

@@ -47,8 +47,10 @@ struct PlanParams {
   int xt_gu;             // tokens per gate_up unit
   int xt_dn;             // tokens per down unit
   int grid;              // CTAs of the persistent expert kernels (<= kMaxGrid)
-  int32_t* cta_first_gu; // [grid] first work expert of each CTA's unit range
-  int32_t* cta_first_dn; // [grid]
+  // Per stage: [0, grid] first unit of each CTA (entry grid = total units),
+  // then [grid + 1, 2 grid + 1) the work expert each CTA starts in.
+  int32_t* cta_gu;
+  int32_t* cta_dn;
 };
 
 // Single-CTA align: optional fused top-k (logits != nullptr), the
@@ -86,12 +88,12 @@ struct ExpertArgs {
 
 cudaError_t launch_gate_up(const LaunchCfg& c, const ExpertArgs& a, const GemvShape& g,
                            const uint16_t* x, const int32_t* sorted_ids, const Plan* plan,
-                           const WorkExpert* work, const int32_t* cta_first, float* h, float* hs,
+                           const WorkExpert* work, const int32_t* cta, float* h, float* hs,
                            int* status, int grid);
 
 cudaError_t launch_down(const LaunchCfg& c, const ExpertArgs& a, const GemvShape& g,
                         const int32_t* sorted_ids, const Plan* plan, const WorkExpert* work,
-                        const int32_t* cta_first, const float* h, const float* hs, float* y,
+                        const int32_t* cta, const float* h, const float* hs, float* y,
                         float* ys, int* status, int grid);
 
 // out[t] = sum_j w[t][j] y[t*k+j] + sigmoid(x[t].w_sg) ys[t]   (bf16, RNE)

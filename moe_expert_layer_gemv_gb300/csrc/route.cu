@@ -196,25 +196,80 @@ __device__ int block_exclusive_scan(int v, int* scratch, int* total) {
   return base + inc - v;
 }
 
+// Estimated cost of a unit with nt tokens, in token-equivalents: a fixed part
+// for streaming the unit's weight rows plus one per token of arithmetic.
+constexpr int kUnitBaseCost = 4;
+
+// First unit of the CTA whose share of the cost starts at `target`, given
+// work expert i's cost prefix `c0`, first unit `u0`, tiles, token count n and
+// tokens per group xt (units are numbered group-major).
+__device__ int unit_at_cost(int64_t target, int64_t c0, int u0, int tiles, int n, int xt) {
+  const int groups = (int)ceil_div(n, xt);
+  const int nt_last = n - (groups - 1) * xt;
+  const int64_t per_full = (int64_t)tiles * (kUnitBaseCost + xt);
+  const int64_t r = target - c0;
+  int g, t;
+  if (groups > 1 && r < (groups - 1) * per_full) {
+    g = (int)(r / per_full);
+    t = (int)((r - g * per_full) / (kUnitBaseCost + xt));
+  } else {
+    g = groups - 1;
+    t = (int)((r - (int64_t)(groups - 1) * per_full) / (kUnitBaseCost + nt_last));
+    t = min(t, tiles - 1);
+  }
+  return u0 + g * tiles + t;
+}
+
+// Splits one stage's units over the grid by estimated cost: CTA c gets units
+// [cta[c], cta[c+1]) and starts in work expert cta[grid + 1 + c].
+__device__ void split_by_cost(int n_work, const int* s_cost, const int* s_unit, const int* s_n,
+                              const int* s_tiles, int64_t total_cost, int total_units, int xt,
+                              int grid, int32_t* cta) {
+  for (int c = threadIdx.x; c <= grid; c += blockDim.x) {
+    if (c == grid || n_work == 0) {
+      cta[c] = c == grid ? total_units : 0;
+      if (c < grid) cta[grid + 1 + c] = 0;
+      continue;
+    }
+    const int64_t target = total_cost * c / grid;
+    int lo = 0, hi = n_work - 1;
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (s_cost[mid] <= target) lo = mid; else hi = mid - 1;
+    }
+    cta[c] = c == 0 ? 0 : unit_at_cost(target, s_cost[lo], s_unit[lo], s_tiles[lo], s_n[lo], xt);
+    cta[grid + 1 + c] = lo;
+  }
+}
+
 // Work plan: one WorkExpert per touched routed expert (ascending id), then the
-// shared expert; gate_up / down work units counted per expert; and for every
-// CTA of the persistent expert kernels, the work expert its unit range starts
-// in.  Called by all 1024 threads; cnt/off are per-expert counts and padded
-// offsets; tmp holds >= 2 * (E + 1) ints of shared memory.
+// shared expert; gate_up / down work units counted per expert; and each CTA's
+// range of units for both expert stages, balanced by estimated cost.  Called by
+// all 1024 threads; cnt/off are per-expert counts and padded offsets; tmp holds
+// >= 7 * (E + 1) ints of shared memory.
 __device__ void build_plan(const int* cnt, const int* off, int E, int T, int num_post_pad,
                            const PlanParams& pp, int* scratch, int* tmp) {
   __syncthreads();
   const int e = threadIdx.x;
   const int c = (e < E) ? cnt[e] : 0;
   const int flag = c > 0;
-  int n_routed, tot_gu, tot_dn;
+  const int ggu = (int)ceil_div(c, pp.xt_gu), gdn = (int)ceil_div(c, pp.xt_dn);
+  int n_routed, tot_gu, tot_dn, cost_gu, cost_dn;
   const int idx = block_exclusive_scan(flag, scratch, &n_routed);
-  const int ugu = flag ? pp.tiles_gu * (int)ceil_div(c, pp.xt_gu) : 0;
-  const int udn = flag ? pp.tiles_dn * (int)ceil_div(c, pp.xt_dn) : 0;
-  const int egu = block_exclusive_scan(ugu, scratch, &tot_gu);
-  const int edn = block_exclusive_scan(udn, scratch, &tot_dn);
-  int* s_gu = tmp;          // [n_work] first gate_up unit of each work expert
-  int* s_dn = tmp + E + 1;  // [n_work] first down unit
+  const int egu = block_exclusive_scan(flag ? pp.tiles_gu * ggu : 0, scratch, &tot_gu);
+  const int edn = block_exclusive_scan(flag ? pp.tiles_dn * gdn : 0, scratch, &tot_dn);
+  const int cgu = block_exclusive_scan(
+      flag ? pp.tiles_gu * (ggu * kUnitBaseCost + c) : 0, scratch, &cost_gu);
+  const int cdn = block_exclusive_scan(
+      flag ? pp.tiles_dn * (gdn * kUnitBaseCost + c) : 0, scratch, &cost_dn);
+  const int W = E + 1;
+  int* s_ugu = tmp;
+  int* s_udn = tmp + W;
+  int* s_cgu = tmp + 2 * W;
+  int* s_cdn = tmp + 3 * W;
+  int* s_n = tmp + 4 * W;
+  int* s_tgu = tmp + 5 * W;
+  int* s_tdn = tmp + 6 * W;
   if (flag) {
     WorkExpert we;
     we.expert = e;
@@ -224,12 +279,18 @@ __device__ void build_plan(const int* cnt, const int* off, int E, int T, int num
     we.unit_dn = edn;
     we.pad_[0] = we.pad_[1] = we.pad_[2] = 0;
     pp.work[idx] = we;
-    s_gu[idx] = egu;
-    s_dn[idx] = edn;
+    s_ugu[idx] = egu;
+    s_udn[idx] = edn;
+    s_cgu[idx] = cgu;
+    s_cdn[idx] = cdn;
+    s_n[idx] = c;
+    s_tgu[idx] = pp.tiles_gu;
+    s_tdn[idx] = pp.tiles_dn;
   }
   const bool has_shared = pp.tiles_gu_shared > 0 && T > 0;
   const int n_work = n_routed + (has_shared ? 1 : 0);
   if (has_shared) {
+    const int sg = (int)ceil_div(T, pp.xt_gu), sd = (int)ceil_div(T, pp.xt_dn);
     if (threadIdx.x == 0) {
       WorkExpert we;
       we.expert = -1;
@@ -239,30 +300,24 @@ __device__ void build_plan(const int* cnt, const int* off, int E, int T, int num
       we.unit_dn = tot_dn;
       we.pad_[0] = we.pad_[1] = we.pad_[2] = 0;
       pp.work[n_routed] = we;
-      s_gu[n_routed] = tot_gu;
-      s_dn[n_routed] = tot_dn;
+      s_ugu[n_routed] = tot_gu;
+      s_udn[n_routed] = tot_dn;
+      s_cgu[n_routed] = cost_gu;
+      s_cdn[n_routed] = cost_dn;
+      s_n[n_routed] = T;
+      s_tgu[n_routed] = pp.tiles_gu_shared;
+      s_tdn[n_routed] = pp.tiles_dn_shared;
     }
-    tot_gu += pp.tiles_gu_shared * (int)ceil_div(T, pp.xt_gu);
-    tot_dn += pp.tiles_dn_shared * (int)ceil_div(T, pp.xt_dn);
+    tot_gu += pp.tiles_gu_shared * sg;
+    tot_dn += pp.tiles_dn_shared * sd;
+    cost_gu += pp.tiles_gu_shared * (sg * kUnitBaseCost + T);
+    cost_dn += pp.tiles_dn_shared * (sd * kUnitBaseCost + T);
   }
   __syncthreads();
-  // CTA c's range starts in the last work expert whose first unit <= its begin.
-  for (int cta = threadIdx.x; cta < pp.grid; cta += blockDim.x) {
-    const int ug = unit_begin(cta, tot_gu, pp.grid), ud = unit_begin(cta, tot_dn, pp.grid);
-    int lo = 0, hi = n_work - 1;
-    while (lo < hi) {
-      const int mid = (lo + hi + 1) >> 1;
-      if (s_gu[mid] <= ug) lo = mid; else hi = mid - 1;
-    }
-    pp.cta_first_gu[cta] = n_work > 0 ? lo : 0;
-    lo = 0;
-    hi = n_work - 1;
-    while (lo < hi) {
-      const int mid = (lo + hi + 1) >> 1;
-      if (s_dn[mid] <= ud) lo = mid; else hi = mid - 1;
-    }
-    pp.cta_first_dn[cta] = n_work > 0 ? lo : 0;
-  }
+  split_by_cost(n_work, s_cgu, s_ugu, s_n, s_tgu, cost_gu, tot_gu, pp.xt_gu, pp.grid,
+                pp.cta_gu);
+  split_by_cost(n_work, s_cdn, s_udn, s_n, s_tdn, cost_dn, tot_dn, pp.xt_dn, pp.grid,
+                pp.cta_dn);
   if (threadIdx.x == 0) {
     Plan p;
     p.n_work = n_work;
@@ -383,7 +438,7 @@ __global__ void __launch_bounds__(kAlignThreads)
   int* cnt = sm;               // [E]
   int* off = cnt + E;          // [E]
   int* scratch = off + E;      // [32]
-  int* tmp = scratch + 32;     // [2 * (E + 1)]
+  int* tmp = scratch + 32;     // [7 * (E + 1)]
   pdl_wait();
   pdl_trigger();
   const int S = T * k;
@@ -453,7 +508,7 @@ cudaError_t launch_align(const LaunchCfg& c, const float* logits, int T, int E, 
 cudaError_t launch_plan(const LaunchCfg& c, int T, int E, int k, int B,
                         const int32_t* sorted_ids, const int32_t* num_post_pad,
                         const int32_t* expert_offsets, const PlanParams& pp, int* status) {
-  const size_t smem = (4 * (size_t)E + 34) * sizeof(int);
+  const size_t smem = (2 * (size_t)E + 32 + 7 * ((size_t)E + 1)) * sizeof(int);
   PlanParams p = pp;
   void* args[] = {&T, &E, &k, &B, &sorted_ids, &num_post_pad, &expert_offsets, &p, &status};
   return launch_kernel(c, (const void*)plan_kernel, dim3(1), dim3(kAlignThreads), smem, args);
