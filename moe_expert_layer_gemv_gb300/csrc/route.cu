@@ -34,7 +34,10 @@ __device__ __forceinline__ float dot8_bf16(uint4 a, uint4 b, float acc) {
 }
 
 // grid = (ceil(E / (8/wpe)), ceil(T / 8)), block = 256.  `wpe` warps share one
-// expert row (split along d); each CTA stages 8 tokens of x in shared memory.
+// expert row (split along d); each lane holds its CH 16-byte chunks of the row
+// in registers, all requested before anything waits; each CTA stages 8 tokens
+// of x in shared memory.
+template <int CH>
 __global__ void __launch_bounds__(kRouterWarps * 32)
     router_logits_kernel(const uint16_t* __restrict__ x, const uint16_t* __restrict__ wr,
                          float* __restrict__ logits, int T, int d, int E, int wpe) {
@@ -48,12 +51,15 @@ __global__ void __launch_bounds__(kRouterWarps * 32)
   const int e = blockIdx.x * epc + warp / wpe;
   const int q = warp % wpe;
 
-  // Router weights are inputs that no kernel of this library writes: start
-  // fetching them before waiting on the predecessor.
-  uint4 wpre = make_uint4(0, 0, 0, 0);
+  // Router weights are inputs that no kernel of this library writes: request
+  // them before waiting on the predecessor.
   const uint4* wrow = reinterpret_cast<const uint4*>(wr + (size_t)min(e, E - 1) * d);
-  const int c0 = q * 32 + lane;
-  if (e < E && c0 < nch) wpre = __ldg(wrow + c0);
+  uint4 w[CH];
+#pragma unroll
+  for (int i = 0; i < CH; ++i) {
+    const int c = q * 32 + lane + i * wpe * 32;
+    w[i] = (e < E && c < nch) ? __ldg(wrow + c) : make_uint4(0, 0, 0, 0);
+  }
 
   pdl_wait();
   const uint4* xg = reinterpret_cast<const uint4*>(x + (size_t)t0 * d);
@@ -63,13 +69,14 @@ __global__ void __launch_bounds__(kRouterWarps * 32)
 
   float acc[kRouterTokens];
 #pragma unroll
-  for (int j = 0; j < kRouterTokens; ++j) acc[j] = 0.f;
-  if (e < E) {
-    for (int c = c0; c < nch; c += wpe * 32) {
-      const uint4 w = (c == c0) ? wpre : __ldg(wrow + c);
+  for (int j = 0; j < kRouterTokens; ++j) {
+    acc[j] = 0.f;
+    if (j < nt) {
 #pragma unroll
-      for (int j = 0; j < kRouterTokens; ++j)
-        if (j < nt) acc[j] = dot8_bf16(w, xs[j * nch + c], acc[j]);
+      for (int i = 0; i < CH; ++i) {
+        const int c = q * 32 + lane + i * wpe * 32;
+        if (c < nch) acc[j] = dot8_bf16(w[i], xs[j * nch + c], acc[j]);
+      }
     }
   }
 #pragma unroll
@@ -94,14 +101,15 @@ __global__ void __launch_bounds__(kRouterWarps * 32)
 // logit first, equal logits -> lower id (softmax is increasing, so this is the
 // order of the probabilities).  Weights: exp(l - max) normalised over the
 // selected experts (renormalize) or over all E.
-__device__ void warp_topk(const float* __restrict__ L, int E, int k, int renormalize,
-                          int32_t* ids, float* w, int32_t* ids_copy, float* w_copy) {
+template <int NV>
+__device__ void warp_topk_nv(const float* __restrict__ L, int E, int k, int renormalize,
+                             int32_t* ids, float* w, int32_t* ids_copy, float* w_copy) {
   const int lane = threadIdx.x & 31;
   const int nv = (E + 31) >> 5;
-  float v[32];
+  float v[NV];
   float mx = -INFINITY;
 #pragma unroll
-  for (int i = 0; i < 32; ++i) {
+  for (int i = 0; i < NV; ++i) {
     v[i] = -INFINITY;
     const int e = lane + 32 * i;
     if (i < nv && e < E) {
@@ -114,7 +122,7 @@ __device__ void warp_topk(const float* __restrict__ L, int E, int k, int renorma
   float z = 0.f;
   if (!renormalize) {
 #pragma unroll
-    for (int i = 0; i < 32; ++i)
+    for (int i = 0; i < NV; ++i)
       if (i < nv && lane + 32 * i < E) z += expf(v[i] - mx);
     z = warp_sum(z);
   }
@@ -125,7 +133,7 @@ __device__ void warp_topk(const float* __restrict__ L, int E, int k, int renorma
     float bv = -INFINITY;
     int bi = 0x7fffffff;
 #pragma unroll
-    for (int i = 0; i < 32; ++i) {
+    for (int i = 0; i < NV; ++i) {
       const int e = lane + 32 * i;
       if (i < nv && e < E && !((taken >> i) & 1u) && (bi == 0x7fffffff || v[i] > bv)) {
         bv = v[i];
@@ -156,6 +164,19 @@ __device__ void warp_topk(const float* __restrict__ L, int E, int k, int renorma
     if (ids_copy) ids_copy[lane] = my_id;
     if (w_copy) w_copy[lane] = wt;
   }
+}
+
+// Dispatch on the number of logits each lane holds (E / 32, rounded up to a
+// power of two, E <= 1024).
+__device__ void warp_topk(const float* __restrict__ L, int E, int k, int renormalize,
+                          int32_t* ids, float* w, int32_t* ids_copy, float* w_copy) {
+  const int nv = (E + 31) >> 5;
+  if (nv <= 1) warp_topk_nv<1>(L, E, k, renormalize, ids, w, ids_copy, w_copy);
+  else if (nv <= 2) warp_topk_nv<2>(L, E, k, renormalize, ids, w, ids_copy, w_copy);
+  else if (nv <= 4) warp_topk_nv<4>(L, E, k, renormalize, ids, w, ids_copy, w_copy);
+  else if (nv <= 8) warp_topk_nv<8>(L, E, k, renormalize, ids, w, ids_copy, w_copy);
+  else if (nv <= 16) warp_topk_nv<16>(L, E, k, renormalize, ids, w, ids_copy, w_copy);
+  else warp_topk_nv<32>(L, E, k, renormalize, ids, w, ids_copy, w_copy);
 }
 
 __global__ void __launch_bounds__(256)
@@ -203,18 +224,18 @@ constexpr int kUnitBaseCost = 4;
 // First unit of the CTA whose share of the cost starts at `target`, given
 // work expert i's cost prefix `c0`, first unit `u0`, tiles, token count n and
 // tokens per group xt (units are numbered group-major).
-__device__ int unit_at_cost(int64_t target, int64_t c0, int u0, int tiles, int n, int xt) {
-  const int groups = (int)ceil_div(n, xt);
+__device__ int unit_at_cost(int target, int c0, int u0, int tiles, int n, int xt) {
+  const int groups = (n + xt - 1) / xt;
   const int nt_last = n - (groups - 1) * xt;
-  const int64_t per_full = (int64_t)tiles * (kUnitBaseCost + xt);
-  const int64_t r = target - c0;
+  const int per_full = tiles * (kUnitBaseCost + xt);
+  const int r = target - c0;
   int g, t;
   if (groups > 1 && r < (groups - 1) * per_full) {
-    g = (int)(r / per_full);
-    t = (int)((r - g * per_full) / (kUnitBaseCost + xt));
+    g = r / per_full;
+    t = (r - g * per_full) / (kUnitBaseCost + xt);
   } else {
     g = groups - 1;
-    t = (int)((r - (int64_t)(groups - 1) * per_full) / (kUnitBaseCost + nt_last));
+    t = (r - (groups - 1) * per_full) / (kUnitBaseCost + nt_last);
     t = min(t, tiles - 1);
   }
   return u0 + g * tiles + t;
@@ -223,15 +244,18 @@ __device__ int unit_at_cost(int64_t target, int64_t c0, int u0, int tiles, int n
 // Splits one stage's units over the grid by estimated cost: CTA c gets units
 // [cta[c], cta[c+1]) and starts in work expert cta[grid + 1 + c].
 __device__ void split_by_cost(int n_work, const int* s_cost, const int* s_unit, const int* s_n,
-                              const int* s_tiles, int64_t total_cost, int total_units, int xt,
+                              const int* s_tiles, int total_cost, int total_units, int xt,
                               int grid, int32_t* cta) {
+  // CTA c's share starts at cost c * total / grid, taken in fp32: monotone in c,
+  // and exact enough for balancing (no 64-bit division on the device).
+  const float per_cta = (float)total_cost / (float)grid;
   for (int c = threadIdx.x; c <= grid; c += blockDim.x) {
     if (c == grid || n_work == 0) {
       cta[c] = c == grid ? total_units : 0;
       if (c < grid) cta[grid + 1 + c] = 0;
       continue;
     }
-    const int64_t target = total_cost * c / grid;
+    const int target = min(total_cost, (int)((float)c * per_cta));
     int lo = 0, hi = n_work - 1;
     while (lo < hi) {
       const int mid = (lo + hi + 1) >> 1;
@@ -466,6 +490,7 @@ cudaError_t launch_router_logits(const LaunchCfg& c, const uint16_t* x, const ui
                                  float* logits, int T, int d, int E, int sms) {
   if (T == 0) return cudaSuccess;
   const int ty = (int)ceil_div(T, kRouterTokens);
+  const int nch = d / 8;
   int wpe = 8;
   for (int cand = 1; cand <= 8; cand <<= 1) {
     if (ceil_div(E, kRouterWarps / cand) * ty >= sms) {
@@ -473,13 +498,18 @@ cudaError_t launch_router_logits(const LaunchCfg& c, const uint16_t* x, const ui
       break;
     }
   }
+  while (wpe < 8 && ceil_div(nch, wpe * 32) > 8) wpe <<= 1;  // at most 8 chunks per lane
+  const int ch = (int)ceil_div(nch, wpe * 32);
   const size_t smem = (size_t)kRouterTokens * d * 2;
-  cudaError_t e = ensure_smem((const void*)router_logits_kernel, (int)smem);
+  const void* fn = ch <= 1 ? (const void*)router_logits_kernel<1>
+                 : ch <= 2 ? (const void*)router_logits_kernel<2>
+                 : ch <= 4 ? (const void*)router_logits_kernel<4>
+                           : (const void*)router_logits_kernel<8>;
+  cudaError_t e = ensure_smem(fn, (int)smem);
   if (e != cudaSuccess) return e;
   dim3 grid((unsigned)ceil_div(E, kRouterWarps / wpe), (unsigned)ty);
   void* args[] = {&x, &wr, &logits, &T, &d, &E, &wpe};
-  return launch_kernel(c, (const void*)router_logits_kernel, grid, dim3(kRouterWarps * 32), smem,
-                       args);
+  return launch_kernel(c, fn, grid, dim3(kRouterWarps * 32), smem, args);
 }
 
 cudaError_t launch_topk(const LaunchCfg& c, const float* logits, int T, int E, int k,
