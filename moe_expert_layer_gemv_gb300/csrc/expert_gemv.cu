@@ -507,8 +507,13 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) down_kernel(const DnArgs
     fence_barrier_init();
   }
   __syncthreads();
-  pdl_wait();
-  pdl_trigger();
+  // Consumers need the predecessor's h; the producer first streams the weight
+  // rows of its first units, which do not depend on it.  The plan it reads was
+  // written by the align step, which completed before the gate_up stage began.
+  if (warp != kConsumerWarps) {
+    pdl_wait();
+    pdl_trigger();
+  }
 
   const Plan plan = *a.plan;
   const int xt = a.xt;
@@ -529,41 +534,55 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) down_kernel(const DnArgs
     const uint64_t pol_h = policy_evict_last();  // h rows are re-read by every row tile
     int j = 0;
     bool ok = true;
-    for (int u = u_begin; u < u_end; ++u, ++j) {
-      const int s = j % NS, use = j / NS;
-      cur.seek(u);
-      const WorkExpert& we = cur.we;
-      const int local = u - cur.ubeg;
-      const int grp = local / cur.tiles, tile = local - grp * cur.tiles;
-      const bool shared = we.expert < 0;
-      const int RD = shared ? a.rds : a.rd;
-      const int Iw = shared ? a.Is : a.I;
-      const int r0 = tile * RD;
-      const int nr = min(RD, a.d - r0);
-      const int g0 = grp * xt;
-      const int nt = min(xt, we.n_tok - g0);
-      if (use > 0 && !mbar_wait(&empty[s], (uint32_t)((use - 1) & 1), a.status)) {
-        ok = false;
-        break;
+    const int n_pre = min(NS, u_end - u_begin);  // units whose weights go before the wait
+    for (int pass = 0; pass < 2 && ok; ++pass) {
+      // pass 0: weight rows of the first n_pre units; pass 1: everything else.
+      if (pass == 1) {
+        pdl_wait();
+        pdl_trigger();
+        if (u_begin < u_end) cur.load(a.cta[gridDim.x + 1 + blockIdx.x]);
       }
-      uint8_t* st = stages + (size_t)s * a.stage_bytes;
-      const int rb = shared ? Iw * 2 : rowb;
-      const int sb = shared ? 0 : srowb;
-      const uint32_t bytes = (uint32_t)nr * (rb + sb) + (uint32_t)nt * Iw * 4;
-      if (lane == 0) mbar_arrive_expect_tx(&full[s], bytes);
-      __syncwarp();
-      if (lane == 0) {
-        const uint8_t* wb = shared ? a.sdn : a.dn + (size_t)we.expert * a.d * rb;
-        bulk_g2s(st, wb + (size_t)r0 * rb, nr * rb, &full[s], pol_w);
-      }
-      if (kFmt && !shared && lane == 1) {
-        const uint8_t* sbase =
-            reinterpret_cast<const uint8_t*>(a.dn_scales) + (size_t)we.expert * a.d * sb;
-        bulk_g2s(st + RD * rb, sbase + (size_t)r0 * sb, nr * sb, &full[s], pol_w);
-      }
-      if (lane == 2) {
-        const float* hsrc = shared ? a.hs + (size_t)g0 * Iw : a.h + (size_t)(we.pos + g0) * Iw;
-        bulk_g2s(st + RD * (rb + sb), hsrc, nt * Iw * 4, &full[s], pol_h);
+      j = 0;
+      for (int u = u_begin; u < (pass == 0 ? u_begin + n_pre : u_end); ++u, ++j) {
+        const int s = j % NS, use = j / NS;
+        cur.seek(u);
+        const WorkExpert& we = cur.we;
+        const int local = u - cur.ubeg;
+        const int grp = local / cur.tiles, tile = local - grp * cur.tiles;
+        const bool shared = we.expert < 0;
+        const int RD = shared ? a.rds : a.rd;
+        const int Iw = shared ? a.Is : a.I;
+        const int r0 = tile * RD;
+        const int nr = min(RD, a.d - r0);
+        const int g0 = grp * xt;
+        const int nt = min(xt, we.n_tok - g0);
+        const bool pre = j < n_pre;  // weights already issued in pass 0
+        if (pass == 1 && !pre && use > 0 &&
+            !mbar_wait(&empty[s], (uint32_t)((use - 1) & 1), a.status)) {
+          ok = false;
+          break;
+        }
+        uint8_t* st = stages + (size_t)s * a.stage_bytes;
+        const int rb = shared ? Iw * 2 : rowb;
+        const int sb = shared ? 0 : srowb;
+        if (pass == 0 || !pre) {
+          const uint32_t bytes = (uint32_t)nr * (rb + sb) + (uint32_t)nt * Iw * 4;
+          if (lane == 0) mbar_arrive_expect_tx(&full[s], bytes);
+          __syncwarp();
+          if (lane == 0) {
+            const uint8_t* wb = shared ? a.sdn : a.dn + (size_t)we.expert * a.d * rb;
+            bulk_g2s(st, wb + (size_t)r0 * rb, nr * rb, &full[s], pol_w);
+          }
+          if (kFmt && !shared && lane == 1) {
+            const uint8_t* sbase =
+                reinterpret_cast<const uint8_t*>(a.dn_scales) + (size_t)we.expert * a.d * sb;
+            bulk_g2s(st + RD * rb, sbase + (size_t)r0 * sb, nr * sb, &full[s], pol_w);
+          }
+        }
+        if (pass == 1 && lane == 2) {
+          const float* hsrc = shared ? a.hs + (size_t)g0 * Iw : a.h + (size_t)(we.pos + g0) * Iw;
+          bulk_g2s(st + RD * (rb + sb), hsrc, nt * Iw * 4, &full[s], pol_h);
+        }
       }
     }
     if (!ok) drain_stages(full, j, NS, a.status);

@@ -20,6 +20,7 @@ constexpr int kRouterWarps = 8;
 constexpr int kRouterTokens = 8;  // tokens per router CTA
 constexpr int kAlignThreads = 1024;
 constexpr int kAlignWarps = kAlignThreads / 32;
+constexpr int kAlignSmemSlots = 4096;  // routing slots kept in shared memory by align
 
 __device__ __forceinline__ float dot8_bf16(uint4 a, uint4 b, float acc) {
   acc = fmaf(bf16lo(a.x), bf16lo(b.x), acc);
@@ -61,11 +62,22 @@ __global__ void __launch_bounds__(kRouterWarps * 32)
     w[i] = (e < E && c < nch) ? __ldg(wrow + c) : make_uint4(0, 0, 0, 0);
   }
 
-  pdl_wait();
-  const uint4* xg = reinterpret_cast<const uint4*>(x + (size_t)t0 * d);
-  for (int i = threadIdx.x; i < nt * nch; i += blockDim.x) xs[i] = xg[i];
+  __shared__ __align__(8) uint64_t xbar;
+  if (threadIdx.x == 0) {
+    mbar_init(&xbar, 1);
+    fence_barrier_init();
+  }
   __syncthreads();
+  pdl_wait();
+  // The token tile is contiguous: one bulk copy, completion on xbar.
+  if (threadIdx.x == 0) {
+    const uint32_t bytes = (uint32_t)nt * d * 2;
+    mbar_arrive_expect_tx(&xbar, bytes);
+    bulk_g2s(xs, x + (size_t)t0 * d, bytes, &xbar, policy_evict_last());
+  }
+  const bool ok = mbar_wait(&xbar, 0, nullptr);
   pdl_trigger();
+  if (!ok) return;  // unreachable unless the copy never lands; logits are then left unwritten
 
   float acc[kRouterTokens];
 #pragma unroll
@@ -103,7 +115,7 @@ __global__ void __launch_bounds__(kRouterWarps * 32)
 // selected experts (renormalize) or over all E.
 template <int NV>
 __device__ void warp_topk_nv(const float* __restrict__ L, int E, int k, int renormalize,
-                             int32_t* ids, float* w, int32_t* ids_copy, float* w_copy) {
+                             int& out_id, float& out_w) {
   const int lane = threadIdx.x & 31;
   const int nv = (E + 31) >> 5;
   float v[NV];
@@ -157,26 +169,35 @@ __device__ void warp_topk_nv(const float* __restrict__ L, int E, int k, int reno
       my_e = ev;
     }
   }
-  if (lane < k) {
-    const float wt = renormalize ? my_e / selsum : my_e / z;
-    ids[lane] = my_id;
-    w[lane] = wt;
-    if (ids_copy) ids_copy[lane] = my_id;
-    if (w_copy) w_copy[lane] = wt;
-  }
+  out_id = my_id;
+  out_w = renormalize ? my_e / selsum : my_e / z;
 }
 
 // Dispatch on the number of logits each lane holds (E / 32, rounded up to a
-// power of two, E <= 1024).
-__device__ void warp_topk(const float* __restrict__ L, int E, int k, int renormalize,
-                          int32_t* ids, float* w, int32_t* ids_copy, float* w_copy) {
+// power of two, E <= 1024).  Lane j < k receives the j-th selected expert and
+// its weight.
+__device__ void warp_topk(const float* __restrict__ L, int E, int k, int renormalize, int& id,
+                          float& wt) {
   const int nv = (E + 31) >> 5;
-  if (nv <= 1) warp_topk_nv<1>(L, E, k, renormalize, ids, w, ids_copy, w_copy);
-  else if (nv <= 2) warp_topk_nv<2>(L, E, k, renormalize, ids, w, ids_copy, w_copy);
-  else if (nv <= 4) warp_topk_nv<4>(L, E, k, renormalize, ids, w, ids_copy, w_copy);
-  else if (nv <= 8) warp_topk_nv<8>(L, E, k, renormalize, ids, w, ids_copy, w_copy);
-  else if (nv <= 16) warp_topk_nv<16>(L, E, k, renormalize, ids, w, ids_copy, w_copy);
-  else warp_topk_nv<32>(L, E, k, renormalize, ids, w, ids_copy, w_copy);
+  if (nv <= 1) warp_topk_nv<1>(L, E, k, renormalize, id, wt);
+  else if (nv <= 2) warp_topk_nv<2>(L, E, k, renormalize, id, wt);
+  else if (nv <= 4) warp_topk_nv<4>(L, E, k, renormalize, id, wt);
+  else if (nv <= 8) warp_topk_nv<8>(L, E, k, renormalize, id, wt);
+  else if (nv <= 16) warp_topk_nv<16>(L, E, k, renormalize, id, wt);
+  else warp_topk_nv<32>(L, E, k, renormalize, id, wt);
+}
+
+// Stores one token's selection (lanes j < k) to its destinations.
+__device__ __forceinline__ void store_topk(int k, int id, float wt, int32_t* ids, float* w,
+                                           int32_t* ids_copy, float* w_copy, int32_t* ids_smem) {
+  const int lane = threadIdx.x & 31;
+  if (lane < k) {
+    ids[lane] = id;
+    w[lane] = wt;
+    if (ids_copy) ids_copy[lane] = id;
+    if (w_copy) w_copy[lane] = wt;
+    if (ids_smem) ids_smem[lane] = id;
+  }
 }
 
 __global__ void __launch_bounds__(256)
@@ -186,8 +207,12 @@ __global__ void __launch_bounds__(256)
   pdl_trigger();
   const int t = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
   if (t >= T) return;
-  warp_topk(logits + (size_t)t * E, E, k, renormalize, ids + (size_t)t * k, w + (size_t)t * k,
-            ids_copy ? ids_copy + (size_t)t * k : nullptr, w_copy ? w_copy + (size_t)t * k : nullptr);
+  int id;
+  float wt;
+  warp_topk(logits + (size_t)t * E, E, k, renormalize, id, wt);
+  store_topk(k, id, wt, ids + (size_t)t * k, w + (size_t)t * k,
+             ids_copy ? ids_copy + (size_t)t * k : nullptr,
+             w_copy ? w_copy + (size_t)t * k : nullptr, nullptr);
 }
 
 // Exclusive scan of one int per thread over a 1024-thread block.
@@ -366,8 +391,10 @@ __global__ void __launch_bounds__(kAlignThreads)
   int* cnt = hist + kAlignWarps * E;  // [E]
   int* off = cnt + E;                 // [E]
   int* scratch = off + E;             // [32]
+  int* sids = scratch + 32;           // [kAlignSmemSlots] when S fits
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int S = T * k;
+  const bool ids_in_smem = S <= kAlignSmemSlots;
 
   for (int i = threadIdx.x; i < kAlignWarps * E; i += kAlignThreads) hist[i] = 0;
   pdl_wait();
@@ -375,12 +402,20 @@ __global__ void __launch_bounds__(kAlignThreads)
 
   // Optional fused top-k: one warp per token.
   if (logits != nullptr) {
-    for (int t = warp; t < T; t += kAlignWarps)
-      warp_topk(logits + (size_t)t * E, E, k, renormalize, ids + (size_t)t * k,
-                w + (size_t)t * k, ids_copy ? ids_copy + (size_t)t * k : nullptr,
-                w_copy ? w_copy + (size_t)t * k : nullptr);
+    for (int t = warp; t < T; t += kAlignWarps) {
+      int id;
+      float wt;
+      warp_topk(logits + (size_t)t * E, E, k, renormalize, id, wt);
+      store_topk(k, id, wt, ids + (size_t)t * k, w + (size_t)t * k,
+                 ids_copy ? ids_copy + (size_t)t * k : nullptr,
+                 w_copy ? w_copy + (size_t)t * k : nullptr,
+                 ids_in_smem ? sids + (size_t)t * k : nullptr);
+    }
+  } else if (ids_in_smem) {
+    for (int s = threadIdx.x; s < S; s += kAlignThreads) sids[s] = ids[s];
   }
   __syncthreads();
+  const int32_t* src = ids_in_smem ? sids : ids;
 
   // Phase 1: each warp counts the experts of a contiguous chunk of slots.
   const int chunk = (int)ceil_div(S, kAlignWarps);
@@ -389,7 +424,7 @@ __global__ void __launch_bounds__(kAlignThreads)
     const int s = base + lane;
     int e = -1;
     if (s < s_end) {
-      e = ids[s];
+      e = src[s];
       if (e < 0 || e >= E) {
         record_status(status, kStatusDeviceCheck);
         e = -1;
@@ -434,7 +469,7 @@ __global__ void __launch_bounds__(kAlignThreads)
     const int s = base + lane;
     int e = -1;
     if (s < s_end) {
-      e = ids[s];
+      e = src[s];
       if (e < 0 || e >= E) e = -1;
     }
     const unsigned peers = __match_any_sync(0xffffffffu, e);
@@ -526,7 +561,7 @@ cudaError_t launch_align(const LaunchCfg& c, const float* logits, int T, int E, 
                          float* w_copy, int B, int32_t* sorted_ids, int32_t* block_ids,
                          int32_t* num_post_pad, int32_t* expert_offsets, const PlanParams& pp,
                          int* status) {
-  const size_t smem = ((size_t)kAlignWarps * E + 2 * (size_t)E + 32) * sizeof(int);
+  const size_t smem = ((size_t)kAlignWarps * E + 2 * (size_t)E + 32 + kAlignSmemSlots) * sizeof(int);
   cudaError_t e = ensure_smem((const void*)align_kernel, (int)smem);
   if (e != cudaSuccess) return e;
   PlanParams p = pp;
