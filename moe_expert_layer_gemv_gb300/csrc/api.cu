@@ -3,13 +3,13 @@
 //
 // moe_layer_forward enqueues, all on one stream and chained by programmatic
 // dependent launch (no host synchronisation anywhere):
-//   1. router GEMV                       (many CTAs)
-//   2. top-k + align + work plan         (one CTA; top-k fused for T <= 128,
-//                                         a separate warp-per-token kernel above)
-//   3. gate_up + SwiGLU                  (persistent, bulk-copy pipeline)
-//   4. down                              (persistent, bulk-copy pipeline)
-//   5. combine + shared-expert gate      (one CTA per token)
-// The shared expert rides in stages 3-4 as one more work expert, so its weight
+//   1. routing: at decode sizes (T <= 128) one launch -- router GEMV over many
+//      CTAs, top-k by the last CTA of each token tile, align + work plan by the
+//      last tile; above that, router, top-k and align as three launches
+//   2. gate_up + SwiGLU                  (persistent, bulk-copy pipeline)
+//   3. down                              (persistent, bulk-copy pipeline)
+//   4. combine + shared-expert gate      (one CTA per token and column block)
+// The shared expert rides in stages 2-3 as one more work expert, so its weight
 // stream overlaps the routed experts' ("veloGB10", Kernel work: shared-expert
 // work overlapped with the MoE step; small kernels -- the expert routing --
 // folded into their neighbours).
@@ -28,7 +28,6 @@ namespace {
 std::atomic<uint64_t> g_launches{0};
 
 constexpr int kMaxDevices = 64;
-constexpr int kFusedTopkMaxT = 128;
 constexpr size_t kAlign = 256;
 
 struct DeviceInfo {
@@ -63,7 +62,7 @@ bool device_info(DeviceInfo* out) {
 constexpr int kGemvSmemBudget = 228 * 1024 / kCtasPerSm - 1024 - 512;
 
 struct Layout {
-  size_t header, plan, work, cta, logits, ids, w, sorted, blocks, npp, offs, h, hs, y, ys, total;
+  size_t header, plan, work, cta, logits, sg, ids, w, sorted, blocks, npp, offs, h, hs, y, ys, total;
   int64_t cap;
 };
 
@@ -83,6 +82,7 @@ Layout layout_of(const moe_dims_t& dm) {
   L.work = carve(&c, sizeof(WorkExpert) * (size_t)(dm.E + 1));
   L.cta = carve(&c, sizeof(int32_t) * 4 * ((size_t)kMaxGrid + 1));
   L.logits = carve(&c, sizeof(float) * (size_t)dm.T * dm.E);
+  L.sg = carve(&c, sizeof(float) * (size_t)dm.T);
   L.ids = carve(&c, sizeof(int32_t) * (size_t)S);
   L.w = carve(&c, sizeof(float) * (size_t)S);
   L.sorted = carve(&c, sizeof(int32_t) * (size_t)L.cap);
@@ -206,7 +206,7 @@ moe_status_t record(void* const* events, int which, cudaStream_t st) {
 
 // Stages 3-5 given a plan already in the workspace.
 moe_status_t run_experts(const moe_dims_t& dm, const void* x, const float* topk_w,
-                         const int32_t* sorted_ids, const moe_expert_weights_t* ex,
+                         const float* sg, const int32_t* sorted_ids, const moe_expert_weights_t* ex,
                          const moe_shared_weights_t* sh, void* out, void* ws, const Layout& L,
                          const ExpertPlan& ep, cudaStream_t st, void* const* events) {
   const LaunchCfg next{st, true};
@@ -225,7 +225,7 @@ moe_status_t run_experts(const moe_dims_t& dm, const void* x, const float* topk_
                   ys, status, ep.pp.grid) != cudaSuccess)
     return MOE_ERR_CUDA;
   if ((s = record(events, MOE_EV_DOWN, st)) != MOE_OK) return s;
-  if (launch_combine(next, dm.T, dm.d, dm.top_k, topk_w, y, sh ? ys : nullptr,
+  if (launch_combine(next, dm.T, dm.d, dm.top_k, topk_w, y, sh ? ys : nullptr, sh ? sg : nullptr,
                      static_cast<const uint16_t*>(x),
                      sh ? static_cast<const uint16_t*>(sh->gate_w) : nullptr,
                      static_cast<uint16_t*>(out)) != cudaSuccess)
@@ -261,21 +261,32 @@ moe_status_t layer_forward(const moe_dims_t* dims, const void* x, const void* ro
   int32_t* sorted = at<int32_t>(ws, L.sorted);
 
   if ((s = record(events, MOE_EV_BEGIN, st)) != MOE_OK) return s;
-  if (launch_router_logits(first, static_cast<const uint16_t*>(x),
-                           static_cast<const uint16_t*>(router_w), logits, dm.T, dm.d, dm.E,
+  const uint16_t* w_sg = sh ? static_cast<const uint16_t*>(sh->gate_w) : nullptr;
+  float* sg = at<float>(ws, L.sg);
+  if (fused_route_supported(dm.T, dm.E, dm.top_k)) {
+    if (launch_route_fused(first, static_cast<const uint16_t*>(x),
+                           static_cast<const uint16_t*>(router_w), w_sg, logits, sg, dm.T, dm.d,
+                           dm.E, dm.top_k, dm.renormalize, ids, w, ids_out, w_out, dm.block_size,
+                           sorted, at<int32_t>(ws, L.blocks), at<int32_t>(ws, L.npp),
+                           at<int32_t>(ws, L.offs), ep.pp, status, status + kRouteCounterBase,
                            di.sms) != cudaSuccess)
-    return MOE_ERR_CUDA;
-  const bool fused = dm.T <= kFusedTopkMaxT;
-  if (!fused && launch_topk(next, logits, dm.T, dm.E, dm.top_k, dm.renormalize, ids, w, ids_out,
-                            w_out) != cudaSuccess)
-    return MOE_ERR_CUDA;
-  if (launch_align(next, fused ? logits : nullptr, dm.T, dm.E, dm.top_k, dm.renormalize, ids, w,
-                   fused ? ids_out : nullptr, fused ? w_out : nullptr, dm.block_size, sorted,
-                   at<int32_t>(ws, L.blocks), at<int32_t>(ws, L.npp), at<int32_t>(ws, L.offs),
-                   ep.pp, status) != cudaSuccess)
-    return MOE_ERR_CUDA;
+      return MOE_ERR_CUDA;
+  } else {
+    if (launch_router_logits(first, static_cast<const uint16_t*>(x),
+                             static_cast<const uint16_t*>(router_w), w_sg, logits, sg, dm.T, dm.d,
+                             dm.E, di.sms, status) != cudaSuccess)
+      return MOE_ERR_CUDA;
+    if (launch_topk(next, logits, dm.T, dm.E, dm.top_k, dm.renormalize, ids, w, ids_out,
+                    w_out) != cudaSuccess)
+      return MOE_ERR_CUDA;
+    if (launch_align(next, nullptr, dm.T, dm.E, dm.top_k, dm.renormalize, ids, w, nullptr,
+                     nullptr, dm.block_size, sorted, at<int32_t>(ws, L.blocks),
+                     at<int32_t>(ws, L.npp), at<int32_t>(ws, L.offs), ep.pp,
+                     status) != cudaSuccess)
+      return MOE_ERR_CUDA;
+  }
   if ((s = record(events, MOE_EV_ROUTED, st)) != MOE_OK) return s;
-  if ((s = run_experts(dm, x, w, sorted, ex, sh, out, ws, L, ep, st, events)) != MOE_OK)
+  if ((s = run_experts(dm, x, w, sg, sorted, ex, sh, out, ws, L, ep, st, events)) != MOE_OK)
     return s;
   return record(events, MOE_EV_END, st);
 }
@@ -368,8 +379,8 @@ moe_status_t moe_route(const moe_dims_t* dims, const void* x, const void* router
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   float* logits = at<float>(workspace, L.logits);
   if (launch_router_logits(LaunchCfg{st, false}, static_cast<const uint16_t*>(x),
-                           static_cast<const uint16_t*>(router_w), logits, dm.T, dm.d, dm.E,
-                           di.sms) != cudaSuccess)
+                           static_cast<const uint16_t*>(router_w), nullptr, logits, nullptr, dm.T,
+                           dm.d, dm.E, di.sms, at<int>(workspace, L.header)) != cudaSuccess)
     return MOE_ERR_CUDA;
   return cuda_status(launch_topk(LaunchCfg{st, true}, logits, dm.T, dm.E, dm.top_k,
                                  dm.renormalize, topk_ids, topk_weights, nullptr, nullptr));
@@ -426,8 +437,8 @@ moe_status_t moe_expert_forward(const moe_dims_t* dims, const void* x, const flo
                   num_post_pad, expert_offsets, ep.pp, at<int>(workspace, L.header)) !=
       cudaSuccess)
     return MOE_ERR_CUDA;
-  return run_experts(dm, x, topk_weights, sorted_ids, experts, shared, out, workspace, L, ep, st,
-                     nullptr);
+  return run_experts(dm, x, topk_weights, nullptr, sorted_ids, experts, shared, out, workspace, L,
+                     ep, st, nullptr);
 }
 
 moe_status_t moe_layer_forward(const moe_dims_t* dims, const void* x, const void* router_w,

@@ -18,14 +18,17 @@ constexpr int kCols = kThreads * 8;  // output columns per CTA
 // grid = (T, ceil(d / kCols)); each thread writes 8 consecutive outputs.
 __global__ void __launch_bounds__(kThreads)
     combine_kernel(int d, int k, const float* __restrict__ w, const float* __restrict__ y,
-                   const float* __restrict__ ys, const uint16_t* __restrict__ x,
-                   const uint16_t* __restrict__ w_sg, uint16_t* __restrict__ out) {
+                   const float* __restrict__ ys, const float* __restrict__ sg,
+                   const uint16_t* __restrict__ x, const uint16_t* __restrict__ w_sg,
+                   uint16_t* __restrict__ out) {
   __shared__ float red[kThreads / 32];
   const int t = blockIdx.x;
   pdl_wait();
   pdl_trigger();
   float gate = 0.f;
-  if (ys != nullptr) {
+  if (ys != nullptr && sg != nullptr) {
+    gate = sigmoid(sg[t]);
+  } else if (ys != nullptr) {
     // x[t] . w_sg: per-thread strided partials, warp sums, then warps in order.
     const uint4* xr = reinterpret_cast<const uint4*>(x + (size_t)t * d);
     const uint4* gr = reinterpret_cast<const uint4*>(w_sg);
@@ -94,10 +97,10 @@ __global__ void __launch_bounds__(kThreads)
 }  // namespace
 
 cudaError_t launch_combine(const LaunchCfg& c, int T, int d, int k, const float* w,
-                           const float* y, const float* ys, const uint16_t* x,
+                           const float* y, const float* ys, const float* sg, const uint16_t* x,
                            const uint16_t* w_sg, uint16_t* out) {
   if (T == 0) return cudaSuccess;
-  void* args[] = {&d, &k, &w, &y, &ys, &x, &w_sg, &out};
+  void* args[] = {&d, &k, &w, &y, &ys, &sg, &x, &w_sg, &out};
   return launch_kernel(c, (const void*)combine_kernel, dim3(T, (unsigned)ceil_div(d, kCols)),
                        dim3(kThreads), 0, args);
 }

@@ -26,16 +26,6 @@ cudaError_t launch_kernel(const LaunchCfg& c, const void* fn, dim3 grid, dim3 bl
 // Sets a kernel's dynamic shared-memory limit once per (device, kernel).
 cudaError_t ensure_smem(const void* fn, int bytes);
 
-// ------------------------------------------------------------------ routing
-// logits[t][e] = x[t] . wr[e] (fp32 accumulate).
-cudaError_t launch_router_logits(const LaunchCfg& c, const uint16_t* x, const uint16_t* wr,
-                                 float* logits, int T, int d, int E, int sms);
-
-// Per token: softmax over E, top-k (ties -> lower id), (re)normalised weights.
-cudaError_t launch_topk(const LaunchCfg& c, const float* logits, int T, int E, int k,
-                        int renormalize, int32_t* ids, float* w, int32_t* ids_copy,
-                        float* w_copy);
-
 // Parameters of the work plan built after align (see Plan / WorkExpert).
 struct PlanParams {
   WorkExpert* work;      // [E + 1]
@@ -52,6 +42,34 @@ struct PlanParams {
   int32_t* cta_gu;
   int32_t* cta_dn;
 };
+
+// ------------------------------------------------------------------ routing
+// Largest T routed by the single-launch decode path (route_kernel).
+constexpr int kFusedRouteMaxT = 128;
+// Workspace-header ints used as arrival counters by route_kernel (the status
+// word is int 0): [kRouteCounterBase] tiles done, then one per token tile.
+constexpr int kRouteCounterBase = 16;
+
+// logits[t][e] = x[t] . wr[e]; sg[t] = x[t] . w_sg when w_sg (fp32 accumulate).
+cudaError_t launch_router_logits(const LaunchCfg& c, const uint16_t* x, const uint16_t* wr,
+                                 const uint16_t* w_sg, float* logits, float* sg, int T, int d,
+                                 int E, int sms, int* status);
+
+// Whether launch_route_fused handles these dims.
+bool fused_route_supported(int T, int E, int k);
+
+// Router + top-k + align + plan in one launch (decode sizes).
+cudaError_t launch_route_fused(const LaunchCfg& c, const uint16_t* x, const uint16_t* wr,
+                               const uint16_t* w_sg, float* logits, float* sg, int T, int d,
+                               int E, int k, int renormalize, int32_t* ids, float* w,
+                               int32_t* ids_copy, float* w_copy, int B, int32_t* sorted_ids,
+                               int32_t* block_ids, int32_t* num_post_pad, int32_t* expert_offsets,
+                               const PlanParams& pp, int* status, int* counters, int sms);
+
+// Per token: softmax over E, top-k (ties -> lower id), (re)normalised weights.
+cudaError_t launch_topk(const LaunchCfg& c, const float* logits, int T, int E, int k,
+                        int renormalize, int32_t* ids, float* w, int32_t* ids_copy,
+                        float* w_copy);
 
 // Single-CTA align: optional fused top-k (logits != nullptr), the
 // moe_align_block_size layout, and optionally the work plan (pp.work != nullptr).
@@ -96,9 +114,10 @@ cudaError_t launch_down(const LaunchCfg& c, const ExpertArgs& a, const GemvShape
                         const int32_t* cta, const float* h, const float* hs, float* y,
                         float* ys, int* status, int grid);
 
-// out[t] = sum_j w[t][j] y[t*k+j] + sigmoid(x[t].w_sg) ys[t]   (bf16, RNE)
+// out[t] = sum_j w[t][j] y[t*k+j] + sigmoid(sg[t]) ys[t]   (bf16, RNE); sg[t] =
+// x[t] . w_sg, read from `sg` when given, else computed here.
 cudaError_t launch_combine(const LaunchCfg& c, int T, int d, int k, const float* w,
-                           const float* y, const float* ys, const uint16_t* x,
+                           const float* y, const float* ys, const float* sg, const uint16_t* x,
                            const uint16_t* w_sg, uint16_t* out);
 
 // Host-side tile/stage choices for the two GEMV stages.

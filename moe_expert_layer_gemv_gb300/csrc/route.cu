@@ -2,12 +2,19 @@
 // and the work plan of the grouped expert stages.
 //
 // Router: logits = x . Wr^T spread over many CTAs (the router fold spread across
-// more of the GPU: "veloGB10", Kernel work).  Top-k without a sort: k rounds of
-// a warp-wide argmax over the logits held in registers (the sort-free
-// verify-path top-k: "Qwen3.8 Flash-Next - GB10 UltraFast", How it works).
-// Align: a stable counting sort by expert that keeps arrival order and pads
-// every expert to the block size (the moe_align_block_size arrival-order shim:
-// same page, What this fork adds), with no atomics, so it is deterministic.
+// more of the GPU: "veloGB10", Kernel work); the shared expert's gate x . w_sg
+// rides along as one more row.  Top-k without a sort: k rounds of a warp-wide
+// argmax over the logits held in registers (the sort-free verify-path top-k:
+// "Qwen3.8 Flash-Next - GB10 UltraFast", How it works).  Align: a stable
+// counting sort by expert that keeps arrival order and pads every expert to the
+// block size (the moe_align_block_size arrival-order shim: same page, What this
+// fork adds), with no atomics on the data, so it is deterministic.
+//
+// At decode sizes the whole routing step is one launch (route_kernel): router
+// CTAs write logits; the last CTA of each token tile to finish (an integer
+// arrival counter) selects that tile's top-k; the last tile to finish runs the
+// align and builds the work plan ("veloGB10", Kernel work: the expert routing
+// folded into its neighbours).
 #include <math.h>
 
 #include "launch.h"
@@ -17,11 +24,13 @@ namespace moe {
 namespace {
 
 constexpr int kRouterWarps = 8;
-constexpr int kRouterTokens = 8;  // tokens per router CTA
+constexpr int kRouterThreads = kRouterWarps * 32;
+constexpr int kRouterTokens = 8;  // tokens per router CTA (one token tile)
 constexpr int kAlignThreads = 1024;
-constexpr int kAlignWarps = kAlignThreads / 32;
-constexpr int kAlignSmemSlots = 4096;  // routing slots kept in shared memory by align
+constexpr int kAlignSmemSlots = 4096;  // routing slots the align step keeps in shared memory
+constexpr int kScanScratch = 32 * 8;   // ints of scratch for block_scan<V <= 8>
 
+// ------------------------------------------------------------------ router
 __device__ __forceinline__ float dot8_bf16(uint4 a, uint4 b, float acc) {
   acc = fmaf(bf16lo(a.x), bf16lo(b.x), acc);
   acc = fmaf(bf16hi(a.x), bf16hi(b.x), acc);
@@ -34,35 +43,42 @@ __device__ __forceinline__ float dot8_bf16(uint4 a, uint4 b, float acc) {
   return acc;
 }
 
-// grid = (ceil(E / (8/wpe)), ceil(T / 8)), block = 256.  `wpe` warps share one
-// expert row (split along d); each lane holds its CH 16-byte chunks of the row
-// in registers, all requested before anything waits; each CTA stages 8 tokens
-// of x in shared memory.
-template <int CH>
-__global__ void __launch_bounds__(kRouterWarps * 32)
-    router_logits_kernel(const uint16_t* __restrict__ x, const uint16_t* __restrict__ wr,
-                         float* __restrict__ logits, int T, int d, int E, int wpe) {
-  extern __shared__ uint4 xs[];  // [kRouterTokens][d/8]
-  __shared__ float red[kRouterWarps][kRouterTokens];
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int nch = d >> 3;
-  const int t0 = blockIdx.y * kRouterTokens;
-  const int nt = min(kRouterTokens, T - t0);
-  const int epc = kRouterWarps / wpe;
-  const int e = blockIdx.x * epc + warp / wpe;
-  const int q = warp % wpe;
+struct RouterArgs {
+  const uint16_t* x;       // [T][d]
+  const uint16_t* wr;      // [E][d]
+  const uint16_t* w_sg;    // [d] shared-expert gate row, or null
+  float* logits;           // [T][E]
+  float* sg;               // [T] x . w_sg (when w_sg)
+  int T, d, E, wpe;
+};
 
-  // Router weights are inputs that no kernel of this library writes: request
-  // them before waiting on the predecessor.
-  const uint4* wrow = reinterpret_cast<const uint4*>(wr + (size_t)min(e, E - 1) * d);
+// One router CTA: rows [blockIdx.x * epc, +epc) of the E routed rows plus the
+// gate row (index E), `wpe` warps per row split along d, one token tile of 8
+// tokens staged in shared memory (xs, >= 8 * d bf16) by one bulk copy.  Each
+// lane holds its CH 16-byte chunks of its row, requested before any wait.
+template <int CH>
+__device__ __forceinline__ void router_tile(const RouterArgs& a, uint4* xs, int* status) {
+  __shared__ float red[kRouterWarps][kRouterTokens];
+  __shared__ __align__(8) uint64_t xbar;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int d = a.d, nch = d >> 3;
+  const int rows = a.E + (a.w_sg ? 1 : 0);
+  const int t0 = blockIdx.y * kRouterTokens;
+  const int nt = min(kRouterTokens, a.T - t0);
+  const int epc = kRouterWarps / a.wpe;
+  const int e = blockIdx.x * epc + warp / a.wpe;
+  const int q = warp % a.wpe;
+
+  // Router and gate weights are inputs that no kernel of this library writes:
+  // request them before waiting on the predecessor.
+  const uint16_t* rowp = (e < a.E) ? a.wr + (size_t)e * d : a.w_sg;
   uint4 w[CH];
 #pragma unroll
   for (int i = 0; i < CH; ++i) {
-    const int c = q * 32 + lane + i * wpe * 32;
-    w[i] = (e < E && c < nch) ? __ldg(wrow + c) : make_uint4(0, 0, 0, 0);
+    const int c = q * 32 + lane + i * a.wpe * 32;
+    w[i] = (e < rows && c < nch) ? __ldg(reinterpret_cast<const uint4*>(rowp) + c)
+                                 : make_uint4(0, 0, 0, 0);
   }
-
-  __shared__ __align__(8) uint64_t xbar;
   if (threadIdx.x == 0) {
     mbar_init(&xbar, 1);
     fence_barrier_init();
@@ -73,11 +89,9 @@ __global__ void __launch_bounds__(kRouterWarps * 32)
   if (threadIdx.x == 0) {
     const uint32_t bytes = (uint32_t)nt * d * 2;
     mbar_arrive_expect_tx(&xbar, bytes);
-    bulk_g2s(xs, x + (size_t)t0 * d, bytes, &xbar, policy_evict_last());
+    bulk_g2s(xs, a.x + (size_t)t0 * d, bytes, &xbar, policy_evict_last());
   }
-  const bool ok = mbar_wait(&xbar, 0, nullptr);
-  pdl_trigger();
-  if (!ok) return;  // unreachable unless the copy never lands; logits are then left unwritten
+  mbar_wait(&xbar, 0, status);  // on a timeout the logits are garbage; the status says so
 
   float acc[kRouterTokens];
 #pragma unroll
@@ -86,7 +100,7 @@ __global__ void __launch_bounds__(kRouterWarps * 32)
     if (j < nt) {
 #pragma unroll
       for (int i = 0; i < CH; ++i) {
-        const int c = q * 32 + lane + i * wpe * 32;
+        const int c = q * 32 + lane + i * a.wpe * 32;
         if (c < nch) acc[j] = dot8_bf16(w[i], xs[j * nch + c], acc[j]);
       }
     }
@@ -101,18 +115,30 @@ __global__ void __launch_bounds__(kRouterWarps * 32)
   if (threadIdx.x < epc * kRouterTokens) {
     const int g = threadIdx.x / kRouterTokens, j = threadIdx.x % kRouterTokens;
     const int eo = blockIdx.x * epc + g;
-    if (eo < E && j < nt) {
+    if (eo < rows && j < nt) {
       float s = 0.f;
-      for (int p = 0; p < wpe; ++p) s += red[g * wpe + p][j];
-      logits[(size_t)(t0 + j) * E + eo] = s;
+      for (int p = 0; p < a.wpe; ++p) s += red[g * a.wpe + p][j];
+      if (eo < a.E)
+        a.logits[(size_t)(t0 + j) * a.E + eo] = s;
+      else
+        a.sg[t0 + j] = s;
     }
   }
 }
 
+template <int CH>
+__global__ void __launch_bounds__(kRouterThreads) router_logits_kernel(RouterArgs a, int* status) {
+  extern __shared__ __align__(16) uint4 xs[];
+  router_tile<CH>(a, xs, status);
+  pdl_trigger();
+}
+
+// ------------------------------------------------------------------ top-k
 // One warp selects the top-k of one token's E (<= 1024) logits.  Order: larger
 // logit first, equal logits -> lower id (softmax is increasing, so this is the
 // order of the probabilities).  Weights: exp(l - max) normalised over the
-// selected experts (renormalize) or over all E.
+// selected experts (renormalize) or over all E.  Logits are read at L2 (they
+// may have been written by other CTAs of the same launch).
 template <int NV>
 __device__ void warp_topk_nv(const float* __restrict__ L, int E, int k, int renormalize,
                              int& out_id, float& out_w) {
@@ -125,7 +151,7 @@ __device__ void warp_topk_nv(const float* __restrict__ L, int E, int k, int reno
     v[i] = -INFINITY;
     const int e = lane + 32 * i;
     if (i < nv && e < E) {
-      v[i] = L[e];
+      v[i] = __ldcg(L + e);
       mx = fmaxf(mx, v[i]);
     }
   }
@@ -173,9 +199,8 @@ __device__ void warp_topk_nv(const float* __restrict__ L, int E, int k, int reno
   out_w = renormalize ? my_e / selsum : my_e / z;
 }
 
-// Dispatch on the number of logits each lane holds (E / 32, rounded up to a
-// power of two, E <= 1024).  Lane j < k receives the j-th selected expert and
-// its weight.
+// Dispatch on the number of logits each lane holds (E / 32 rounded up to a
+// power of two).  Lane j < k receives the j-th selected expert and its weight.
 __device__ void warp_topk(const float* __restrict__ L, int E, int k, int renormalize, int& id,
                           float& wt) {
   const int nv = (E + 31) >> 5;
@@ -187,16 +212,20 @@ __device__ void warp_topk(const float* __restrict__ L, int E, int k, int renorma
   else warp_topk_nv<32>(L, E, k, renormalize, id, wt);
 }
 
-// Stores one token's selection (lanes j < k) to its destinations.
-__device__ __forceinline__ void store_topk(int k, int id, float wt, int32_t* ids, float* w,
-                                           int32_t* ids_copy, float* w_copy, int32_t* ids_smem) {
+// Top-k of token t, stored (lanes j < k) to the routing buffers.
+__device__ __forceinline__ void topk_token(const float* logits, int t, int E, int k,
+                                           int renormalize, int32_t* ids, float* w,
+                                           int32_t* ids_copy, float* w_copy) {
+  int id;
+  float wt;
+  warp_topk(logits + (size_t)t * E, E, k, renormalize, id, wt);
   const int lane = threadIdx.x & 31;
   if (lane < k) {
-    ids[lane] = id;
-    w[lane] = wt;
-    if (ids_copy) ids_copy[lane] = id;
-    if (w_copy) w_copy[lane] = wt;
-    if (ids_smem) ids_smem[lane] = id;
+    const size_t o = (size_t)t * k + lane;
+    ids[o] = id;
+    w[o] = wt;
+    if (ids_copy) ids_copy[o] = id;
+    if (w_copy) w_copy[o] = wt;
   }
 }
 
@@ -206,49 +235,56 @@ __global__ void __launch_bounds__(256)
   pdl_wait();
   pdl_trigger();
   const int t = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
-  if (t >= T) return;
-  int id;
-  float wt;
-  warp_topk(logits + (size_t)t * E, E, k, renormalize, id, wt);
-  store_topk(k, id, wt, ids + (size_t)t * k, w + (size_t)t * k,
-             ids_copy ? ids_copy + (size_t)t * k : nullptr,
-             w_copy ? w_copy + (size_t)t * k : nullptr, nullptr);
+  if (t < T) topk_token(logits, t, E, k, renormalize, ids, w, ids_copy, w_copy);
 }
 
-// Exclusive scan of one int per thread over a 1024-thread block.
-__device__ int block_exclusive_scan(int v, int* scratch, int* total) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  int inc = v;
+// ------------------------------------------------------------------ block scan
+// Exclusive scan of V ints per thread over the CTA (blockDim a multiple of 32,
+// <= 1024).  scratch: >= 32 * V ints.  Every thread gets the totals.
+template <int V>
+__device__ void block_scan(const int (&v)[V], int (&ex)[V], int (&tot)[V], int* scratch) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
+  int inc[V];
 #pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    const int n = __shfl_up_sync(0xffffffffu, inc, o);
-    if (lane >= o) inc += n;
-  }
-  if (lane == 31) scratch[warp] = inc;
-  __syncthreads();
-  if (warp == 0) {
-    int s = scratch[lane];
+  for (int i = 0; i < V; ++i) {
+    inc[i] = v[i];
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
-      const int n = __shfl_up_sync(0xffffffffu, s, o);
-      if (lane >= o) s += n;
+      const int n = __shfl_up_sync(0xffffffffu, inc[i], o);
+      if (lane >= o) inc[i] += n;
     }
-    scratch[lane] = s;
+    if (lane == 31) scratch[i * 32 + warp] = inc[i];
   }
   __syncthreads();
-  const int base = warp ? scratch[warp - 1] : 0;
-  *total = scratch[kAlignWarps - 1];
+  if (warp == 0) {
+#pragma unroll
+    for (int i = 0; i < V; ++i) {
+      int s = lane < nw ? scratch[i * 32 + lane] : 0;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int n = __shfl_up_sync(0xffffffffu, s, o);
+        if (lane >= o) s += n;
+      }
+      scratch[i * 32 + lane] = s;
+    }
+  }
   __syncthreads();
-  return base + inc - v;
+#pragma unroll
+  for (int i = 0; i < V; ++i) {
+    ex[i] = (warp ? scratch[i * 32 + warp - 1] : 0) + inc[i] - v[i];
+    tot[i] = scratch[i * 32 + nw - 1];
+  }
+  __syncthreads();
 }
 
+// Thread-owned runs of experts: thread i owns [i * run, min(E, (i + 1) * run)).
+__device__ __forceinline__ int expert_run(int E) { return (E + blockDim.x - 1) / blockDim.x; }
+
+// ------------------------------------------------------------------ plan
 // Estimated cost of a unit with nt tokens, in token-equivalents: a fixed part
 // for streaming the unit's weight rows plus one per token of arithmetic.
 constexpr int kUnitBaseCost = 4;
 
-// First unit of the CTA whose share of the cost starts at `target`, given
-// work expert i's cost prefix `c0`, first unit `u0`, tiles, token count n and
-// tokens per group xt (units are numbered group-major).
 __device__ int unit_at_cost(int target, int c0, int u0, int tiles, int n, int xt) {
   const int groups = (n + xt - 1) / xt;
   const int nt_last = n - (groups - 1) * xt;
@@ -271,8 +307,8 @@ __device__ int unit_at_cost(int target, int c0, int u0, int tiles, int n, int xt
 __device__ void split_by_cost(int n_work, const int* s_cost, const int* s_unit, const int* s_n,
                               const int* s_tiles, int total_cost, int total_units, int xt,
                               int grid, int32_t* cta) {
-  // CTA c's share starts at cost c * total / grid, taken in fp32: monotone in c,
-  // and exact enough for balancing (no 64-bit division on the device).
+  // CTA c's share starts at cost c * total / grid, taken in fp32: monotone in c
+  // and exact enough for balancing.
   const float per_cta = (float)total_cost / (float)grid;
   for (int c = threadIdx.x; c <= grid; c += blockDim.x) {
     if (c == grid || n_work == 0) {
@@ -291,26 +327,29 @@ __device__ void split_by_cost(int n_work, const int* s_cost, const int* s_unit, 
   }
 }
 
-// Work plan: one WorkExpert per touched routed expert (ascending id), then the
-// shared expert; gate_up / down work units counted per expert; and each CTA's
-// range of units for both expert stages, balanced by estimated cost.  Called by
-// all 1024 threads; cnt/off are per-expert counts and padded offsets; tmp holds
-// >= 7 * (E + 1) ints of shared memory.
+// Work plan from per-expert counts (cnt) and padded offsets (off), both in
+// shared memory: one WorkExpert per touched routed expert (ascending id), then
+// the shared expert; unit counts and costs per expert; each CTA's unit range
+// for both expert stages.  All threads call it.  tmp: >= 7 * (E + 1) ints.
 __device__ void build_plan(const int* cnt, const int* off, int E, int T, int num_post_pad,
                            const PlanParams& pp, int* scratch, int* tmp) {
-  __syncthreads();
-  const int e = threadIdx.x;
-  const int c = (e < E) ? cnt[e] : 0;
-  const int flag = c > 0;
-  const int ggu = (int)ceil_div(c, pp.xt_gu), gdn = (int)ceil_div(c, pp.xt_dn);
-  int n_routed, tot_gu, tot_dn, cost_gu, cost_dn;
-  const int idx = block_exclusive_scan(flag, scratch, &n_routed);
-  const int egu = block_exclusive_scan(flag ? pp.tiles_gu * ggu : 0, scratch, &tot_gu);
-  const int edn = block_exclusive_scan(flag ? pp.tiles_dn * gdn : 0, scratch, &tot_dn);
-  const int cgu = block_exclusive_scan(
-      flag ? pp.tiles_gu * (ggu * kUnitBaseCost + c) : 0, scratch, &cost_gu);
-  const int cdn = block_exclusive_scan(
-      flag ? pp.tiles_dn * (gdn * kUnitBaseCost + c) : 0, scratch, &cost_dn);
+  const int run = expert_run(E);
+  const int e0 = threadIdx.x * run, e1 = min(E, e0 + run);
+  // Per-expert values: touched flag, gate_up units, down units, their costs.
+  int loc[5] = {0, 0, 0, 0, 0};
+  for (int e = e0; e < e1; ++e) {
+    const int c = cnt[e];
+    if (c > 0) {
+      const int ggu = (c + pp.xt_gu - 1) / pp.xt_gu, gdn = (c + pp.xt_dn - 1) / pp.xt_dn;
+      loc[0] += 1;
+      loc[1] += pp.tiles_gu * ggu;
+      loc[2] += pp.tiles_dn * gdn;
+      loc[3] += pp.tiles_gu * (ggu * kUnitBaseCost + c);
+      loc[4] += pp.tiles_dn * (gdn * kUnitBaseCost + c);
+    }
+  }
+  int ex[5], tot[5];
+  block_scan<5>(loc, ex, tot, scratch);
   const int W = E + 1;
   int* s_ugu = tmp;
   int* s_udn = tmp + W;
@@ -319,27 +358,38 @@ __device__ void build_plan(const int* cnt, const int* off, int E, int T, int num
   int* s_n = tmp + 4 * W;
   int* s_tgu = tmp + 5 * W;
   int* s_tdn = tmp + 6 * W;
-  if (flag) {
+  int idx = ex[0], ugu = ex[1], udn = ex[2], cgu = ex[3], cdn = ex[4];
+  for (int e = e0; e < e1; ++e) {
+    const int c = cnt[e];
+    if (c == 0) continue;
+    const int ggu = (c + pp.xt_gu - 1) / pp.xt_gu, gdn = (c + pp.xt_dn - 1) / pp.xt_dn;
     WorkExpert we;
     we.expert = e;
     we.n_tok = c;
     we.pos = off[e];
-    we.unit_gu = egu;
-    we.unit_dn = edn;
+    we.unit_gu = ugu;
+    we.unit_dn = udn;
     we.pad_[0] = we.pad_[1] = we.pad_[2] = 0;
     pp.work[idx] = we;
-    s_ugu[idx] = egu;
-    s_udn[idx] = edn;
+    s_ugu[idx] = ugu;
+    s_udn[idx] = udn;
     s_cgu[idx] = cgu;
     s_cdn[idx] = cdn;
     s_n[idx] = c;
     s_tgu[idx] = pp.tiles_gu;
     s_tdn[idx] = pp.tiles_dn;
+    ++idx;
+    ugu += pp.tiles_gu * ggu;
+    udn += pp.tiles_dn * gdn;
+    cgu += pp.tiles_gu * (ggu * kUnitBaseCost + c);
+    cdn += pp.tiles_dn * (gdn * kUnitBaseCost + c);
   }
+  const int n_routed = tot[0];
+  int tot_gu = tot[1], tot_dn = tot[2], cost_gu = tot[3], cost_dn = tot[4];
   const bool has_shared = pp.tiles_gu_shared > 0 && T > 0;
   const int n_work = n_routed + (has_shared ? 1 : 0);
   if (has_shared) {
-    const int sg = (int)ceil_div(T, pp.xt_gu), sd = (int)ceil_div(T, pp.xt_dn);
+    const int sg = (T + pp.xt_gu - 1) / pp.xt_gu, sd = (T + pp.xt_dn - 1) / pp.xt_dn;
     if (threadIdx.x == 0) {
       WorkExpert we;
       we.expert = -1;
@@ -363,10 +413,8 @@ __device__ void build_plan(const int* cnt, const int* off, int E, int T, int num
     cost_dn += pp.tiles_dn_shared * (sd * kUnitBaseCost + T);
   }
   __syncthreads();
-  split_by_cost(n_work, s_cgu, s_ugu, s_n, s_tgu, cost_gu, tot_gu, pp.xt_gu, pp.grid,
-                pp.cta_gu);
-  split_by_cost(n_work, s_cdn, s_udn, s_n, s_tdn, cost_dn, tot_dn, pp.xt_dn, pp.grid,
-                pp.cta_dn);
+  split_by_cost(n_work, s_cgu, s_ugu, s_n, s_tgu, cost_gu, tot_gu, pp.xt_gu, pp.grid, pp.cta_gu);
+  split_by_cost(n_work, s_cdn, s_udn, s_n, s_tdn, cost_dn, tot_dn, pp.xt_dn, pp.grid, pp.cta_dn);
   if (threadIdx.x == 0) {
     Plan p;
     p.n_work = n_work;
@@ -378,47 +426,37 @@ __device__ void build_plan(const int* cnt, const int* off, int E, int T, int num
   }
 }
 
-// Single CTA of 1024 threads.  Shared memory: hist [32][E] int, cnt [E],
-// off [E], scratch [32].
-__global__ void __launch_bounds__(kAlignThreads)
-    align_kernel(const float* __restrict__ logits, int T, int E, int k, int renormalize,
-                 int32_t* ids, float* w, int32_t* ids_copy, float* w_copy, int B,
-                 int32_t* __restrict__ sorted_ids, int32_t* __restrict__ block_ids,
-                 int32_t* __restrict__ num_post_pad, int32_t* __restrict__ expert_offsets,
-                 PlanParams pp, int* status) {
-  extern __shared__ int sm[];
-  int* hist = sm;                     // [32][E]
-  int* cnt = hist + kAlignWarps * E;  // [E]
-  int* off = cnt + E;                 // [E]
-  int* scratch = off + E;             // [32]
-  int* sids = scratch + 32;           // [kAlignSmemSlots] when S fits
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+// ------------------------------------------------------------------ align
+struct AlignOut {
+  int32_t* sorted_ids;
+  int32_t* block_ids;
+  int32_t* num_post_pad;
+  int32_t* expert_offsets;
+};
+
+// Shared-memory ints the align step needs for E experts and nw warps; the last
+// kAlignSmemSlots hold the routing ids when they fit.
+__host__ __device__ constexpr size_t align_smem_ints(int E, int nw) {
+  return (size_t)nw * E + 2 * (size_t)E + kScanScratch + 7 * ((size_t)E + 1) + kAlignSmemSlots;
+}
+
+// moe_align_block_size (+ the work plan when pp.work) on all threads of the
+// CTA.  src: the S = T * k expert ids (shared or global memory).  smem: at
+// least align_smem_ints(E, blockDim / 32) ints.
+__device__ void align_block(const int32_t* src, int T, int k, int E, int B, const AlignOut& o,
+                            const PlanParams& pp, int* status, int* smem) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
   const int S = T * k;
-  const bool ids_in_smem = S <= kAlignSmemSlots;
-
-  for (int i = threadIdx.x; i < kAlignWarps * E; i += kAlignThreads) hist[i] = 0;
-  pdl_wait();
-  pdl_trigger();
-
-  // Optional fused top-k: one warp per token.
-  if (logits != nullptr) {
-    for (int t = warp; t < T; t += kAlignWarps) {
-      int id;
-      float wt;
-      warp_topk(logits + (size_t)t * E, E, k, renormalize, id, wt);
-      store_topk(k, id, wt, ids + (size_t)t * k, w + (size_t)t * k,
-                 ids_copy ? ids_copy + (size_t)t * k : nullptr,
-                 w_copy ? w_copy + (size_t)t * k : nullptr,
-                 ids_in_smem ? sids + (size_t)t * k : nullptr);
-    }
-  } else if (ids_in_smem) {
-    for (int s = threadIdx.x; s < S; s += kAlignThreads) sids[s] = ids[s];
-  }
+  int* hist = smem;                   // [nw][E]
+  int* cnt = hist + nw * E;           // [E]
+  int* off = cnt + E;                 // [E]
+  int* scratch = off + E;             // [kScanScratch]
+  int* tmp = scratch + kScanScratch;  // [7 * (E + 1)]
+  for (int i = threadIdx.x; i < nw * E; i += blockDim.x) hist[i] = 0;
   __syncthreads();
-  const int32_t* src = ids_in_smem ? sids : ids;
 
   // Phase 1: each warp counts the experts of a contiguous chunk of slots.
-  const int chunk = (int)ceil_div(S, kAlignWarps);
+  const int chunk = (S + nw - 1) / nw;
   const int s_begin = warp * chunk, s_end = min(S, s_begin + chunk);
   for (int base = s_begin; base < s_end; base += 32) {
     const int s = base + lane;
@@ -436,31 +474,37 @@ __global__ void __launch_bounds__(kAlignThreads)
   }
   __syncthreads();
 
-  // Phase 2: per expert, exclusive base of each warp's chunk; totals.
-  const int e_me = threadIdx.x;
-  int padded = 0;
-  if (e_me < E) {
-    int run = 0;
-    for (int q = 0; q < kAlignWarps; ++q) {
-      const int c = hist[q * E + e_me];
-      hist[q * E + e_me] = run;
-      run += c;
+  // Phase 2: per expert, each warp's exclusive base and the count; padded
+  // offsets by a block scan over thread-owned runs of experts.
+  const int run = expert_run(E);
+  const int e0 = threadIdx.x * run, e1 = min(E, e0 + run);
+  int loc[1] = {0};
+  for (int e = e0; e < e1; ++e) {
+    int r = 0;
+    for (int q = 0; q < nw; ++q) {
+      const int c = hist[q * E + e];
+      hist[q * E + e] = r;
+      r += c;
     }
-    cnt[e_me] = run;
-    padded = (int)round_up(run, B);
+    cnt[e] = r;
+    loc[0] += (r + B - 1) / B * B;
   }
-  int total;
-  const int my_off = block_exclusive_scan(padded, scratch, &total);
-  if (e_me < E) {
-    off[e_me] = my_off;
-    expert_offsets[e_me] = my_off;
+  int ex[1], tot[1];
+  block_scan<1>(loc, ex, tot, scratch);
+  int p0 = ex[0];
+  for (int e = e0; e < e1; ++e) {
+    const int padded = (cnt[e] + B - 1) / B * B;
+    off[e] = p0;
+    o.expert_offsets[e] = p0;
     // Pad positions get the sentinel S; every block of the run names e.
-    for (int p = my_off + cnt[e_me]; p < my_off + padded; ++p) sorted_ids[p] = S;
-    for (int b = my_off / B; b < (my_off + padded) / B; ++b) block_ids[b] = e_me;
+    for (int p = p0 + cnt[e]; p < p0 + padded; ++p) o.sorted_ids[p] = S;
+    for (int b = p0 / B; b < (p0 + padded) / B; ++b) o.block_ids[b] = e;
+    p0 += padded;
   }
+  const int total = tot[0];
   if (threadIdx.x == 0) {
-    expert_offsets[E] = total;
-    *num_post_pad = total;
+    o.expert_offsets[E] = total;
+    *o.num_post_pad = total;
   }
   __syncthreads();
 
@@ -478,33 +522,57 @@ __global__ void __launch_bounds__(kAlignThreads)
     __syncwarp();
     if (e >= 0) {
       const int rank = __popc(peers & ((1u << lane) - 1u));
-      sorted_ids[off[e] + rank_base + rank] = s;
+      o.sorted_ids[off[e] + rank_base + rank] = s;
       if (lane == __ffs(peers) - 1) hist[warp * E + e] = rank_base + __popc(peers);
     }
     __syncwarp();
   }
-
-  if (pp.work != nullptr) build_plan(cnt, off, E, T, total, pp, scratch, hist);
+  if (pp.work != nullptr) build_plan(cnt, off, E, T, total, pp, scratch, tmp);
 }
 
-// Plan from an existing align layout: counts recovered from the padded runs
-// (a run's trailing entries equal to the sentinel are padding).
+// One CTA of 1024 threads: optional top-k for all T tokens, then align_block.
+__global__ void __launch_bounds__(kAlignThreads)
+    align_kernel(const float* __restrict__ logits, int T, int E, int k, int renormalize,
+                 int32_t* ids, float* w, int32_t* ids_copy, float* w_copy, int B, AlignOut o,
+                 PlanParams pp, int* status) {
+  extern __shared__ int sm[];
+  const int nw = kAlignThreads / 32;
+  int* sids = sm + align_smem_ints(E, nw) - kAlignSmemSlots;
+  const int S = T * k;
+  pdl_wait();
+  pdl_trigger();
+  if (logits != nullptr) {
+    for (int t = threadIdx.x >> 5; t < T; t += nw)
+      topk_token(logits, t, E, k, renormalize, ids, w, ids_copy, w_copy);
+    __threadfence_block();
+    __syncthreads();
+  }
+  const int32_t* src = ids;
+  if (S <= kAlignSmemSlots) {
+    for (int s = threadIdx.x; s < S; s += blockDim.x) sids[s] = __ldcg(ids + s);
+    src = sids;
+  }
+  __syncthreads();
+  align_block(src, T, k, E, B, o, pp, status, sm);
+}
+
+// Plan from an existing align layout (moe_expert_forward): counts recovered
+// from the padded runs (a run's trailing sentinel entries are padding).
 __global__ void __launch_bounds__(kAlignThreads)
     plan_kernel(int T, int E, int k, int B, const int32_t* __restrict__ sorted_ids,
                 const int32_t* __restrict__ num_post_pad, const int32_t* __restrict__ expert_offsets,
                 PlanParams pp, int* status) {
   extern __shared__ int sm[];
-  int* cnt = sm;               // [E]
-  int* off = cnt + E;          // [E]
-  int* scratch = off + E;      // [32]
-  int* tmp = scratch + 32;     // [7 * (E + 1)]
+  int* cnt = sm;                      // [E]
+  int* off = cnt + E;                 // [E]
+  int* scratch = off + E;             // [kScanScratch]
+  int* tmp = scratch + kScanScratch;  // [7 * (E + 1)]
   pdl_wait();
   pdl_trigger();
   const int S = T * k;
-  const int e = threadIdx.x;
-  if (e < E) {
+  const int cap = S + E * (B - 1);
+  for (int e = threadIdx.x; e < E; e += blockDim.x) {
     const int o = expert_offsets[e], o1 = expert_offsets[e + 1];
-    const int cap = S + E * (B - 1);
     int c = o1 - o;
     if (o < 0 || c < 0 || c % B != 0 || o1 > cap) {
       record_status(status, kStatusDeviceCheck);
@@ -519,22 +587,94 @@ __global__ void __launch_bounds__(kAlignThreads)
   build_plan(cnt, off, E, T, *num_post_pad, pp, scratch, tmp);
 }
 
-}  // namespace
+// ------------------------------------------------------------------ fused route
+struct RouteArgs {
+  RouterArgs r;
+  int k, renormalize, B;
+  int32_t* ids;          // workspace routing [T][k]
+  float* w;
+  int32_t* ids_copy;     // caller copies (may be null)
+  float* w_copy;
+  AlignOut o;
+  PlanParams pp;
+  int* status;
+  int* counters;         // [0]: tiles done; [1 + y]: CTAs done in token tile y
+};
 
-cudaError_t launch_router_logits(const LaunchCfg& c, const uint16_t* x, const uint16_t* wr,
-                                 float* logits, int T, int d, int E, int sms) {
-  if (T == 0) return cudaSuccess;
+// Decode-size routing in one launch.  grid = (router CTAs per tile, token
+// tiles), 256 threads.  Dynamic shared memory: max(router tile, align step).
+// Every CTA arrives on its tile's counter exactly once, whatever happened
+// before, so the counters return to zero by the end of every launch.
+template <int CH>
+__global__ void __launch_bounds__(kRouterThreads) route_kernel(RouteArgs a) {
+  extern __shared__ __align__(16) int dsm[];
+  __shared__ int s_last;
+  router_tile<CH>(a.r, reinterpret_cast<uint4*>(dsm), a.status);
+  pdl_trigger();
+
+  // Arrival on this token tile; the last CTA to arrive selects its top-k.
+  __threadfence();
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    const int old = atomicAdd(&a.counters[1 + blockIdx.y], 1);
+    s_last = old == (int)gridDim.x - 1;
+    if (s_last) a.counters[1 + blockIdx.y] = 0;  // ready for the next call
+  }
+  __syncthreads();
+  if (!s_last) return;
+  __threadfence();
+  const int t = blockIdx.y * kRouterTokens + (threadIdx.x >> 5);
+  if ((threadIdx.x >> 5) < kRouterTokens && t < a.r.T)
+    topk_token(a.r.logits, t, a.r.E, a.k, a.renormalize, a.ids, a.w, a.ids_copy, a.w_copy);
+
+  // Arrival of this tile; the last tile to finish runs the align and the plan.
+  __threadfence();
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    const int old = atomicAdd(&a.counters[0], 1);
+    s_last = old == (int)gridDim.y - 1;
+    if (s_last) a.counters[0] = 0;
+  }
+  __syncthreads();
+  if (!s_last) return;
+  __threadfence();
+  const int S = a.r.T * a.k;
+  int* sids = dsm + align_smem_ints(a.r.E, kRouterWarps) - kAlignSmemSlots;
+  for (int s = threadIdx.x; s < S; s += blockDim.x) sids[s] = __ldcg(a.ids + s);
+  __syncthreads();
+  align_block(sids, a.r.T, a.k, a.r.E, a.B, a.o, a.pp, a.status, dsm);
+}
+
+// Router CTA shape: warps per expert row (wpe) and 16-byte chunks per lane.
+void router_shape(int T, int d, int rows, int sms, int* wpe_out, int* ch_out) {
   const int ty = (int)ceil_div(T, kRouterTokens);
   const int nch = d / 8;
   int wpe = 8;
   for (int cand = 1; cand <= 8; cand <<= 1) {
-    if (ceil_div(E, kRouterWarps / cand) * ty >= sms) {
+    if (ceil_div(rows, kRouterWarps / cand) * ty >= sms) {
       wpe = cand;
       break;
     }
   }
   while (wpe < 8 && ceil_div(nch, wpe * 32) > 8) wpe <<= 1;  // at most 8 chunks per lane
-  const int ch = (int)ceil_div(nch, wpe * 32);
+  *wpe_out = wpe;
+  *ch_out = (int)ceil_div(nch, wpe * 32);
+}
+
+}  // namespace
+
+bool fused_route_supported(int T, int E, int k) {
+  return T <= kFusedRouteMaxT && (size_t)T * k <= (size_t)kAlignSmemSlots && E <= 1024;
+}
+
+cudaError_t launch_router_logits(const LaunchCfg& c, const uint16_t* x, const uint16_t* wr,
+                                 const uint16_t* w_sg, float* logits, float* sg, int T, int d,
+                                 int E, int sms, int* status) {
+  if (T == 0) return cudaSuccess;
+  RouterArgs a{x, wr, w_sg, logits, sg, T, d, E, 0};
+  const int rows = E + (w_sg ? 1 : 0);
+  int ch;
+  router_shape(T, d, rows, sms, &a.wpe, &ch);
   const size_t smem = (size_t)kRouterTokens * d * 2;
   const void* fn = ch <= 1 ? (const void*)router_logits_kernel<1>
                  : ch <= 2 ? (const void*)router_logits_kernel<2>
@@ -542,9 +682,47 @@ cudaError_t launch_router_logits(const LaunchCfg& c, const uint16_t* x, const ui
                            : (const void*)router_logits_kernel<8>;
   cudaError_t e = ensure_smem(fn, (int)smem);
   if (e != cudaSuccess) return e;
-  dim3 grid((unsigned)ceil_div(E, kRouterWarps / wpe), (unsigned)ty);
-  void* args[] = {&x, &wr, &logits, &T, &d, &E, &wpe};
-  return launch_kernel(c, fn, grid, dim3(kRouterWarps * 32), smem, args);
+  dim3 grid((unsigned)ceil_div(rows, kRouterWarps / a.wpe), (unsigned)ceil_div(T, kRouterTokens));
+  void* args[] = {&a, &status};
+  return launch_kernel(c, fn, grid, dim3(kRouterThreads), smem, args);
+}
+
+cudaError_t launch_route_fused(const LaunchCfg& c, const uint16_t* x, const uint16_t* wr,
+                               const uint16_t* w_sg, float* logits, float* sg, int T, int d,
+                               int E, int k, int renormalize, int32_t* ids, float* w,
+                               int32_t* ids_copy, float* w_copy, int B, int32_t* sorted_ids,
+                               int32_t* block_ids, int32_t* num_post_pad, int32_t* expert_offsets,
+                               const PlanParams& pp, int* status, int* counters, int sms) {
+  if (T == 0) return cudaSuccess;
+  RouteArgs a;
+  a.r = RouterArgs{x, wr, w_sg, logits, sg, T, d, E, 0};
+  const int rows = E + (w_sg ? 1 : 0);
+  int ch;
+  router_shape(T, d, rows, sms, &a.r.wpe, &ch);
+  a.k = k;
+  a.renormalize = renormalize;
+  a.B = B;
+  a.ids = ids;
+  a.w = w;
+  a.ids_copy = ids_copy;
+  a.w_copy = w_copy;
+  a.o = AlignOut{sorted_ids, block_ids, num_post_pad, expert_offsets};
+  a.pp = pp;
+  a.status = status;
+  a.counters = counters;
+  size_t smem = (size_t)kRouterTokens * d * 2;
+  const size_t asmem = align_smem_ints(E, kRouterWarps) * sizeof(int);
+  if (asmem > smem) smem = asmem;
+  const void* fn = ch <= 1 ? (const void*)route_kernel<1>
+                 : ch <= 2 ? (const void*)route_kernel<2>
+                 : ch <= 4 ? (const void*)route_kernel<4>
+                           : (const void*)route_kernel<8>;
+  cudaError_t e = ensure_smem(fn, (int)smem);
+  if (e != cudaSuccess) return e;
+  dim3 grid((unsigned)ceil_div(rows, kRouterWarps / a.r.wpe),
+            (unsigned)ceil_div(T, kRouterTokens));
+  void* args[] = {&a};
+  return launch_kernel(c, fn, grid, dim3(kRouterThreads), smem, args);
 }
 
 cudaError_t launch_topk(const LaunchCfg& c, const float* logits, int T, int E, int k,
@@ -561,19 +739,22 @@ cudaError_t launch_align(const LaunchCfg& c, const float* logits, int T, int E, 
                          float* w_copy, int B, int32_t* sorted_ids, int32_t* block_ids,
                          int32_t* num_post_pad, int32_t* expert_offsets, const PlanParams& pp,
                          int* status) {
-  const size_t smem = ((size_t)kAlignWarps * E + 2 * (size_t)E + 32 + kAlignSmemSlots) * sizeof(int);
+  const size_t smem = align_smem_ints(E, kAlignThreads / 32) * sizeof(int);
   cudaError_t e = ensure_smem((const void*)align_kernel, (int)smem);
   if (e != cudaSuccess) return e;
+  AlignOut o{sorted_ids, block_ids, num_post_pad, expert_offsets};
   PlanParams p = pp;
   void* args[] = {&logits, &T, &E, &k, &renormalize, &ids, &w, &ids_copy, &w_copy, &B,
-                  &sorted_ids, &block_ids, &num_post_pad, &expert_offsets, &p, &status};
+                  &o, &p, &status};
   return launch_kernel(c, (const void*)align_kernel, dim3(1), dim3(kAlignThreads), smem, args);
 }
 
 cudaError_t launch_plan(const LaunchCfg& c, int T, int E, int k, int B,
                         const int32_t* sorted_ids, const int32_t* num_post_pad,
                         const int32_t* expert_offsets, const PlanParams& pp, int* status) {
-  const size_t smem = (2 * (size_t)E + 32 + 7 * ((size_t)E + 1)) * sizeof(int);
+  const size_t smem = (2 * (size_t)E + kScanScratch + 7 * ((size_t)E + 1)) * sizeof(int);
+  cudaError_t e = ensure_smem((const void*)plan_kernel, (int)smem);
+  if (e != cudaSuccess) return e;
   PlanParams p = pp;
   void* args[] = {&T, &E, &k, &B, &sorted_ids, &num_post_pad, &expert_offsets, &p, &status};
   return launch_kernel(c, (const void*)plan_kernel, dim3(1), dim3(kAlignThreads), smem, args);
