@@ -279,10 +279,9 @@ moe_status_t layer_forward(const moe_dims_t* dims, const void* x, const void* ro
     if (launch_topk(next, logits, dm.T, dm.E, dm.top_k, dm.renormalize, ids, w, ids_out,
                     w_out) != cudaSuccess)
       return MOE_ERR_CUDA;
-    if (launch_align(next, nullptr, dm.T, dm.E, dm.top_k, dm.renormalize, ids, w, nullptr,
-                     nullptr, dm.block_size, sorted, at<int32_t>(ws, L.blocks),
-                     at<int32_t>(ws, L.npp), at<int32_t>(ws, L.offs), ep.pp,
-                     status) != cudaSuccess)
+    if (launch_align(next, ids, dm.T, dm.E, dm.top_k, dm.block_size, sorted,
+                     at<int32_t>(ws, L.blocks), at<int32_t>(ws, L.npp), at<int32_t>(ws, L.offs),
+                     ep.pp, status) != cudaSuccess)
       return MOE_ERR_CUDA;
   }
   if ((s = record(events, MOE_EV_ROUTED, st)) != MOE_OK) return s;
@@ -402,11 +401,10 @@ moe_status_t moe_align_block_size(const moe_dims_t* dims, const int32_t* topk_id
   Layout L;
   if ((s = check_ws(dm, workspace, workspace_bytes, &L)) != MOE_OK) return s;
   PlanParams none = {};
-  return cuda_status(launch_align(LaunchCfg{static_cast<cudaStream_t>(stream), false}, nullptr,
-                                  dm.T, dm.E, dm.top_k, dm.renormalize,
-                                  const_cast<int32_t*>(topk_ids), nullptr, nullptr, nullptr,
-                                  dm.block_size, sorted_ids, block_expert_ids, num_post_pad,
-                                  expert_offsets, none, at<int>(workspace, L.header)));
+  return cuda_status(launch_align(LaunchCfg{static_cast<cudaStream_t>(stream), false}, topk_ids,
+                                  dm.T, dm.E, dm.top_k, dm.block_size, sorted_ids,
+                                  block_expert_ids, num_post_pad, expert_offsets, none,
+                                  at<int>(workspace, L.header)));
 }
 
 moe_status_t moe_expert_forward(const moe_dims_t* dims, const void* x, const float* topk_weights,

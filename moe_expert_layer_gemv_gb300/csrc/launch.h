@@ -71,13 +71,11 @@ cudaError_t launch_topk(const LaunchCfg& c, const float* logits, int T, int E, i
                         int renormalize, int32_t* ids, float* w, int32_t* ids_copy,
                         float* w_copy);
 
-// Single-CTA align: optional fused top-k (logits != nullptr), the
-// moe_align_block_size layout, and optionally the work plan (pp.work != nullptr).
-cudaError_t launch_align(const LaunchCfg& c, const float* logits, int T, int E, int k,
-                         int renormalize, int32_t* ids, float* w, int32_t* ids_copy,
-                         float* w_copy, int B, int32_t* sorted_ids, int32_t* block_ids,
-                         int32_t* num_post_pad, int32_t* expert_offsets, const PlanParams& pp,
-                         int* status);
+// Single-CTA moe_align_block_size of the given ids, and the work plan when
+// pp.work != nullptr.
+cudaError_t launch_align(const LaunchCfg& c, const int32_t* ids, int T, int E, int k, int B,
+                         int32_t* sorted_ids, int32_t* block_ids, int32_t* num_post_pad,
+                         int32_t* expert_offsets, const PlanParams& pp, int* status);
 
 // Work plan from an existing align layout (moe_expert_forward path).
 cudaError_t launch_plan(const LaunchCfg& c, int T, int E, int k, int B,

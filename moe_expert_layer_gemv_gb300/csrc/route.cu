@@ -136,67 +136,81 @@ __global__ void __launch_bounds__(kRouterThreads) router_logits_kernel(RouterArg
 // ------------------------------------------------------------------ top-k
 // One warp selects the top-k of one token's E (<= 1024) logits.  Order: larger
 // logit first, equal logits -> lower id (softmax is increasing, so this is the
-// order of the probabilities).  Weights: exp(l - max) normalised over the
-// selected experts (renormalize) or over all E.  Logits are read at L2 (they
-// may have been written by other CTAs of the same launch).
+// order of the probabilities).  Each lane sorts its NV logits (ids lane + 32 i)
+// once; then each of the k rounds is one warp max over the lanes' heads and
+// one warp min over the ids holding it, and the winning lane pops its head.
+// Weights: exp(l - max) normalised over the selected experts (renormalize) or
+// over all E.  Logits are read at L2 (they may have been written by other CTAs
+// of the same launch).
+
+// Order-preserving map of a float to an unsigned key (key 0 is never produced
+// by a finite or infinite float, so it marks an empty slot).
+__device__ __forceinline__ uint32_t float_key(float f) {
+  uint32_t b = __float_as_uint(f);
+  if (b == 0x80000000u) b = 0u;  // -0 and +0 are the same logit
+  return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
+}
+__device__ __forceinline__ float key_float(uint32_t k) {
+  return __uint_as_float((k & 0x80000000u) ? (k & 0x7fffffffu) : ~k);
+}
+
 template <int NV>
 __device__ void warp_topk_nv(const float* __restrict__ L, int E, int k, int renormalize,
                              int& out_id, float& out_w) {
   const int lane = threadIdx.x & 31;
-  const int nv = (E + 31) >> 5;
-  float v[NV];
-  float mx = -INFINITY;
+  uint32_t key[NV];
+  int id[NV];
 #pragma unroll
   for (int i = 0; i < NV; ++i) {
-    v[i] = -INFINITY;
     const int e = lane + 32 * i;
-    if (i < nv && e < E) {
-      v[i] = __ldcg(L + e);
-      mx = fmaxf(mx, v[i]);
+    id[i] = e;
+    key[i] = e < E ? float_key(__ldcg(L + e)) : 0u;
+  }
+  // Per-lane sort, descending key; equal keys keep ascending id (stable).
+#pragma unroll
+  for (int pass = 0; pass < NV; ++pass) {
+#pragma unroll
+    for (int i = pass & 1; i + 1 < NV; i += 2) {
+      if (key[i + 1] > key[i]) {
+        const uint32_t tk = key[i];
+        key[i] = key[i + 1];
+        key[i + 1] = tk;
+        const int ti = id[i];
+        id[i] = id[i + 1];
+        id[i + 1] = ti;
+      }
     }
   }
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+  const uint32_t kmax = __reduce_max_sync(0xffffffffu, key[0]);
+  const float mx = key_float(kmax);
   float z = 0.f;
   if (!renormalize) {
 #pragma unroll
     for (int i = 0; i < NV; ++i)
-      if (i < nv && lane + 32 * i < E) z += expf(v[i] - mx);
+      if (key[i] != 0u) z += expf(key_float(key[i]) - mx);
     z = warp_sum(z);
   }
-  uint32_t taken = 0;
   int my_id = 0;
-  float my_e = 0.f, selsum = 0.f;
+  uint32_t my_key = 0;
   for (int j = 0; j < k; ++j) {
-    float bv = -INFINITY;
-    int bi = 0x7fffffff;
-#pragma unroll
-    for (int i = 0; i < NV; ++i) {
-      const int e = lane + 32 * i;
-      if (i < nv && e < E && !((taken >> i) & 1u) && (bi == 0x7fffffff || v[i] > bv)) {
-        bv = v[i];
-        bi = e;
-      }
-    }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-      const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
-      const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
-      if (oi != 0x7fffffff && (bi == 0x7fffffff || ov > bv || (ov == bv && oi < bi))) {
-        bv = ov;
-        bi = oi;
-      }
-    }
-    if (bi != 0x7fffffff && (bi & 31) == lane) taken |= 1u << (bi >> 5);
-    const float ev = expf(bv - mx);
-    selsum += ev;
+    const uint32_t m = __reduce_max_sync(0xffffffffu, key[0]);
+    const uint32_t win = __reduce_min_sync(0xffffffffu, key[0] == m ? (uint32_t)id[0] : 0xffffffffu);
     if (lane == j) {
-      my_id = bi;
-      my_e = ev;
+      my_id = (int)win;
+      my_key = m;
+    }
+    if (key[0] == m && (uint32_t)id[0] == win) {  // the winning lane pops its head
+#pragma unroll
+      for (int i = 0; i + 1 < NV; ++i) {
+        key[i] = key[i + 1];
+        id[i] = id[i + 1];
+      }
+      key[NV - 1] = 0u;
     }
   }
+  const float ev = lane < k ? expf(key_float(my_key) - mx) : 0.f;
   out_id = my_id;
-  out_w = renormalize ? my_e / selsum : my_e / z;
+  out_w = ev / (renormalize ? warp_sum(ev) : z);
 }
 
 // Dispatch on the number of logits each lane holds (E / 32 rounded up to a
@@ -327,29 +341,53 @@ __device__ void split_by_cost(int n_work, const int* s_cost, const int* s_unit, 
   }
 }
 
-// Work plan from per-expert counts (cnt) and padded offsets (off), both in
-// shared memory: one WorkExpert per touched routed expert (ascending id), then
-// the shared expert; unit counts and costs per expert; each CTA's unit range
-// for both expert stages.  All threads call it.  tmp: >= 7 * (E + 1) ints.
-__device__ void build_plan(const int* cnt, const int* off, int E, int T, int num_post_pad,
-                           const PlanParams& pp, int* scratch, int* tmp) {
+// Per-expert quantities scanned over the experts: padded length, touched
+// flag, gate_up units, down units, and their estimated costs.
+constexpr int kVals = 6;
+__device__ __forceinline__ void expert_vals(int c, int B, const PlanParams& pp, int (&v)[kVals]) {
+  const int ggu = (c + pp.xt_gu - 1) / pp.xt_gu, gdn = (c + pp.xt_dn - 1) / pp.xt_dn;
+  const bool t = c > 0;
+  v[0] = (c + B - 1) / B * B;
+  v[1] = t ? 1 : 0;
+  v[2] = t ? pp.tiles_gu * ggu : 0;
+  v[3] = t ? pp.tiles_dn * gdn : 0;
+  v[4] = t ? pp.tiles_gu * (ggu * kUnitBaseCost + c) : 0;
+  v[5] = t ? pp.tiles_dn * (gdn * kUnitBaseCost + c) : 0;
+}
+
+struct AlignOut {
+  int32_t* sorted_ids;
+  int32_t* block_ids;
+  int32_t* num_post_pad;
+  int32_t* expert_offsets;
+};
+
+// Plan totals every thread needs for the split.
+struct PlanTotals {
+  int n_work, units_gu, units_dn, cost_gu, cost_dn, num_post_pad;
+};
+
+// From per-expert counts cnt[E] (shared memory): one block scan of the
+// expert_vals over thread-owned runs of experts, then
+//   - when o: padded offsets into off[] and the align outputs (offsets,
+//     sentinel pads, block ids, num_post_pad); otherwise off[] is given;
+//   - when pp.work: the work list (one entry per touched expert, ascending id,
+//     then the shared expert) and the arrays split_stages() searches.
+// Ends with a CTA barrier.  tmp: >= 7 * (E + 1) ints; scratch: kScanScratch.
+__device__ PlanTotals layout_and_plan(const int* cnt, int* off, int E, int T, int S, int B,
+                                      const AlignOut* o, const PlanParams& pp, int* scratch,
+                                      int* tmp) {
   const int run = expert_run(E);
   const int e0 = threadIdx.x * run, e1 = min(E, e0 + run);
-  // Per-expert values: touched flag, gate_up units, down units, their costs.
-  int loc[5] = {0, 0, 0, 0, 0};
+  int loc[kVals] = {0, 0, 0, 0, 0, 0};
   for (int e = e0; e < e1; ++e) {
-    const int c = cnt[e];
-    if (c > 0) {
-      const int ggu = (c + pp.xt_gu - 1) / pp.xt_gu, gdn = (c + pp.xt_dn - 1) / pp.xt_dn;
-      loc[0] += 1;
-      loc[1] += pp.tiles_gu * ggu;
-      loc[2] += pp.tiles_dn * gdn;
-      loc[3] += pp.tiles_gu * (ggu * kUnitBaseCost + c);
-      loc[4] += pp.tiles_dn * (gdn * kUnitBaseCost + c);
-    }
+    int v[kVals];
+    expert_vals(cnt[e], B, pp, v);
+#pragma unroll
+    for (int i = 0; i < kVals; ++i) loc[i] += v[i];
   }
-  int ex[5], tot[5];
-  block_scan<5>(loc, ex, tot, scratch);
+  int ex[kVals], tot[kVals];
+  block_scan<kVals>(loc, ex, tot, scratch);
   const int W = E + 1;
   int* s_ugu = tmp;
   int* s_udn = tmp + W;
@@ -358,91 +396,107 @@ __device__ void build_plan(const int* cnt, const int* off, int E, int T, int num
   int* s_n = tmp + 4 * W;
   int* s_tgu = tmp + 5 * W;
   int* s_tdn = tmp + 6 * W;
-  int idx = ex[0], ugu = ex[1], udn = ex[2], cgu = ex[3], cdn = ex[4];
+  int acc[kVals];
+#pragma unroll
+  for (int i = 0; i < kVals; ++i) acc[i] = ex[i];
   for (int e = e0; e < e1; ++e) {
     const int c = cnt[e];
-    if (c == 0) continue;
-    const int ggu = (c + pp.xt_gu - 1) / pp.xt_gu, gdn = (c + pp.xt_dn - 1) / pp.xt_dn;
-    WorkExpert we;
-    we.expert = e;
-    we.n_tok = c;
-    we.pos = off[e];
-    we.unit_gu = ugu;
-    we.unit_dn = udn;
-    we.pad_[0] = we.pad_[1] = we.pad_[2] = 0;
-    pp.work[idx] = we;
-    s_ugu[idx] = ugu;
-    s_udn[idx] = udn;
-    s_cgu[idx] = cgu;
-    s_cdn[idx] = cdn;
-    s_n[idx] = c;
-    s_tgu[idx] = pp.tiles_gu;
-    s_tdn[idx] = pp.tiles_dn;
-    ++idx;
-    ugu += pp.tiles_gu * ggu;
-    udn += pp.tiles_dn * gdn;
-    cgu += pp.tiles_gu * (ggu * kUnitBaseCost + c);
-    cdn += pp.tiles_dn * (gdn * kUnitBaseCost + c);
+    int v[kVals];
+    expert_vals(c, B, pp, v);
+    if (o != nullptr) {
+      const int p0 = acc[0];
+      off[e] = p0;
+      o->expert_offsets[e] = p0;
+      // Pad positions get the sentinel S; every block of the run names e.
+      for (int p = p0 + c; p < p0 + v[0]; ++p) o->sorted_ids[p] = S;
+      for (int b = p0 / B; b < (p0 + v[0]) / B; ++b) o->block_ids[b] = e;
+    }
+    if (pp.work != nullptr && c > 0) {
+      const int idx = acc[1];
+      WorkExpert we;
+      we.expert = e;
+      we.n_tok = c;
+      we.pos = off[e];
+      we.unit_gu = acc[2];
+      we.unit_dn = acc[3];
+      we.pad_[0] = we.pad_[1] = we.pad_[2] = 0;
+      pp.work[idx] = we;
+      s_ugu[idx] = acc[2];
+      s_udn[idx] = acc[3];
+      s_cgu[idx] = acc[4];
+      s_cdn[idx] = acc[5];
+      s_n[idx] = c;
+      s_tgu[idx] = pp.tiles_gu;
+      s_tdn[idx] = pp.tiles_dn;
+    }
+#pragma unroll
+    for (int i = 0; i < kVals; ++i) acc[i] += v[i];
   }
-  const int n_routed = tot[0];
-  int tot_gu = tot[1], tot_dn = tot[2], cost_gu = tot[3], cost_dn = tot[4];
-  const bool has_shared = pp.tiles_gu_shared > 0 && T > 0;
-  const int n_work = n_routed + (has_shared ? 1 : 0);
-  if (has_shared) {
+  if (o != nullptr && threadIdx.x == 0) {
+    o->expert_offsets[E] = tot[0];
+    *o->num_post_pad = tot[0];
+  }
+  PlanTotals pt{tot[1], tot[2], tot[3], tot[4], tot[5], tot[0]};
+  if (pp.work != nullptr && pp.tiles_gu_shared > 0 && T > 0) {
     const int sg = (T + pp.xt_gu - 1) / pp.xt_gu, sd = (T + pp.xt_dn - 1) / pp.xt_dn;
     if (threadIdx.x == 0) {
       WorkExpert we;
       we.expert = -1;
       we.n_tok = T;
       we.pos = 0;
-      we.unit_gu = tot_gu;
-      we.unit_dn = tot_dn;
+      we.unit_gu = pt.units_gu;
+      we.unit_dn = pt.units_dn;
       we.pad_[0] = we.pad_[1] = we.pad_[2] = 0;
-      pp.work[n_routed] = we;
-      s_ugu[n_routed] = tot_gu;
-      s_udn[n_routed] = tot_dn;
-      s_cgu[n_routed] = cost_gu;
-      s_cdn[n_routed] = cost_dn;
-      s_n[n_routed] = T;
-      s_tgu[n_routed] = pp.tiles_gu_shared;
-      s_tdn[n_routed] = pp.tiles_dn_shared;
+      pp.work[pt.n_work] = we;
+      s_ugu[pt.n_work] = pt.units_gu;
+      s_udn[pt.n_work] = pt.units_dn;
+      s_cgu[pt.n_work] = pt.cost_gu;
+      s_cdn[pt.n_work] = pt.cost_dn;
+      s_n[pt.n_work] = T;
+      s_tgu[pt.n_work] = pp.tiles_gu_shared;
+      s_tdn[pt.n_work] = pp.tiles_dn_shared;
     }
-    tot_gu += pp.tiles_gu_shared * sg;
-    tot_dn += pp.tiles_dn_shared * sd;
-    cost_gu += pp.tiles_gu_shared * (sg * kUnitBaseCost + T);
-    cost_dn += pp.tiles_dn_shared * (sd * kUnitBaseCost + T);
+    pt.n_work += 1;
+    pt.units_gu += pp.tiles_gu_shared * sg;
+    pt.units_dn += pp.tiles_dn_shared * sd;
+    pt.cost_gu += pp.tiles_gu_shared * (sg * kUnitBaseCost + T);
+    pt.cost_dn += pp.tiles_dn_shared * (sd * kUnitBaseCost + T);
   }
   __syncthreads();
-  split_by_cost(n_work, s_cgu, s_ugu, s_n, s_tgu, cost_gu, tot_gu, pp.xt_gu, pp.grid, pp.cta_gu);
-  split_by_cost(n_work, s_cdn, s_udn, s_n, s_tdn, cost_dn, tot_dn, pp.xt_dn, pp.grid, pp.cta_dn);
+  return pt;
+}
+
+// Both stages' CTA ranges and the Plan record.
+__device__ void split_stages(const PlanTotals& pt, int E, const PlanParams& pp, const int* tmp) {
+  const int W = E + 1;
+  split_by_cost(pt.n_work, tmp + 2 * W, tmp, tmp + 4 * W, tmp + 5 * W, pt.cost_gu, pt.units_gu,
+                pp.xt_gu, pp.grid, pp.cta_gu);
+  split_by_cost(pt.n_work, tmp + 3 * W, tmp + W, tmp + 4 * W, tmp + 6 * W, pt.cost_dn,
+                pt.units_dn, pp.xt_dn, pp.grid, pp.cta_dn);
   if (threadIdx.x == 0) {
     Plan p;
-    p.n_work = n_work;
-    p.units_gu = tot_gu;
-    p.units_dn = tot_dn;
-    p.num_post_pad = num_post_pad;
+    p.n_work = pt.n_work;
+    p.units_gu = pt.units_gu;
+    p.units_dn = pt.units_dn;
+    p.num_post_pad = pt.num_post_pad;
     p.pad_[0] = p.pad_[1] = p.pad_[2] = p.pad_[3] = 0;
     *pp.plan = p;
   }
 }
 
 // ------------------------------------------------------------------ align
-struct AlignOut {
-  int32_t* sorted_ids;
-  int32_t* block_ids;
-  int32_t* num_post_pad;
-  int32_t* expert_offsets;
-};
-
 // Shared-memory ints the align step needs for E experts and nw warps; the last
-// kAlignSmemSlots hold the routing ids when they fit.
+// kAlignSmemSlots hold the routing ids (and, for small S, their ranks) when
+// they fit.
 __host__ __device__ constexpr size_t align_smem_ints(int E, int nw) {
-  return (size_t)nw * E + 2 * (size_t)E + kScanScratch + 7 * ((size_t)E + 1) + kAlignSmemSlots;
+  return (size_t)nw * E + 2 * (size_t)E + kScanScratch + 7 * ((size_t)E + 1) +
+         2 * (size_t)kAlignSmemSlots;
 }
 
 // moe_align_block_size (+ the work plan when pp.work) on all threads of the
-// CTA.  src: the S = T * k expert ids (shared or global memory).  smem: at
-// least align_smem_ints(E, blockDim / 32) ints.
+// CTA.  src: the S = T * k expert ids (shared or global memory).  Counting:
+// per-warp histograms over contiguous chunks of slots (any S).  smem: at least
+// align_smem_ints(E, blockDim / 32) ints.
 __device__ void align_block(const int32_t* src, int T, int k, int E, int B, const AlignOut& o,
                             const PlanParams& pp, int* status, int* smem) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
@@ -455,7 +509,7 @@ __device__ void align_block(const int32_t* src, int T, int k, int E, int B, cons
   for (int i = threadIdx.x; i < nw * E; i += blockDim.x) hist[i] = 0;
   __syncthreads();
 
-  // Phase 1: each warp counts the experts of a contiguous chunk of slots.
+  // Each warp counts the experts of a contiguous chunk of slots.
   const int chunk = (S + nw - 1) / nw;
   const int s_begin = warp * chunk, s_end = min(S, s_begin + chunk);
   for (int base = s_begin; base < s_end; base += 32) {
@@ -473,13 +527,8 @@ __device__ void align_block(const int32_t* src, int T, int k, int E, int B, cons
     __syncwarp();
   }
   __syncthreads();
-
-  // Phase 2: per expert, each warp's exclusive base and the count; padded
-  // offsets by a block scan over thread-owned runs of experts.
-  const int run = expert_run(E);
-  const int e0 = threadIdx.x * run, e1 = min(E, e0 + run);
-  int loc[1] = {0};
-  for (int e = e0; e < e1; ++e) {
+  // Per expert: each warp's exclusive base (in place) and the count.
+  for (int e = threadIdx.x; e < E; e += blockDim.x) {
     int r = 0;
     for (int q = 0; q < nw; ++q) {
       const int c = hist[q * E + e];
@@ -487,28 +536,11 @@ __device__ void align_block(const int32_t* src, int T, int k, int E, int B, cons
       r += c;
     }
     cnt[e] = r;
-    loc[0] += (r + B - 1) / B * B;
-  }
-  int ex[1], tot[1];
-  block_scan<1>(loc, ex, tot, scratch);
-  int p0 = ex[0];
-  for (int e = e0; e < e1; ++e) {
-    const int padded = (cnt[e] + B - 1) / B * B;
-    off[e] = p0;
-    o.expert_offsets[e] = p0;
-    // Pad positions get the sentinel S; every block of the run names e.
-    for (int p = p0 + cnt[e]; p < p0 + padded; ++p) o.sorted_ids[p] = S;
-    for (int b = p0 / B; b < (p0 + padded) / B; ++b) o.block_ids[b] = e;
-    p0 += padded;
-  }
-  const int total = tot[0];
-  if (threadIdx.x == 0) {
-    o.expert_offsets[E] = total;
-    *o.num_post_pad = total;
   }
   __syncthreads();
+  const PlanTotals pt = layout_and_plan(cnt, off, E, T, S, B, &o, pp, scratch, tmp);
 
-  // Phase 3: scatter in arrival order.
+  // Scatter in arrival order.
   for (int base = s_begin; base < s_end; base += 32) {
     const int s = base + lane;
     int e = -1;
@@ -527,13 +559,54 @@ __device__ void align_block(const int32_t* src, int T, int k, int E, int B, cons
     }
     __syncwarp();
   }
-  if (pp.work != nullptr) build_plan(cnt, off, E, T, total, pp, scratch, tmp);
+  if (pp.work != nullptr) split_stages(pt, E, pp, tmp);
 }
 
-// One CTA of 1024 threads: optional top-k for all T tokens, then align_block.
+// The same for S <= kAlignSmemSlots with the ids in shared memory (sids):
+// warp 0 walks the slots in order, 32 at a time, giving every slot its rank
+// among the earlier slots of its expert, so no per-warp histograms are needed.
+__device__ void align_block_small(const int32_t* sids, int T, int k, int E, int B,
+                                  const AlignOut& o, const PlanParams& pp, int* status,
+                                  int* smem) {
+  const int lane = threadIdx.x & 31;
+  const int S = T * k;
+  int* cnt = smem;                    // [E]
+  int* off = cnt + E;                 // [E]
+  int* scratch = off + E;             // [kScanScratch]
+  int* tmp = scratch + kScanScratch;  // [7 * (E + 1)]
+  int* rank = tmp + 7 * (E + 1);      // [S]
+  for (int e = threadIdx.x; e < E; e += blockDim.x) cnt[e] = 0;
+  __syncthreads();
+  if (threadIdx.x < 32) {
+    for (int base = 0; base < S; base += 32) {
+      const int s = base + lane;
+      int e = -1;
+      if (s < S) {
+        e = sids[s];
+        if (e < 0 || e >= E) {
+          record_status(status, kStatusDeviceCheck);
+          e = -1;
+        }
+      }
+      const unsigned peers = __match_any_sync(0xffffffffu, e);
+      if (e >= 0) rank[s] = cnt[e] + __popc(peers & ((1u << lane) - 1u));
+      __syncwarp();
+      if (e >= 0 && lane == __ffs(peers) - 1) cnt[e] += __popc(peers);
+      __syncwarp();
+    }
+  }
+  __syncthreads();
+  const PlanTotals pt = layout_and_plan(cnt, off, E, T, S, B, &o, pp, scratch, tmp);
+  for (int s = threadIdx.x; s < S; s += blockDim.x) {
+    const int e = sids[s];
+    if (e >= 0 && e < E) o.sorted_ids[off[e] + rank[s]] = s;
+  }
+  if (pp.work != nullptr) split_stages(pt, E, pp, tmp);
+}
+
+// One CTA of 1024 threads: the align (and plan) of given routing ids.
 __global__ void __launch_bounds__(kAlignThreads)
-    align_kernel(const float* __restrict__ logits, int T, int E, int k, int renormalize,
-                 int32_t* ids, float* w, int32_t* ids_copy, float* w_copy, int B, AlignOut o,
+    align_kernel(const int32_t* __restrict__ ids, int T, int E, int k, int B, AlignOut o,
                  PlanParams pp, int* status) {
   extern __shared__ int sm[];
   const int nw = kAlignThreads / 32;
@@ -541,19 +614,13 @@ __global__ void __launch_bounds__(kAlignThreads)
   const int S = T * k;
   pdl_wait();
   pdl_trigger();
-  if (logits != nullptr) {
-    for (int t = threadIdx.x >> 5; t < T; t += nw)
-      topk_token(logits, t, E, k, renormalize, ids, w, ids_copy, w_copy);
-    __threadfence_block();
-    __syncthreads();
-  }
-  const int32_t* src = ids;
   if (S <= kAlignSmemSlots) {
     for (int s = threadIdx.x; s < S; s += blockDim.x) sids[s] = __ldcg(ids + s);
-    src = sids;
+    __syncthreads();
+    align_block_small(sids, T, k, E, B, o, pp, status, sm);
+  } else {
+    align_block(ids, T, k, E, B, o, pp, status, sm);
   }
-  __syncthreads();
-  align_block(src, T, k, E, B, o, pp, status, sm);
 }
 
 // Plan from an existing align layout (moe_expert_forward): counts recovered
@@ -584,7 +651,9 @@ __global__ void __launch_bounds__(kAlignThreads)
     off[e] = o;
   }
   __syncthreads();
-  build_plan(cnt, off, E, T, *num_post_pad, pp, scratch, tmp);
+  PlanTotals pt = layout_and_plan(cnt, off, E, T, S, B, nullptr, pp, scratch, tmp);
+  pt.num_post_pad = *num_post_pad;
+  split_stages(pt, E, pp, tmp);
 }
 
 // ------------------------------------------------------------------ fused route
@@ -627,22 +696,25 @@ __global__ void __launch_bounds__(kRouterThreads) route_kernel(RouteArgs a) {
   if ((threadIdx.x >> 5) < kRouterTokens && t < a.r.T)
     topk_token(a.r.logits, t, a.r.E, a.k, a.renormalize, a.ids, a.w, a.ids_copy, a.w_copy);
 
-  // Arrival of this tile; the last tile to finish runs the align and the plan.
+  // Arrival of this tile; the last tile to finish runs the align and the plan
+  // (with one token tile, this CTA is already the last).
   __threadfence();
   __syncthreads();
-  if (threadIdx.x == 0) {
-    const int old = atomicAdd(&a.counters[0], 1);
-    s_last = old == (int)gridDim.y - 1;
-    if (s_last) a.counters[0] = 0;
+  if (gridDim.y > 1) {
+    if (threadIdx.x == 0) {
+      const int old = atomicAdd(&a.counters[0], 1);
+      s_last = old == (int)gridDim.y - 1;
+      if (s_last) a.counters[0] = 0;
+    }
+    __syncthreads();
+    if (!s_last) return;
+    __threadfence();
   }
-  __syncthreads();
-  if (!s_last) return;
-  __threadfence();
   const int S = a.r.T * a.k;
   int* sids = dsm + align_smem_ints(a.r.E, kRouterWarps) - kAlignSmemSlots;
   for (int s = threadIdx.x; s < S; s += blockDim.x) sids[s] = __ldcg(a.ids + s);
   __syncthreads();
-  align_block(sids, a.r.T, a.k, a.r.E, a.B, a.o, a.pp, a.status, dsm);
+  align_block_small(sids, a.r.T, a.k, a.r.E, a.B, a.o, a.pp, a.status, dsm);
 }
 
 // Router CTA shape: warps per expert row (wpe) and 16-byte chunks per lane.
@@ -734,25 +806,22 @@ cudaError_t launch_topk(const LaunchCfg& c, const float* logits, int T, int E, i
   return launch_kernel(c, (const void*)topk_kernel, grid, dim3(256), 0, args);
 }
 
-cudaError_t launch_align(const LaunchCfg& c, const float* logits, int T, int E, int k,
-                         int renormalize, int32_t* ids, float* w, int32_t* ids_copy,
-                         float* w_copy, int B, int32_t* sorted_ids, int32_t* block_ids,
-                         int32_t* num_post_pad, int32_t* expert_offsets, const PlanParams& pp,
-                         int* status) {
+cudaError_t launch_align(const LaunchCfg& c, const int32_t* ids, int T, int E, int k, int B,
+                         int32_t* sorted_ids, int32_t* block_ids, int32_t* num_post_pad,
+                         int32_t* expert_offsets, const PlanParams& pp, int* status) {
   const size_t smem = align_smem_ints(E, kAlignThreads / 32) * sizeof(int);
   cudaError_t e = ensure_smem((const void*)align_kernel, (int)smem);
   if (e != cudaSuccess) return e;
   AlignOut o{sorted_ids, block_ids, num_post_pad, expert_offsets};
   PlanParams p = pp;
-  void* args[] = {&logits, &T, &E, &k, &renormalize, &ids, &w, &ids_copy, &w_copy, &B,
-                  &o, &p, &status};
+  void* args[] = {&ids, &T, &E, &k, &B, &o, &p, &status};
   return launch_kernel(c, (const void*)align_kernel, dim3(1), dim3(kAlignThreads), smem, args);
 }
 
 cudaError_t launch_plan(const LaunchCfg& c, int T, int E, int k, int B,
                         const int32_t* sorted_ids, const int32_t* num_post_pad,
                         const int32_t* expert_offsets, const PlanParams& pp, int* status) {
-  const size_t smem = (2 * (size_t)E + kScanScratch + 7 * ((size_t)E + 1)) * sizeof(int);
+  const size_t smem = (2 * (size_t)E + kScanScratch + 7 * ((size_t)E + 1)) * sizeof(int);  // plan_kernel
   cudaError_t e = ensure_smem((const void*)plan_kernel, (int)smem);
   if (e != cudaSuccess) return e;
   PlanParams p = pp;
