@@ -316,29 +316,25 @@ __device__ int unit_at_cost(int target, int c0, int u0, int tiles, int n, int xt
   return u0 + g * tiles + t;
 }
 
-// Splits one stage's units over the grid by estimated cost: CTA c gets units
-// [cta[c], cta[c+1]) and starts in work expert cta[grid + 1 + c].
-__device__ void split_by_cost(int n_work, const int* s_cost, const int* s_unit, const int* s_n,
-                              const int* s_tiles, int total_cost, int total_units, int xt,
-                              int grid, int32_t* cta) {
-  // CTA c's share starts at cost c * total / grid, taken in fp32: monotone in c
-  // and exact enough for balancing.
-  const float per_cta = (float)total_cost / (float)grid;
-  for (int c = threadIdx.x; c <= grid; c += blockDim.x) {
-    if (c == grid || n_work == 0) {
-      cta[c] = c == grid ? total_units : 0;
-      if (c < grid) cta[grid + 1 + c] = 0;
-      continue;
-    }
-    const int target = min(total_cost, (int)((float)c * per_cta));
-    int lo = 0, hi = n_work - 1;
-    while (lo < hi) {
-      const int mid = (lo + hi + 1) >> 1;
-      if (s_cost[mid] <= target) lo = mid; else hi = mid - 1;
-    }
-    cta[c] = c == 0 ? 0 : unit_at_cost(target, s_cost[lo], s_unit[lo], s_tiles[lo], s_n[lo], xt);
-    cta[grid + 1 + c] = lo;
+// CTA c of one stage gets units [cta[c], cta[c+1]) and starts in work expert
+// cta[grid + 1 + c]: its share of the stage's estimated cost starts at
+// c * total / grid (taken in fp32: monotone in c, exact enough for balancing).
+__device__ void split_one(int c, int n_work, const int* s_cost, const int* s_unit, const int* s_n,
+                          const int* s_tiles, int total_cost, int total_units, int xt, int grid,
+                          int32_t* cta) {
+  if (c == grid || n_work == 0) {
+    cta[c] = c == grid ? total_units : 0;
+    if (c < grid) cta[grid + 1 + c] = 0;
+    return;
   }
+  const int target = min(total_cost, (int)((float)c * ((float)total_cost / (float)grid)));
+  int lo = 0, hi = n_work - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (s_cost[mid] <= target) lo = mid; else hi = mid - 1;
+  }
+  cta[c] = c == 0 ? 0 : unit_at_cost(target, s_cost[lo], s_unit[lo], s_tiles[lo], s_n[lo], xt);
+  cta[grid + 1 + c] = lo;
 }
 
 // Per-expert quantities scanned over the experts: padded length, touched
@@ -466,13 +462,18 @@ __device__ PlanTotals layout_and_plan(const int* cnt, int* off, int E, int T, in
   return pt;
 }
 
-// Both stages' CTA ranges and the Plan record.
+// Both stages' CTA ranges (one pass over 2 * (grid + 1) items) and the Plan.
 __device__ void split_stages(const PlanTotals& pt, int E, const PlanParams& pp, const int* tmp) {
   const int W = E + 1;
-  split_by_cost(pt.n_work, tmp + 2 * W, tmp, tmp + 4 * W, tmp + 5 * W, pt.cost_gu, pt.units_gu,
+  const int per = pp.grid + 1;
+  for (int i = threadIdx.x; i < 2 * per; i += blockDim.x) {
+    if (i < per)
+      split_one(i, pt.n_work, tmp + 2 * W, tmp, tmp + 4 * W, tmp + 5 * W, pt.cost_gu, pt.units_gu,
                 pp.xt_gu, pp.grid, pp.cta_gu);
-  split_by_cost(pt.n_work, tmp + 3 * W, tmp + W, tmp + 4 * W, tmp + 6 * W, pt.cost_dn,
+    else
+      split_one(i - per, pt.n_work, tmp + 3 * W, tmp + W, tmp + 4 * W, tmp + 6 * W, pt.cost_dn,
                 pt.units_dn, pp.xt_dn, pp.grid, pp.cta_dn);
+  }
   if (threadIdx.x == 0) {
     Plan p;
     p.n_work = pt.n_work;
