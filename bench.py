@@ -147,17 +147,19 @@ def algorithmic(shape, ids_list):
             "touched": statistics.mean(touched), "flops": flops}
 
 
-def kernel_traffic(src_name, workload):
-    """ncu dram bytes per launch for the dominant kernel, if recorded for the
-    current source of that kernel (profiles/<kernel>_<workload>.json)."""
+def kernel_traffic(src_name, workload, algorithmic_bytes):
+    """DRAM bytes (read + write) per launch of the dominant kernel, from the ncu
+    capture recorded in profiles/gate_up_<workload>.json -- scaled from the
+    captured token batch to this run's by the algorithmic bytes -- or None when
+    the kernel source changed since the capture."""
     prof = os.path.join(ROOT, "profiles", f"gate_up_{workload}.json")
     src = os.path.join(ROOT, "moe_expert_layer_gemv_gb300", "csrc", src_name)
     try:
         rec = json.load(open(prof))
         h = hashlib.sha256(open(src, "rb").read()).hexdigest()
         if rec.get("source_sha256") == h:
-            return rec.get("dram_bytes_per_launch")
-    except (OSError, ValueError):
+            return rec["dram_bytes_per_launch"] * algorithmic_bytes / rec["algorithmic_bytes_of_capture"]
+    except (OSError, ValueError, KeyError):
         pass
     return None
 
@@ -341,7 +343,7 @@ def main():
     peaks, peak_kind = measured_peaks()
     gu_ms = stage_ms["gate_up"]
     achieved = alg["gate_up_bytes"] / (gu_ms * 1e-3) / 1e9
-    traffic = kernel_traffic("expert_gemv.cu", shape.name)
+    traffic = kernel_traffic("expert_gemv.cu", shape.name, alg["gate_up_bytes"])
     if rank == 0:
         tok_s = world * shape.T / (ms * 1e-3)
         line = {
