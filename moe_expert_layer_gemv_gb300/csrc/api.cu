@@ -62,9 +62,20 @@ bool device_info(DeviceInfo* out) {
 constexpr int kGemvSmemBudget = 228 * 1024 / kCtasPerSm - 1024 - 512;
 
 struct Layout {
-  size_t header, plan, work, cta, logits, sg, ids, w, sorted, blocks, npp, offs, h, hs, y, ys, total;
+  size_t header, plan, work, cta, logits, sg, htc, ids, w, sorted, blocks, npp, offs, h, hs, y, ys, total;
   int64_t cap;
+  bool tc;           // the dims qualify for the tensor-core expert path
+  int hs0, h_rows;   // tensor-core path: first shared-expert row of htc, rows of htc
 };
+
+// Smallest T routed through the tensor-core grouped GEMMs (below it, the
+// weight-streaming GEMVs).
+constexpr int kTcMinT = 256;
+
+bool tc_dims(const moe_dims_t& dm) {
+  return dm.T >= kTcMinT && dm.weight_format == MOE_WEIGHTS_BF16 && dm.block_size % 128 == 0 &&
+         dm.I % 128 == 0 && dm.d % 256 == 0 && (dm.I_shared == 0 || dm.I_shared == dm.I);
+}
 
 size_t carve(size_t* cursor, size_t bytes) {
   const size_t at = *cursor;
@@ -93,6 +104,10 @@ Layout layout_of(const moe_dims_t& dm) {
   L.hs = carve(&c, sizeof(float) * (size_t)dm.T * dm.I_shared);
   L.y = carve(&c, sizeof(float) * (size_t)S * dm.d);
   L.ys = carve(&c, sizeof(float) * (size_t)dm.T * dm.d);
+  L.tc = tc_dims(dm);
+  L.hs0 = (int)round_up(L.cap, 128);
+  L.h_rows = L.hs0 + (int)round_up(dm.T, 128);
+  L.htc = carve(&c, L.tc ? sizeof(uint16_t) * (size_t)L.h_rows * dm.I : 0);
   L.total = c;
   return L;
 }
@@ -155,6 +170,8 @@ moe_status_t check_weights(const moe_dims_t& dm, const moe_expert_weights_t* ex,
 struct ExpertPlan {
   GemvShape gu, dn;
   PlanParams pp;
+  bool tc;  // run the expert stages on the tensor cores
+  int sms;
 };
 
 moe_status_t expert_plan(const moe_dims_t& dm, void* ws, const Layout& L, int sms,
@@ -172,6 +189,10 @@ moe_status_t expert_plan(const moe_dims_t& dm, void* ws, const Layout& L, int sm
   pp.tiles_dn_shared = dm.I_shared > 0 ? (int)ceil_div(dm.d, ep->dn.rg_shared) : 0;
   pp.xt_gu = ep->gu.xt;
   pp.xt_dn = ep->dn.xt;
+  ep->sms = sms;
+  ep->tc = L.tc && tc_supported(dm.weight_format, dm.d, dm.I, dm.I_shared, dm.block_size);
+  pp.tc_nb_gu = ep->tc ? tc_tiles_per_mblock_gu(dm.I) : 0;
+  pp.tc_nb_dn = ep->tc ? tc_tiles_per_mblock_dn(dm.d) : 0;
   pp.grid = kCtasPerSm * sms < kMaxGrid ? kCtasPerSm * sms : kMaxGrid;
   pp.cta_gu = at<int32_t>(ws, L.cta);
   pp.cta_dn = at<int32_t>(ws, L.cta) + 2 * (kMaxGrid + 1);
@@ -217,13 +238,24 @@ moe_status_t run_experts(const moe_dims_t& dm, const void* x, const float* topk_
   float* y = at<float>(ws, L.y);
   float* ys = at<float>(ws, L.ys);
   moe_status_t s;
-  if (launch_gate_up(next, a, ep.gu, static_cast<const uint16_t*>(x), sorted_ids, ep.pp.plan,
-                     ep.pp.work, ep.pp.cta_gu, h, hs, status, ep.pp.grid) != cudaSuccess)
-    return MOE_ERR_CUDA;
-  if ((s = record(events, MOE_EV_GATE_UP, st)) != MOE_OK) return s;
-  if (launch_down(next, a, ep.dn, sorted_ids, ep.pp.plan, ep.pp.work, ep.pp.cta_dn, h, hs, y,
-                  ys, status, ep.pp.grid) != cudaSuccess)
-    return MOE_ERR_CUDA;
+  if (ep.tc) {
+    uint16_t* htc = at<uint16_t>(ws, L.htc);
+    if (launch_tc(next, false, a, static_cast<const uint16_t*>(x), sorted_ids, ep.pp.plan,
+                  ep.pp.work, htc, L.hs0, L.h_rows, y, ys, status, ep.sms) != cudaSuccess)
+      return MOE_ERR_CUDA;
+    if ((s = record(events, MOE_EV_GATE_UP, st)) != MOE_OK) return s;
+    if (launch_tc(next, true, a, static_cast<const uint16_t*>(x), sorted_ids, ep.pp.plan,
+                  ep.pp.work, htc, L.hs0, L.h_rows, y, ys, status, ep.sms) != cudaSuccess)
+      return MOE_ERR_CUDA;
+  } else {
+    if (launch_gate_up(next, a, ep.gu, static_cast<const uint16_t*>(x), sorted_ids, ep.pp.plan,
+                       ep.pp.work, ep.pp.cta_gu, h, hs, status, ep.pp.grid) != cudaSuccess)
+      return MOE_ERR_CUDA;
+    if ((s = record(events, MOE_EV_GATE_UP, st)) != MOE_OK) return s;
+    if (launch_down(next, a, ep.dn, sorted_ids, ep.pp.plan, ep.pp.work, ep.pp.cta_dn, h, hs, y,
+                    ys, status, ep.pp.grid) != cudaSuccess)
+      return MOE_ERR_CUDA;
+  }
   if ((s = record(events, MOE_EV_DOWN, st)) != MOE_OK) return s;
   if (launch_combine(next, dm.T, dm.d, dm.top_k, topk_w, y, sh ? ys : nullptr, sh ? sg : nullptr,
                      static_cast<const uint16_t*>(x),

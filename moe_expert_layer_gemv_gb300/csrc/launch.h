@@ -36,6 +36,8 @@ struct PlanParams {
   int tiles_dn_shared;
   int xt_gu;             // tokens per gate_up unit
   int xt_dn;             // tokens per down unit
+  int tc_nb_gu;          // tensor-core path: N blocks per expert (0 = no tensor-core plan)
+  int tc_nb_dn;
   int grid;              // CTAs of the persistent expert kernels (<= kMaxGrid)
   // Per stage: [0, grid] first unit of each CTA (entry grid = total units),
   // then [grid + 1, 2 grid + 1) the work expert each CTA starts in.
@@ -117,6 +119,16 @@ cudaError_t launch_down(const LaunchCfg& c, const ExpertArgs& a, const GemvShape
 cudaError_t launch_combine(const LaunchCfg& c, int T, int d, int k, const float* w,
                            const float* y, const float* ys, const float* sg, const uint16_t* x,
                            const uint16_t* w_sg, uint16_t* out);
+
+// Tensor-core grouped GEMMs (prefill): whether the dims qualify, and one
+// stage's launch (down = false: gate_up + SwiGLU into h; true: down into y/ys).
+bool tc_supported(int fmt, int d, int I, int Is, int B);
+cudaError_t launch_tc(const LaunchCfg& c, bool down, const ExpertArgs& e, const uint16_t* x,
+                      const int32_t* sorted_ids, const Plan* plan, const WorkExpert* work,
+                      uint16_t* h, int hs0, int h_rows, float* y, float* ys, int* status,
+                      int grid);
+int tc_tiles_per_mblock_gu(int I);
+int tc_tiles_per_mblock_dn(int d);
 
 // Host-side tile/stage choices for the two GEMV stages.
 GemvShape gate_up_shape(int fmt, int d, int I, int Is, int smem_budget);

@@ -338,10 +338,13 @@ __device__ void split_one(int c, int n_work, const int* s_cost, const int* s_uni
 }
 
 // Per-expert quantities scanned over the experts: padded length, touched
-// flag, gate_up units, down units, and their estimated costs.
-constexpr int kVals = 6;
+// flag, gate_up units, down units, their estimated costs, and (tensor-core
+// path) gate_up and down tiles of 128 rows.
+constexpr int kVals = 8;
+constexpr int kTcRows = 128;
 __device__ __forceinline__ void expert_vals(int c, int B, const PlanParams& pp, int (&v)[kVals]) {
   const int ggu = (c + pp.xt_gu - 1) / pp.xt_gu, gdn = (c + pp.xt_dn - 1) / pp.xt_dn;
+  const int mb = (c + kTcRows - 1) / kTcRows;
   const bool t = c > 0;
   v[0] = (c + B - 1) / B * B;
   v[1] = t ? 1 : 0;
@@ -349,6 +352,8 @@ __device__ __forceinline__ void expert_vals(int c, int B, const PlanParams& pp, 
   v[3] = t ? pp.tiles_dn * gdn : 0;
   v[4] = t ? pp.tiles_gu * (ggu * kUnitBaseCost + c) : 0;
   v[5] = t ? pp.tiles_dn * (gdn * kUnitBaseCost + c) : 0;
+  v[6] = mb * pp.tc_nb_gu;
+  v[7] = mb * pp.tc_nb_dn;
 }
 
 struct AlignOut {
@@ -360,7 +365,7 @@ struct AlignOut {
 
 // Plan totals every thread needs for the split.
 struct PlanTotals {
-  int n_work, units_gu, units_dn, cost_gu, cost_dn, num_post_pad;
+  int n_work, units_gu, units_dn, cost_gu, cost_dn, num_post_pad, tc_gu, tc_dn;
 };
 
 // From per-expert counts cnt[E] (shared memory): one block scan of the
@@ -375,7 +380,7 @@ __device__ PlanTotals layout_and_plan(const int* cnt, int* off, int E, int T, in
                                       int* tmp) {
   const int run = expert_run(E);
   const int e0 = threadIdx.x * run, e1 = min(E, e0 + run);
-  int loc[kVals] = {0, 0, 0, 0, 0, 0};
+  int loc[kVals] = {0, 0, 0, 0, 0, 0, 0, 0};
   for (int e = e0; e < e1; ++e) {
     int v[kVals];
     expert_vals(cnt[e], B, pp, v);
@@ -415,7 +420,9 @@ __device__ PlanTotals layout_and_plan(const int* cnt, int* off, int E, int T, in
       we.pos = off[e];
       we.unit_gu = acc[2];
       we.unit_dn = acc[3];
-      we.pad_[0] = we.pad_[1] = we.pad_[2] = 0;
+      we.pad_[0] = acc[6];  // first tensor-core tile, gate_up
+      we.pad_[1] = acc[7];  // first tensor-core tile, down
+      we.pad_[2] = 0;
       pp.work[idx] = we;
       s_ugu[idx] = acc[2];
       s_udn[idx] = acc[3];
@@ -432,7 +439,7 @@ __device__ PlanTotals layout_and_plan(const int* cnt, int* off, int E, int T, in
     o->expert_offsets[E] = tot[0];
     *o->num_post_pad = tot[0];
   }
-  PlanTotals pt{tot[1], tot[2], tot[3], tot[4], tot[5], tot[0]};
+  PlanTotals pt{tot[1], tot[2], tot[3], tot[4], tot[5], tot[0], tot[6], tot[7]};
   if (pp.work != nullptr && pp.tiles_gu_shared > 0 && T > 0) {
     const int sg = (T + pp.xt_gu - 1) / pp.xt_gu, sd = (T + pp.xt_dn - 1) / pp.xt_dn;
     if (threadIdx.x == 0) {
@@ -442,7 +449,9 @@ __device__ PlanTotals layout_and_plan(const int* cnt, int* off, int E, int T, in
       we.pos = 0;
       we.unit_gu = pt.units_gu;
       we.unit_dn = pt.units_dn;
-      we.pad_[0] = we.pad_[1] = we.pad_[2] = 0;
+      we.pad_[0] = pt.tc_gu;
+      we.pad_[1] = pt.tc_dn;
+      we.pad_[2] = 0;
       pp.work[pt.n_work] = we;
       s_ugu[pt.n_work] = pt.units_gu;
       s_udn[pt.n_work] = pt.units_dn;
@@ -457,6 +466,9 @@ __device__ PlanTotals layout_and_plan(const int* cnt, int* off, int E, int T, in
     pt.units_dn += pp.tiles_dn_shared * sd;
     pt.cost_gu += pp.tiles_gu_shared * (sg * kUnitBaseCost + T);
     pt.cost_dn += pp.tiles_dn_shared * (sd * kUnitBaseCost + T);
+    const int mbs = (T + kTcRows - 1) / kTcRows;
+    pt.tc_gu += mbs * pp.tc_nb_gu;
+    pt.tc_dn += mbs * pp.tc_nb_dn;
   }
   __syncthreads();
   return pt;
@@ -480,7 +492,9 @@ __device__ void split_stages(const PlanTotals& pt, int E, const PlanParams& pp, 
     p.units_gu = pt.units_gu;
     p.units_dn = pt.units_dn;
     p.num_post_pad = pt.num_post_pad;
-    p.pad_[0] = p.pad_[1] = p.pad_[2] = p.pad_[3] = 0;
+    p.pad_[0] = pt.tc_gu;  // tensor-core tiles, gate_up
+    p.pad_[1] = pt.tc_dn;  // tensor-core tiles, down
+    p.pad_[2] = p.pad_[3] = 0;
     *pp.plan = p;
   }
 }

@@ -241,3 +241,33 @@ def test_timed_entry_point_matches_and_records_events():
     assert torch.equal(a, b)
     times = [ev[i].elapsed_time(ev[i + 1]) for i in range(abi.MOE_EV_COUNT - 1)]
     assert all(t >= 0 for t in times)
+
+
+# ----------------------------------------------------------------------------- tensor-core path
+# Dims with T >= 256, 128-row align blocks, I % 128 == 0, d % 256 == 0 and a
+# shared expert of the routed width run the expert stages as grouped tcgen05
+# GEMMs.
+
+
+@pytest.mark.parametrize("over,seed", [
+    ({"T": 256, "d": 256, "E": 4, "k": 2, "I": 128, "Is": 128, "block": 128}, 0),
+    ({"T": 300, "d": 512, "E": 16, "k": 4, "I": 256, "Is": 256, "block": 128}, 1),
+    ({"T": 512, "d": 768, "E": 9, "k": 3, "I": 384, "Is": 0, "block": 128}, 2),
+    ({"T": 257, "d": 256, "E": 64, "k": 8, "I": 128, "Is": 128, "block": 256}, 3),
+])
+def test_tensor_core_path_parity(over, seed):
+    r = layer_parity(I.make_inputs(I.shape("verify_t8", **over), seed))
+    print(f"tc {over}: rel-L2 {r['rel']:.2e} max/rms {r['max']:.2e}")
+
+
+def test_tensor_core_path_one_expert_holds_every_token():
+    s = I.shape("verify_t8", T=384, d=256, E=8, k=1, I=128, Is=128, block=128)
+    inp = I.make_inputs(s, 4)
+    inp["x"] = inp["x"].abs()
+    wr = torch.zeros((s.E, s.d), dtype=torch.bfloat16)
+    wr[5] = 1.0
+    inp["router_w"] = wr
+    layer, out, ids, w = run_layer(inp)
+    assert np.all(ids == 5)
+    ov = oracle.layer(*oracle_args(inp), ids_override=ids)
+    compare_out(bf16_to_f64(out), ov["out"])
