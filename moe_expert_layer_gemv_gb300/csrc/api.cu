@@ -77,6 +77,11 @@ bool tc_dims(const moe_dims_t& dm) {
          dm.I % 128 == 0 && dm.d % 256 == 0 && (dm.I_shared == 0 || dm.I_shared == dm.I);
 }
 
+// Router logits on the tensor cores from the same T up.
+bool use_tc_router(const moe_dims_t& dm) {
+  return dm.T >= kTcMinT && tc_router_supported(dm.T, dm.d, dm.E);
+}
+
 size_t carve(size_t* cursor, size_t bytes) {
   const size_t at = *cursor;
   *cursor += (bytes + kAlign - 1) / kAlign * kAlign;
@@ -304,10 +309,18 @@ moe_status_t layer_forward(const moe_dims_t* dims, const void* x, const void* ro
                            di.sms) != cudaSuccess)
       return MOE_ERR_CUDA;
   } else {
-    if (launch_router_logits(first, static_cast<const uint16_t*>(x),
-                             static_cast<const uint16_t*>(router_w), w_sg, logits, sg, dm.T, dm.d,
-                             dm.E, di.sms, status) != cudaSuccess)
+    if (use_tc_router(dm)) {
+      // The shared-expert gate logit is then computed by the combine kernel.
+      if (launch_tc_router(first, static_cast<const uint16_t*>(x),
+                           static_cast<const uint16_t*>(router_w), logits, dm.T, dm.d, dm.E,
+                           status, di.sms) != cudaSuccess)
+        return MOE_ERR_CUDA;
+      sg = nullptr;
+    } else if (launch_router_logits(first, static_cast<const uint16_t*>(x),
+                                    static_cast<const uint16_t*>(router_w), w_sg, logits, sg,
+                                    dm.T, dm.d, dm.E, di.sms, status) != cudaSuccess) {
       return MOE_ERR_CUDA;
+    }
     if (launch_topk(next, logits, dm.T, dm.E, dm.top_k, dm.renormalize, ids, w, ids_out,
                     w_out) != cudaSuccess)
       return MOE_ERR_CUDA;
@@ -409,10 +422,15 @@ moe_status_t moe_route(const moe_dims_t* dims, const void* x, const void* router
   if (!device_info(&di)) return MOE_ERR_CUDA;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   float* logits = at<float>(workspace, L.logits);
-  if (launch_router_logits(LaunchCfg{st, false}, static_cast<const uint16_t*>(x),
-                           static_cast<const uint16_t*>(router_w), nullptr, logits, nullptr, dm.T,
-                           dm.d, dm.E, di.sms, at<int>(workspace, L.header)) != cudaSuccess)
-    return MOE_ERR_CUDA;
+  const cudaError_t err =
+      use_tc_router(dm)
+          ? launch_tc_router(LaunchCfg{st, false}, static_cast<const uint16_t*>(x),
+                             static_cast<const uint16_t*>(router_w), logits, dm.T, dm.d, dm.E,
+                             at<int>(workspace, L.header), di.sms)
+          : launch_router_logits(LaunchCfg{st, false}, static_cast<const uint16_t*>(x),
+                                 static_cast<const uint16_t*>(router_w), nullptr, logits, nullptr,
+                                 dm.T, dm.d, dm.E, di.sms, at<int>(workspace, L.header));
+  if (err != cudaSuccess) return MOE_ERR_CUDA;
   return cuda_status(launch_topk(LaunchCfg{st, true}, logits, dm.T, dm.E, dm.top_k,
                                  dm.renormalize, topk_ids, topk_weights, nullptr, nullptr));
 }

@@ -1,31 +1,36 @@
-// grouped_tc.cu -- grouped expert GEMMs on the 5th-generation tensor cores for
-// prefill-sized T ("veloGB10", Kernel work: grouped MoE expert kernels for
-// decode *and prefill*; faster prefill MoE expert kernel and a reworked expert
-// schedule).  Two kernels over the moe_align_block_size layout with 128-row
-// blocks:
-//   gate_up_tc: H[p, n] = silu(X[tok(p)] . Wg[e][n]) * (X[tok(p)] . Wu[e][n])
-//   down_tc:    Y[slot(p), :] = H[p] . Wd[e]^T
-// where p runs over the padded sorted positions of expert e and tok(p) is the
-// token of slot sorted_ids[p] (the shared expert is one more "expert" whose
-// rows are the T tokens themselves).
+// grouped_tc.cu -- GEMMs on the 5th-generation tensor cores for prefill-sized T
+// ("veloGB10", Kernel work: grouped MoE expert kernels for decode *and
+// prefill*; faster prefill MoE expert kernel and a reworked expert schedule).
+// One persistent, warp-specialised kernel in three modes:
+//   gate_up: H[p, n] = silu(X[tok(p)] . Wg[e][n]) * (X[tok(p)] . Wu[e][n])
+//   down:    Y[slot(p), :] = H[p] . Wd[e]^T
+//   dense:   L[t, e] = X[t] . Wr[e]            (router logits)
+// where p runs over the padded sorted positions of expert e (moe_align_block_size
+// layout, 128-row blocks) and tok(p) is the token of slot sorted_ids[p]; the
+// shared expert is one more "expert" whose rows are the T tokens themselves.
 //
-// One CTA per SM, persistent, warp-specialised:
-//   warp 0      producer: TMA loads into a 4-stage shared-memory ring.  The A
-//               tile (128 rows x 64 K) is gathered row by row with
-//               cp.async.bulk.tensor ... tile::gather4 (gate_up: rows of x
-//               picked through sorted_ids) or loaded tiled (down: rows of H);
-//               the B tile (256 weight rows x 64 K) is a tiled load.  Both
-//               land 128-byte swizzled, K-major, and complete the stage's
-//               mbarrier by transaction bytes.
-//   warp 1      one thread issues tcgen05.mma (M=128, N=256, K=16, bf16 in,
-//               fp32 accumulate) into one of two TMEM accumulators (2 x 256
-//               columns) and releases each stage with tcgen05.commit.
-//   warps 2-5   epilogue: tcgen05.ld of the accumulator (warp q owns TMEM
-//               lanes 32q..32q+31 = tile rows), SwiGLU -> bf16 H (gate_up) or
-//               fp32 rows scattered to their slots (down).
-// Tiles are (work expert, N block, M block) with the M blocks of one N block
-// consecutive, handed to CTAs round-robin, so the CTAs working on an expert's
-// weight block at the same time share it through L2.
+// One CTA per SM:
+//   warp 0      producer.  B tiles (BN weight rows x 64 K, 128-byte swizzled,
+//               K-major) by tiled TMA; A tiles (128 rows x 64 K) by tiled TMA
+//               (down: rows of H; dense: rows of X) or, for gate_up, gathered
+//               row by row with 16-byte cp.async into the same swizzled layout
+//               (a TMA gather moves only 512 bytes per instruction and its issue
+//               rate, not memory, bounded the whole kernel).  The gathered A of
+//               a stage is published kTcLag stages later, after this warp's
+//               copies of it have completed and been fenced for the tensor core.
+//   warp 1      one thread issues tcgen05.mma (M=128, N=BN, K=16, bf16 in, fp32
+//               accumulate) into one of two TMEM accumulators and releases each
+//               stage with tcgen05.commit.
+//   warps 2-5   epilogue: tcgen05.ld of the accumulator (warp q owns TMEM lanes
+//               32q..32q+31 = tile rows).  gate_up: SwiGLU -> bf16 H rows.
+//               down / dense: fp32 rows go through a per-warp shared-memory
+//               transpose so that 8 lanes store each 128-byte row segment
+//               together (one thread per row would write 16-byte pieces of 32
+//               rows per instruction).
+// gate_up / down tiles are (work expert, N block, M block) with the M blocks of
+// one N block consecutive, handed to CTAs round-robin, so the CTAs working on an
+// expert's weight block at the same time share it through L2.  Dense tiles are
+// (M block, N block) with the N blocks of one M block consecutive.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <cuda_bf16.h>
@@ -38,21 +43,34 @@ namespace moe {
 
 namespace {
 
-constexpr int kTcThreads = 192;       // 6 warps
-constexpr int kTcStages = 4;
-constexpr int kTcBM = 128;            // rows per tile (tcgen05 M)
-constexpr int kTcBN = 256;            // weight rows per tile (tcgen05 N)
-constexpr int kTcBK = 64;             // K per stage: one 128-byte swizzle atom of bf16
-constexpr int kTcAStage = kTcBM * kTcBK * 2;  // 16 KB
-constexpr int kTcBStage = kTcBN * kTcBK * 2;  // 32 KB
-constexpr int kTcStageBytes = kTcAStage + kTcBStage;
-constexpr int kTcTmemCols = 2 * kTcBN;  // two accumulators
-constexpr int kTcSmemBytes = 1024 + kTcStages * kTcStageBytes + 1024;  // barriers + ring + alignment
+enum TcMode { kGateUp = 0, kDown = 1, kDense = 2 };
 
-// Instruction descriptor, kind::f16: D fp32, A and B bf16, both K-major,
-// N >> 3 at bit 17, M >> 4 at bit 24.
-constexpr uint32_t kTcIdesc = (1u << 4) | (1u << 7) | (1u << 10) |
-                              ((uint32_t)(kTcBN >> 3) << 17) | ((uint32_t)(kTcBM >> 4) << 24);
+constexpr int kTcThreads = 192;              // 6 warps
+constexpr int kTcBM = 128;                   // rows per tile (tcgen05 M)
+constexpr int kTcBK = 64;                    // K per stage: one 128-byte swizzle atom of bf16
+constexpr int kTcAStage = kTcBM * kTcBK * 2;  // 16 KB
+constexpr int kTcRingBytes = 192 * 1024;     // stage ring
+constexpr int kTcLag = 2;                    // gathered stages in flight before publication
+constexpr int kTcStgStride = 36;             // floats per row of the epilogue transpose
+constexpr int kTcStgBytes = 4 * 32 * kTcStgStride * 4;
+constexpr int kTcHeadBytes = 1024;           // barriers, TMEM slot, flags
+
+template <int BN>
+struct TcCfg {
+  static_assert(BN % 32 == 0 && BN >= 32 && BN <= 256, "N tile");
+  static constexpr int kBStage = BN * kTcBK * 2;
+  static constexpr int kStageBytes = kTcAStage + kBStage;
+  static constexpr int kStages = kTcRingBytes / kStageBytes > 8 ? 8 : kTcRingBytes / kStageBytes;
+  static constexpr int kTmemCols = 2 * BN;  // two accumulators (a power of two >= 32)
+  static constexpr int kSmemBytes = kTcHeadBytes + kStages * kStageBytes + 1024 + kTcStgBytes;
+  // Instruction descriptor, kind::f16: D fp32, A and B bf16, both K-major,
+  // N >> 3 at bit 17, M >> 4 at bit 24.
+  static constexpr uint32_t kIdesc = (1u << 4) | (1u << 7) | (1u << 10) |
+                                     ((uint32_t)(BN >> 3) << 17) |
+                                     ((uint32_t)(kTcBM >> 4) << 24);
+};
+static_assert(TcCfg<256>::kStages > kTcLag, "the gather lag must leave stages to consume");
+static_assert(TcCfg<256>::kSmemBytes <= 227 * 1024, "shared memory");
 
 // Shared-memory matrix descriptor for a K-major operand stored with the
 // 128-byte swizzle: 8-row groups 1024 bytes apart (stride byte offset), the
@@ -63,12 +81,12 @@ __device__ __forceinline__ uint64_t desc_sw128(uint32_t saddr) {
 }
 
 __device__ __forceinline__ void umma(uint32_t tmem_d, uint64_t adesc, uint64_t bdesc,
-                                     uint32_t accumulate) {
+                                     uint32_t idesc, uint32_t accumulate) {
   asm volatile(
       "{\n\t.reg .pred p;\n\t"
       "setp.ne.b32 p, %4, 0;\n\t"
       "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}\n" ::"r"(tmem_d),
-      "l"(adesc), "l"(bdesc), "r"(kTcIdesc), "r"(accumulate)
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
       : "memory");
 }
 
@@ -112,31 +130,42 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map
       : "memory");
 }
 
-// Four rows (r0..r3) x one box of columns, landing at 4 consecutive 128-byte rows.
-__device__ __forceinline__ void tma_gather4(uint32_t dst, const CUtensorMap* map, int x, int r0,
-                                            int r1, int r2, int r3, uint64_t* bar) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes"
-      " [%0], [%1, {%2, %3, %4, %5, %6}], [%7];" ::"r"(dst),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(r0), "r"(r1), "r"(r2), "r"(r3),
-      "r"(smem_u32(bar))
-      : "memory");
+// 16-byte global -> shared copy; src_bytes 0 writes zeros and reads nothing.
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, uint32_t src_bytes) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src),
+               "r"(src_bytes)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() {
+  asm volatile("cp.async.commit_group;" ::: "memory");
+}
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+// Orders this thread's completed shared-memory writes before later reads of
+// the same bytes by the tensor core (async proxy).
+__device__ __forceinline__ void fence_proxy_async() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
 struct TcArgs {
-  CUtensorMap tm_a;   // gate_up: x [T][d] box {64, 1} (gather4); down: H [rows][I] box {64, 128}
-  CUtensorMap tm_b;   // routed weights: gate_up [E*2I][d] box {64, 128}; down [E*d][I] box {64, 256}
+  CUtensorMap tm_a;   // down: H [rows][I] box {64, 128}; dense: X [T][d] box {64, 128}
+  CUtensorMap tm_b;   // gate_up [E*2I][d] box {64, BN/2}; down [E*d][I] / dense [E][d] box {64, BN}
   CUtensorMap tm_bs;  // shared-expert weights, same boxes (unused without a shared expert)
+  const uint16_t* x;  // gate_up: X [T][d], gathered with cp.async
   const int32_t* sorted_ids;
   const Plan* plan;
   const WorkExpert* work;
   uint16_t* h;        // bf16 [rows][I]: routed rows at their sorted positions, shared at hs0 + t
-  float* y;           // [T*k][d]
-  float* ys;          // [T][d]
+  float* y;           // down: [T*k][d]; dense: logits [T][ld_out]
+  float* ys;          // down: [T][d]
   int* status;
   int T, d, I, k, hs0;
-  int nb;             // N blocks per expert (gate_up: I / 128; down: d / 256)
-  int kb;             // K blocks per tile (gate_up: d / 64; down: I / 64)
+  int nb;             // N blocks per expert (gate_up: I / (BN/2); down: d / BN; dense: E / BN)
+  int kb;             // K blocks per tile (gate_up, dense: d / 64; down: I / 64)
+  int dense_tiles;    // dense: ceil(T / 128) * nb
+  int ld_out;         // dense: row stride of the logits
 };
 
 // Which work expert holds tile t (tiles numbered per the plan, WorkExpert
@@ -149,27 +178,76 @@ __device__ __forceinline__ void tile_seek(const WorkExpert* work, int n_work, in
   }
 }
 
-// kDown = false: gate_up + SwiGLU; true: down.
-template <bool kDown>
+// Tile t of a grouped mode: expert record, N block, M block.
+struct TileIdx {
+  bool shared;
+  int nbk, mb;
+};
+__device__ __forceinline__ TileIdx grouped_tile(const WorkExpert& we, int slot, int t) {
+  TileIdx ti;
+  ti.shared = we.expert < 0;
+  const int mblocks = (we.n_tok + kTcBM - 1) / kTcBM;
+  const int local = t - we.pad_[slot];
+  ti.nbk = local / mblocks;
+  ti.mb = local - ti.nbk * mblocks;
+  return ti;
+}
+
+// fp32 epilogue of one accumulator (down / dense): row `lane` of this warp's
+// 32 rows goes to rowp (nullptr = not stored), columns [0, BN).  Each 32-column
+// slice passes through the warp's transpose buffer so that stores are 128-byte
+// row segments.
+template <int BN>
+__device__ __forceinline__ void store_rows_f32(uint32_t tacc, float* rowp, float* stg, int lane) {
+  const unsigned long long mine = reinterpret_cast<unsigned long long>(rowp);
+  const int sub = lane >> 3, ch = lane & 7;
+#pragma unroll 1
+  for (int c0 = 0; c0 < BN; c0 += 32) {
+    uint32_t v[32];
+    tmem_ld32(tacc + c0, v);
+    tmem_ld_wait();
+#pragma unroll
+    for (int j = 0; j < 8; ++j)
+      *reinterpret_cast<uint4*>(stg + lane * kTcStgStride + 4 * j) =
+          make_uint4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
+    __syncwarp();
+#pragma unroll
+    for (int p = 0; p < 8; ++p) {
+      const int r = 4 * p + sub;
+      float* dst = reinterpret_cast<float*>(__shfl_sync(0xffffffffu, mine, r));
+      const uint4 val = *reinterpret_cast<const uint4*>(stg + r * kTcStgStride + 4 * ch);
+      if (dst != nullptr) *reinterpret_cast<uint4*>(dst + c0 + 4 * ch) = val;
+    }
+    __syncwarp();
+  }
+}
+
+template <int kMode, int BN>
 __global__ void __launch_bounds__(kTcThreads, 1) grouped_tc_kernel(const __grid_constant__ TcArgs a) {
+  using Cfg = TcCfg<BN>;
+  constexpr int NS = Cfg::kStages;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
-  // Barriers and the TMEM slot first; the ring starts at the next 1 KB boundary.
+  // Head (barriers, TMEM slot, flags), then the ring at the next 1 KB boundary,
+  // then the epilogue transpose buffers.
   uint64_t* full = reinterpret_cast<uint64_t*>(smem_raw);
-  uint64_t* empty = full + kTcStages;
-  uint64_t* acc_full = empty + kTcStages;
+  uint64_t* empty = full + NS;
+  uint64_t* acc_full = empty + NS;
   uint64_t* acc_empty = acc_full + 2;
   uint64_t* drain = acc_empty + 2;  // used only after an abort
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   volatile int* n_issued = abort_flag + 1;    // stages filled by the producer
   volatile int* n_consumed = abort_flag + 2;  // stages whose full barrier the MMA thread saw
-  const uint32_t ring = (smem_u32(smem_raw) + 1024 + 1023) & ~1023u;
+  const uint32_t ring = (smem_u32(smem_raw) + kTcHeadBytes + 1023) & ~1023u;
+  float* stg_all = reinterpret_cast<float*>(smem_raw + (ring - smem_u32(smem_raw)) +
+                                            NS * Cfg::kStageBytes);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int slot = kDown ? 1 : 0;  // WorkExpert pad_ field with the first tile
+  const int slot = kMode == kDown ? 1 : 0;  // WorkExpert pad_ field with the first tile
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < kTcStages; ++s) {
-      mbar_init(&full[s], 1);
+    for (int s = 0; s < NS; ++s) {
+      // gate_up: one arrival with the B bytes at issue, one when the gathered A is published.
+      mbar_init(&full[s], kMode == kGateUp ? 2 : 1);
       mbar_init(&empty[s], 1);
     }
     for (int c = 0; c < 2; ++c) {
@@ -185,7 +263,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) grouped_tc_kernel(const __grid_
   if (warp == 1) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
                      smem_u32(tmem_slot)),
-                 "r"(kTcTmemCols)
+                 "r"(Cfg::kTmemCols)
                  : "memory");
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
   }
@@ -196,40 +274,54 @@ __global__ void __launch_bounds__(kTcThreads, 1) grouped_tc_kernel(const __grid_
   pdl_wait();
   pdl_trigger();
 
-  const Plan plan = *a.plan;
-  const int n_tiles = kDown ? plan.pad_[1] : plan.pad_[0];
+  Plan plan;
+  int n_tiles;
+  if (kMode == kDense) {
+    plan.n_work = 0;
+    n_tiles = a.dense_tiles;
+  } else {
+    plan = *a.plan;
+    n_tiles = kMode == kDown ? plan.pad_[1] : plan.pad_[0];
+  }
   const int S = a.T * a.k;
 
   if (warp == 0) {
     // -------------------------------------------------------------- producer
     int i = 0;
-    WorkExpert we = a.work[0];
-    int it = 0;
-    bool ok = true;
-    for (int t = blockIdx.x; t < n_tiles && ok; t += gridDim.x) {
-      tile_seek(a.work, plan.n_work, slot, t, i, we);
-      const bool shared = we.expert < 0;
-      const int mblocks = (we.n_tok + kTcBM - 1) / kTcBM;
-      const int local = t - we.pad_[slot];
-      const int nbk = local / mblocks, mb = local - nbk * mblocks;
-      const int row0 = shared ? (kDown ? a.hs0 : 0) + mb * kTcBM : we.pos + mb * kTcBM;
-      // gate_up: the tokens of this lane's 4 rows (pads and rows past T read token 0).
-      int tok[4] = {0, 0, 0, 0};
-      if (!kDown) {
+    WorkExpert we;
+    if (kMode != kDense) we = a.work[0];
+    int it = 0, published = 0;
+    const int sub = lane >> 3, ch = lane & 7;  // gather: row sub + 4 j, 16-byte chunk ch
+    for (int t = blockIdx.x; t < n_tiles; t += gridDim.x) {
+      TileIdx ti;
+      if (kMode == kDense) {
+        ti.shared = false;
+        ti.mb = t / a.nb;
+        ti.nbk = t - ti.mb * a.nb;
+      } else {
+        tile_seek(a.work, plan.n_work, slot, t, i, we);
+        ti = grouped_tile(we, slot, t);
+      }
+      // gate_up: element offsets of this lane's 32 source rows in X (-1: pad, zero-filled).
+      int roff[32];
+      if (kMode == kGateUp) {
 #pragma unroll
-        for (int r = 0; r < 4; ++r) {
-          const int m = mb * kTcBM + lane * 4 + r;  // row within the expert
-          if (shared) {
-            tok[r] = m < a.T ? m : 0;
+        for (int j = 0; j < 32; ++j) {
+          const int m = ti.mb * kTcBM + 4 * j + sub;  // row within the expert
+          int tok = -1;
+          if (ti.shared) {
+            if (m < a.T) tok = m;
           } else if (m < we.n_tok) {
             const int sl = a.sorted_ids[we.pos + m];
-            tok[r] = (sl >= 0 && sl < S) ? sl / a.k : 0;
+            if (sl >= 0 && sl < S) tok = sl / a.k;
           }
+          roff[j] = tok < 0 ? -1 : tok * a.d;
         }
       }
-      const CUtensorMap* tb = shared ? &a.tm_bs : &a.tm_b;
+      const CUtensorMap* tb = ti.shared ? &a.tm_bs : &a.tm_b;
+      bool ok = true;
       for (int kb = 0; kb < a.kb; ++kb, ++it) {
-        const int s = it % kTcStages, use = it / kTcStages;
+        const int s = it % NS, use = it / NS;
         if (lane == 0 && use > 0 &&
             !mbar_wait(&empty[s], (uint32_t)((use - 1) & 1), a.status)) {
           *abort_flag = 1;
@@ -239,26 +331,54 @@ __global__ void __launch_bounds__(kTcThreads, 1) grouped_tc_kernel(const __grid_
           ok = false;
           break;
         }
-        const uint32_t sa = ring + s * kTcStageBytes, sb = sa + kTcAStage;
-        if (lane == 0) mbar_arrive_expect_tx(&full[s], kTcStageBytes);
-        __syncwarp();
+        const uint32_t sa = ring + s * Cfg::kStageBytes, sb = sa + kTcAStage;
         const int kx = kb * kTcBK;
-        if (kDown) {
-          if (lane == 0) tma_load_2d(sa, &a.tm_a, kx, row0, &full[s]);
-          if (lane == 1) {
-            const int wrow = (shared ? 0 : we.expert * a.d) + nbk * kTcBN;
-            tma_load_2d(sb, tb, kx, wrow, &full[s]);
+        if (lane == 0) {
+          mbar_arrive_expect_tx(&full[s], kMode == kGateUp ? Cfg::kBStage : Cfg::kStageBytes);
+          if (kMode == kGateUp) {
+            const int base = ti.shared ? 0 : we.expert * 2 * a.I;
+            tma_load_2d(sb, tb, kx, base + ti.nbk * (BN / 2), &full[s]);
+            tma_load_2d(sb + Cfg::kBStage / 2, tb, kx, base + a.I + ti.nbk * (BN / 2), &full[s]);
+          } else if (kMode == kDown) {
+            const int row0 = (ti.shared ? a.hs0 : we.pos) + ti.mb * kTcBM;
+            tma_load_2d(sa, &a.tm_a, kx, row0, &full[s]);
+            tma_load_2d(sb, tb, kx, (ti.shared ? 0 : we.expert * a.d) + ti.nbk * BN, &full[s]);
+          } else {
+            tma_load_2d(sa, &a.tm_a, kx, ti.mb * kTcBM, &full[s]);
+            tma_load_2d(sb, tb, kx, ti.nbk * BN, &full[s]);
           }
-        } else {
-          tma_gather4(sa + lane * 4 * 128, &a.tm_a, kx, tok[0], tok[1], tok[2], tok[3], &full[s]);
-          if (lane == 0) {
-            const int base = shared ? 0 : we.expert * 2 * a.I;
-            tma_load_2d(sb, tb, kx, base + nbk * (kTcBN / 2), &full[s]);
-            tma_load_2d(sb + kTcBStage / 2, tb, kx, base + a.I + nbk * (kTcBN / 2), &full[s]);
+        }
+        if (kMode == kGateUp) {
+          // Row r of the tile lands at r * 128 with its 16-byte chunks permuted
+          // by r mod 8: the layout a 128-byte-swizzled TMA box would produce.
+#pragma unroll
+          for (int j = 0; j < 32; ++j) {
+            const int r = 4 * j + sub;
+            const uint32_t dst = sa + r * 128 + ((ch ^ (r & 7)) << 4);
+            const uint16_t* src = a.x + (roff[j] < 0 ? 0 : roff[j] + kx + 8 * ch);
+            cp_async16(dst, src, roff[j] < 0 ? 0u : 16u);
+          }
+          cp_async_commit();
+          if (it + 1 - published > kTcLag) {
+            cp_async_wait<kTcLag>();
+            fence_proxy_async();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&full[published % NS]);
+            ++published;
           }
         }
         if (lane == 0) *n_issued = it + 1;
       }
+      if (!ok) break;
+    }
+    if (kMode == kGateUp) {
+      // Publish the gathered stages still held back (also after an abort, so
+      // that the teardown below can wait for every issued stage).
+      cp_async_wait<0>();
+      fence_proxy_async();
+      __syncwarp();
+      if (lane == 0)
+        for (; published < it; ++published) mbar_arrive(&full[published % NS]);
     }
   } else if (warp == 1) {
     // -------------------------------------------------------------- MMA issuer
@@ -271,10 +391,10 @@ __global__ void __launch_bounds__(kTcThreads, 1) grouped_tc_kernel(const __grid_
         }
         if (*abort_flag) break;
         tc_fence_after();
-        const uint32_t dtm = tmem_base + acc * kTcBN;
+        const uint32_t dtm = tmem_base + acc * BN;
         bool ok = true;
         for (int kb = 0; kb < a.kb; ++kb, ++it) {
-          const int s = it % kTcStages, use = it / kTcStages;
+          const int s = it % NS, use = it / NS;
           if (!mbar_wait(&full[s], (uint32_t)(use & 1), a.status)) {
             *abort_flag = 1;
             ok = false;
@@ -282,10 +402,10 @@ __global__ void __launch_bounds__(kTcThreads, 1) grouped_tc_kernel(const __grid_
           }
           *n_consumed = it + 1;
           tc_fence_after();
-          const uint32_t sa = ring + s * kTcStageBytes, sb = sa + kTcAStage;
+          const uint32_t sa = ring + s * Cfg::kStageBytes, sb = sa + kTcAStage;
 #pragma unroll
           for (int kk = 0; kk < kTcBK / 16; ++kk)
-            umma(dtm, desc_sw128(sa + kk * 32), desc_sw128(sb + kk * 32),
+            umma(dtm, desc_sw128(sa + kk * 32), desc_sw128(sb + kk * 32), Cfg::kIdesc,
                  (kb > 0 || kk > 0) ? 1u : 0u);
           umma_commit(&empty[s]);  // the stage is free once these MMAs have read it
         }
@@ -297,34 +417,38 @@ __global__ void __launch_bounds__(kTcThreads, 1) grouped_tc_kernel(const __grid_
   } else {
     // -------------------------------------------------------------- epilogue
     const int q = warp & 3;  // TMEM lane quarter this warp may access
+    float* stg = stg_all + q * 32 * kTcStgStride;
     int i = 0;
-    WorkExpert we = a.work[0];
+    WorkExpert we;
+    if (kMode != kDense) we = a.work[0];
     int j = 0;
     for (int t = blockIdx.x; t < n_tiles; t += gridDim.x, ++j) {
-      tile_seek(a.work, plan.n_work, slot, t, i, we);
-      const bool shared = we.expert < 0;
-      const int mblocks = (we.n_tok + kTcBM - 1) / kTcBM;
-      const int local = t - we.pad_[slot];
-      const int nbk = local / mblocks, mb = local - nbk * mblocks;
+      TileIdx ti;
+      if (kMode == kDense) {
+        ti.shared = false;
+        ti.mb = t / a.nb;
+        ti.nbk = t - ti.mb * a.nb;
+      } else {
+        tile_seek(a.work, plan.n_work, slot, t, i, we);
+        ti = grouped_tile(we, slot, t);
+      }
       const int acc = j & 1;
-      bool ok = true;
       if (lane == 0 && !mbar_wait(&acc_full[acc], (uint32_t)((j >> 1) & 1), a.status)) {
         *abort_flag = 1;
       }
       __syncwarp();
-      if (*abort_flag) ok = false;
-      if (!ok) break;
+      if (*abort_flag) break;
       tc_fence_after();
-      const int m = mb * kTcBM + q * 32 + lane;  // this thread's row within the expert
-      const uint32_t tacc = tmem_base + acc * kTcBN + ((uint32_t)(q * 32) << 16);
-      if (!kDown) {
-        const int hrow = shared ? a.hs0 + m : we.pos + m;
-        uint16_t* hp = a.h + (size_t)hrow * a.I + nbk * (kTcBN / 2);
+      const int m = ti.mb * kTcBM + q * 32 + lane;  // this thread's row within the expert
+      const uint32_t tacc = tmem_base + acc * BN + ((uint32_t)(q * 32) << 16);
+      if (kMode == kGateUp) {
+        const int hrow = ti.shared ? a.hs0 + m : we.pos + m;
+        uint16_t* hp = a.h + (size_t)hrow * a.I + ti.nbk * (BN / 2);
 #pragma unroll 1
-        for (int c0 = 0; c0 < kTcBN / 2; c0 += 32) {
+        for (int c0 = 0; c0 < BN / 2; c0 += 32) {
           uint32_t g[32], u[32];
           tmem_ld32(tacc + c0, g);
-          tmem_ld32(tacc + kTcBN / 2 + c0, u);
+          tmem_ld32(tacc + BN / 2 + c0, u);
           tmem_ld_wait();
           uint32_t packed[16];
 #pragma unroll
@@ -340,25 +464,16 @@ __global__ void __launch_bounds__(kTcThreads, 1) grouped_tc_kernel(const __grid_
             dst[c] = make_uint4(packed[4 * c], packed[4 * c + 1], packed[4 * c + 2], packed[4 * c + 3]);
         }
       } else {
-        float* yp = nullptr;
-        if (shared) {
-          if (m < a.T) yp = a.ys + (size_t)m * a.d + nbk * kTcBN;
+        float* rowp = nullptr;
+        if (kMode == kDense) {
+          if (m < a.T) rowp = a.y + (size_t)m * a.ld_out + ti.nbk * BN;
+        } else if (ti.shared) {
+          if (m < a.T) rowp = a.ys + (size_t)m * a.d + ti.nbk * BN;
         } else if (m < we.n_tok) {
           const int sl = a.sorted_ids[we.pos + m];
-          if (sl >= 0 && sl < S) yp = a.y + (size_t)sl * a.d + nbk * kTcBN;
+          if (sl >= 0 && sl < S) rowp = a.y + (size_t)sl * a.d + ti.nbk * BN;
         }
-#pragma unroll 1
-        for (int c0 = 0; c0 < kTcBN; c0 += 32) {
-          uint32_t v[32];
-          tmem_ld32(tacc + c0, v);
-          tmem_ld_wait();
-          if (yp != nullptr) {
-            uint4* dst = reinterpret_cast<uint4*>(yp + c0);
-#pragma unroll
-            for (int c = 0; c < 8; ++c)
-              dst[c] = make_uint4(v[4 * c], v[4 * c + 1], v[4 * c + 2], v[4 * c + 3]);
-          }
-        }
+        store_rows_f32<BN>(tacc, rowp, stg, lane);
       }
       tc_fence_before();
       __syncwarp();
@@ -375,7 +490,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) grouped_tc_kernel(const __grid_
   if (*abort_flag) {
     if (warp == 0 && lane == 0) {
       for (int it = *n_consumed; it < *n_issued; ++it)
-        mbar_wait(&full[it % kTcStages], (uint32_t)((it / kTcStages) & 1), nullptr);
+        mbar_wait(&full[it % NS], (uint32_t)((it / NS) & 1), nullptr);
     }
     if (warp == 1 && lane == 0) {
       umma_commit(drain);
@@ -387,7 +502,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) grouped_tc_kernel(const __grid_
   tc_fence_after();
   if (warp == 1)
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base),
-                 "r"(kTcTmemCols)
+                 "r"(Cfg::kTmemCols)
                  : "memory");
 }
 
@@ -406,7 +521,7 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 }
 
 // 2D bf16 tensor map over [rows][cols] (row-major), box {64 cols, box_rows},
-// 128-byte swizzle.
+// 128-byte swizzle; reads past the last row return zeros.
 bool make_map(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols, uint32_t box_rows) {
   PFN_cuTensorMapEncodeTiled_v12000 fn = encode_fn();
   if (fn == nullptr) return false;
@@ -419,35 +534,54 @@ bool make_map(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols, ui
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+constexpr int kTcBNExpert = 256;  // N tile of the expert GEMMs
+constexpr int kTcBNRouter = 64;   // N tile of the router GEMM (E / 64 tiles per M block)
+
+template <int kMode, int BN>
+cudaError_t launch_mode(const LaunchCfg& c, TcArgs& a, int grid) {
+  const void* fn = (const void*)grouped_tc_kernel<kMode, BN>;
+  cudaError_t err = ensure_smem(fn, TcCfg<BN>::kSmemBytes);
+  if (err != cudaSuccess) return err;
+  void* args[] = {&a};
+  return launch_kernel(c, fn, dim3(grid), dim3(kTcThreads), TcCfg<BN>::kSmemBytes, args);
+}
+
 }  // namespace
 
 bool tc_supported(int fmt, int d, int I, int Is, int B) {
-  return fmt == 0 && B % kTcBM == 0 && I % (kTcBN / 2) == 0 && d % kTcBN == 0 &&
+  return fmt == 0 && B % kTcBM == 0 && I % (kTcBNExpert / 2) == 0 && d % kTcBNExpert == 0 &&
          (Is == 0 || Is == I) && encode_fn() != nullptr;
+}
+
+bool tc_router_supported(int T, int d, int E) {
+  return E % kTcBNRouter == 0 && d % kTcBK == 0 && (int64_t)T * d < (1ll << 31) &&
+         encode_fn() != nullptr;
 }
 
 cudaError_t launch_tc(const LaunchCfg& c, bool down, const ExpertArgs& e, const uint16_t* x,
                       const int32_t* sorted_ids, const Plan* plan, const WorkExpert* work,
                       uint16_t* h, int hs0, int h_rows, float* y, float* ys, int* status,
                       int grid) {
+  constexpr int BN = kTcBNExpert;
   TcArgs a;
   memset(&a, 0, sizeof(a));
   bool ok;
   if (!down) {
-    ok = make_map(&a.tm_a, x, (uint64_t)e.T, (uint64_t)e.d, 1) &&
-         make_map(&a.tm_b, e.gate_up, (uint64_t)e.E * 2 * e.I, (uint64_t)e.d, kTcBN / 2) &&
+    if ((int64_t)e.T * e.d >= (1ll << 31)) return cudaErrorInvalidValue;
+    ok = make_map(&a.tm_b, e.gate_up, (uint64_t)e.E * 2 * e.I, (uint64_t)e.d, BN / 2) &&
          (e.s_gate_up == nullptr ||
-          make_map(&a.tm_bs, e.s_gate_up, 2ull * e.Is, (uint64_t)e.d, kTcBN / 2));
-    a.nb = e.I / (kTcBN / 2);
+          make_map(&a.tm_bs, e.s_gate_up, 2ull * e.Is, (uint64_t)e.d, BN / 2));
+    a.nb = e.I / (BN / 2);
     a.kb = e.d / kTcBK;
   } else {
     ok = make_map(&a.tm_a, h, (uint64_t)h_rows, (uint64_t)e.I, kTcBM) &&
-         make_map(&a.tm_b, e.down, (uint64_t)e.E * e.d, (uint64_t)e.I, kTcBN) &&
-         (e.s_down == nullptr || make_map(&a.tm_bs, e.s_down, (uint64_t)e.d, (uint64_t)e.Is, kTcBN));
-    a.nb = e.d / kTcBN;
+         make_map(&a.tm_b, e.down, (uint64_t)e.E * e.d, (uint64_t)e.I, BN) &&
+         (e.s_down == nullptr || make_map(&a.tm_bs, e.s_down, (uint64_t)e.d, (uint64_t)e.Is, BN));
+    a.nb = e.d / BN;
     a.kb = e.I / kTcBK;
   }
   if (!ok) return cudaErrorInvalidValue;
+  a.x = x;
   a.sorted_ids = sorted_ids;
   a.plan = plan;
   a.work = work;
@@ -460,14 +594,31 @@ cudaError_t launch_tc(const LaunchCfg& c, bool down, const ExpertArgs& e, const 
   a.I = e.I;
   a.k = e.k;
   a.hs0 = hs0;
-  const void* fn = down ? (const void*)grouped_tc_kernel<true> : (const void*)grouped_tc_kernel<false>;
-  cudaError_t err = ensure_smem(fn, kTcSmemBytes);
-  if (err != cudaSuccess) return err;
-  void* args[] = {&a};
-  return launch_kernel(c, fn, dim3(grid), dim3(kTcThreads), kTcSmemBytes, args);
+  return down ? launch_mode<kDown, BN>(c, a, grid) : launch_mode<kGateUp, BN>(c, a, grid);
 }
 
-int tc_tiles_per_mblock_gu(int I) { return I / (kTcBN / 2); }
-int tc_tiles_per_mblock_dn(int d) { return d / kTcBN; }
+cudaError_t launch_tc_router(const LaunchCfg& c, const uint16_t* x, const uint16_t* wr,
+                             float* logits, int T, int d, int E, int* status, int sms) {
+  constexpr int BN = kTcBNRouter;
+  TcArgs a;
+  memset(&a, 0, sizeof(a));
+  if (!make_map(&a.tm_a, x, (uint64_t)T, (uint64_t)d, kTcBM) ||
+      !make_map(&a.tm_b, wr, (uint64_t)E, (uint64_t)d, BN))
+    return cudaErrorInvalidValue;
+  a.y = logits;
+  a.status = status;
+  a.T = T;
+  a.d = d;
+  a.k = 1;
+  a.nb = E / BN;
+  a.kb = d / kTcBK;
+  a.dense_tiles = (int)ceil_div(T, kTcBM) * a.nb;
+  a.ld_out = E;
+  const int grid = a.dense_tiles < sms ? a.dense_tiles : sms;
+  return launch_mode<kDense, BN>(c, a, grid);
+}
+
+int tc_tiles_per_mblock_gu(int I) { return I / (kTcBNExpert / 2); }
+int tc_tiles_per_mblock_dn(int d) { return d / kTcBNExpert; }
 
 }  // namespace moe

@@ -127,6 +127,12 @@ cudaError_t launch_tc(const LaunchCfg& c, bool down, const ExpertArgs& e, const 
                       const int32_t* sorted_ids, const Plan* plan, const WorkExpert* work,
                       uint16_t* h, int hs0, int h_rows, float* y, float* ys, int* status,
                       int grid);
+// Router logits on the tensor cores: logits[t][e] = x[t] . wr[e] (fp32
+// accumulate), for E % 64 == 0, d % 64 == 0, T * d < 2^31.
+bool tc_router_supported(int T, int d, int E);
+cudaError_t launch_tc_router(const LaunchCfg& c, const uint16_t* x, const uint16_t* wr,
+                             float* logits, int T, int d, int E, int* status, int sms);
+
 int tc_tiles_per_mblock_gu(int I);
 int tc_tiles_per_mblock_dn(int d);
 
