@@ -9,15 +9,19 @@
 // layout, 128-row blocks) and tok(p) is the token of slot sorted_ids[p]; the
 // shared expert is one more "expert" whose rows are the T tokens themselves.
 //
-// One CTA per SM:
-//   warp 0      producer.  B tiles (BN weight rows x 64 K, 128-byte swizzled,
-//               K-major) by tiled TMA; A tiles (128 rows x 64 K) by tiled TMA
-//               (down: rows of H; dense: rows of X) or, for gate_up, gathered
-//               row by row with 16-byte cp.async into the same swizzled layout
-//               (a TMA gather moves only 512 bytes per instruction and its issue
-//               rate, not memory, bounded the whole kernel).  The gathered A of
-//               a stage is published kTcLag stages later, after this warp's
-//               copies of it have completed and been fenced for the tensor core.
+// One CTA per SM, 8 warps:
+//   warp 0      B producer: weight tiles (BN rows x 64 K, 128-byte swizzled,
+//               K-major) by tiled TMA, completing the stage's B barrier by
+//               transaction bytes.
+//   warps 6-7   A producers: the 128 rows x 64 K activation tile (gate_up: rows
+//               of X picked through sorted_ids; down: rows of H; dense: rows of
+//               X) with 16-byte cp.async into the same swizzled layout, half the
+//               rows each.  A stage's A is published kTcLag stages later, after
+//               the warp's copies of it have completed and been fenced for the
+//               tensor core.  (A TMA gather moves only 512 bytes per
+//               instruction, and one warp issuing both operands stalls each on
+//               the other: the memory pipes of the LSU and the TMA unit run in
+//               parallel only when different warps feed them.)
 //   warp 1      one thread issues tcgen05.mma (M=128, N=BN, K=16, bf16 in, fp32
 //               accumulate) into one of two TMEM accumulators and releases each
 //               stage with tcgen05.commit.
@@ -45,8 +49,11 @@ namespace {
 
 enum TcMode { kGateUp = 0, kDown = 1, kDense = 2 };
 
-constexpr int kTcThreads = 192;              // 6 warps
 constexpr int kTcBM = 128;                   // rows per tile (tcgen05 M)
+constexpr int kTcGatherWarps = 2;            // A producers
+constexpr int kTcGatherWarp0 = 6;            // first A producer warp
+constexpr int kTcThreads = 32 * (kTcGatherWarp0 + kTcGatherWarps);
+constexpr int kTcRowsPerLane = kTcBM / 4 / kTcGatherWarps;  // A rows one lane copies per stage
 constexpr int kTcBK = 64;                    // K per stage: one 128-byte swizzle atom of bf16
 constexpr int kTcAStage = kTcBM * kTcBK * 2;  // 16 KB
 constexpr int kTcRingBytes = 192 * 1024;     // stage ring
@@ -150,14 +157,13 @@ __device__ __forceinline__ void fence_proxy_async() {
 }
 
 struct TcArgs {
-  CUtensorMap tm_a;   // down: H [rows][I] box {64, 128}; dense: X [T][d] box {64, 128}
   CUtensorMap tm_b;   // gate_up [E*2I][d] box {64, BN/2}; down [E*d][I] / dense [E][d] box {64, BN}
   CUtensorMap tm_bs;  // shared-expert weights, same boxes (unused without a shared expert)
-  const uint16_t* x;  // gate_up: X [T][d], gathered with cp.async
+  const uint16_t* x;  // X [T][d] (gate_up, dense)
   const int32_t* sorted_ids;
   const Plan* plan;
   const WorkExpert* work;
-  uint16_t* h;        // bf16 [rows][I]: routed rows at their sorted positions, shared at hs0 + t
+  uint16_t* h;        // bf16 [h_rows][I]: routed rows at their sorted positions, shared at hs0 + t
   float* y;           // down: [T*k][d]; dense: logits [T][ld_out]
   float* ys;          // down: [T][d]
   int* status;
@@ -191,6 +197,13 @@ __device__ __forceinline__ TileIdx grouped_tile(const WorkExpert& we, int slot, 
   ti.nbk = local / mblocks;
   ti.mb = local - ti.nbk * mblocks;
   return ti;
+}
+
+// silu(g) * u with the fast exponential and division intrinsics (a few ulp of
+// fp32; the result is rounded to bf16).  For g -> -inf the divisor overflows
+// and the quotient is 0, the limit of silu.
+__device__ __forceinline__ float swiglu_fast(float g, float u) {
+  return __fdividef(g * u, 1.0f + __expf(-g));
 }
 
 // fp32 epilogue of one accumulator (down / dense): row `lane` of this warp's
@@ -229,15 +242,16 @@ __global__ void __launch_bounds__(kTcThreads, 1) grouped_tc_kernel(const __grid_
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   // Head (barriers, TMEM slot, flags), then the ring at the next 1 KB boundary,
   // then the epilogue transpose buffers.
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem_raw);
-  uint64_t* empty = full + NS;
+  uint64_t* full_b = reinterpret_cast<uint64_t*>(smem_raw);  // B landed (transaction bytes)
+  uint64_t* full_a = full_b + NS;                             // A published by every A producer
+  uint64_t* empty = full_a + NS;
   uint64_t* acc_full = empty + NS;
   uint64_t* acc_empty = acc_full + 2;
   uint64_t* drain = acc_empty + 2;  // used only after an abort
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
-  volatile int* n_issued = abort_flag + 1;    // stages filled by the producer
-  volatile int* n_consumed = abort_flag + 2;  // stages whose full barrier the MMA thread saw
+  volatile int* n_issued = abort_flag + 1;    // stages whose B copy warp 0 issued
+  volatile int* n_consumed = abort_flag + 2;  // stages whose barriers the MMA thread saw
   const uint32_t ring = (smem_u32(smem_raw) + kTcHeadBytes + 1023) & ~1023u;
   float* stg_all = reinterpret_cast<float*>(smem_raw + (ring - smem_u32(smem_raw)) +
                                             NS * Cfg::kStageBytes);
@@ -246,8 +260,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) grouped_tc_kernel(const __grid_
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < NS; ++s) {
-      // gate_up: one arrival with the B bytes at issue, one when the gathered A is published.
-      mbar_init(&full[s], kMode == kGateUp ? 2 : 1);
+      mbar_init(&full_b[s], 1);
+      mbar_init(&full_a[s], kTcGatherWarps);
       mbar_init(&empty[s], 1);
     }
     for (int c = 0; c < 2; ++c) {
@@ -286,13 +300,13 @@ __global__ void __launch_bounds__(kTcThreads, 1) grouped_tc_kernel(const __grid_
   const int S = a.T * a.k;
 
   if (warp == 0) {
-    // -------------------------------------------------------------- producer
+    // ------------------------------------------------------------ B producer
     int i = 0;
     WorkExpert we;
     if (kMode != kDense) we = a.work[0];
-    int it = 0, published = 0;
-    const int sub = lane >> 3, ch = lane & 7;  // gather: row sub + 4 j, 16-byte chunk ch
-    for (int t = blockIdx.x; t < n_tiles; t += gridDim.x) {
+    int it = 0;
+    bool ok = true;
+    for (int t = blockIdx.x; t < n_tiles && ok; t += gridDim.x) {
       TileIdx ti;
       if (kMode == kDense) {
         ti.shared = false;
@@ -302,24 +316,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) grouped_tc_kernel(const __grid_
         tile_seek(a.work, plan.n_work, slot, t, i, we);
         ti = grouped_tile(we, slot, t);
       }
-      // gate_up: element offsets of this lane's 32 source rows in X (-1: pad, zero-filled).
-      int roff[32];
-      if (kMode == kGateUp) {
-#pragma unroll
-        for (int j = 0; j < 32; ++j) {
-          const int m = ti.mb * kTcBM + 4 * j + sub;  // row within the expert
-          int tok = -1;
-          if (ti.shared) {
-            if (m < a.T) tok = m;
-          } else if (m < we.n_tok) {
-            const int sl = a.sorted_ids[we.pos + m];
-            if (sl >= 0 && sl < S) tok = sl / a.k;
-          }
-          roff[j] = tok < 0 ? -1 : tok * a.d;
-        }
-      }
       const CUtensorMap* tb = ti.shared ? &a.tm_bs : &a.tm_b;
-      bool ok = true;
       for (int kb = 0; kb < a.kb; ++kb, ++it) {
         const int s = it % NS, use = it / NS;
         if (lane == 0 && use > 0 &&
@@ -331,55 +328,98 @@ __global__ void __launch_bounds__(kTcThreads, 1) grouped_tc_kernel(const __grid_
           ok = false;
           break;
         }
-        const uint32_t sa = ring + s * Cfg::kStageBytes, sb = sa + kTcAStage;
-        const int kx = kb * kTcBK;
         if (lane == 0) {
-          mbar_arrive_expect_tx(&full[s], kMode == kGateUp ? Cfg::kBStage : Cfg::kStageBytes);
+          const uint32_t sb = ring + s * Cfg::kStageBytes + kTcAStage;
+          const int kx = kb * kTcBK;
+          mbar_arrive_expect_tx(&full_b[s], Cfg::kBStage);
           if (kMode == kGateUp) {
             const int base = ti.shared ? 0 : we.expert * 2 * a.I;
-            tma_load_2d(sb, tb, kx, base + ti.nbk * (BN / 2), &full[s]);
-            tma_load_2d(sb + Cfg::kBStage / 2, tb, kx, base + a.I + ti.nbk * (BN / 2), &full[s]);
+            tma_load_2d(sb, tb, kx, base + ti.nbk * (BN / 2), &full_b[s]);
+            tma_load_2d(sb + Cfg::kBStage / 2, tb, kx, base + a.I + ti.nbk * (BN / 2), &full_b[s]);
           } else if (kMode == kDown) {
-            const int row0 = (ti.shared ? a.hs0 : we.pos) + ti.mb * kTcBM;
-            tma_load_2d(sa, &a.tm_a, kx, row0, &full[s]);
-            tma_load_2d(sb, tb, kx, (ti.shared ? 0 : we.expert * a.d) + ti.nbk * BN, &full[s]);
+            tma_load_2d(sb, tb, kx, (ti.shared ? 0 : we.expert * a.d) + ti.nbk * BN, &full_b[s]);
           } else {
-            tma_load_2d(sa, &a.tm_a, kx, ti.mb * kTcBM, &full[s]);
-            tma_load_2d(sb, tb, kx, ti.nbk * BN, &full[s]);
+            tma_load_2d(sb, tb, kx, ti.nbk * BN, &full_b[s]);
           }
+          *n_issued = it + 1;
         }
-        if (kMode == kGateUp) {
-          // Row r of the tile lands at r * 128 with its 16-byte chunks permuted
-          // by r mod 8: the layout a 128-byte-swizzled TMA box would produce.
-#pragma unroll
-          for (int j = 0; j < 32; ++j) {
-            const int r = 4 * j + sub;
-            const uint32_t dst = sa + r * 128 + ((ch ^ (r & 7)) << 4);
-            const uint16_t* src = a.x + (roff[j] < 0 ? 0 : roff[j] + kx + 8 * ch);
-            cp_async16(dst, src, roff[j] < 0 ? 0u : 16u);
-          }
-          cp_async_commit();
-          if (it + 1 - published > kTcLag) {
-            cp_async_wait<kTcLag>();
-            fence_proxy_async();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&full[published % NS]);
-            ++published;
-          }
-        }
-        if (lane == 0) *n_issued = it + 1;
       }
-      if (!ok) break;
     }
-    if (kMode == kGateUp) {
-      // Publish the gathered stages still held back (also after an abort, so
-      // that the teardown below can wait for every issued stage).
-      cp_async_wait<0>();
-      fence_proxy_async();
-      __syncwarp();
-      if (lane == 0)
-        for (; published < it; ++published) mbar_arrive(&full[published % NS]);
+  } else if (warp >= kTcGatherWarp0) {
+    // ------------------------------------------------------------ A producers
+    const int g = warp - kTcGatherWarp0;
+    const int sub = lane >> 3, ch = lane & 7;  // rows 4 j + sub, 16-byte chunk ch
+    const uint16_t* asrc = kMode == kDown ? a.h : a.x;
+    int i = 0;
+    WorkExpert we;
+    if (kMode != kDense) we = a.work[0];
+    int it = 0, published = 0;
+    bool ok = true;
+    for (int t = blockIdx.x; t < n_tiles && ok; t += gridDim.x) {
+      TileIdx ti;
+      if (kMode == kDense) {
+        ti.shared = false;
+        ti.mb = t / a.nb;
+        ti.nbk = t - ti.mb * a.nb;
+      } else {
+        tile_seek(a.work, plan.n_work, slot, t, i, we);
+        ti = grouped_tile(we, slot, t);
+      }
+      // Element offsets of this lane's source rows (-1: a pad row, zero-filled).
+      int roff[kTcRowsPerLane];
+#pragma unroll
+      for (int jj = 0; jj < kTcRowsPerLane; ++jj) {
+        const int m = ti.mb * kTcBM + 4 * (g * kTcRowsPerLane + jj) + sub;  // row within the expert
+        int o = -1;
+        if (kMode == kDown) {
+          o = ((ti.shared ? a.hs0 : we.pos) + m) * a.I;
+        } else if (kMode == kDense || ti.shared) {
+          if (m < a.T) o = m * a.d;
+        } else if (m < we.n_tok) {
+          const int sl = a.sorted_ids[we.pos + m];
+          if (sl >= 0 && sl < S) o = (sl / a.k) * a.d;
+        }
+        roff[jj] = o;
+      }
+      for (int kb = 0; kb < a.kb; ++kb, ++it) {
+        const int s = it % NS, use = it / NS;
+        if (lane == 0 && use > 0 &&
+            !mbar_wait(&empty[s], (uint32_t)((use - 1) & 1), a.status)) {
+          *abort_flag = 1;
+        }
+        __syncwarp();
+        if (*abort_flag) {
+          ok = false;
+          break;
+        }
+        const uint32_t sa = ring + s * Cfg::kStageBytes;
+        const int kx = kb * kTcBK;
+        // Row r of the tile lands at r * 128 with its 16-byte chunks permuted by
+        // r mod 8: the layout a 128-byte-swizzled TMA box would produce.
+#pragma unroll
+        for (int jj = 0; jj < kTcRowsPerLane; ++jj) {
+          const int r = 4 * (g * kTcRowsPerLane + jj) + sub;
+          const uint32_t dst = sa + r * 128 + ((ch ^ (r & 7)) << 4);
+          const uint16_t* src = asrc + (roff[jj] < 0 ? 0 : roff[jj] + kx + 8 * ch);
+          cp_async16(dst, src, roff[jj] < 0 ? 0u : 16u);
+        }
+        cp_async_commit();
+        if (it + 1 - published > kTcLag) {
+          cp_async_wait<kTcLag>();
+          fence_proxy_async();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&full_a[published % NS]);
+          ++published;
+        }
+      }
     }
+    // Publish the stages still held back (also after an abort: the MMA thread
+    // may be waiting for them; every copy of this warp has landed by now).
+    cp_async_wait<0>();
+    fence_proxy_async();
+    __syncwarp();
+    if (lane == 0)
+      for (; published < it; ++published) mbar_arrive(&full_a[published % NS]);
   } else if (warp == 1) {
     // -------------------------------------------------------------- MMA issuer
     if (lane == 0) {
@@ -395,7 +435,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) grouped_tc_kernel(const __grid_
         bool ok = true;
         for (int kb = 0; kb < a.kb; ++kb, ++it) {
           const int s = it % NS, use = it / NS;
-          if (!mbar_wait(&full[s], (uint32_t)(use & 1), a.status)) {
+          if (!mbar_wait(&full_b[s], (uint32_t)(use & 1), a.status) ||
+              !mbar_wait(&full_a[s], (uint32_t)(use & 1), a.status)) {
             *abort_flag = 1;
             ok = false;
             break;
@@ -453,8 +494,9 @@ __global__ void __launch_bounds__(kTcThreads, 1) grouped_tc_kernel(const __grid_
           uint32_t packed[16];
 #pragma unroll
           for (int c = 0; c < 16; ++c) {
-            const float h0 = silu(__uint_as_float(g[2 * c])) * __uint_as_float(u[2 * c]);
-            const float h1 = silu(__uint_as_float(g[2 * c + 1])) * __uint_as_float(u[2 * c + 1]);
+            const float h0 = swiglu_fast(__uint_as_float(g[2 * c]), __uint_as_float(u[2 * c]));
+            const float h1 =
+                swiglu_fast(__uint_as_float(g[2 * c + 1]), __uint_as_float(u[2 * c + 1]));
             const __nv_bfloat162 v = __floats2bfloat162_rn(h0, h1);
             packed[c] = *reinterpret_cast<const uint32_t*>(&v);
           }
@@ -483,14 +525,15 @@ __global__ void __launch_bounds__(kTcThreads, 1) grouped_tc_kernel(const __grid_
 
   // Teardown.  Normally every copy was consumed and every MMA retired before
   // the epilogue saw its last accumulator.  After an abort (a bounded wait ran
-  // out), wait -- again bounded -- for the copies still in flight and for the
-  // MMAs already issued, so that neither shared memory nor TMEM is written
-  // after this CTA releases them.
+  // out), wait -- again bounded -- for the B copies still in flight (the A
+  // producers drained their own copies above) and for the MMAs already issued,
+  // so that neither shared memory nor TMEM is written after this CTA releases
+  // them.
   __syncthreads();
   if (*abort_flag) {
     if (warp == 0 && lane == 0) {
       for (int it = *n_consumed; it < *n_issued; ++it)
-        mbar_wait(&full[it % NS], (uint32_t)((it / NS) & 1), nullptr);
+        mbar_wait(&full_b[it % NS], (uint32_t)((it / NS) & 1), nullptr);
     }
     if (warp == 1 && lane == 0) {
       umma_commit(drain);
@@ -574,8 +617,8 @@ cudaError_t launch_tc(const LaunchCfg& c, bool down, const ExpertArgs& e, const 
     a.nb = e.I / (BN / 2);
     a.kb = e.d / kTcBK;
   } else {
-    ok = make_map(&a.tm_a, h, (uint64_t)h_rows, (uint64_t)e.I, kTcBM) &&
-         make_map(&a.tm_b, e.down, (uint64_t)e.E * e.d, (uint64_t)e.I, BN) &&
+    if ((int64_t)h_rows * e.I >= (1ll << 31)) return cudaErrorInvalidValue;
+    ok = make_map(&a.tm_b, e.down, (uint64_t)e.E * e.d, (uint64_t)e.I, BN) &&
          (e.s_down == nullptr || make_map(&a.tm_bs, e.s_down, (uint64_t)e.d, (uint64_t)e.Is, BN));
     a.nb = e.d / BN;
     a.kb = e.I / kTcBK;
@@ -602,9 +645,8 @@ cudaError_t launch_tc_router(const LaunchCfg& c, const uint16_t* x, const uint16
   constexpr int BN = kTcBNRouter;
   TcArgs a;
   memset(&a, 0, sizeof(a));
-  if (!make_map(&a.tm_a, x, (uint64_t)T, (uint64_t)d, kTcBM) ||
-      !make_map(&a.tm_b, wr, (uint64_t)E, (uint64_t)d, BN))
-    return cudaErrorInvalidValue;
+  if (!make_map(&a.tm_b, wr, (uint64_t)E, (uint64_t)d, BN)) return cudaErrorInvalidValue;
+  a.x = x;
   a.y = logits;
   a.status = status;
   a.T = T;
