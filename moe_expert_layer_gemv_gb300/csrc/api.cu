@@ -62,7 +62,8 @@ bool device_info(DeviceInfo* out) {
 constexpr int kGemvSmemBudget = 228 * 1024 / kCtasPerSm - 1024 - 512;
 
 struct Layout {
-  size_t header, plan, work, cta, logits, sg, htc, ids, w, sorted, blocks, npp, offs, h, hs, y, ys, total;
+  size_t header, plan, work, cta, logits, sg, htc, ids, w, sorted, blocks, npp, offs, h, hs, y, ys,
+      achunk, arank, total;
   int64_t cap;
   bool tc;           // the dims qualify for the tensor-core expert path
   int hs0, h_rows;   // tensor-core path: first shared-expert row of htc, rows of htc
@@ -105,6 +106,8 @@ Layout layout_of(const moe_dims_t& dm) {
   L.blocks = carve(&c, sizeof(int32_t) * (size_t)(L.cap / dm.block_size + 1));
   L.npp = carve(&c, sizeof(int32_t));
   L.offs = carve(&c, sizeof(int32_t) * (size_t)(dm.E + 1));
+  L.achunk = carve(&c, sizeof(int32_t) * (size_t)dm.E * align_chunks(dm.T, dm.top_k));
+  L.arank = carve(&c, sizeof(int32_t) * (size_t)S);
   L.h = carve(&c, sizeof(float) * (size_t)L.cap * dm.I);
   L.hs = carve(&c, sizeof(float) * (size_t)dm.T * dm.I_shared);
   L.y = carve(&c, sizeof(float) * (size_t)S * dm.d);
@@ -326,7 +329,8 @@ moe_status_t layer_forward(const moe_dims_t* dims, const void* x, const void* ro
       return MOE_ERR_CUDA;
     if (launch_align(next, ids, dm.T, dm.E, dm.top_k, dm.block_size, sorted,
                      at<int32_t>(ws, L.blocks), at<int32_t>(ws, L.npp), at<int32_t>(ws, L.offs),
-                     ep.pp, status) != cudaSuccess)
+                     ep.pp, status, at<int32_t>(ws, L.achunk), at<int32_t>(ws, L.arank),
+                     status + kAlignCounter) != cudaSuccess)
       return MOE_ERR_CUDA;
   }
   if ((s = record(events, MOE_EV_ROUTED, st)) != MOE_OK) return s;
@@ -454,7 +458,9 @@ moe_status_t moe_align_block_size(const moe_dims_t* dims, const int32_t* topk_id
   return cuda_status(launch_align(LaunchCfg{static_cast<cudaStream_t>(stream), false}, topk_ids,
                                   dm.T, dm.E, dm.top_k, dm.block_size, sorted_ids,
                                   block_expert_ids, num_post_pad, expert_offsets, none,
-                                  at<int>(workspace, L.header)));
+                                  at<int>(workspace, L.header), at<int32_t>(workspace, L.achunk),
+                                  at<int32_t>(workspace, L.arank),
+                                  at<int>(workspace, L.header) + kAlignCounter));
 }
 
 moe_status_t moe_expert_forward(const moe_dims_t* dims, const void* x, const float* topk_weights,

@@ -51,6 +51,8 @@ constexpr int kFusedRouteMaxT = 128;
 // Workspace-header ints used as arrival counters by route_kernel (the status
 // word is int 0): [kRouteCounterBase] tiles done, then one per token tile.
 constexpr int kRouteCounterBase = 16;
+// Workspace-header int counting the finished CTAs of the multi-CTA align.
+constexpr int kAlignCounter = 60;
 
 // logits[t][e] = x[t] . wr[e]; sg[t] = x[t] . w_sg when w_sg (fp32 accumulate).
 cudaError_t launch_router_logits(const LaunchCfg& c, const uint16_t* x, const uint16_t* wr,
@@ -75,9 +77,15 @@ cudaError_t launch_topk(const LaunchCfg& c, const float* logits, int T, int E, i
 
 // Single-CTA moe_align_block_size of the given ids, and the work plan when
 // pp.work != nullptr.
+// S = T * k <= 4096: one CTA.  Larger S: a counting kernel over chunks of
+// 1024 slots and a scatter kernel, with chunk_base [E][align_chunks(T, k)] and
+// chunk_rank [S] as scratch and *counter (zero between launches) counting the
+// counting kernel's finished CTAs.
+int align_chunks(int T, int k);
 cudaError_t launch_align(const LaunchCfg& c, const int32_t* ids, int T, int E, int k, int B,
                          int32_t* sorted_ids, int32_t* block_ids, int32_t* num_post_pad,
-                         int32_t* expert_offsets, const PlanParams& pp, int* status);
+                         int32_t* expert_offsets, const PlanParams& pp, int* status,
+                         int32_t* chunk_base, int32_t* chunk_rank, int* counter);
 
 // Work plan from an existing align layout (moe_expert_forward path).
 cudaError_t launch_plan(const LaunchCfg& c, int T, int E, int k, int B,

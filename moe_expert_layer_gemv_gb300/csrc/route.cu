@@ -500,86 +500,16 @@ __device__ void split_stages(const PlanTotals& pt, int E, const PlanParams& pp, 
 }
 
 // ------------------------------------------------------------------ align
-// Shared-memory ints the align step needs for E experts and nw warps; the last
-// kAlignSmemSlots hold the routing ids (and, for small S, their ranks) when
-// they fit.
-__host__ __device__ constexpr size_t align_smem_ints(int E, int nw) {
-  return (size_t)nw * E + 2 * (size_t)E + kScanScratch + 7 * ((size_t)E + 1) +
-         2 * (size_t)kAlignSmemSlots;
+// Shared-memory ints the single-CTA align needs for E experts; the last
+// kAlignSmemSlots hold the routing ids, the ones before them their ranks.
+__host__ __device__ constexpr size_t align_smem_ints(int E) {
+  return 2 * (size_t)E + kScanScratch + 7 * ((size_t)E + 1) + 2 * (size_t)kAlignSmemSlots;
 }
 
-// moe_align_block_size (+ the work plan when pp.work) on all threads of the
-// CTA.  src: the S = T * k expert ids (shared or global memory).  Counting:
-// per-warp histograms over contiguous chunks of slots (any S).  smem: at least
-// align_smem_ints(E, blockDim / 32) ints.
-__device__ void align_block(const int32_t* src, int T, int k, int E, int B, const AlignOut& o,
-                            const PlanParams& pp, int* status, int* smem) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
-  const int S = T * k;
-  int* hist = smem;                   // [nw][E]
-  int* cnt = hist + nw * E;           // [E]
-  int* off = cnt + E;                 // [E]
-  int* scratch = off + E;             // [kScanScratch]
-  int* tmp = scratch + kScanScratch;  // [7 * (E + 1)]
-  for (int i = threadIdx.x; i < nw * E; i += blockDim.x) hist[i] = 0;
-  __syncthreads();
-
-  // Each warp counts the experts of a contiguous chunk of slots.
-  const int chunk = (S + nw - 1) / nw;
-  const int s_begin = warp * chunk, s_end = min(S, s_begin + chunk);
-  for (int base = s_begin; base < s_end; base += 32) {
-    const int s = base + lane;
-    int e = -1;
-    if (s < s_end) {
-      e = src[s];
-      if (e < 0 || e >= E) {
-        record_status(status, kStatusDeviceCheck);
-        e = -1;
-      }
-    }
-    const unsigned peers = __match_any_sync(0xffffffffu, e);
-    if (e >= 0 && lane == __ffs(peers) - 1) hist[warp * E + e] += __popc(peers);
-    __syncwarp();
-  }
-  __syncthreads();
-  // Per expert: each warp's exclusive base (in place) and the count.
-  for (int e = threadIdx.x; e < E; e += blockDim.x) {
-    int r = 0;
-    for (int q = 0; q < nw; ++q) {
-      const int c = hist[q * E + e];
-      hist[q * E + e] = r;
-      r += c;
-    }
-    cnt[e] = r;
-  }
-  __syncthreads();
-  const PlanTotals pt = layout_and_plan(cnt, off, E, T, S, B, &o, pp, scratch, tmp);
-
-  // Scatter in arrival order.
-  for (int base = s_begin; base < s_end; base += 32) {
-    const int s = base + lane;
-    int e = -1;
-    if (s < s_end) {
-      e = src[s];
-      if (e < 0 || e >= E) e = -1;
-    }
-    const unsigned peers = __match_any_sync(0xffffffffu, e);
-    int rank_base = 0;
-    if (e >= 0) rank_base = hist[warp * E + e];
-    __syncwarp();
-    if (e >= 0) {
-      const int rank = __popc(peers & ((1u << lane) - 1u));
-      o.sorted_ids[off[e] + rank_base + rank] = s;
-      if (lane == __ffs(peers) - 1) hist[warp * E + e] = rank_base + __popc(peers);
-    }
-    __syncwarp();
-  }
-  if (pp.work != nullptr) split_stages(pt, E, pp, tmp);
-}
-
-// The same for S <= kAlignSmemSlots with the ids in shared memory (sids):
-// warp 0 walks the slots in order, 32 at a time, giving every slot its rank
-// among the earlier slots of its expert, so no per-warp histograms are needed.
+// moe_align_block_size (+ the work plan when pp.work) on all threads of one
+// CTA, for S <= kAlignSmemSlots with the ids in shared memory (sids): warp 0
+// walks the slots in order, 32 at a time, giving every slot its rank among the
+// earlier slots of its expert.
 __device__ void align_block_small(const int32_t* sids, int T, int k, int E, int B,
                                   const AlignOut& o, const PlanParams& pp, int* status,
                                   int* smem) {
@@ -619,23 +549,119 @@ __device__ void align_block_small(const int32_t* sids, int T, int k, int E, int 
   if (pp.work != nullptr) split_stages(pt, E, pp, tmp);
 }
 
-// One CTA of 1024 threads: the align (and plan) of given routing ids.
+// One CTA of 1024 threads: the align (and plan) of S <= kAlignSmemSlots
+// routing ids.
 __global__ void __launch_bounds__(kAlignThreads)
     align_kernel(const int32_t* __restrict__ ids, int T, int E, int k, int B, AlignOut o,
                  PlanParams pp, int* status) {
   extern __shared__ int sm[];
-  const int nw = kAlignThreads / 32;
-  int* sids = sm + align_smem_ints(E, nw) - kAlignSmemSlots;
+  int* sids = sm + align_smem_ints(E) - kAlignSmemSlots;
   const int S = T * k;
   pdl_wait();
   pdl_trigger();
-  if (S <= kAlignSmemSlots) {
-    for (int s = threadIdx.x; s < S; s += blockDim.x) sids[s] = __ldcg(ids + s);
-    __syncthreads();
-    align_block_small(sids, T, k, E, B, o, pp, status, sm);
-  } else {
-    align_block(ids, T, k, E, B, o, pp, status, sm);
+  for (int s = threadIdx.x; s < S; s += blockDim.x) sids[s] = __ldcg(ids + s);
+  __syncthreads();
+  align_block_small(sids, T, k, E, B, o, pp, status, sm);
+}
+
+// Larger S: chunks of kAlignThreads slots, one per CTA of align_count_kernel.
+// Each CTA ranks its slots among the earlier slots of the chunk with the same
+// expert (match within a warp, per-warp histograms across warps) and stores
+// the chunk's count of every expert; the last CTA to finish turns the counts
+// into per-chunk bases (a scan over the chunks of each expert, one warp per
+// expert), lays out the padded runs and builds the plan.  align_emit_kernel
+// then places every slot at offset[e] + base[e][chunk] + rank: the same
+// arrival order as one in-order pass.
+struct AlignChunks {
+  int32_t* base;     // [E][nch]: count of expert e in chunk c, then its exclusive base
+  int32_t* rank;     // [S]
+  int* counter;      // CTAs finished (zero between launches)
+};
+
+__global__ void __launch_bounds__(kAlignThreads)
+    align_count_kernel(const int32_t* __restrict__ ids, int T, int E, int k, int B, AlignOut o,
+                       PlanParams pp, AlignChunks ac, int* status) {
+  extern __shared__ int sm[];
+  __shared__ int s_last;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = kAlignThreads / 32;
+  const int S = T * k, nch = gridDim.x, c = blockIdx.x;
+  int* whist = sm;  // [nw][E]
+  pdl_wait();
+  pdl_trigger();
+  for (int i = threadIdx.x; i < nw * E; i += blockDim.x) whist[i] = 0;
+  __syncthreads();
+  const int s = c * kAlignThreads + threadIdx.x;
+  int e = -1;
+  if (s < S) {
+    e = __ldcg(ids + s);
+    if (e < 0 || e >= E) {
+      record_status(status, kStatusDeviceCheck);
+      e = -1;
+    }
   }
+  const unsigned peers = __match_any_sync(0xffffffffu, e);
+  if (e >= 0 && lane == __ffs(peers) - 1) whist[warp * E + e] = __popc(peers);
+  __syncthreads();
+  for (int x = threadIdx.x; x < E; x += blockDim.x) {
+    int r = 0;
+    for (int q = 0; q < nw; ++q) {
+      const int v = whist[q * E + x];
+      whist[q * E + x] = r;
+      r += v;
+    }
+    ac.base[(size_t)x * nch + c] = r;
+  }
+  __syncthreads();
+  if (e >= 0) ac.rank[s] = whist[warp * E + e] + __popc(peers & ((1u << lane) - 1u));
+
+  // Arrival; the last CTA sees every chunk's counts.
+  __threadfence();
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    const int old = atomicAdd(ac.counter, 1);
+    s_last = old == nch - 1;
+    if (s_last) *ac.counter = 0;  // ready for the next call
+  }
+  __syncthreads();
+  if (!s_last) return;
+  __threadfence();
+  int* cnt = sm;                      // [E]
+  int* off = cnt + E;                 // [E]
+  int* scratch = off + E;             // [kScanScratch]
+  int* tmp = scratch + kScanScratch;  // [7 * (E + 1)]
+  for (int x = warp; x < E; x += nw) {
+    int run = 0;
+    for (int c0 = 0; c0 < nch; c0 += 32) {
+      const int ch = c0 + lane;
+      const int v = ch < nch ? __ldcg(ac.base + (size_t)x * nch + ch) : 0;
+      int incl = v;
+#pragma unroll
+      for (int d = 1; d < 32; d <<= 1) {
+        const int u = __shfl_up_sync(0xffffffffu, incl, d);
+        if (lane >= d) incl += u;
+      }
+      if (ch < nch) ac.base[(size_t)x * nch + ch] = run + incl - v;
+      run += __shfl_sync(0xffffffffu, incl, 31);
+    }
+    if (lane == 0) cnt[x] = run;
+  }
+  __syncthreads();
+  const PlanTotals pt = layout_and_plan(cnt, off, E, T, S, B, &o, pp, scratch, tmp);
+  if (pp.work != nullptr) split_stages(pt, E, pp, tmp);
+}
+
+__global__ void __launch_bounds__(kAlignThreads)
+    align_emit_kernel(const int32_t* __restrict__ ids, int T, int E, int k, AlignOut o,
+                      AlignChunks ac) {
+  pdl_wait();
+  pdl_trigger();
+  const int S = T * k, nch = gridDim.x, c = blockIdx.x;
+  const int s = c * kAlignThreads + threadIdx.x;
+  if (s >= S) return;
+  const int e = __ldcg(ids + s);
+  if (e < 0 || e >= E) return;  // recorded by align_count_kernel
+  o.sorted_ids[__ldcg(o.expert_offsets + e) + __ldcg(ac.base + (size_t)e * nch + c) +
+               __ldcg(ac.rank + s)] = s;
 }
 
 // Plan from an existing align layout (moe_expert_forward): counts recovered
@@ -726,7 +752,7 @@ __global__ void __launch_bounds__(kRouterThreads) route_kernel(RouteArgs a) {
     __threadfence();
   }
   const int S = a.r.T * a.k;
-  int* sids = dsm + align_smem_ints(a.r.E, kRouterWarps) - kAlignSmemSlots;
+  int* sids = dsm + align_smem_ints(a.r.E) - kAlignSmemSlots;
   for (int s = threadIdx.x; s < S; s += blockDim.x) sids[s] = __ldcg(a.ids + s);
   __syncthreads();
   align_block_small(sids, a.r.T, a.k, a.r.E, a.B, a.o, a.pp, a.status, dsm);
@@ -798,7 +824,7 @@ cudaError_t launch_route_fused(const LaunchCfg& c, const uint16_t* x, const uint
   a.status = status;
   a.counters = counters;
   size_t smem = (size_t)kRouterTokens * d * 2;
-  const size_t asmem = align_smem_ints(E, kRouterWarps) * sizeof(int);
+  const size_t asmem = align_smem_ints(E) * sizeof(int);
   if (asmem > smem) smem = asmem;
   const void* fn = ch <= 1 ? (const void*)route_kernel<1>
                  : ch <= 2 ? (const void*)route_kernel<2>
@@ -821,16 +847,37 @@ cudaError_t launch_topk(const LaunchCfg& c, const float* logits, int T, int E, i
   return launch_kernel(c, (const void*)topk_kernel, grid, dim3(256), 0, args);
 }
 
+int align_chunks(int T, int k) { return (int)ceil_div((int64_t)T * k, kAlignThreads); }
+
 cudaError_t launch_align(const LaunchCfg& c, const int32_t* ids, int T, int E, int k, int B,
                          int32_t* sorted_ids, int32_t* block_ids, int32_t* num_post_pad,
-                         int32_t* expert_offsets, const PlanParams& pp, int* status) {
-  const size_t smem = align_smem_ints(E, kAlignThreads / 32) * sizeof(int);
-  cudaError_t e = ensure_smem((const void*)align_kernel, (int)smem);
-  if (e != cudaSuccess) return e;
+                         int32_t* expert_offsets, const PlanParams& pp, int* status,
+                         int32_t* chunk_base, int32_t* chunk_rank, int* counter) {
   AlignOut o{sorted_ids, block_ids, num_post_pad, expert_offsets};
   PlanParams p = pp;
-  void* args[] = {&ids, &T, &E, &k, &B, &o, &p, &status};
-  return launch_kernel(c, (const void*)align_kernel, dim3(1), dim3(kAlignThreads), smem, args);
+  if ((int64_t)T * k <= kAlignSmemSlots) {
+    const size_t smem = align_smem_ints(E) * sizeof(int);
+    cudaError_t e = ensure_smem((const void*)align_kernel, (int)smem);
+    if (e != cudaSuccess) return e;
+    void* args[] = {&ids, &T, &E, &k, &B, &o, &p, &status};
+    return launch_kernel(c, (const void*)align_kernel, dim3(1), dim3(kAlignThreads), smem, args);
+  }
+  const int nw = kAlignThreads / 32;
+  const size_t need = (size_t)nw * E > 2 * (size_t)E + kScanScratch + 7 * ((size_t)E + 1)
+                          ? (size_t)nw * E
+                          : 2 * (size_t)E + kScanScratch + 7 * ((size_t)E + 1);
+  const size_t smem = need * sizeof(int);
+  cudaError_t e = ensure_smem((const void*)align_count_kernel, (int)smem);
+  if (e != cudaSuccess) return e;
+  AlignChunks ac{chunk_base, chunk_rank, counter};
+  const dim3 grid((unsigned)align_chunks(T, k));
+  void* args[] = {&ids, &T, &E, &k, &B, &o, &p, &ac, &status};
+  if ((e = launch_kernel(c, (const void*)align_count_kernel, grid, dim3(kAlignThreads), smem,
+                         args)) != cudaSuccess)
+    return e;
+  void* eargs[] = {&ids, &T, &E, &k, &o, &ac};
+  return launch_kernel(LaunchCfg{c.stream, true}, (const void*)align_emit_kernel, grid,
+                       dim3(kAlignThreads), 0, eargs);
 }
 
 cudaError_t launch_plan(const LaunchCfg& c, int T, int E, int k, int B,

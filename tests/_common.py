@@ -41,17 +41,34 @@ def bf16_to_f64(t: torch.Tensor) -> np.ndarray:
     return t.detach().to("cpu").to(torch.float64).numpy()
 
 
+def bf16_half_ulp(x):
+    """Half a bf16 unit in the last place at each |x| (8 significant bits):
+    the largest error of rounding x to the nearest bf16."""
+    x = np.asarray(x, np.float64)
+    _, p = np.frexp(x)  # |x| = m 2^p, m in [0.5, 1): ulp = 2^(p - 8)
+    return np.where(x != 0, np.ldexp(1.0, p - 9), 0.0)
+
+
 def compare_out(gpu_out, ref_out):
-    """Returns (rel_l2, max_abs / rms) and asserts the pass bar."""
+    """Returns (rel_l2, max_abs / rms) and asserts the pass bar.
+
+    The output is bf16, so even the correctly rounded exact result is off by
+    up to half a bf16 ulp, which at a 6-sigma element lying just above a power
+    of two is ~2.3% of rms: more than the 2e-2 rms bound itself.  The bound is
+    therefore applied to the error of the computation, the rounding to the
+    output type allowed on top: |out - exact| <= 2e-2 rms + half_ulp(exact).
+    rel-L2 is taken as is (rounding alone contributes ~1.7e-3)."""
     g = np.asarray(gpu_out, np.float64)
     r = np.asarray(ref_out, np.float64)
     assert g.shape == r.shape
     assert np.all(np.isfinite(g))
     rms = float(np.sqrt(np.mean(r * r)))
     rel = float(np.linalg.norm(g - r) / max(np.linalg.norm(r), 1e-300))
-    mx = float(np.abs(g - r).max() / max(rms, 1e-300)) if g.size else 0.0
+    err = np.abs(g - r)
+    mx = float((err - bf16_half_ulp(r)).max() / max(rms, 1e-300)) if g.size else 0.0
+    literal = float(err.max() / max(rms, 1e-300)) if g.size else 0.0
     assert rel <= REL_L2_TOL, f"rel-L2 {rel:.3e} > {REL_L2_TOL}"
-    assert mx <= MAX_ABS_TOL, f"max-abs/rms {mx:.3e} > {MAX_ABS_TOL}"
+    assert mx <= MAX_ABS_TOL, f"max-abs/rms beyond bf16 rounding {mx:.3e} > {MAX_ABS_TOL} (raw {literal:.3e})"
     return rel, mx
 
 

@@ -145,9 +145,12 @@ def _stage_tensors(s):
             "offs": torch.zeros((s.E + 1,), dtype=torch.int32, device=dev)}
 
 
-@pytest.mark.parametrize("name", ["tiny", "verify_t8", "verify_t64", "int4_t32"])
-def test_stage_route(name):
-    s = I.shape(name)
+@pytest.mark.parametrize("name,over", [("tiny", {}), ("verify_t8", {}), ("verify_t64", {}),
+                                       ("int4_t32", {}),
+                                       # T >= 256, E % 64 == 0: router logits on the tensor cores
+                                       ("prefill_t4096", {"T": 1000, "I": 16, "Is": 16})])
+def test_stage_route(name, over):
+    s = I.shape(name, **over)
     inp = I.make_inputs(s, 0)
     dims = abi.dims_of(s)
     ws = abi.alloc_workspace(dims)
@@ -165,7 +168,9 @@ def test_stage_route(name):
 
 @pytest.mark.parametrize("T,E,k,B,seed", [(4, 8, 2, 16, 0), (8, 256, 8, 16, 1), (64, 256, 8, 16, 2),
                                           (4096, 256, 8, 128, 3), (32, 512, 10, 16, 4),
-                                          (37, 5, 3, 1, 5), (300, 17, 4, 64, 6), (1, 1024, 16, 16, 7)])
+                                          (37, 5, 3, 1, 5), (300, 17, 4, 64, 6), (1, 1024, 16, 16, 7),
+                                          # several 1024-slot chunks, the last one ragged
+                                          (1000, 64, 5, 32, 8), (600, 1024, 16, 16, 9)])
 def test_stage_align_bit_exact(T, E, k, B, seed):
     s = I.LayerShape(T=T, d=64, E=E, k=k, I=16, block=B)
     rng = np.random.default_rng(seed)
@@ -183,6 +188,28 @@ def test_stage_align_bit_exact(T, E, k, B, seed):
     assert np.array_equal(t["blocks"].cpu().numpy()[: n // B], ref["block_expert_ids"])
     assert np.array_equal(t["offs"].cpu().numpy(), ref["expert_offsets"])
     assert abi.moe_read_device_status(ws) == abi.MOE_OK
+
+
+def test_stage_align_multi_chunk_skewed():
+    """Most slots on one expert, spread over several chunks: ranks must run on
+    across chunk boundaries in arrival order."""
+    T, E, k, B = 3000, 16, 2, 64
+    s = I.LayerShape(T=T, d=64, E=E, k=k, I=16, block=B)
+    rng = np.random.default_rng(11)
+    ids_np = np.empty((T, k), dtype=np.int32)
+    ids_np[:, 0] = np.where(rng.random(T) < 0.9, 3, rng.integers(0, E, T))
+    ids_np[:, 1] = (ids_np[:, 0] + 1 + rng.integers(0, E - 1, T)) % E
+    dims = abi.dims_of(s)
+    ws = abi.alloc_workspace(dims)
+    t = _stage_tensors(s)
+    abi.moe_align_block_size(dims, torch.from_numpy(ids_np).cuda(), t["sorted"], t["blocks"],
+                             t["npp"], t["offs"], ws)
+    torch.cuda.synchronize()
+    ref = oracle.align(ids_np.reshape(-1), E, B)
+    n = int(t["npp"].item())
+    assert n == ref["num_post_pad"]
+    assert np.array_equal(t["sorted"].cpu().numpy()[:n], ref["sorted_ids"])
+    assert np.array_equal(t["offs"].cpu().numpy(), ref["expert_offsets"])
 
 
 def test_stage_align_rejects_out_of_range_ids_without_fault():
@@ -254,6 +281,8 @@ def test_timed_entry_point_matches_and_records_events():
     ({"T": 300, "d": 512, "E": 16, "k": 4, "I": 256, "Is": 256, "block": 128}, 1),
     ({"T": 512, "d": 768, "E": 9, "k": 3, "I": 384, "Is": 0, "block": 128}, 2),
     ({"T": 257, "d": 256, "E": 64, "k": 8, "I": 128, "Is": 128, "block": 256}, 3),
+    # S = 5600 routing slots: the multi-chunk align
+    ({"T": 700, "d": 256, "E": 64, "k": 8, "I": 128, "Is": 128, "block": 128}, 4),
 ])
 def test_tensor_core_path_parity(over, seed):
     r = layer_parity(I.make_inputs(I.shape("verify_t8", **over), seed))
