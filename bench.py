@@ -147,6 +147,20 @@ def algorithmic(shape, ids_list):
             "touched": statistics.mean(touched), "flops": flops}
 
 
+def tensor_core_path(s):
+    """Whether the library runs this layer's expert stages as grouped tcgen05
+    GEMMs (its dispatch rule: T >= 256, bf16 routed weights, 128-row align
+    blocks, I % 128 == 0, d % 256 == 0, shared expert absent or as wide)."""
+    return (s.T >= 256 and s.fmt == "bf16" and s.block % 128 == 0 and s.I % 128 == 0
+            and s.d % 256 == 0 and s.Is in (0, s.I))
+
+
+def gate_up_flops(s):
+    """Algorithmic flops of the gate_up stage: real routed rows (no padding)
+    plus the shared expert."""
+    return 2 * s.T * s.k * 2 * s.I * s.d + 2 * s.T * 2 * s.Is * s.d
+
+
 def kernel_traffic(src_name, workload, algorithmic_bytes):
     """DRAM bytes (read + write) per launch of the dominant kernel, from the ncu
     capture recorded in profiles/gate_up_<workload>.json -- scaled from the
@@ -343,7 +357,11 @@ def main():
     peaks, peak_kind = measured_peaks()
     gu_ms = stage_ms["gate_up"]
     achieved = alg["gate_up_bytes"] / (gu_ms * 1e-3) / 1e9
-    traffic = kernel_traffic("expert_gemv.cu", shape.name, alg["gate_up_bytes"])
+    tc = tensor_core_path(shape)
+    traffic = kernel_traffic("grouped_tc.cu" if tc else "expert_gemv.cu", shape.name,
+                             alg["gate_up_bytes"])
+    kname = ("grouped_tc_kernel<gate_up, N=256>" if tc else
+             f"gate_up_kernel<{'int4' if shape.fmt == 'int4' else 'bf16'}>")
     if rank == 0:
         tok_s = world * shape.T / (ms * 1e-3)
         line = {
@@ -362,7 +380,8 @@ def main():
             "touched_experts": alg["touched"],
             "stage_us": {k: v * 1e3 for k, v in stage_ms.items()},
             "timed_pass_us": ms_timed * 1e3,
-            "roofline": {"kernel": "gate_up_kernel", "bound": "hbm", "achieved": achieved,
+            "layer_tflops": alg["flops"] / (ms * 1e-3) / 1e12,
+            "roofline": {"kernel": kname, "bound": "hbm", "achieved": achieved,
                          "peak": peaks["hbm_gbs"], "unit": "GB/s",
                          "frac": achieved / peaks["hbm_gbs"], "traffic": traffic,
                          "algorithmic_bytes": alg["gate_up_bytes"], "peak_source": peak_kind},
@@ -374,6 +393,12 @@ def main():
             "gpu_launches": gpu_launches,
             "clocks": clk,
         }
+        if tc:
+            gtf = gate_up_flops(shape) / (gu_ms * 1e-3) / 1e12
+            line["roofline"]["tensor"] = {
+                "achieved": gtf, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+                "frac": gtf / peaks["bf16_tflops"],
+                "note": "gate_up algorithmic flops (real rows) / stage time vs measured bf16 burst peak"}
         print(json.dumps(line), flush=True)
     if world > 1:
         dist.destroy_process_group()
