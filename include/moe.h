@@ -29,6 +29,13 @@
  *   - `stream` is a cudaStream_t passed as void* (NULL = the legacy default
  *     stream).  Calls are asynchronous: they enqueue kernels and return; no
  *     call synchronises the host except moe_read_device_status().
+ *   - Every kernel is launched with programmatic dependent launch, the first
+ *     of a call included: it may start while the stream's previous kernel
+ *     finishes, but it reads nothing the caller may write (x, ids, layouts)
+ *     and writes nothing until that kernel has completed.  A caller kernel
+ *     launched programmatically just before a call must itself wait for its
+ *     own predecessor (griddepcontrol.wait) if that predecessor writes this
+ *     call's inputs.
  *   - Argument errors are detected on the host and returned before anything is
  *     launched.  A failed launch returns MOE_ERR_CUDA.  A kernel that detects a
  *     data-dependent fault (an expert id out of range, a pipeline wait that ran

@@ -2,7 +2,9 @@
 // carve-up, and the launch sequence of each call on the caller's stream.
 //
 // moe_layer_forward enqueues, all on one stream and chained by programmatic
-// dependent launch (no host synchronisation anywhere):
+// dependent launch (no host synchronisation anywhere; the first kernel too may
+// start while the stream's previous kernel finishes: it requests only the
+// router weights before its griddepcontrol.wait):
 //   1. routing: at decode sizes (T <= 128) one launch -- router GEMV over many
 //      CTAs, top-k by the last CTA of each token tile, align + work plan by the
 //      last tile; above that, router, top-k and align as three launches
@@ -293,7 +295,7 @@ moe_status_t layer_forward(const moe_dims_t* dims, const void* x, const void* ro
   if ((s = expert_plan(dm, ws, L, di.sms, &ep)) != MOE_OK) return s;
 
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  const LaunchCfg first{st, false}, next{st, true};
+  const LaunchCfg next{st, true};
   int* status = at<int>(ws, L.header);
   float* logits = at<float>(ws, L.logits);
   int32_t* ids = at<int32_t>(ws, L.ids);
@@ -304,7 +306,7 @@ moe_status_t layer_forward(const moe_dims_t* dims, const void* x, const void* ro
   const uint16_t* w_sg = sh ? static_cast<const uint16_t*>(sh->gate_w) : nullptr;
   float* sg = at<float>(ws, L.sg);
   if (fused_route_supported(dm.T, dm.E, dm.top_k)) {
-    if (launch_route_fused(first, static_cast<const uint16_t*>(x),
+    if (launch_route_fused(next, static_cast<const uint16_t*>(x),
                            static_cast<const uint16_t*>(router_w), w_sg, logits, sg, dm.T, dm.d,
                            dm.E, dm.top_k, dm.renormalize, ids, w, ids_out, w_out, dm.block_size,
                            sorted, at<int32_t>(ws, L.blocks), at<int32_t>(ws, L.npp),
@@ -314,12 +316,12 @@ moe_status_t layer_forward(const moe_dims_t* dims, const void* x, const void* ro
   } else {
     if (use_tc_router(dm)) {
       // The shared-expert gate logit is then computed by the combine kernel.
-      if (launch_tc_router(first, static_cast<const uint16_t*>(x),
+      if (launch_tc_router(next, static_cast<const uint16_t*>(x),
                            static_cast<const uint16_t*>(router_w), logits, dm.T, dm.d, dm.E,
                            status, di.sms) != cudaSuccess)
         return MOE_ERR_CUDA;
       sg = nullptr;
-    } else if (launch_router_logits(first, static_cast<const uint16_t*>(x),
+    } else if (launch_router_logits(next, static_cast<const uint16_t*>(x),
                                     static_cast<const uint16_t*>(router_w), w_sg, logits, sg,
                                     dm.T, dm.d, dm.E, di.sms, status) != cudaSuccess) {
       return MOE_ERR_CUDA;
@@ -428,10 +430,10 @@ moe_status_t moe_route(const moe_dims_t* dims, const void* x, const void* router
   float* logits = at<float>(workspace, L.logits);
   const cudaError_t err =
       use_tc_router(dm)
-          ? launch_tc_router(LaunchCfg{st, false}, static_cast<const uint16_t*>(x),
+          ? launch_tc_router(LaunchCfg{st, true}, static_cast<const uint16_t*>(x),
                              static_cast<const uint16_t*>(router_w), logits, dm.T, dm.d, dm.E,
                              at<int>(workspace, L.header), di.sms)
-          : launch_router_logits(LaunchCfg{st, false}, static_cast<const uint16_t*>(x),
+          : launch_router_logits(LaunchCfg{st, true}, static_cast<const uint16_t*>(x),
                                  static_cast<const uint16_t*>(router_w), nullptr, logits, nullptr,
                                  dm.T, dm.d, dm.E, di.sms, at<int>(workspace, L.header));
   if (err != cudaSuccess) return MOE_ERR_CUDA;
@@ -455,7 +457,7 @@ moe_status_t moe_align_block_size(const moe_dims_t* dims, const int32_t* topk_id
   Layout L;
   if ((s = check_ws(dm, workspace, workspace_bytes, &L)) != MOE_OK) return s;
   PlanParams none = {};
-  return cuda_status(launch_align(LaunchCfg{static_cast<cudaStream_t>(stream), false}, topk_ids,
+  return cuda_status(launch_align(LaunchCfg{static_cast<cudaStream_t>(stream), true}, topk_ids,
                                   dm.T, dm.E, dm.top_k, dm.block_size, sorted_ids,
                                   block_expert_ids, num_post_pad, expert_offsets, none,
                                   at<int>(workspace, L.header), at<int32_t>(workspace, L.achunk),
@@ -487,7 +489,7 @@ moe_status_t moe_expert_forward(const moe_dims_t* dims, const void* x, const flo
   ExpertPlan ep;
   if ((s = expert_plan(dm, workspace, L, di.sms, &ep)) != MOE_OK) return s;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  if (launch_plan(LaunchCfg{st, false}, dm.T, dm.E, dm.top_k, dm.block_size, sorted_ids,
+  if (launch_plan(LaunchCfg{st, true}, dm.T, dm.E, dm.top_k, dm.block_size, sorted_ids,
                   num_post_pad, expert_offsets, ep.pp, at<int>(workspace, L.header)) !=
       cudaSuccess)
     return MOE_ERR_CUDA;
