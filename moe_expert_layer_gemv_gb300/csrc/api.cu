@@ -132,7 +132,7 @@ moe_status_t check_dims(const moe_dims_t* dm) {
     return MOE_ERR_INVALID_ARG;
   if (d.renormalize != 0 && d.renormalize != 1) return MOE_ERR_INVALID_ARG;
   if (d.T > 65536 || d.d < 8 || d.d > 8192 || d.d % 8 != 0) return MOE_ERR_UNSUPPORTED;
-  if (d.E > 1024 || d.top_k > d.E || d.top_k > 16) return MOE_ERR_UNSUPPORTED;
+  if (d.E > 1024 || d.top_k > d.E || d.top_k > kMaxTopK) return MOE_ERR_UNSUPPORTED;
   if (d.I < 8 || d.I > 4096 || d.I % 8 != 0) return MOE_ERR_UNSUPPORTED;
   if (d.I_shared != 0 && (d.I_shared < 8 || d.I_shared > 4096 || d.I_shared % 8 != 0))
     return MOE_ERR_UNSUPPORTED;

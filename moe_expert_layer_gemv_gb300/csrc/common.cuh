@@ -41,6 +41,9 @@ struct WorkExpert {
 // The persistent expert kernels run at most this many CTAs.
 constexpr int kMaxGrid = 1024;
 
+// Largest top_k the library accepts.
+constexpr int kMaxTopK = 16;
+
 struct Plan {
   int32_t n_work;      // number of WorkExpert entries
   int32_t units_gu;    // total gate_up units

@@ -226,10 +226,12 @@ __device__ void warp_topk(const float* __restrict__ L, int E, int k, int renorma
   else warp_topk_nv<32>(L, E, k, renormalize, id, wt);
 }
 
-// Top-k of token t, stored (lanes j < k) to the routing buffers.
+// Top-k of token t, stored (lanes j < k) to the routing buffers (and, when
+// ids_smem, to shared memory at the same slot index).
 __device__ __forceinline__ void topk_token(const float* logits, int t, int E, int k,
                                            int renormalize, int32_t* ids, float* w,
-                                           int32_t* ids_copy, float* w_copy) {
+                                           int32_t* ids_copy, float* w_copy,
+                                           int32_t* ids_smem = nullptr) {
   int id;
   float wt;
   warp_topk(logits + (size_t)t * E, E, k, renormalize, id, wt);
@@ -238,6 +240,7 @@ __device__ __forceinline__ void topk_token(const float* logits, int t, int E, in
     const size_t o = (size_t)t * k + lane;
     ids[o] = id;
     w[o] = wt;
+    if (ids_smem) ids_smem[o] = id;
     if (ids_copy) ids_copy[o] = id;
     if (w_copy) w_copy[o] = wt;
   }
@@ -734,8 +737,12 @@ __global__ void __launch_bounds__(kRouterThreads) route_kernel(RouteArgs a) {
   if (!s_last) return;
   __threadfence();
   const int t = blockIdx.y * kRouterTokens + (threadIdx.x >> 5);
+  // With one token tile this CTA runs the align too: the ids go straight to
+  // its shared-memory slots (the router's x tile there is no longer needed).
+  int* sids = dsm + align_smem_ints(a.r.E) - kAlignSmemSlots;
   if ((threadIdx.x >> 5) < kRouterTokens && t < a.r.T)
-    topk_token(a.r.logits, t, a.r.E, a.k, a.renormalize, a.ids, a.w, a.ids_copy, a.w_copy);
+    topk_token(a.r.logits, t, a.r.E, a.k, a.renormalize, a.ids, a.w, a.ids_copy, a.w_copy,
+               gridDim.y == 1 ? sids : nullptr);
 
   // Arrival of this tile; the last tile to finish runs the align and the plan
   // (with one token tile, this CTA is already the last).
@@ -751,10 +758,11 @@ __global__ void __launch_bounds__(kRouterThreads) route_kernel(RouteArgs a) {
     if (!s_last) return;
     __threadfence();
   }
-  const int S = a.r.T * a.k;
-  int* sids = dsm + align_smem_ints(a.r.E) - kAlignSmemSlots;
-  for (int s = threadIdx.x; s < S; s += blockDim.x) sids[s] = __ldcg(a.ids + s);
-  __syncthreads();
+  if (gridDim.y > 1) {
+    const int S = a.r.T * a.k;
+    for (int s = threadIdx.x; s < S; s += blockDim.x) sids[s] = __ldcg(a.ids + s);
+    __syncthreads();
+  }
   align_block_small(sids, a.r.T, a.k, a.r.E, a.B, a.o, a.pp, a.status, dsm);
 }
 
