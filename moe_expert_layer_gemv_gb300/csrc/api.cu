@@ -314,20 +314,22 @@ moe_status_t layer_forward(const moe_dims_t* dims, const void* x, const void* ro
                            di.sms) != cudaSuccess)
       return MOE_ERR_CUDA;
   } else {
-    if (use_tc_router(dm)) {
-      // The shared-expert gate logit is then computed by the combine kernel.
+    // After the tensor-core router the top-k kernel also takes the
+    // shared-expert gate logit x . w_sg (one warp per token).
+    const bool tc_router = use_tc_router(dm);
+    if (tc_router) {
       if (launch_tc_router(next, static_cast<const uint16_t*>(x),
                            static_cast<const uint16_t*>(router_w), logits, dm.T, dm.d, dm.E,
                            status, di.sms) != cudaSuccess)
         return MOE_ERR_CUDA;
-      sg = nullptr;
     } else if (launch_router_logits(next, static_cast<const uint16_t*>(x),
                                     static_cast<const uint16_t*>(router_w), w_sg, logits, sg,
                                     dm.T, dm.d, dm.E, di.sms, status) != cudaSuccess) {
       return MOE_ERR_CUDA;
     }
-    if (launch_topk(next, logits, dm.T, dm.E, dm.top_k, dm.renormalize, ids, w, ids_out,
-                    w_out) != cudaSuccess)
+    if (launch_topk(next, logits, dm.T, dm.E, dm.top_k, dm.renormalize, ids, w, ids_out, w_out,
+                    static_cast<const uint16_t*>(x), dm.d, tc_router ? w_sg : nullptr,
+                    tc_router ? sg : nullptr) != cudaSuccess)
       return MOE_ERR_CUDA;
     if (launch_align(next, ids, dm.T, dm.E, dm.top_k, dm.block_size, sorted,
                      at<int32_t>(ws, L.blocks), at<int32_t>(ws, L.npp), at<int32_t>(ws, L.offs),
@@ -438,7 +440,8 @@ moe_status_t moe_route(const moe_dims_t* dims, const void* x, const void* router
                                  dm.T, dm.d, dm.E, di.sms, at<int>(workspace, L.header));
   if (err != cudaSuccess) return MOE_ERR_CUDA;
   return cuda_status(launch_topk(LaunchCfg{st, true}, logits, dm.T, dm.E, dm.top_k,
-                                 dm.renormalize, topk_ids, topk_weights, nullptr, nullptr));
+                                 dm.renormalize, topk_ids, topk_weights, nullptr, nullptr,
+                                 nullptr, dm.d, nullptr, nullptr));
 }
 
 moe_status_t moe_align_block_size(const moe_dims_t* dims, const int32_t* topk_ids,

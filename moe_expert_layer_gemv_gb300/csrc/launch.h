@@ -71,9 +71,10 @@ cudaError_t launch_route_fused(const LaunchCfg& c, const uint16_t* x, const uint
                                const PlanParams& pp, int* status, int* counters, int sms);
 
 // Per token: softmax over E, top-k (ties -> lower id), (re)normalised weights.
+// With w_sg and sg also sg[t] = x[t] . w_sg (fp32, one warp per token).
 cudaError_t launch_topk(const LaunchCfg& c, const float* logits, int T, int E, int k,
                         int renormalize, int32_t* ids, float* w, int32_t* ids_copy,
-                        float* w_copy);
+                        float* w_copy, const uint16_t* x, int d, const uint16_t* w_sg, float* sg);
 
 // Single-CTA moe_align_block_size of the given ids, and the work plan when
 // pp.work != nullptr.

@@ -246,13 +246,27 @@ __device__ __forceinline__ void topk_token(const float* logits, int t, int E, in
   }
 }
 
+// One warp per token: its top-k and, when sg, the shared-expert gate logit
+// sg[t] = x[t] . w_sg (fp32, lane partials then the warp's butterfly sum).
 __global__ void __launch_bounds__(256)
     topk_kernel(const float* __restrict__ logits, int T, int E, int k, int renormalize,
-                int32_t* ids, float* w, int32_t* ids_copy, float* w_copy) {
+                int32_t* ids, float* w, int32_t* ids_copy, float* w_copy,
+                const uint16_t* __restrict__ x, int d, const uint16_t* __restrict__ w_sg,
+                float* sg) {
   pdl_wait();
   pdl_trigger();
   const int t = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
-  if (t < T) topk_token(logits, t, E, k, renormalize, ids, w, ids_copy, w_copy);
+  if (t >= T) return;
+  topk_token(logits, t, E, k, renormalize, ids, w, ids_copy, w_copy);
+  if (sg != nullptr) {
+    const int lane = threadIdx.x & 31;
+    const uint4* xr = reinterpret_cast<const uint4*>(x + (size_t)t * d);
+    const uint4* gr = reinterpret_cast<const uint4*>(w_sg);
+    float acc = 0.f;
+    for (int c = lane; c < d / 8; c += 32) acc = dot8_bf16(xr[c], gr[c], acc);
+    acc = warp_sum(acc);
+    if (lane == 0) sg[t] = acc;
+  }
 }
 
 // ------------------------------------------------------------------ block scan
@@ -481,7 +495,8 @@ __device__ PlanTotals layout_and_plan(const int* cnt, int* off, int E, int T, in
 __device__ void split_stages(const PlanTotals& pt, int E, const PlanParams& pp, const int* tmp) {
   const int W = E + 1;
   const int per = pp.grid + 1;
-  for (int i = threadIdx.x; i < 2 * per; i += blockDim.x) {
+  // The tensor-core kernels walk the plan by tiles, not by these ranges.
+  for (int i = threadIdx.x; pp.tc_nb_gu == 0 && i < 2 * per; i += blockDim.x) {
     if (i < per)
       split_one(i, pt.n_work, tmp + 2 * W, tmp, tmp + 4 * W, tmp + 5 * W, pt.cost_gu, pt.units_gu,
                 pp.xt_gu, pp.grid, pp.cta_gu);
@@ -848,10 +863,12 @@ cudaError_t launch_route_fused(const LaunchCfg& c, const uint16_t* x, const uint
 
 cudaError_t launch_topk(const LaunchCfg& c, const float* logits, int T, int E, int k,
                         int renormalize, int32_t* ids, float* w, int32_t* ids_copy,
-                        float* w_copy) {
+                        float* w_copy, const uint16_t* x, int d, const uint16_t* w_sg,
+                        float* sg) {
   if (T == 0) return cudaSuccess;
   dim3 grid((unsigned)ceil_div(T, 8));
-  void* args[] = {&logits, &T, &E, &k, &renormalize, &ids, &w, &ids_copy, &w_copy};
+  void* args[] = {&logits, &T, &E, &k, &renormalize, &ids, &w, &ids_copy, &w_copy,
+                  &x, &d, &w_sg, &sg};
   return launch_kernel(c, (const void*)topk_kernel, grid, dim3(256), 0, args);
 }
 
