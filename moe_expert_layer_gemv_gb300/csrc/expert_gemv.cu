@@ -132,33 +132,36 @@ __device__ __forceinline__ void fma8f(uint4 w, float4 p, float4 q, float& a0, fl
   a1 = fmaf(bf16hi(w.w), q.w, a1);
 }
 
-// Signed int4 value (nibble - 8) as an exact float: (2^23 + nibble) - (2^23 + 8).
-__device__ __forceinline__ float nib(uint32_t v, int sh) {
-  return __uint_as_float(0x4b000000u | ((v >> sh) & 15u)) - 8388616.0f;
+// Packed fp32 pairs (element 2j in the low word, 2j + 1 in the high word): one
+// instruction does both lanes' fma / sub, each rounded as the scalar would be.
+__device__ __forceinline__ uint64_t f2(uint32_t lo, uint32_t hi) {
+  return ((uint64_t)hi << 32) | lo;
+}
+__device__ __forceinline__ uint64_t ffma2(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t r;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
+  return r;
+}
+__device__ __forceinline__ float f2sum(uint64_t v) {
+  return __uint_as_float((uint32_t)v) + __uint_as_float((uint32_t)(v >> 32));
 }
 
-// The 8 codes of word v (element 2b in the low nibble of byte b) against 8 bf16.
-__device__ __forceinline__ void fma8_int4(uint32_t v, uint4 x, float& a0, float& a1) {
-  a0 = fmaf(nib(v, 0), bf16lo(x.x), a0);
-  a1 = fmaf(nib(v, 4), bf16hi(x.x), a1);
-  a0 = fmaf(nib(v, 8), bf16lo(x.y), a0);
-  a1 = fmaf(nib(v, 12), bf16hi(x.y), a1);
-  a0 = fmaf(nib(v, 16), bf16lo(x.z), a0);
-  a1 = fmaf(nib(v, 20), bf16hi(x.z), a1);
-  a0 = fmaf(nib(v, 24), bf16lo(x.w), a0);
-  a1 = fmaf(nib(v, 28), bf16hi(x.w), a1);
+// The 8 codes of word v as exact float pairs (code - 8): element 2j is the low
+// nibble of byte j, 2j + 1 its high nibble; each is placed under the exponent
+// of 2^23 by one byte permute, then 2^23 + 8 comes off both halves at once.
+__device__ __forceinline__ void dequant8(uint32_t v, uint64_t (&q)[4]) {
+  const uint32_t lo = v & 0x0F0F0F0Fu, hi = (v >> 4) & 0x0F0F0F0Fu;
+  const uint32_t mag = 0x4B000000u;          // 2^23
+  const uint64_t off = f2(0x4B000008u, 0x4B000008u);  // 2^23 + 8 in both halves
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const uint64_t e = f2(__byte_perm(lo, mag, 0x7540 + j), __byte_perm(hi, mag, 0x7540 + j));
+    asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(q[j]) : "l"(e), "l"(off));
+  }
 }
 
-__device__ __forceinline__ void fma8_int4f(uint32_t v, float4 p, float4 q, float& a0, float& a1) {
-  a0 = fmaf(nib(v, 0), p.x, a0);
-  a1 = fmaf(nib(v, 4), p.y, a1);
-  a0 = fmaf(nib(v, 8), p.z, a0);
-  a1 = fmaf(nib(v, 12), p.w, a1);
-  a0 = fmaf(nib(v, 16), q.x, a0);
-  a1 = fmaf(nib(v, 20), q.y, a1);
-  a0 = fmaf(nib(v, 24), q.z, a0);
-  a1 = fmaf(nib(v, 28), q.w, a1);
-}
+// Two bf16 (element 2j low, 2j + 1 high) as an fp32 pair.
+__device__ __forceinline__ uint64_t bf16x2_f2(uint32_t w) { return f2(w << 16, w & 0xffff0000u); }
 
 // ------------------------------------------------------------------ gate_up math
 // One warp: gate row at wg, up row at wu (shared addresses), NT token rows at
@@ -191,7 +194,9 @@ __device__ __forceinline__ void gu_rows_bf16(uint32_t wg, uint32_t wu, uint32_t 
 }
 
 // int4 weights: a 16-byte chunk is 32 codes = one scale group; the group's
-// bf16 scales at sg / su (one per chunk).
+// bf16 scales at sg / su (one per chunk).  Each code is dequantised once and
+// used for every token; per token the group's products go into an
+// (even, odd) pair of partial sums, then scale x pair sum into the total.
 template <int NT>
 __device__ __forceinline__ void gu_rows_int4(uint32_t wg, uint32_t wu, uint32_t sg, uint32_t su,
                                              uint32_t xa, uint32_t xs, int ngroups, int lane,
@@ -203,21 +208,31 @@ __device__ __forceinline__ void gu_rows_int4(uint32_t wg, uint32_t wu, uint32_t 
     const uint32_t off = (uint32_t)c * 16u;
     const uint4 vg = lds128(wg + off), vu = lds128(wu + off);
     const float fg = lds_bf16(sg + 2u * c), fu = lds_bf16(su + 2u * c);
+    const uint32_t wgk[4] = {vg.x, vg.y, vg.z, vg.w}, wuk[4] = {vu.x, vu.y, vu.z, vu.w};
+    uint64_t pg[NT], pu[NT];
+#pragma unroll
+    for (int q = 0; q < NT; ++q) pg[q] = pu[q] = 0ull;
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      uint64_t qg[4], qu[4];
+      dequant8(wgk[k], qg);
+      dequant8(wuk[k], qu);
+#pragma unroll
+      for (int q = 0; q < NT; ++q) {
+        const uint4 xv = lds128(xa + q * xs + 4u * off + 16u * k);
+        const uint32_t xw[4] = {xv.x, xv.y, xv.z, xv.w};
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const uint64_t xp = bf16x2_f2(xw[j]);
+          pg[q] = ffma2(qg[j], xp, pg[q]);
+          pu[q] = ffma2(qu[j], xp, pu[q]);
+        }
+      }
+    }
 #pragma unroll
     for (int q = 0; q < NT; ++q) {
-      const uint32_t xr = xa + q * xs + 4u * off;
-      const uint4 x0 = lds128(xr), x1 = lds128(xr + 16), x2 = lds128(xr + 32), x3 = lds128(xr + 48);
-      float p0 = 0.f, p1 = 0.f, r0 = 0.f, r1 = 0.f;
-      fma8_int4(vg.x, x0, p0, p1);
-      fma8_int4(vg.y, x1, p0, p1);
-      fma8_int4(vg.z, x2, p0, p1);
-      fma8_int4(vg.w, x3, p0, p1);
-      fma8_int4(vu.x, x0, r0, r1);
-      fma8_int4(vu.y, x1, r0, r1);
-      fma8_int4(vu.z, x2, r0, r1);
-      fma8_int4(vu.w, x3, r0, r1);
-      ga[q] = fmaf(fg, p0 + p1, ga[q]);
-      ua[q] = fmaf(fu, r0 + r1, ua[q]);
+      ga[q] = fmaf(fg, f2sum(pg[q]), ga[q]);
+      ua[q] = fmaf(fu, f2sum(pu[q]), ua[q]);
     }
   }
 #pragma unroll
@@ -273,31 +288,36 @@ __device__ __forceinline__ void dn_rows2(uint32_t wa, uint32_t wb, uint32_t sa, 
       }
     }
   } else {
+    // Codes dequantised once per group, h already fp32 pairs in shared memory.
     for (int c = sl; c < Iw / 32; c += 8) {
       const uint32_t off = (uint32_t)c * 16u;
       const uint4 va = lds128(wa + off), vb = lds128(wb + off);
       const float fa = lds_bf16(sa + 2u * c), fb = lds_bf16(sbb + 2u * c);
+      const uint32_t wak[4] = {va.x, va.y, va.z, va.w}, wbk[4] = {vb.x, vb.y, vb.z, vb.w};
+      uint64_t pa[NT], pb[NT];
+#pragma unroll
+      for (int q = 0; q < NT; ++q) pa[q] = pb[q] = 0ull;
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        uint64_t qa[4], qb[4];
+        dequant8(wak[k], qa);
+        dequant8(wbk[k], qb);
+#pragma unroll
+        for (int q = 0; q < NT; ++q) {
+          const uint32_t hr = ha + q * hsb + 8u * off + 32u * k;
+          const uint4 h0 = lds128(hr), h1 = lds128(hr + 16);
+          const uint64_t hp[4] = {f2(h0.x, h0.y), f2(h0.z, h0.w), f2(h1.x, h1.y), f2(h1.z, h1.w)};
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            pa[q] = ffma2(qa[j], hp[j], pa[q]);
+            pb[q] = ffma2(qb[j], hp[j], pb[q]);
+          }
+        }
+      }
 #pragma unroll
       for (int q = 0; q < NT; ++q) {
-        const uint32_t hr = ha + q * hsb + 8u * off;
-        float p0 = 0.f, p1 = 0.f, r0 = 0.f, r1 = 0.f;
-        float4 h0 = lds128f(hr), h1 = lds128f(hr + 16);
-        fma8_int4f(va.x, h0, h1, p0, p1);
-        fma8_int4f(vb.x, h0, h1, r0, r1);
-        h0 = lds128f(hr + 32);
-        h1 = lds128f(hr + 48);
-        fma8_int4f(va.y, h0, h1, p0, p1);
-        fma8_int4f(vb.y, h0, h1, r0, r1);
-        h0 = lds128f(hr + 64);
-        h1 = lds128f(hr + 80);
-        fma8_int4f(va.z, h0, h1, p0, p1);
-        fma8_int4f(vb.z, h0, h1, r0, r1);
-        h0 = lds128f(hr + 96);
-        h1 = lds128f(hr + 112);
-        fma8_int4f(va.w, h0, h1, p0, p1);
-        fma8_int4f(vb.w, h0, h1, r0, r1);
-        a0[q] = fmaf(fa, p0 + p1, a0[q]);
-        b0[q] = fmaf(fb, r0 + r1, b0[q]);
+        a0[q] = fmaf(fa, f2sum(pa[q]), a0[q]);
+        b0[q] = fmaf(fb, f2sum(pb[q]), b0[q]);
       }
     }
   }
