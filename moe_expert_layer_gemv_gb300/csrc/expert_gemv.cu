@@ -160,6 +160,10 @@ __device__ __forceinline__ void dequant8(uint32_t v, uint64_t (&q)[4]) {
   }
 }
 
+__device__ __forceinline__ uint32_t word(const uint4& v, int k) {
+  return k == 0 ? v.x : (k == 1 ? v.y : (k == 2 ? v.z : v.w));
+}
+
 // Two bf16 (element 2j low, 2j + 1 high) as an fp32 pair.
 __device__ __forceinline__ uint64_t bf16x2_f2(uint32_t w) { return f2(w << 16, w & 0xffff0000u); }
 
@@ -193,46 +197,44 @@ __device__ __forceinline__ void gu_rows_bf16(uint32_t wg, uint32_t wu, uint32_t 
   }
 }
 
-// int4 weights: a 16-byte chunk is 32 codes = one scale group; the group's
-// bf16 scales at sg / su (one per chunk).  Each code is dequantised once and
-// used for every token; per token the group's products go into an
-// (even, odd) pair of partial sums, then scale x pair sum into the total.
+// int4 weights: 32 codes (16 bytes) form one scale group, with bf16 scales at
+// sg / su.  Lane l takes the 8-code words w = l, l + 32, ... of the rows, so
+// the lanes' x chunks and code words are consecutive in shared memory (no bank
+// conflicts).  Each word's codes are dequantised once and used for every token;
+// per token its 8 products go into an (even, odd) pair, and scale x pair sum
+// into the total.
 template <int NT>
 __device__ __forceinline__ void gu_rows_int4(uint32_t wg, uint32_t wu, uint32_t sg, uint32_t su,
-                                             uint32_t xa, uint32_t xs, int ngroups, int lane,
+                                             uint32_t xa, uint32_t xs, int nwords, int lane,
                                              float* g, float* u) {
   float ga[NT], ua[NT];
 #pragma unroll
   for (int q = 0; q < NT; ++q) ga[q] = ua[q] = 0.f;
-  for (int c = lane; c < ngroups; c += 32) {
-    const uint32_t off = (uint32_t)c * 16u;
-    const uint4 vg = lds128(wg + off), vu = lds128(wu + off);
-    const float fg = lds_bf16(sg + 2u * c), fu = lds_bf16(su + 2u * c);
-    const uint32_t wgk[4] = {vg.x, vg.y, vg.z, vg.w}, wuk[4] = {vu.x, vu.y, vu.z, vu.w};
-    uint64_t pg[NT], pu[NT];
-#pragma unroll
-    for (int q = 0; q < NT; ++q) pg[q] = pu[q] = 0ull;
-#pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      uint64_t qg[4], qu[4];
-      dequant8(wgk[k], qg);
-      dequant8(wuk[k], qu);
-#pragma unroll
-      for (int q = 0; q < NT; ++q) {
-        const uint4 xv = lds128(xa + q * xs + 4u * off + 16u * k);
-        const uint32_t xw[4] = {xv.x, xv.y, xv.z, xv.w};
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          const uint64_t xp = bf16x2_f2(xw[j]);
-          pg[q] = ffma2(qg[j], xp, pg[q]);
-          pu[q] = ffma2(qu[j], xp, pu[q]);
-        }
-      }
-    }
+#pragma unroll 2
+  for (int w = lane; w < nwords; w += 32) {
+    uint32_t cg, cu;
+    asm volatile("ld.shared.u32 %0, [%1];" : "=r"(cg) : "r"(wg + 4u * w));
+    asm volatile("ld.shared.u32 %0, [%1];" : "=r"(cu) : "r"(wu + 4u * w));
+    const float fg = lds_bf16(sg + 2u * (w >> 2)), fu = lds_bf16(su + 2u * (w >> 2));
+    uint64_t qg[4], qu[4];
+    dequant8(cg, qg);
+    dequant8(cu, qu);
 #pragma unroll
     for (int q = 0; q < NT; ++q) {
-      ga[q] = fmaf(fg, f2sum(pg[q]), ga[q]);
-      ua[q] = fmaf(fu, f2sum(pu[q]), ua[q]);
+      const uint4 xv = lds128(xa + q * xs + 16u * w);
+      uint64_t pg = 0ull, pu = 0ull;
+      const uint64_t x0 = bf16x2_f2(xv.x), x1 = bf16x2_f2(xv.y);
+      const uint64_t x2 = bf16x2_f2(xv.z), x3 = bf16x2_f2(xv.w);
+      pg = ffma2(qg[0], x0, pg);
+      pu = ffma2(qu[0], x0, pu);
+      pg = ffma2(qg[1], x1, pg);
+      pu = ffma2(qu[1], x1, pu);
+      pg = ffma2(qg[2], x2, pg);
+      pu = ffma2(qu[2], x2, pu);
+      pg = ffma2(qg[3], x3, pg);
+      pu = ffma2(qu[3], x3, pu);
+      ga[q] = fmaf(fg, f2sum(pg), ga[q]);
+      ua[q] = fmaf(fu, f2sum(pu), ua[q]);
     }
   }
 #pragma unroll
@@ -250,7 +252,7 @@ __device__ __forceinline__ void gu_warp(uint32_t wg, uint32_t wu, uint32_t sg, u
                                         size_t hstride) {
   float g[NT], u[NT];
   if (kInt4)
-    gu_rows_int4<NT>(wg, wu, sg, su, xa, xs, d / 32, lane, g, u);
+    gu_rows_int4<NT>(wg, wu, sg, su, xa, xs, d / 8, lane, g, u);
   else
     gu_rows_bf16<NT>(wg, wu, xa, xs, d / 8, lane, g, u);
   float gv = g[0], uv = u[0];
@@ -281,37 +283,55 @@ __device__ __forceinline__ void dn_rows2(uint32_t wa, uint32_t wb, uint32_t sa, 
       const uint4 va = lds128(wa + off), vb = lds128(wb + off);
 #pragma unroll
       for (int q = 0; q < NT; ++q) {
-        const float4 hp = lds128f(ha + q * hsb + 2u * off);
-        const float4 hq = lds128f(ha + q * hsb + 2u * off + 16u);
+        // Lanes sl >= 4 load the chunk's upper 16 bytes first (the lanes' h
+        // chunks are 32 bytes apart: this puts one load's lanes on distinct
+        // banks); the products are taken in the same order either way.
+        const uint32_t hb = ha + q * hsb + 2u * off;
+        const bool up = (sl >> 2) & 1;
+        const float4 first = lds128f(hb + (up ? 16u : 0u));
+        const float4 second = lds128f(hb + (up ? 0u : 16u));
+        const float4 hp = up ? second : first, hq = up ? first : second;
         fma8f(va, hp, hq, a0[q], a1[q]);
         fma8f(vb, hp, hq, b0[q], b1[q]);
       }
     }
   } else {
     // Codes dequantised once per group, h already fp32 pairs in shared memory.
+    // Lane sl's h chunks lie 128 bytes apart from its neighbours': it takes the
+    // group's words in the order (k + sl) mod 4 and, for sl >= 4, the upper 16
+    // bytes of each word first, so one load instruction's lanes hit distinct
+    // banks.
     for (int c = sl; c < Iw / 32; c += 8) {
       const uint32_t off = (uint32_t)c * 16u;
       const uint4 va = lds128(wa + off), vb = lds128(wb + off);
       const float fa = lds_bf16(sa + 2u * c), fb = lds_bf16(sbb + 2u * c);
-      const uint32_t wak[4] = {va.x, va.y, va.z, va.w}, wbk[4] = {vb.x, vb.y, vb.z, vb.w};
+      const bool up = (sl >> 2) & 1;  // upper half first
       uint64_t pa[NT], pb[NT];
 #pragma unroll
       for (int q = 0; q < NT; ++q) pa[q] = pb[q] = 0ull;
 #pragma unroll
-      for (int k = 0; k < 4; ++k) {
+      for (int k0 = 0; k0 < 4; ++k0) {
+        const int k = (k0 + sl) & 3;
         uint64_t qa[4], qb[4];
-        dequant8(wak[k], qa);
-        dequant8(wbk[k], qb);
+        dequant8(word(va, k), qa);
+        dequant8(word(vb, k), qb);
+        // Pairs in load order: 2, 3 then 0, 1 for the upper-first lanes.
+        const uint64_t qa0 = up ? qa[2] : qa[0], qa1 = up ? qa[3] : qa[1];
+        const uint64_t qa2 = up ? qa[0] : qa[2], qa3 = up ? qa[1] : qa[3];
+        const uint64_t qb0 = up ? qb[2] : qb[0], qb1 = up ? qb[3] : qb[1];
+        const uint64_t qb2 = up ? qb[0] : qb[2], qb3 = up ? qb[1] : qb[3];
 #pragma unroll
         for (int q = 0; q < NT; ++q) {
-          const uint32_t hr = ha + q * hsb + 8u * off + 32u * k;
-          const uint4 h0 = lds128(hr), h1 = lds128(hr + 16);
-          const uint64_t hp[4] = {f2(h0.x, h0.y), f2(h0.z, h0.w), f2(h1.x, h1.y), f2(h1.z, h1.w)};
-#pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            pa[q] = ffma2(qa[j], hp[j], pa[q]);
-            pb[q] = ffma2(qb[j], hp[j], pb[q]);
-          }
+          const uint32_t hr = ha + q * hsb + 8u * off + 32u * (uint32_t)k;
+          const uint4 h0 = lds128(hr + (up ? 16u : 0u)), h1 = lds128(hr + (up ? 0u : 16u));
+          pa[q] = ffma2(qa0, f2(h0.x, h0.y), pa[q]);
+          pb[q] = ffma2(qb0, f2(h0.x, h0.y), pb[q]);
+          pa[q] = ffma2(qa1, f2(h0.z, h0.w), pa[q]);
+          pb[q] = ffma2(qb1, f2(h0.z, h0.w), pb[q]);
+          pa[q] = ffma2(qa2, f2(h1.x, h1.y), pa[q]);
+          pb[q] = ffma2(qb2, f2(h1.x, h1.y), pb[q]);
+          pa[q] = ffma2(qa3, f2(h1.z, h1.w), pa[q]);
+          pb[q] = ffma2(qb3, f2(h1.z, h1.w), pb[q]);
         }
       }
 #pragma unroll
