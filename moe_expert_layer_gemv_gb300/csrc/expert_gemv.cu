@@ -109,29 +109,6 @@ __device__ __forceinline__ float lds_bf16(uint32_t addr) {
 }
 
 // ------------------------------------------------------------------ dot pieces
-// Two independent accumulators (even / odd elements) for 8 bf16 products.
-__device__ __forceinline__ void fma8(uint4 w, uint4 x, float& a0, float& a1) {
-  a0 = fmaf(bf16lo(w.x), bf16lo(x.x), a0);
-  a1 = fmaf(bf16hi(w.x), bf16hi(x.x), a1);
-  a0 = fmaf(bf16lo(w.y), bf16lo(x.y), a0);
-  a1 = fmaf(bf16hi(w.y), bf16hi(x.y), a1);
-  a0 = fmaf(bf16lo(w.z), bf16lo(x.z), a0);
-  a1 = fmaf(bf16hi(w.z), bf16hi(x.z), a1);
-  a0 = fmaf(bf16lo(w.w), bf16lo(x.w), a0);
-  a1 = fmaf(bf16hi(w.w), bf16hi(x.w), a1);
-}
-
-__device__ __forceinline__ void fma8f(uint4 w, float4 p, float4 q, float& a0, float& a1) {
-  a0 = fmaf(bf16lo(w.x), p.x, a0);
-  a1 = fmaf(bf16hi(w.x), p.y, a1);
-  a0 = fmaf(bf16lo(w.y), p.z, a0);
-  a1 = fmaf(bf16hi(w.y), p.w, a1);
-  a0 = fmaf(bf16lo(w.z), q.x, a0);
-  a1 = fmaf(bf16hi(w.z), q.y, a1);
-  a0 = fmaf(bf16lo(w.w), q.z, a0);
-  a1 = fmaf(bf16hi(w.w), q.w, a1);
-}
-
 // Packed fp32 pairs (element 2j in the low word, 2j + 1 in the high word): one
 // instruction does both lanes' fma / sub, each rounded as the scalar would be.
 __device__ __forceinline__ uint64_t f2(uint32_t lo, uint32_t hi) {
@@ -171,29 +148,43 @@ __device__ __forceinline__ uint64_t bf16x2_f2(uint32_t w) { return f2(w << 16, w
 // One warp: gate row at wg, up row at wu (shared addresses), NT token rows at
 // xa + q * xs.  bf16 weights; 16-byte chunks strided over the lanes.  Returns
 // the per-token full dot products in every lane.
+// The (even, odd) products of each bf16 pair go into an fp32 pair with one
+// packed fma: the order of the sums is that of two scalar accumulators.
 template <int NT>
 __device__ __forceinline__ void gu_rows_bf16(uint32_t wg, uint32_t wu, uint32_t xa, uint32_t xs,
                                              int nch, int lane, float* g, float* u) {
-  float g0[NT], g1[NT], u0[NT], u1[NT];
+  uint64_t pg[NT], pu[NT];
 #pragma unroll
-  for (int q = 0; q < NT; ++q) g0[q] = g1[q] = u0[q] = u1[q] = 0.f;
+  for (int q = 0; q < NT; ++q) pg[q] = pu[q] = 0ull;
 #pragma unroll 2
   for (int c = lane; c < nch; c += 32) {
     const uint32_t off = (uint32_t)c * 16u;
     const uint4 vg = lds128(wg + off), vu = lds128(wu + off);
+    const uint64_t g0 = bf16x2_f2(vg.x), g1 = bf16x2_f2(vg.y), g2 = bf16x2_f2(vg.z),
+                   g3 = bf16x2_f2(vg.w);
+    const uint64_t u0 = bf16x2_f2(vu.x), u1 = bf16x2_f2(vu.y), u2 = bf16x2_f2(vu.z),
+                   u3 = bf16x2_f2(vu.w);
     uint4 xv[NT];
 #pragma unroll
     for (int q = 0; q < NT; ++q) xv[q] = lds128(xa + q * xs + off);
 #pragma unroll
     for (int q = 0; q < NT; ++q) {
-      fma8(vg, xv[q], g0[q], g1[q]);
-      fma8(vu, xv[q], u0[q], u1[q]);
+      const uint64_t x0 = bf16x2_f2(xv[q].x), x1 = bf16x2_f2(xv[q].y), x2 = bf16x2_f2(xv[q].z),
+                     x3 = bf16x2_f2(xv[q].w);
+      pg[q] = ffma2(g0, x0, pg[q]);
+      pu[q] = ffma2(u0, x0, pu[q]);
+      pg[q] = ffma2(g1, x1, pg[q]);
+      pu[q] = ffma2(u1, x1, pu[q]);
+      pg[q] = ffma2(g2, x2, pg[q]);
+      pu[q] = ffma2(u2, x2, pu[q]);
+      pg[q] = ffma2(g3, x3, pg[q]);
+      pu[q] = ffma2(u3, x3, pu[q]);
     }
   }
 #pragma unroll
   for (int q = 0; q < NT; ++q) {
-    g[q] = warp_sum(g0[q] + g1[q]);
-    u[q] = warp_sum(u0[q] + u1[q]);
+    g[q] = warp_sum(f2sum(pg[q]));
+    u[q] = warp_sum(f2sum(pu[q]));
   }
 }
 
@@ -277,10 +268,18 @@ __device__ __forceinline__ void dn_rows2(uint32_t wa, uint32_t wb, uint32_t sa, 
 #pragma unroll
   for (int q = 0; q < NT; ++q) a0[q] = a1[q] = b0[q] = b1[q] = 0.f;
   if (!kInt4) {
+    // (even, odd) pairs with packed fmas: the sums of a0/a1 and b0/b1 in order.
+    uint64_t pa[NT], pb[NT];
+#pragma unroll
+    for (int q = 0; q < NT; ++q) pa[q] = pb[q] = 0ull;
 #pragma unroll 2
     for (int c = sl; c < Iw / 8; c += 8) {
       const uint32_t off = (uint32_t)c * 16u;
       const uint4 va = lds128(wa + off), vb = lds128(wb + off);
+      const uint64_t wa0 = bf16x2_f2(va.x), wa1 = bf16x2_f2(va.y), wa2 = bf16x2_f2(va.z),
+                     wa3 = bf16x2_f2(va.w);
+      const uint64_t wb0 = bf16x2_f2(vb.x), wb1 = bf16x2_f2(vb.y), wb2 = bf16x2_f2(vb.z),
+                     wb3 = bf16x2_f2(vb.w);
 #pragma unroll
       for (int q = 0; q < NT; ++q) {
         // Lanes sl >= 4 load the chunk's upper 16 bytes first (the lanes' h
@@ -291,9 +290,26 @@ __device__ __forceinline__ void dn_rows2(uint32_t wa, uint32_t wb, uint32_t sa, 
         const float4 first = lds128f(hb + (up ? 16u : 0u));
         const float4 second = lds128f(hb + (up ? 0u : 16u));
         const float4 hp = up ? second : first, hq = up ? first : second;
-        fma8f(va, hp, hq, a0[q], a1[q]);
-        fma8f(vb, hp, hq, b0[q], b1[q]);
+        const uint64_t h0 = f2(__float_as_uint(hp.x), __float_as_uint(hp.y));
+        const uint64_t h1 = f2(__float_as_uint(hp.z), __float_as_uint(hp.w));
+        const uint64_t h2 = f2(__float_as_uint(hq.x), __float_as_uint(hq.y));
+        const uint64_t h3 = f2(__float_as_uint(hq.z), __float_as_uint(hq.w));
+        pa[q] = ffma2(wa0, h0, pa[q]);
+        pb[q] = ffma2(wb0, h0, pb[q]);
+        pa[q] = ffma2(wa1, h1, pa[q]);
+        pb[q] = ffma2(wb1, h1, pb[q]);
+        pa[q] = ffma2(wa2, h2, pa[q]);
+        pb[q] = ffma2(wb2, h2, pb[q]);
+        pa[q] = ffma2(wa3, h3, pa[q]);
+        pb[q] = ffma2(wb3, h3, pb[q]);
       }
+    }
+#pragma unroll
+    for (int q = 0; q < NT; ++q) {
+      a0[q] = __uint_as_float((uint32_t)pa[q]);
+      a1[q] = __uint_as_float((uint32_t)(pa[q] >> 32));
+      b0[q] = __uint_as_float((uint32_t)pb[q]);
+      b1[q] = __uint_as_float((uint32_t)(pb[q] >> 32));
     }
   } else {
     // Codes dequantised once per group, h already fp32 pairs in shared memory.
