@@ -120,8 +120,11 @@ const char* moe_status_string(moe_status_t status);
  * 0 and the status says why). */
 moe_status_t moe_workspace_bytes(const moe_dims_t* dims, size_t* bytes);
 
-/* Zero a workspace's control words (the device status word) on `stream`.  Call
- * once after allocating it. */
+/* Zero a workspace's control words on `stream`: the device status word and the
+ * arrival counters of the routing and align kernels (each launch returns its
+ * counters to zero).  Call once after allocating the workspace, and again if a
+ * call left MOE_ERR_TIMEOUT in the status word (its launches may have stopped
+ * short of resetting a counter). */
 moe_status_t moe_workspace_init(void* workspace, size_t workspace_bytes, void* stream);
 
 /* Router GEMV + softmax + top-k + renormalisation ("veloGB10", Kernel work:
