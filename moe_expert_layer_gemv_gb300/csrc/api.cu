@@ -199,6 +199,16 @@ moe_status_t expert_plan(const moe_dims_t& dm, void* ws, const Layout& L, int sm
   pp.tiles_dn_shared = dm.I_shared > 0 ? (int)ceil_div(dm.d, ep->dn.rg_shared) : 0;
   pp.xt_gu = ep->gu.xt;
   pp.xt_dn = ep->dn.xt;
+  // Unit costs of the static CTA split, in tokens of arithmetic (chosen by
+  // timing the decode layers).  A bf16 gate_up unit streams its weight rows
+  // from HBM in about the time of four tokens' arithmetic on them.  A bf16
+  // down unit is worth about three: each of its tokens re-reads an h row from
+  // shared memory per row pair.  Beside the dequant-bound int4 experts, down
+  // units of both kinds balance best at eight.
+  pp.base_gu = 4;
+  pp.base_dn = fmt ? 8 : 3;
+  pp.base_gu_s = 4;
+  pp.base_dn_s = fmt ? 8 : 3;
   ep->sms = sms;
   ep->tc = L.tc && tc_supported(dm.weight_format, dm.d, dm.I, dm.I_shared, dm.block_size);
   pp.tc_nb_gu = ep->tc ? tc_tiles_per_mblock_gu(dm.I) : 0;

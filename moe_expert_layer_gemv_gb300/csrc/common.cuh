@@ -147,6 +147,12 @@ __device__ __forceinline__ uint64_t policy_evict_last() {
 
 // Global -> shared bulk copy (non-tensor TMA).  dst, src 16-byte aligned; bytes
 // a multiple of 16.  Completion is signalled on `bar` as transaction bytes.
+// Bulk prefetch of [src, src + bytes) into L2 (no completion to wait for);
+// src 16-byte aligned, bytes a multiple of 16.
+__device__ __forceinline__ void bulk_prefetch_l2(const void* src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
+}
+
 __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar,
                                          uint64_t policy) {
   asm volatile(

@@ -36,6 +36,7 @@ struct GuArgs {
   const uint8_t* gu;          // routed gate_up: bf16 [E][2I][d] or codes [E][2I][d/2]
   const uint16_t* gu_scales;  // int4 scales [E][2I][d/32]
   const uint8_t* sgu;         // shared gate_up bf16 [2Is][d] (may be null)
+  const uint8_t* sdn;         // shared down bf16 [d][Is] (prefetched into L2 only)
   const uint16_t* x;          // [T][d]
   const int32_t* sorted_ids;
   const Plan* plan;
@@ -382,6 +383,17 @@ __device__ void drain_stages(uint64_t* full, int issued, int n_stages, int* stat
 }
 
 // --------------------------------------------------------------------------- gate_up
+// This CTA's 16-byte-aligned slice of [p, p + bytes) (bytes a multiple of 16),
+// prefetched into L2 in pieces of at most 64 KB.
+__device__ __forceinline__ void prefetch_slice_l2(const uint8_t* p, size_t bytes) {
+  if (p == nullptr) return;
+  const size_t per = (ceil_div(bytes, (size_t)gridDim.x) + 15) & ~(size_t)15;
+  const size_t b0 = per * blockIdx.x;
+  const size_t b1 = min(bytes, b0 + per);
+  for (size_t b = b0; b < b1; b += 65536)
+    bulk_prefetch_l2(p + b, (uint32_t)min((size_t)65536, b1 - b));
+}
+
 template <int kFmt>
 __global__ void __launch_bounds__(kThreads, kCtasPerSm) gate_up_kernel(const GuArgs a) {
   extern __shared__ __align__(128) uint8_t smem[];
@@ -398,6 +410,14 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) gate_up_kernel(const GuA
       mbar_init(&empty[s], kConsumerWarps);
     }
     fence_barrier_init();
+  }
+  // The shared expert's weights do not depend on the routing: each CTA
+  // prefetches its slice of them into L2 while the routing kernel still runs
+  // and HBM is otherwise idle, which takes their reads out of the weight stream
+  // of this stage and the next.
+  if (threadIdx.x == kConsumerWarps * 32 && a.sgu != nullptr) {
+    prefetch_slice_l2(a.sgu, (size_t)4 * a.Is * a.d);
+    prefetch_slice_l2(a.sdn, (size_t)2 * a.Is * a.d);
   }
   __syncthreads();
   pdl_wait();
@@ -439,23 +459,6 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) gate_up_kernel(const GuA
       const int nr = min(RG, Iw - r0);
       const int g0 = grp * xt;
       const int nt = min(xt, we.n_tok - g0);
-      // Token rows of this group: looked up once per (work expert, group).
-      if (cur.i != tok_i || grp != tok_g) {
-        tok_i = cur.i;
-        tok_g = grp;
-        tok = 0;
-        if (lane >= 4 && lane < 4 + nt) {
-          tok = g0 + lane - 4;
-          if (!shared) {
-            const int slot = a.sorted_ids[we.pos + g0 + lane - 4];
-            tok = slot / a.k;
-            if (slot < 0 || tok >= a.T) {
-              record_status(a.status, kStatusDeviceCheck);
-              tok = 0;
-            }
-          }
-        }
-      }
       if (use > 0 && !mbar_wait(&empty[s], (uint32_t)((use - 1) & 1), a.status)) {
         ok = false;
         break;
@@ -478,6 +481,24 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) gate_up_kernel(const GuA
         if (lane == 3)
           bulk_g2s(st + 2 * RG * rb + RG * sb, sbase + (size_t)(Iw + r0) * sb, nr * sb, &full[s],
                    pol_w);
+      }
+      // Token rows of this group (looked up once per (work expert, group)),
+      // after the weight copies are under way: they come from L2.
+      if (cur.i != tok_i || grp != tok_g) {
+        tok_i = cur.i;
+        tok_g = grp;
+        tok = 0;
+        if (lane >= 4 && lane < 4 + nt) {
+          tok = g0 + lane - 4;
+          if (!shared) {
+            const int slot = a.sorted_ids[we.pos + g0 + lane - 4];
+            tok = slot / a.k;
+            if (slot < 0 || tok >= a.T) {
+              record_status(a.status, kStatusDeviceCheck);
+              tok = 0;
+            }
+          }
+        }
       }
       const int xoff = 2 * RG * (rb + sb);
       if (lane >= 4 && lane < 4 + nt)
@@ -776,6 +797,7 @@ cudaError_t launch_gate_up(const LaunchCfg& c, const ExpertArgs& e, const GemvSh
   a.gu = static_cast<const uint8_t*>(e.gate_up);
   a.gu_scales = e.gate_up_scales;
   a.sgu = reinterpret_cast<const uint8_t*>(e.s_gate_up);
+  a.sdn = reinterpret_cast<const uint8_t*>(e.s_down);
   a.x = x;
   a.sorted_ids = sorted_ids;
   a.plan = plan;

@@ -36,6 +36,10 @@ struct PlanParams {
   int tiles_dn_shared;
   int xt_gu;             // tokens per gate_up unit
   int xt_dn;             // tokens per down unit
+  int base_gu;           // fixed cost of a routed gate_up unit, in tokens of arithmetic
+  int base_dn;           // same for down
+  int base_gu_s;         // same for the shared expert's (bf16) units
+  int base_dn_s;
   int tc_nb_gu;          // tensor-core path: N blocks per expert (0 = no tensor-core plan)
   int tc_nb_dn;
   int grid;              // CTAs of the persistent expert kernels (<= kMaxGrid)

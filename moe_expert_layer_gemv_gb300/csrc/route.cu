@@ -313,21 +313,22 @@ __device__ __forceinline__ int expert_run(int E) { return (E + blockDim.x - 1) /
 
 // ------------------------------------------------------------------ plan
 // Estimated cost of a unit with nt tokens, in token-equivalents: a fixed part
-// for streaming the unit's weight rows plus one per token of arithmetic.
-constexpr int kUnitBaseCost = 4;
+// `base` for streaming (and, int4, dequantising) the unit's weight rows plus
+// one per token of arithmetic.  The routed experts' base and the shared
+// expert's are separate (PlanParams::base_gu / base_gu_s, base_dn / base_dn_s).
 
-__device__ int unit_at_cost(int target, int c0, int u0, int tiles, int n, int xt) {
+__device__ int unit_at_cost(int target, int c0, int u0, int tiles, int n, int xt, int base) {
   const int groups = (n + xt - 1) / xt;
   const int nt_last = n - (groups - 1) * xt;
-  const int per_full = tiles * (kUnitBaseCost + xt);
+  const int per_full = tiles * (base + xt);
   const int r = target - c0;
   int g, t;
   if (groups > 1 && r < (groups - 1) * per_full) {
     g = r / per_full;
-    t = (r - g * per_full) / (kUnitBaseCost + xt);
+    t = (r - g * per_full) / (base + xt);
   } else {
     g = groups - 1;
-    t = (r - (groups - 1) * per_full) / (kUnitBaseCost + nt_last);
+    t = (r - (groups - 1) * per_full) / (base + nt_last);
     t = min(t, tiles - 1);
   }
   return u0 + g * tiles + t;
@@ -337,8 +338,8 @@ __device__ int unit_at_cost(int target, int c0, int u0, int tiles, int n, int xt
 // cta[grid + 1 + c]: its share of the stage's estimated cost starts at
 // c * total / grid (taken in fp32: monotone in c, exact enough for balancing).
 __device__ void split_one(int c, int n_work, const int* s_cost, const int* s_unit, const int* s_n,
-                          const int* s_tiles, int total_cost, int total_units, int xt, int grid,
-                          int32_t* cta) {
+                          const int* s_tiles, int total_cost, int total_units, int xt, int base,
+                          int base_s, bool has_shared, int grid, int32_t* cta) {
   if (c == grid || n_work == 0) {
     cta[c] = c == grid ? total_units : 0;
     if (c < grid) cta[grid + 1 + c] = 0;
@@ -350,7 +351,8 @@ __device__ void split_one(int c, int n_work, const int* s_cost, const int* s_uni
     const int mid = (lo + hi + 1) >> 1;
     if (s_cost[mid] <= target) lo = mid; else hi = mid - 1;
   }
-  cta[c] = c == 0 ? 0 : unit_at_cost(target, s_cost[lo], s_unit[lo], s_tiles[lo], s_n[lo], xt);
+  cta[c] = c == 0 ? 0 : unit_at_cost(target, s_cost[lo], s_unit[lo], s_tiles[lo], s_n[lo], xt,
+                                      has_shared && lo == n_work - 1 ? base_s : base);
   cta[grid + 1 + c] = lo;
 }
 
@@ -367,8 +369,8 @@ __device__ __forceinline__ void expert_vals(int c, int B, const PlanParams& pp, 
   v[1] = t ? 1 : 0;
   v[2] = t ? pp.tiles_gu * ggu : 0;
   v[3] = t ? pp.tiles_dn * gdn : 0;
-  v[4] = t ? pp.tiles_gu * (ggu * kUnitBaseCost + c) : 0;
-  v[5] = t ? pp.tiles_dn * (gdn * kUnitBaseCost + c) : 0;
+  v[4] = t ? pp.tiles_gu * (ggu * pp.base_gu + c) : 0;
+  v[5] = t ? pp.tiles_dn * (gdn * pp.base_dn + c) : 0;
   v[6] = mb * pp.tc_nb_gu;
   v[7] = mb * pp.tc_nb_dn;
 }
@@ -383,6 +385,7 @@ struct AlignOut {
 // Plan totals every thread needs for the split.
 struct PlanTotals {
   int n_work, units_gu, units_dn, cost_gu, cost_dn, num_post_pad, tc_gu, tc_dn;
+  bool has_shared;  // the last work expert is the shared expert
 };
 
 // From per-expert counts cnt[E] (shared memory): one block scan of the
@@ -456,7 +459,7 @@ __device__ PlanTotals layout_and_plan(const int* cnt, int* off, int E, int T, in
     o->expert_offsets[E] = tot[0];
     *o->num_post_pad = tot[0];
   }
-  PlanTotals pt{tot[1], tot[2], tot[3], tot[4], tot[5], tot[0], tot[6], tot[7]};
+  PlanTotals pt{tot[1], tot[2], tot[3], tot[4], tot[5], tot[0], tot[6], tot[7], false};
   if (pp.work != nullptr && pp.tiles_gu_shared > 0 && T > 0) {
     const int sg = (T + pp.xt_gu - 1) / pp.xt_gu, sd = (T + pp.xt_dn - 1) / pp.xt_dn;
     if (threadIdx.x == 0) {
@@ -479,10 +482,11 @@ __device__ PlanTotals layout_and_plan(const int* cnt, int* off, int E, int T, in
       s_tdn[pt.n_work] = pp.tiles_dn_shared;
     }
     pt.n_work += 1;
+    pt.has_shared = true;
     pt.units_gu += pp.tiles_gu_shared * sg;
     pt.units_dn += pp.tiles_dn_shared * sd;
-    pt.cost_gu += pp.tiles_gu_shared * (sg * kUnitBaseCost + T);
-    pt.cost_dn += pp.tiles_dn_shared * (sd * kUnitBaseCost + T);
+    pt.cost_gu += pp.tiles_gu_shared * (sg * pp.base_gu_s + T);
+    pt.cost_dn += pp.tiles_dn_shared * (sd * pp.base_dn_s + T);
     const int mbs = (T + kTcRows - 1) / kTcRows;
     pt.tc_gu += mbs * pp.tc_nb_gu;
     pt.tc_dn += mbs * pp.tc_nb_dn;
@@ -499,10 +503,11 @@ __device__ void split_stages(const PlanTotals& pt, int E, const PlanParams& pp, 
   for (int i = threadIdx.x; pp.tc_nb_gu == 0 && i < 2 * per; i += blockDim.x) {
     if (i < per)
       split_one(i, pt.n_work, tmp + 2 * W, tmp, tmp + 4 * W, tmp + 5 * W, pt.cost_gu, pt.units_gu,
-                pp.xt_gu, pp.grid, pp.cta_gu);
+                pp.xt_gu, pp.base_gu, pp.base_gu_s, pt.has_shared, pp.grid, pp.cta_gu);
     else
       split_one(i - per, pt.n_work, tmp + 3 * W, tmp + W, tmp + 4 * W, tmp + 6 * W, pt.cost_dn,
-                pt.units_dn, pp.xt_dn, pp.grid, pp.cta_dn);
+                pt.units_dn, pp.xt_dn, pp.base_dn, pp.base_dn_s, pt.has_shared, pp.grid,
+                pp.cta_dn);
   }
   if (threadIdx.x == 0) {
     Plan p;
