@@ -179,8 +179,9 @@ def kernel_traffic(src_name, workload, algorithmic_bytes):
 
 
 # --------------------------------------------------------------------------- CPU oracle
-def oracle_tokens_per_s(inp, seconds, nthreads=0):
-    """Time the fp64 oracle on whole batches of the workload until `seconds`."""
+def oracle_tokens_per_s(inp, seconds, nthreads=0, chunk=0):
+    """Time the fp64 oracle on the workload's batch until `seconds`: whole
+    batches, or (chunk > 0) successive runs of `chunk` of its tokens."""
     import oracle
     from moe_expert_layer_gemv_gb300 import inputs as I
 
@@ -197,10 +198,17 @@ def oracle_tokens_per_s(inp, seconds, nthreads=0):
     dims = {"T": s.T, "d": s.d, "E": s.E, "k": s.k, "I": s.I, "Is": s.Is,
             "renormalize": int(s.renormalize)}
     xb, rb = I.bits(inp["x"]), I.bits(inp["router_w"])
+    import numpy as np
+
     tokens, t0 = 0, time.perf_counter()
     while True:
-        oracle.layer(xb, rb, ex, sh, dims, nthreads=nthreads)
-        tokens += s.T
+        if chunk > 0:
+            sel = (tokens + np.arange(chunk, dtype=np.int32)) % s.T
+            oracle.layer(xb, rb, ex, sh, dims, tokens=sel, nthreads=nthreads)
+            tokens += chunk
+        else:
+            oracle.layer(xb, rb, ex, sh, dims, nthreads=nthreads)
+            tokens += s.T
         el = time.perf_counter() - t0
         if el >= seconds:
             break
@@ -271,6 +279,11 @@ def main():
         cpu = {"value": v, "unit": UNIT, "cores": threads, "kind": "oracle",
                "sample": f"{ntok // shape.T} whole steps ({ntok} tokens) of the {shape.name} "
                          f"workload, {el:.1f} s, fp64 OpenMP over tokens"}
+        ch = min(shape.T, 8)
+        v1, _, ntok1, el1 = oracle_tokens_per_s(inp0, args.cpu_seconds / 5, nthreads=1, chunk=ch)
+        cpu["one_thread"] = {"value": v1, "unit": UNIT, "cores": 1,
+                             "sample": f"{ntok1} tokens of the same batch, {ch} per call, "
+                                       f"{el1:.1f} s"}
 
     # Device state: weight copies rotated across steps, token batches rotated.
     props = torch.cuda.get_device_properties(dev)
@@ -305,18 +318,40 @@ def main():
     time.sleep(0.3)
     if world > 1:
         dist.barrier()
-    torch.cuda.synchronize()
-    launches0 = abi.moe_kernel_launch_count()
-    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    ev0.record()
-    for i in range(args.steps):
-        step(i)
-    ev1.record()
-    torch.cuda.synchronize()
-    if world > 1:
-        dist.barrier()
-    gpu_launches = abi.moe_kernel_launch_count() - launches0
-    ms = ev0.elapsed_time(ev1) / args.steps
+    # The K steps run as (up to) 5 rounds with an event at each boundary; the
+    # value is the whole region.  A round set whose per-round times vary by
+    # more than 3 % (coefficient of variation) is run once more.
+    def region_a():
+        torch.cuda.synchronize()
+        n0 = abi.moe_kernel_launch_count()
+        nr = min(5, args.steps)
+        cut = [round(r * args.steps / nr) for r in range(nr + 1)]
+        ev = [torch.cuda.Event(enable_timing=True) for _ in range(nr + 1)]
+        ev[0].record()
+        for r in range(nr):
+            for i in range(cut[r], cut[r + 1]):
+                step(i)
+            ev[r + 1].record()
+        torch.cuda.synchronize()
+        if world > 1:
+            dist.barrier()
+        per = [ev[r].elapsed_time(ev[r + 1]) / (cut[r + 1] - cut[r]) for r in range(nr)]
+        cv = statistics.pstdev(per) / statistics.mean(per)
+        return (ev[0].elapsed_time(ev[nr]) / args.steps, abi.moe_kernel_launch_count() - n0,
+                {"n": nr, "us_per_step": [round(v * 1e3, 2) for v in per],
+                 "median_us": statistics.median(per) * 1e3, "cv": cv})
+
+    ms, gpu_launches, rounds = region_a()
+    first_cv = rounds["cv"]
+    if world > 1:  # every rank takes the same decision
+        c = torch.tensor([first_cv], device=dev)
+        dist.all_reduce(c, op=dist.ReduceOp.MAX)
+        first_cv = c.item()
+    if first_cv > 0.03:
+        if world > 1:
+            dist.barrier()
+        ms, gpu_launches, rounds = region_a()
+        rounds["rerun_after_cv"] = first_cv
 
     # ---- timed region B: same steps with per-stage events (kernel durations)
     evs = [[torch.cuda.Event(enable_timing=True) for _ in range(abi.MOE_EV_COUNT)]
@@ -380,6 +415,7 @@ def main():
             "touched_experts": alg["touched"],
             "stage_us": {k: v * 1e3 for k, v in stage_ms.items()},
             "timed_pass_us": ms_timed * 1e3,
+            "rounds": rounds,
             "layer_tflops": alg["flops"] / (ms * 1e-3) / 1e12,
             "roofline": {"kernel": kname, "bound": "hbm", "achieved": achieved,
                          "peak": peaks["hbm_gbs"], "unit": "GB/s",
