@@ -56,6 +56,26 @@ def dist_env():
     return rank, world, local
 
 
+def ranks_max(vals, dev):
+    """Element-wise max of `vals` over the ranks of the process group (each
+    rank's own values when there is none): per-step times, so the job's time
+    is its slowest replica's."""
+    import torch
+    import torch.distributed as dist
+
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return [float(v) for v in vals]
+    t = torch.tensor([float(v) for v in vals], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return t.tolist()
+
+
+def job_tokens_per_s(T, world, ms_per_step):
+    """Whole-job throughput: every replica processes T tokens per step, and
+    the step time is the max over ranks."""
+    return world * T / (ms_per_step * 1e-3)
+
+
 def measured_peaks():
     try:
         with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
@@ -179,6 +199,15 @@ def kernel_traffic(src_name, workload, algorithmic_bytes):
 
 
 # --------------------------------------------------------------------------- CPU oracle
+def host_cores():
+    """Cores this process may run on (torchrun sets OMP_NUM_THREADS=1 for
+    multi-process jobs, so the oracle is given this count explicitly)."""
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
 def oracle_tokens_per_s(inp, seconds, nthreads=0, chunk=0):
     """Time the fp64 oracle on the workload's batch until `seconds`: whole
     batches, or (chunk > 0) successive runs of `chunk` of its tokens."""
@@ -219,20 +248,19 @@ def oracle_tokens_per_s(inp, seconds, nthreads=0, chunk=0):
 def run_reference(args, shape):
     """The reference arm: the fp64 CPU oracle on the host cores."""
     from moe_expert_layer_gemv_gb300 import inputs as I
-    import oracle
 
     rank, world, _ = dist_env()
     if rank != 0:
         return
     inp = I.make_inputs(shape, seed=0)
+    cores = host_cores()
     for _ in range(args.warmup):
-        oracle_tokens_per_s(inp, 0.0)
+        oracle_tokens_per_s(inp, 0.0, nthreads=cores)
     t0 = time.perf_counter()
     for _ in range(args.steps):
-        oracle_tokens_per_s(inp, 0.0)
+        oracle_tokens_per_s(inp, 0.0, nthreads=cores)
     el = time.perf_counter() - t0
     v = args.steps * shape.T / el
-    cores = oracle.max_threads()
     line = {"impl": "reference", "metric": METRIC, "value": v, "unit": UNIT, "n_gpus": args.gpus,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": el / args.steps * 1e3,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
@@ -275,7 +303,7 @@ def main():
     cpu = None
     inp0 = I.make_inputs(shape, seed=0)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        v, threads, ntok, el = oracle_tokens_per_s(inp0, args.cpu_seconds)
+        v, threads, ntok, el = oracle_tokens_per_s(inp0, args.cpu_seconds, nthreads=host_cores())
         cpu = {"value": v, "unit": UNIT, "cores": threads, "kind": "oracle",
                "sample": f"{ntok // shape.T} whole steps ({ntok} tokens) of the {shape.name} "
                          f"workload, {el:.1f} s, fp64 OpenMP over tokens"}
@@ -342,11 +370,7 @@ def main():
                  "median_us": statistics.median(per) * 1e3, "cv": cv})
 
     ms, gpu_launches, rounds = region_a()
-    first_cv = rounds["cv"]
-    if world > 1:  # every rank takes the same decision
-        c = torch.tensor([first_cv], device=dev)
-        dist.all_reduce(c, op=dist.ReduceOp.MAX)
-        first_cv = c.item()
+    first_cv = ranks_max([rounds["cv"]], dev)[0]  # every rank takes the same decision
     if first_cv > 0.03:
         if world > 1:
             dist.barrier()
@@ -384,10 +408,7 @@ def main():
     ms_e2e = e0.elapsed_time(e1) / args.steps
     clk = clocks.stop()
 
-    if world > 1:
-        t = torch.tensor([ms, ms_e2e], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms, ms_e2e = t.tolist()
+    ms, ms_e2e = ranks_max([ms, ms_e2e], dev)
 
     peaks, peak_kind = measured_peaks()
     gu_ms = stage_ms["gate_up"]
@@ -398,7 +419,7 @@ def main():
     kname = ("grouped_tc_kernel<gate_up, N=256>" if tc else
              f"gate_up_kernel<{'int4' if shape.fmt == 'int4' else 'bf16'}>")
     if rank == 0:
-        tok_s = world * shape.T / (ms * 1e-3)
+        tok_s = job_tokens_per_s(shape.T, world, ms)
         line = {
             "metric": METRIC, "value": tok_s, "unit": UNIT, "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
@@ -422,7 +443,7 @@ def main():
                          "frac": achieved / peaks["hbm_gbs"], "traffic": traffic,
                          "algorithmic_bytes": alg["gate_up_bytes"], "peak_source": peak_kind},
             "cpu_baseline": cpu,
-            "e2e": {"value": world * shape.T / (ms_e2e * 1e-3), "unit": UNIT,
+            "e2e": {"value": job_tokens_per_s(shape.T, world, ms_e2e), "unit": UNIT,
                     "h2d_bytes_per_step": shape.T * shape.d * 2,
                     "d2h_bytes_per_step": shape.T * shape.d * 2,
                     "wall_value": args.steps * world * shape.T / t_wall},
