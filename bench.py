@@ -423,7 +423,9 @@ def main():
         line = {
             "metric": METRIC, "value": tok_s, "unit": UNIT, "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
-            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            # operands as stored (bf16, or int4 codes with bf16 group scales), fp32 accumulate
+            "dtype": "bf16" if shape.fmt == "bf16" else "int4g32+bf16",
             "data": "synthetic",
             "config": {"workload": shape.name, "T": shape.T, "d": shape.d, "E": shape.E,
                        "top_k": shape.k, "I": shape.I, "I_shared": shape.Is, "weights": shape.fmt,
