@@ -29,6 +29,10 @@
  *   - `stream` is a cudaStream_t passed as void* (NULL = the legacy default
  *     stream).  Calls are asynchronous: they enqueue kernels and return; no
  *     call synchronises the host except moe_read_device_status().
+ *   - A call may be captured into a CUDA graph (stream capture) once one eager
+ *     call with the same dims has run on the device, which sets the kernels'
+ *     shared-memory limits; replays then read whatever the captured buffers
+ *     hold.
  *   - Every kernel is launched with programmatic dependent launch, the first
  *     of a call included: it may start while the stream's previous kernel
  *     finishes, but it reads nothing the caller may write (x, ids, layouts)

@@ -300,3 +300,25 @@ def test_tensor_core_path_one_expert_holds_every_token():
     assert np.all(ids == 5)
     ov = oracle.layer(*oracle_args(inp), ids_override=ids)
     compare_out(bf16_to_f64(out), ov["out"])
+
+
+@pytest.mark.parametrize("name", ["tiny", "verify_t8"])
+def test_layer_forward_replays_from_a_cuda_graph(name):
+    """One layer call captured into a CUDA graph and replayed gives the eager
+    call's output bit for bit, for new tokens copied into the captured x too."""
+    s = I.shape(name)
+    layer = MoeLayer(I.make_inputs(s, 0), "cuda")
+    x = I.make_x(s, 100).cuda()
+    out_g = layer.new_out()
+    layer.forward(x, out_g)  # warm-up: one-time kernel attributes stay out of the capture
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        layer.forward(x, out_g)
+    for seed in (101, 102):
+        x.copy_(I.make_x(s, seed).cuda())
+        g.replay()
+        ref = layer.forward(x).clone()
+        torch.cuda.synchronize()
+        assert torch.equal(out_g, ref)
+    assert layer.device_status() == abi.MOE_OK
