@@ -119,3 +119,46 @@ def test_stage_calls_host_side_rejections(lib):
 
 def test_launch_counter_starts_at_zero_without_launches(lib):
     assert abi.moe_kernel_launch_count() == 0
+
+
+def test_header_is_plain_c_and_links_against_the_library(lib, tmp_path):
+    """A C99 program that includes moe.h compiles with warnings as errors, links
+    against libmoe_gb300.so, and gets host-side answers without a GPU."""
+    import shutil
+    import subprocess
+
+    cc = shutil.which("gcc") or shutil.which("cc")
+    if cc is None:
+        pytest.skip("no C compiler")
+    src = tmp_path / "use_moe.c"
+    src.write_text(r'''
+#include <stdio.h>
+#include <string.h>
+#include "moe.h"
+
+int main(void) {
+  moe_dims_t d;
+  size_t n = 0;
+  memset(&d, 0, sizeof d);
+  d.T = 8; d.d = 2048; d.E = 256; d.top_k = 8; d.I = 512; d.I_shared = 512;
+  d.renormalize = 1; d.block_size = 16; d.weight_format = MOE_WEIGHTS_BF16; d.group_size = 32;
+  if (moe_workspace_bytes(&d, &n) != MOE_OK || n == 0) return 1;
+  d.top_k = 0;
+  if (moe_workspace_bytes(&d, &n) == MOE_OK) return 2;
+  if (moe_layer_forward(NULL, NULL, NULL, NULL, NULL, NULL, NULL, NULL, NULL, 0, NULL) == MOE_OK)
+    return 3;
+  printf("%s|%s\n", moe_status_string(MOE_OK), moe_status_string(MOE_ERR_INVALID_ARG));
+  return 0;
+}
+''')
+    exe = tmp_path / "use_moe"
+    so = abi.LIB_PATH
+    p = subprocess.run([cc, "-std=c99", "-Wall", "-Wextra", "-Werror", "-pedantic",
+                        "-I", os.path.join(ROOT, "include"), str(src), "-o", str(exe),
+                        so, "-Wl,-rpath," + os.path.dirname(so)],
+                       capture_output=True, text=True)
+    assert p.returncode == 0, p.stderr
+    r = subprocess.run([str(exe)], capture_output=True, text=True, timeout=60)
+    assert r.returncode == 0, (r.returncode, r.stdout, r.stderr)
+    ok, bad = r.stdout.strip().split("|")
+    assert ok and bad and ok != bad
