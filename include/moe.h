@@ -35,11 +35,16 @@
  *     hold.
  *   - Every kernel is launched with programmatic dependent launch, the first
  *     of a call included: it may start while the stream's previous kernel
- *     finishes, but it reads nothing the caller may write (x, ids, layouts)
- *     and writes nothing until that kernel has completed.  A caller kernel
- *     launched programmatically just before a call must itself wait for its
- *     own predecessor (griddepcontrol.wait) if that predecessor writes this
- *     call's inputs.
+ *     finishes, but it reads no activation, routing or layout input (x, ids,
+ *     weights of the combine, align outputs) and writes nothing until that
+ *     kernel has completed.  WEIGHTS are read earlier: the router rows, the
+ *     down stage's first weight tiles and (as an L2 prefetch) the shared
+ *     expert's weights.  So the kernel enqueued on the stream just before a
+ *     call must not write that call's weights (put another kernel, launched
+ *     without programmatic dependence, between a weight update and the call).
+ *     A caller kernel launched programmatically just before a
+ *     call must itself wait for its own predecessor (griddepcontrol.wait) if
+ *     that predecessor writes this call's inputs.
  *   - Argument errors are detected on the host and returned before anything is
  *     launched.  A failed launch returns MOE_ERR_CUDA.  A kernel that detects a
  *     data-dependent fault (an expert id out of range, a pipeline wait that ran
