@@ -37,11 +37,12 @@
  *     of a call included: it may start while the stream's previous kernel
  *     finishes, but it reads no activation, routing or layout input (x, ids,
  *     weights of the combine, align outputs) and writes nothing until that
- *     kernel has completed.  WEIGHTS are read earlier: the router rows, the
- *     down stage's first weight tiles and (as an L2 prefetch) the shared
- *     expert's weights.  So the kernel enqueued on the stream just before a
- *     call must not write that call's weights (put another kernel, launched
- *     without programmatic dependence, between a weight update and the call).
+ *     kernel has completed.  The one exception is router_w: the first kernel
+ *     of moe_route / moe_layer_forward requests its router rows before that
+ *     wait (every later kernel of a call starts only after the first has
+ *     waited).  So the kernel enqueued on the stream just before such a call
+ *     must not write router_w; put another kernel, launched without
+ *     programmatic dependence, between a router update and the call.
  *     A caller kernel launched programmatically just before a
  *     call must itself wait for its own predecessor (griddepcontrol.wait) if
  *     that predecessor writes this call's inputs.
