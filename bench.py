@@ -42,6 +42,9 @@ def parse():
     p.add_argument("--warmup", type=int, default=20)
     p.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     p.add_argument("--workload", default="verify_t8")
+    p.add_argument("--also", default="tiny,verify_t64,verify_t64_skew,int4_t32,prefill_t4096",
+                   help="further workloads measured in the same run ('' = none); each gets "
+                        "its own entry under 'workloads' in the JSON line")
     p.add_argument("--copies", type=int, default=0, help="weight copies to rotate (0 = auto)")
     p.add_argument("--batches", type=int, default=8, help="token batches to rotate")
     p.add_argument("--cpu-seconds", type=float, default=10.0)
@@ -275,45 +278,25 @@ def run_reference(args, shape):
 
 
 # --------------------------------------------------------------------------- GPU arm
-def main():
-    args = parse()
-    from moe_expert_layer_gemv_gb300 import inputs as I
+def measure(shape, args, dev, world, local, inp0, e2e):
+    """Time one workload on this rank's GPU.
 
-    shape = I.shape(args.workload)
-    if args.impl == "reference":
-        run_reference(args, shape)
-        return
-
-    import numpy as np
+    Region A: `steps` layer calls with inputs resident in HBM, as up to 5
+    rounds with an event at each boundary (a round set whose per-round times
+    vary by more than 3 % is run once more).  Region B: the same steps through
+    moe_layer_forward_timed, events at the stage boundaries (an event between
+    two kernels also stops the second from starting early, so stage times
+    include each stage's launch; region A has none of that).  Region C (e2e):
+    x copied from pinned host memory and out copied back inside the timed
+    loop.  Weight copies rotate so that the bytes in flight exceed L2 several
+    times over."""
     import torch
     import torch.distributed as dist
 
-    from moe_expert_layer_gemv_gb300 import abi, build
+    from moe_expert_layer_gemv_gb300 import abi
+    from moe_expert_layer_gemv_gb300 import inputs as I
     from moe_expert_layer_gemv_gb300.layer import MoeLayer
 
-    rank, world, local = dist_env()
-    if world > 1:
-        dist.init_process_group("nccl")
-    torch.cuda.set_device(local)
-    dev = torch.device("cuda", local)
-    build.build()
-    abi.load()
-
-    # CPU baseline first (before heavy GPU allocations), rank 0 only, N=1 only.
-    cpu = None
-    inp0 = I.make_inputs(shape, seed=0)
-    if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        v, threads, ntok, el = oracle_tokens_per_s(inp0, args.cpu_seconds, nthreads=host_cores())
-        cpu = {"value": v, "unit": UNIT, "cores": threads, "kind": "oracle",
-               "sample": f"{ntok // shape.T} whole steps ({ntok} tokens) of the {shape.name} "
-                         f"workload, {el:.1f} s, fp64 OpenMP over tokens"}
-        ch = min(shape.T, 8)
-        v1, _, ntok1, el1 = oracle_tokens_per_s(inp0, args.cpu_seconds / 5, nthreads=1, chunk=ch)
-        cpu["one_thread"] = {"value": v1, "unit": UNIT, "cores": 1,
-                             "sample": f"{ntok1} tokens of the same batch, {ch} per call, "
-                                       f"{el1:.1f} s"}
-
-    # Device state: weight copies rotated across steps, token batches rotated.
     props = torch.cuda.get_device_properties(dev)
     l2 = getattr(props, "L2_cache_size", 0) or 0
     layer0 = MoeLayer(inp0, dev)
@@ -340,20 +323,19 @@ def main():
         step(i)
     torch.cuda.synchronize()
 
-    # ---- timed region A: the layer, inputs resident in HBM
-    clocks = ClockSampler(local)
-    clocks.start()
-    time.sleep(0.3)
+    steps = args.steps
+    clocks = ClockSampler(local) if e2e else None
+    if clocks:
+        clocks.start()
+        time.sleep(0.3)
     if world > 1:
         dist.barrier()
-    # The K steps run as (up to) 5 rounds with an event at each boundary; the
-    # value is the whole region.  A round set whose per-round times vary by
-    # more than 3 % (coefficient of variation) is run once more.
+
     def region_a():
         torch.cuda.synchronize()
         n0 = abi.moe_kernel_launch_count()
-        nr = min(5, args.steps)
-        cut = [round(r * args.steps / nr) for r in range(nr + 1)]
+        nr = min(5, steps)
+        cut = [round(r * steps / nr) for r in range(nr + 1)]
         ev = [torch.cuda.Event(enable_timing=True) for _ in range(nr + 1)]
         ev[0].record()
         for r in range(nr):
@@ -365,23 +347,22 @@ def main():
             dist.barrier()
         per = [ev[r].elapsed_time(ev[r + 1]) / (cut[r + 1] - cut[r]) for r in range(nr)]
         cv = statistics.pstdev(per) / statistics.mean(per)
-        return (ev[0].elapsed_time(ev[nr]) / args.steps, abi.moe_kernel_launch_count() - n0,
+        return (ev[0].elapsed_time(ev[nr]) / steps, abi.moe_kernel_launch_count() - n0,
                 {"n": nr, "us_per_step": [round(v * 1e3, 2) for v in per],
                  "median_us": statistics.median(per) * 1e3, "cv": cv})
 
-    ms, gpu_launches, rounds = region_a()
+    ms, launches, rounds = region_a()
     first_cv = ranks_max([rounds["cv"]], dev)[0]  # every rank takes the same decision
     if first_cv > 0.03:
         if world > 1:
             dist.barrier()
-        ms, gpu_launches, rounds = region_a()
+        ms, launches, rounds = region_a()
         rounds["rerun_after_cv"] = first_cv
 
-    # ---- timed region B: same steps with per-stage events (kernel durations)
     evs = [[torch.cuda.Event(enable_timing=True) for _ in range(abi.MOE_EV_COUNT)]
-           for _ in range(args.steps)]
+           for _ in range(steps)]
     torch.cuda.synchronize()
-    for i in range(args.steps):
+    for i in range(steps):
         b = i % len(xs)
         layers[i % ncopy].forward_timed(xs[b], outs[b], evs[i])
     torch.cuda.synchronize()
@@ -390,74 +371,149 @@ def main():
                 for j, n in enumerate(stage_names)}
     ms_timed = statistics.mean(e[0].elapsed_time(e[-1]) for e in evs)
 
-    # ---- timed region C: end to end from pinned host memory
-    x_host = [x.cpu().pin_memory() for x in xs]
-    out_host = [torch.empty((shape.T, shape.d), dtype=torch.bfloat16).pin_memory() for _ in xs]
-    torch.cuda.synchronize()
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    t_wall = time.perf_counter()
-    e0.record()
-    for i in range(args.steps):
-        b = i % len(xs)
-        xs[b].copy_(x_host[b], non_blocking=True)
-        layers[i % ncopy].forward(xs[b], outs[b])
-        out_host[b].copy_(outs[b], non_blocking=True)
-    e1.record()
-    torch.cuda.synchronize()
-    t_wall = time.perf_counter() - t_wall
-    ms_e2e = e0.elapsed_time(e1) / args.steps
-    clk = clocks.stop()
+    res = {"ms": ms, "launches": launches, "rounds": rounds, "stage_ms": stage_ms,
+           "ms_timed": ms_timed, "alg": alg, "ncopy": ncopy, "w_bytes": w_bytes,
+           "batches": len(xs)}
+    if e2e:
+        x_host = [x.cpu().pin_memory() for x in xs]
+        out_host = [torch.empty((shape.T, shape.d), dtype=torch.bfloat16).pin_memory() for _ in xs]
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        t_wall = time.perf_counter()
+        e0.record()
+        for i in range(steps):
+            b = i % len(xs)
+            xs[b].copy_(x_host[b], non_blocking=True)
+            layers[i % ncopy].forward(xs[b], outs[b])
+            out_host[b].copy_(outs[b], non_blocking=True)
+        e1.record()
+        torch.cuda.synchronize()
+        res["t_wall"] = time.perf_counter() - t_wall
+        res["ms_e2e"] = e0.elapsed_time(e1) / steps
+    if clocks:
+        res["clocks"] = clocks.stop()
+    del layers, layer0, xs, outs
+    torch.cuda.empty_cache()
+    return res
 
-    ms, ms_e2e = ranks_max([ms, ms_e2e], dev)
 
-    peaks, peak_kind = measured_peaks()
-    gu_ms = stage_ms["gate_up"]
+def roofline_of(shape, m, peaks, peak_kind):
+    """Dominant kernel (the gate_up stage) against its roofline, and the layer
+    figures, from one measure() result."""
+    alg, ms = m["alg"], m["ms"]
+    gu_ms = m["stage_ms"]["gate_up"]
     achieved = alg["gate_up_bytes"] / (gu_ms * 1e-3) / 1e9
     tc = tensor_core_path(shape)
     traffic = kernel_traffic("grouped_tc.cu" if tc else "expert_gemv.cu", shape.name,
                              alg["gate_up_bytes"])
     kname = ("grouped_tc_kernel<gate_up, N=256>" if tc else
              f"gate_up_kernel<{'int4' if shape.fmt == 'int4' else 'bf16'}>")
+    roof = {"kernel": kname, "bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"],
+            "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"], "traffic": traffic,
+            "algorithmic_bytes": alg["gate_up_bytes"], "peak_source": peak_kind}
+    if tc:
+        gtf = gate_up_flops(shape) / (gu_ms * 1e-3) / 1e12
+        roof["tensor"] = {
+            "achieved": gtf, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+            "frac": gtf / peaks["bf16_tflops"],
+            "note": "gate_up algorithmic flops (real rows) / stage time vs measured bf16 burst peak"}
+    layer = {"layer_us": ms * 1e3,
+             "layer_hbm_gbs": alg["layer_bytes"] / (ms * 1e-3) / 1e9,
+             "layer_roofline_frac": alg["layer_bytes"] / (ms * 1e-3) / 1e9 / peaks["hbm_gbs"],
+             "layer_tflops": alg["flops"] / (ms * 1e-3) / 1e12,
+             "touched_experts": alg["touched"],
+             "stage_us": {k: v * 1e3 for k, v in m["stage_ms"].items()},
+             "timed_pass_us": m["ms_timed"] * 1e3,
+             "rounds": m["rounds"]}
+    if tc:
+        layer["layer_tensor_frac"] = layer["layer_tflops"] / peaks["bf16_tflops"]
+    return roof, layer
+
+
+def config_of(shape, world, m):
+    return {"workload": shape.name, "T": shape.T, "d": shape.d, "E": shape.E, "top_k": shape.k,
+            "I": shape.I, "I_shared": shape.Is, "weights": shape.fmt,
+            **({"skew": "router rows of 16 hot experts x4"} if shape.skew else {}),
+            "parallelism": f"replicas{world}" if world > 1 else "single",
+            "l2": f"rotate {m['ncopy']} device copies of all weights "
+                  f"({m['ncopy'] * m['w_bytes'] / 1e9:.2f} GB) and {m['batches']} token batches"}
+
+
+def main():
+    args = parse()
+    from moe_expert_layer_gemv_gb300 import inputs as I
+
+    shape = I.shape(args.workload)
+    if args.impl == "reference":
+        run_reference(args, shape)
+        return
+
+    import torch
+    import torch.distributed as dist
+
+    from moe_expert_layer_gemv_gb300 import abi, build
+
+    rank, world, local = dist_env()
+    if world > 1:
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    build.build()
+    abi.load()
+
+    # CPU baseline first (before heavy GPU allocations), rank 0 only, N=1 only.
+    cpu = None
+    inp0 = I.make_inputs(shape, seed=0)
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        v, threads, ntok, el = oracle_tokens_per_s(inp0, args.cpu_seconds, nthreads=host_cores())
+        cpu = {"value": v, "unit": UNIT, "cores": threads, "kind": "oracle",
+               "sample": f"{ntok // shape.T} whole steps ({ntok} tokens) of the {shape.name} "
+                         f"workload, {el:.1f} s, fp64 OpenMP over tokens"}
+        ch = min(shape.T, 8)
+        v1, _, ntok1, el1 = oracle_tokens_per_s(inp0, args.cpu_seconds / 5, nthreads=1, chunk=ch)
+        cpu["one_thread"] = {"value": v1, "unit": UNIT, "cores": 1,
+                             "sample": f"{ntok1} tokens of the same batch, {ch} per call, "
+                                       f"{el1:.1f} s"}
+
+    m = measure(shape, args, dev, world, local, inp0, e2e=True)
+    del inp0
+    ms, ms_e2e = ranks_max([m["ms"], m["ms_e2e"]], dev)
+    peaks, peak_kind = measured_peaks()
+    m["ms"] = ms
+    roof, layer = roofline_of(shape, m, peaks, peak_kind)
+
+    # The other workloads: same protocol (regions A and B), each its own entry.
+    others = {}
+    for name in [w for w in args.also.split(",") if w and w != shape.name]:
+        sh = I.shape(name)
+        mo = measure(sh, args, dev, world, local, I.make_inputs(sh, seed=0), e2e=False)
+        mo["ms"] = ranks_max([mo["ms"]], dev)[0]
+        r2, l2 = roofline_of(sh, mo, peaks, peak_kind)
+        others[name] = {"config": config_of(sh, world, mo), "value": job_tokens_per_s(sh.T, world, mo["ms"]),
+                        "unit": UNIT, "ms_per_step": mo["ms"], "gpu_launches": mo["launches"],
+                        **l2, "roofline": r2,
+                        "dtype": "bf16" if sh.fmt == "bf16" else "int4g32+bf16"}
+
     if rank == 0:
-        tok_s = job_tokens_per_s(shape.T, world, ms)
         line = {
-            "metric": METRIC, "value": tok_s, "unit": UNIT, "n_gpus": world,
-            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+            "metric": METRIC, "value": job_tokens_per_s(shape.T, world, ms), "unit": UNIT,
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             # operands as stored (bf16, or int4 codes with bf16 group scales), fp32 accumulate
             "dtype": "bf16" if shape.fmt == "bf16" else "int4g32+bf16",
             "data": "synthetic",
-            "config": {"workload": shape.name, "T": shape.T, "d": shape.d, "E": shape.E,
-                       "top_k": shape.k, "I": shape.I, "I_shared": shape.Is, "weights": shape.fmt,
-                       "parallelism": f"replicas{world}" if world > 1 else "single",
-                       "l2": f"rotate {ncopy} device copies of all weights "
-                             f"({ncopy * w_bytes / 1e9:.2f} GB) and {len(xs)} token batches"},
-            "layer_us": ms * 1e3,
-            "layer_hbm_gbs": alg["layer_bytes"] / (ms * 1e-3) / 1e9,
-            "layer_roofline_frac": alg["layer_bytes"] / (ms * 1e-3) / 1e9 / peaks["hbm_gbs"],
-            "touched_experts": alg["touched"],
-            "stage_us": {k: v * 1e3 for k, v in stage_ms.items()},
-            "timed_pass_us": ms_timed * 1e3,
-            "rounds": rounds,
-            "layer_tflops": alg["flops"] / (ms * 1e-3) / 1e12,
-            "roofline": {"kernel": kname, "bound": "hbm", "achieved": achieved,
-                         "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                         "frac": achieved / peaks["hbm_gbs"], "traffic": traffic,
-                         "algorithmic_bytes": alg["gate_up_bytes"], "peak_source": peak_kind},
+            "config": config_of(shape, world, m),
+            **layer,
+            "roofline": roof,
             "cpu_baseline": cpu,
             "e2e": {"value": job_tokens_per_s(shape.T, world, ms_e2e), "unit": UNIT,
                     "h2d_bytes_per_step": shape.T * shape.d * 2,
                     "d2h_bytes_per_step": shape.T * shape.d * 2,
-                    "wall_value": args.steps * world * shape.T / t_wall},
-            "gpu_launches": gpu_launches,
-            "clocks": clk,
+                    "wall_value": args.steps * world * shape.T / m["t_wall"]},
+            "gpu_launches": m["launches"],
+            "clocks": m["clocks"],
+            "workloads": others,
         }
-        if tc:
-            gtf = gate_up_flops(shape) / (gu_ms * 1e-3) / 1e12
-            line["roofline"]["tensor"] = {
-                "achieved": gtf, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
-                "frac": gtf / peaks["bf16_tflops"],
-                "note": "gate_up algorithmic flops (real rows) / stage time vs measured bf16 burst peak"}
         print(json.dumps(line), flush=True)
     if world > 1:
         dist.destroy_process_group()

@@ -87,17 +87,33 @@ typedef enum {
   MOE_WEIGHTS_INT4_G32 = 1  /* symmetric int4, one bf16 scale per 32 values */
 } moe_weight_format_t;
 
+/* Bits of moe_dims_t.flags. */
+enum {
+  /* Batch invariance ("veloGB10", Kernel work: batch-invariant GEMMs, so that a
+   * speculative verify pass gives bitwise the result of plain decode steps).
+   * Every token's routing (ids, weights) and output row are then bitwise the
+   * same whatever the other tokens of the call and whatever T: a token run
+   * alone (T = 1) gives the bytes it gets inside any batch.  Without the flag
+   * this already holds for T < 256 (the weight-streaming path, whose per-token
+   * reduction order is fixed); the flag extends it to every T by keeping
+   * prefill-sized calls off the tensor-core GEMMs, which are much faster
+   * there but reduce in another order. */
+  MOE_FLAG_BATCH_INVARIANT = 1
+};
+
 /* Problem dimensions.  T tokens; d model dim; E routed experts; top_k experts
  * per token; I routed-expert intermediate dim; I_shared shared-expert
  * intermediate dim (0 = no shared expert); renormalize (1: weights sum to 1
  * over the selected experts, 0: raw softmax probabilities); block_size = the
- * align block B; weight_format of the ROUTED experts; group_size (int4 only). */
+ * align block B; weight_format of the ROUTED experts; group_size (int4 only);
+ * flags: MOE_FLAG_* bits (0 = none; unknown bits are rejected). */
 typedef struct {
   int32_t T, d, E, top_k, I, I_shared;
   int32_t renormalize;
   int32_t block_size;
   int32_t weight_format;
   int32_t group_size;
+  int32_t flags;
 } moe_dims_t;
 
 /* Routed expert weights (device).
@@ -134,8 +150,40 @@ moe_status_t moe_workspace_bytes(const moe_dims_t* dims, size_t* bytes);
  * arrival counters of the routing and align kernels (each launch returns its
  * counters to zero).  Call once after allocating the workspace, and again if a
  * call left MOE_ERR_TIMEOUT in the status word (its launches may have stopped
- * short of resetting a counter). */
+ * short of resetting a counter).  Also disarms moe_workspace_inject_stall. */
 moe_status_t moe_workspace_init(void* workspace, size_t workspace_bytes, void* stream);
+
+/* Byte offsets, from the start of a workspace sized for the same dims, of the
+ * routing and aligned layout that moe_layer_forward (and _timed) leave there.
+ * Once such a call has completed on its stream, and until the next call that
+ * uses the workspace, the regions hold:
+ *   topk_ids         int32 [T][top_k]   the call's expert ids
+ *   topk_weights     fp32  [T][top_k]   their weights
+ *   sorted_ids       int32 [num_post_pad]  moe_align_block_size of those ids
+ *   block_expert_ids int32 [num_post_pad / block_size]
+ *   num_post_pad     int32 [1]
+ *   expert_offsets   int32 [E + 1]
+ * with the layout of moe_align_block_size (arrival order, sentinel T*top_k),
+ * so a caller can inspect or reuse it (for instance as the layout argument of
+ * moe_expert_forward).  Entries past num_post_pad are unspecified.  Host-only:
+ * no CUDA call. */
+typedef struct {
+  size_t topk_ids, topk_weights, sorted_ids, block_expert_ids, num_post_pad, expert_offsets;
+} moe_workspace_views_t;
+moe_status_t moe_workspace_views(const moe_dims_t* dims, moe_workspace_views_t* views);
+
+/* Test hook for the bounded pipeline waits (the pages' engine fails instead
+ * of hanging: "veloGB10", the multi-box section's watchdog).  Arms the
+ * workspace so that, in the next layer calls that use it and run the
+ * weight-streaming gate_up kernel (every bf16 call below 256 tokens, every
+ * int4 call), that kernel's copy-issuing warps issue nothing and its waits give
+ * up after about wait_limit_us microseconds (1 ... 1000000) instead of the
+ * normal two seconds.  Those calls then record MOE_ERR_TIMEOUT in the status word; their
+ * output is unspecified.  No memory is read out of bounds and no kernel faults:
+ * the waiting warps simply run out of time.  moe_workspace_init disarms it.
+ * Enqueued on `stream` (one 8-byte write into the workspace header). */
+moe_status_t moe_workspace_inject_stall(void* workspace, size_t workspace_bytes,
+                                        uint32_t wait_limit_us, void* stream);
 
 /* Router GEMV + softmax + top-k + renormalisation ("veloGB10", Kernel work:
  * router spread across the GPU; "Qwen3.8 Flash-Next - GB10 UltraFast", How it
@@ -171,7 +219,12 @@ moe_status_t moe_align_block_size(const moe_dims_t* dims, const int32_t* topk_id
  * grouped MoE expert kernels that never rebuild full weights; shared-expert
  * work overlapped with the MoE step).
  *   x bf16 [T][d]; topk_weights fp32 [T][top_k]; the four align outputs as
- *   produced by moe_align_block_size for the same dims -> out bf16 [T][d]. */
+ *   produced by moe_align_block_size for the same dims -> out bf16 [T][d].
+ * Every slot s < T*top_k must appear exactly once in sorted_ids[0,
+ * num_post_pad), inside its expert's run [expert_offsets[e],
+ * expert_offsets[e+1]), the run's real slots first and its padding (the
+ * sentinel T*top_k) last.  The runs are found from expert_offsets, so
+ * block_expert_ids is accepted for the layout's completeness but not read. */
 moe_status_t moe_expert_forward(const moe_dims_t* dims, const void* x,
                                 const float* topk_weights, const int32_t* sorted_ids,
                                 const int32_t* block_expert_ids, const int32_t* num_post_pad,
@@ -223,19 +276,25 @@ moe_status_t moe_layer_forward_timed(const moe_dims_t* dims, const void* x, cons
  * moe_layer_forward; the scratch lives in one static device array of
  * MOE_STATIC_SCRATCH_BYTES (32 MiB) inside this library, held by every GPU
  * that loads it until the process exits.  This call allocates nothing.
- *   - Dims whose workspace (moe_workspace_bytes) exceeds the array are rejected
- *     with MOE_ERR_WORKSPACE before anything is launched.  Every decode-sized
- *     layer of the workloads here fits; a T=4096 prefill layer does not.
+ *   - Argument errors are returned before anything is enqueued, as for
+ *     moe_layer_forward.  Dims whose workspace (moe_workspace_bytes) exceeds
+ *     the array are rejected with MOE_ERR_WORKSPACE, also before anything is
+ *     enqueued.  Every decode-sized layer of the workloads here fits; a T=4096
+ *     prefill layer does not.
  *   - The first call on a device looks up the array's device address
- *     (cudaGetSymbolAddress) with that device current; make that first call
- *     before any stream capture.
+ *     (cudaGetSymbolAddress) with that device current and keeps it for the
+ *     life of the process; make that first call before any stream capture.
+ *     The kept address is not refreshed if the device's primary context is
+ *     reset (cudaDeviceReset): do not use this call after such a reset.
  *   - All calls share the one array and each call overwrites it (the status
  *     word is cleared at the start of every call).  Calls that overlap on the
  *     GPU -- on two streams, or from two threads -- race on it and give wrong
  *     results: order them on one stream.
- *   - device_status_out (optional device int32, may be NULL) receives this
- *     call's device status word (MOE_OK or the device-detected error) at the
- *     end of the call, in stream order. */
+ *   - device_status_out (optional device int32, 4-byte aligned, may be NULL)
+ *     receives this call's device status word (MOE_OK or the device-detected
+ *     error) at the end of the call, in stream order.
+ *   - T == 0 returns MOE_OK at once and, like the other calls, touches
+ *     nothing: device_status_out is not written either. */
 moe_status_t moe_layer_forward_static(const moe_dims_t* dims, const void* x, const void* router_w,
                                       const moe_expert_weights_t* experts,
                                       const moe_shared_weights_t* shared, void* out,

@@ -19,11 +19,13 @@ MOE_WEIGHTS_BF16, MOE_WEIGHTS_INT4_G32 = 0, 1
 MOE_EV_BEGIN, MOE_EV_ROUTED, MOE_EV_GATE_UP, MOE_EV_DOWN, MOE_EV_END, MOE_EV_COUNT = range(6)
 
 # Every extern "C" symbol include/moe.h declares.
-EXPORTS = ("moe_status_string", "moe_workspace_bytes", "moe_workspace_init", "moe_route",
+EXPORTS = ("moe_status_string", "moe_workspace_bytes", "moe_workspace_init",
+           "moe_workspace_views", "moe_workspace_inject_stall", "moe_route",
            "moe_align_block_size", "moe_expert_forward", "moe_layer_forward",
            "moe_layer_forward_timed", "moe_layer_forward_static", "moe_read_device_status",
            "moe_kernel_launch_count")
 MOE_STATIC_SCRATCH_BYTES = 32 << 20
+MOE_FLAG_BATCH_INVARIANT = 1
 
 
 class MoeError(RuntimeError):
@@ -35,7 +37,14 @@ class MoeError(RuntimeError):
 class moe_dims_t(C.Structure):
     _fields_ = [("T", C.c_int32), ("d", C.c_int32), ("E", C.c_int32), ("top_k", C.c_int32),
                 ("I", C.c_int32), ("I_shared", C.c_int32), ("renormalize", C.c_int32),
-                ("block_size", C.c_int32), ("weight_format", C.c_int32), ("group_size", C.c_int32)]
+                ("block_size", C.c_int32), ("weight_format", C.c_int32), ("group_size", C.c_int32),
+                ("flags", C.c_int32)]
+
+
+class moe_workspace_views_t(C.Structure):
+    _fields_ = [("topk_ids", C.c_size_t), ("topk_weights", C.c_size_t), ("sorted_ids", C.c_size_t),
+                ("block_expert_ids", C.c_size_t), ("num_post_pad", C.c_size_t),
+                ("expert_offsets", C.c_size_t)]
 
 
 class moe_expert_weights_t(C.Structure):
@@ -65,6 +74,8 @@ def load():
     L.moe_status_string.restype = C.c_char_p
     L.moe_workspace_bytes.argtypes = [_D, C.POINTER(C.c_size_t)]
     L.moe_workspace_init.argtypes = [_P, C.c_size_t, _P]
+    L.moe_workspace_views.argtypes = [_D, C.POINTER(moe_workspace_views_t)]
+    L.moe_workspace_inject_stall.argtypes = [_P, C.c_size_t, C.c_uint32, _P]
     L.moe_route.argtypes = [_D, _P, _P, _P, _P, _P, C.c_size_t, _P]
     L.moe_align_block_size.argtypes = [_D, _P, _P, _P, _P, _P, _P, C.c_size_t, _P]
     L.moe_expert_forward.argtypes = [_D, _P, _P, _P, _P, _P, _P, C.POINTER(moe_expert_weights_t),
@@ -108,16 +119,17 @@ def _stream(stream):
 
 
 def make_dims(T, d, E, top_k, I, I_shared=0, renormalize=True, block_size=16,
-              weight_format=MOE_WEIGHTS_BF16, group_size=32) -> moe_dims_t:
+              weight_format=MOE_WEIGHTS_BF16, group_size=32, flags=0) -> moe_dims_t:
     return moe_dims_t(int(T), int(d), int(E), int(top_k), int(I), int(I_shared),
-                      int(bool(renormalize)), int(block_size), int(weight_format), int(group_size))
+                      int(bool(renormalize)), int(block_size), int(weight_format), int(group_size),
+                      int(flags))
 
 
-def dims_of(shape) -> moe_dims_t:
+def dims_of(shape, flags=0) -> moe_dims_t:
     """moe_dims_t of an inputs.LayerShape."""
     fmt = MOE_WEIGHTS_INT4_G32 if shape.fmt == "int4" else MOE_WEIGHTS_BF16
     return make_dims(shape.T, shape.d, shape.E, shape.k, shape.I, shape.Is, shape.renormalize,
-                     shape.block, fmt, shape.group)
+                     shape.block, fmt, shape.group, flags)
 
 
 def expert_weights(gate_up, down, gate_up_scales=None, down_scales=None) -> moe_expert_weights_t:
@@ -140,6 +152,18 @@ def moe_workspace_bytes(dims: moe_dims_t) -> int:
 
 def moe_workspace_init(ws, nbytes: int, stream=None):
     _check(load().moe_workspace_init(_ptr(ws), int(nbytes), _stream(stream)), "moe_workspace_init")
+
+
+def moe_workspace_views(dims: moe_dims_t) -> dict:
+    """Byte offsets of the routing and align layout inside a workspace."""
+    v = moe_workspace_views_t()
+    _check(load().moe_workspace_views(C.byref(dims), C.byref(v)), "moe_workspace_views")
+    return {name: int(getattr(v, name)) for name, _ in moe_workspace_views_t._fields_}
+
+
+def moe_workspace_inject_stall(ws, nbytes: int, wait_limit_us: int, stream=None):
+    _check(load().moe_workspace_inject_stall(_ptr(ws), int(nbytes), int(wait_limit_us),
+                                             _stream(stream)), "moe_workspace_inject_stall")
 
 
 def alloc_workspace(dims: moe_dims_t, device="cuda") -> torch.Tensor:

@@ -20,7 +20,6 @@
 #include <unordered_map>
 #include <utility>
 
-#include "../../include/moe.h"
 #include "launch.h"
 
 namespace moe {
@@ -75,14 +74,19 @@ struct Layout {
 // weight-streaming GEMVs).
 constexpr int kTcMinT = 256;
 
+// Batch-invariant calls stay on the weight-streaming kernels, whose per-token
+// arithmetic does not depend on T.
+bool invariant(const moe_dims_t& dm) { return (dm.flags & MOE_FLAG_BATCH_INVARIANT) != 0; }
+
 bool tc_dims(const moe_dims_t& dm) {
-  return dm.T >= kTcMinT && dm.weight_format == MOE_WEIGHTS_BF16 && dm.block_size % 128 == 0 &&
-         dm.I % 128 == 0 && dm.d % 256 == 0 && (dm.I_shared == 0 || dm.I_shared == dm.I);
+  return dm.T >= kTcMinT && !invariant(dm) && dm.weight_format == MOE_WEIGHTS_BF16 &&
+         dm.block_size % 128 == 0 && dm.I % 128 == 0 && dm.d % 256 == 0 &&
+         (dm.I_shared == 0 || dm.I_shared == dm.I);
 }
 
 // Router logits on the tensor cores from the same T up.
 bool use_tc_router(const moe_dims_t& dm) {
-  return dm.T >= kTcMinT && tc_router_supported(dm.T, dm.d, dm.E);
+  return dm.T >= kTcMinT && !invariant(dm) && tc_router_supported(dm.T, dm.d, dm.E);
 }
 
 size_t carve(size_t* cursor, size_t bytes) {
@@ -137,6 +141,7 @@ moe_status_t check_dims(const moe_dims_t* dm) {
   if (d.I_shared != 0 && (d.I_shared < 8 || d.I_shared > 4096 || d.I_shared % 8 != 0))
     return MOE_ERR_UNSUPPORTED;
   if (d.block_size > 1024) return MOE_ERR_UNSUPPORTED;
+  if ((d.flags & ~(int32_t)MOE_FLAG_BATCH_INVARIANT) != 0) return MOE_ERR_UNSUPPORTED;
   if (d.weight_format == MOE_WEIGHTS_BF16) return MOE_OK;
   if (d.weight_format == MOE_WEIGHTS_INT4_G32) {
     if (d.group_size != 32 || d.d % 256 != 0 || d.I % 256 != 0) return MOE_ERR_UNSUPPORTED;
@@ -285,18 +290,29 @@ moe_status_t run_experts(const moe_dims_t& dm, const void* x, const float* topk_
   return MOE_OK;
 }
 
+}  // namespace
+
+moe_status_t layer_precheck(const moe_dims_t* dims, const void* x, const void* router_w,
+                            const moe_expert_weights_t* ex, const moe_shared_weights_t* sh,
+                            const void* out, const void* ids_out, const void* w_out) {
+  moe_status_t s = check_dims(dims);
+  if (s != MOE_OK || dims->T == 0) return s;
+  if (x == nullptr || router_w == nullptr || out == nullptr) return MOE_ERR_INVALID_ARG;
+  if (!aligned16(x) || !aligned16(router_w) || !aligned16(out)) return MOE_ERR_INVALID_ARG;
+  if ((ids_out && !aligned16(ids_out)) || (w_out && !aligned16(w_out))) return MOE_ERR_INVALID_ARG;
+  return check_weights(*dims, ex, sh);
+}
+
+namespace {
+
 moe_status_t layer_forward(const moe_dims_t* dims, const void* x, const void* router_w,
                            const moe_expert_weights_t* ex, const moe_shared_weights_t* sh,
                            void* out, int32_t* ids_out, float* w_out, void* ws, size_t ws_bytes,
                            void* stream, void* const* events) {
-  moe_status_t s = check_dims(dims);
+  moe_status_t s = layer_precheck(dims, x, router_w, ex, sh, out, ids_out, w_out);
   if (s != MOE_OK) return s;
   const moe_dims_t dm = *dims;
   if (dm.T == 0) return MOE_OK;  // no tokens: nothing read, written or launched
-  if (x == nullptr || router_w == nullptr || out == nullptr) return MOE_ERR_INVALID_ARG;
-  if (!aligned16(x) || !aligned16(router_w) || !aligned16(out)) return MOE_ERR_INVALID_ARG;
-  if ((ids_out && !aligned16(ids_out)) || (w_out && !aligned16(w_out))) return MOE_ERR_INVALID_ARG;
-  if ((s = check_weights(dm, ex, sh)) != MOE_OK) return s;
   Layout L;
   if ((s = check_ws(dm, ws, ws_bytes, &L)) != MOE_OK) return s;
   DeviceInfo di;
@@ -356,6 +372,15 @@ moe_status_t layer_forward(const moe_dims_t* dims, const void* x, const void* ro
 }  // namespace
 
 void count_launch() { g_launches.fetch_add(1, std::memory_order_relaxed); }
+
+namespace {
+__global__ void set_word_kernel(int* word, int value) { *word = value; }
+}  // namespace
+
+cudaError_t launch_set_word(const LaunchCfg& c, int* word, int value) {
+  void* args[] = {&word, &value};
+  return launch_kernel(c, (const void*)set_word_kernel, dim3(1), dim3(1), 0, args);
+}
 
 cudaError_t launch_kernel(const LaunchCfg& c, const void* fn, dim3 grid, dim3 block, size_t smem,
                           void** args) {
@@ -421,6 +446,31 @@ moe_status_t moe_workspace_init(void* workspace, size_t workspace_bytes, void* s
       workspace_bytes < kAlign)
     return MOE_ERR_WORKSPACE;
   return cuda_status(cudaMemsetAsync(workspace, 0, kAlign, static_cast<cudaStream_t>(stream)));
+}
+
+moe_status_t moe_workspace_views(const moe_dims_t* dims, moe_workspace_views_t* views) {
+  if (views == nullptr) return MOE_ERR_INVALID_ARG;
+  moe_status_t s = check_dims(dims);
+  if (s != MOE_OK) return s;
+  const Layout L = layout_of(*dims);
+  views->topk_ids = L.ids;
+  views->topk_weights = L.w;
+  views->sorted_ids = L.sorted;
+  views->block_expert_ids = L.blocks;
+  views->num_post_pad = L.npp;
+  views->expert_offsets = L.offs;
+  return MOE_OK;
+}
+
+moe_status_t moe_workspace_inject_stall(void* workspace, size_t workspace_bytes,
+                                        uint32_t wait_limit_us, void* stream) {
+  if (workspace == nullptr || (reinterpret_cast<uintptr_t>(workspace) % kAlign) != 0 ||
+      workspace_bytes < kAlign)
+    return MOE_ERR_WORKSPACE;
+  if (wait_limit_us < 1 || wait_limit_us > 1000000) return MOE_ERR_INVALID_ARG;
+  return cuda_status(launch_set_word(LaunchCfg{static_cast<cudaStream_t>(stream), false},
+                                     static_cast<int*>(workspace) + kStallWord,
+                                     (int)wait_limit_us));
 }
 
 moe_status_t moe_route(const moe_dims_t* dims, const void* x, const void* router_w,

@@ -119,13 +119,15 @@ __device__ __forceinline__ uint64_t global_timer_ns() {
 }
 
 // Bounded wait for phase `parity` of `bar`.  Returns false (after recording
-// kStatusTimeout) if the phase did not complete within the bounds above.
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, int* status) {
+// kStatusTimeout) if the phase did not complete within limit_ns of wall time
+// or kSpinLimit polls.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, int* status,
+                                          uint64_t limit_ns = kWaitLimitNs) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = global_timer_ns();
   for (uint32_t i = 1; i < kSpinLimit; ++i) {
     if (mbar_try_wait(bar, parity)) return true;
-    if ((i & 15u) == 0 && global_timer_ns() - t0 > kWaitLimitNs) break;
+    if ((i & 15u) == 0 && global_timer_ns() - t0 > limit_ns) break;
   }
   record_status(status, kStatusTimeout);
   return false;

@@ -423,6 +423,11 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) gate_up_kernel(const GuA
   pdl_wait();
   pdl_trigger();
 
+  // The stall test hook (moe_workspace_inject_stall): the producer issues
+  // nothing and the consumers' waits give up after the armed limit.
+  const int stall_us = a.status ? __ldcg(a.status + kStallWord) : 0;
+  const uint64_t wait_ns = stall_us > 0 ? (uint64_t)stall_us * 1000u : kWaitLimitNs;
+
   const Plan plan = *a.plan;
   const int d = a.d;
   const int xt = a.xt;
@@ -441,6 +446,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) gate_up_kernel(const GuA
 
   if (warp == kConsumerWarps) {
     // ------------------------------------------------------------ producer
+    if (stall_us > 0) return;  // nothing issued, nothing in flight
     const uint64_t pol_w = policy_evict_first();
     const uint64_t pol_x = policy_evict_last();
     int j = 0;
@@ -529,7 +535,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) gate_up_kernel(const GuA
     const int nsub = kConsumerWarps / RG;
     const int p = warp % RG, tsub = warp / RG;
     const int cnt = (p < nr && nt > tsub) ? (nt - tsub + nsub - 1) / nsub : 0;
-    if (!mbar_wait(&full[s], (uint32_t)(use & 1), a.status)) break;
+    if (!mbar_wait(&full[s], (uint32_t)(use & 1), a.status, wait_ns)) break;
     const uint32_t st = stages_sa + (uint32_t)(s * a.stage_bytes);
     const uint32_t wg = st + p * rb, wu = st + RG * rb + p * rb;
     const uint32_t sg = st + 2 * RG * rb + p * sb, su = sg + RG * sb;

@@ -6,6 +6,7 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include "../../include/moe.h"
 #include "common.cuh"
 
 namespace moe {
@@ -57,6 +58,19 @@ constexpr int kFusedRouteMaxT = 128;
 constexpr int kRouteCounterBase = 16;
 // Workspace-header int counting the finished CTAs of the multi-CTA align.
 constexpr int kAlignCounter = 60;
+// Workspace-header int holding the stall test hook (moe_workspace_inject_stall):
+// 0 = off, else the gate_up stage's wait limit in microseconds, its producers
+// issuing nothing.
+constexpr int kStallWord = 62;
+
+// *word = value, one thread, in stream order (the stall hook's arming write).
+cudaError_t launch_set_word(const LaunchCfg& c, int* word, int value);
+
+// The host-side argument checks of moe_layer_forward other than the workspace:
+// dims, pointers, alignment, weights (MOE_OK also for T == 0).
+moe_status_t layer_precheck(const moe_dims_t* dims, const void* x, const void* router_w,
+                            const moe_expert_weights_t* ex, const moe_shared_weights_t* sh,
+                            const void* out, const void* ids_out, const void* w_out);
 
 // logits[t][e] = x[t] . wr[e]; sg[t] = x[t] . w_sg when w_sg (fp32 accumulate).
 cudaError_t launch_router_logits(const LaunchCfg& c, const uint16_t* x, const uint16_t* wr,

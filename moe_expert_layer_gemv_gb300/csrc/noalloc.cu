@@ -17,7 +17,7 @@
 // address is what the launches get.
 #include <mutex>
 
-#include "../../include/moe.h"
+#include "launch.h"
 
 namespace {
 
@@ -51,13 +51,16 @@ extern "C" moe_status_t moe_layer_forward_static(const moe_dims_t* dims, const v
                                                  const moe_shared_weights_t* shared, void* out,
                                                  int32_t* topk_ids_out, float* topk_weights_out,
                                                  int32_t* device_status_out, void* stream) {
-  size_t need = 0;
-  moe_status_t s = moe_workspace_bytes(dims, &need);
+  // Every host-side check comes before anything is enqueued.
+  moe_status_t s = moe::layer_precheck(dims, x, router_w, experts, shared, out, topk_ids_out,
+                                       topk_weights_out);
   if (s != MOE_OK) return s;
+  size_t need = 0;
+  if ((s = moe_workspace_bytes(dims, &need)) != MOE_OK) return s;
   if (need > (size_t)MOE_STATIC_SCRATCH_BYTES) return MOE_ERR_WORKSPACE;
   if (device_status_out && (reinterpret_cast<uintptr_t>(device_status_out) & 3u) != 0)
     return MOE_ERR_INVALID_ARG;
-  if (dims->T == 0) return MOE_OK;
+  if (dims->T == 0) return MOE_OK;  // nothing enqueued, device_status_out untouched
   void* ws = nullptr;
   if ((s = scratch_address(&ws)) != MOE_OK) return s;
   cudaStream_t st = static_cast<cudaStream_t>(stream);

@@ -49,87 +49,130 @@ struct RouterArgs {
   const uint16_t* w_sg;    // [d] shared-expert gate row, or null
   float* logits;           // [T][E]
   float* sg;               // [T] x . w_sg (when w_sg)
-  int T, d, E, wpe;
+  int T, d, E, wpe;        // wpe: warps per router row (1, 2, 4 or 8)
 };
 
-// One router CTA: rows [blockIdx.x * epc, +epc) of the E routed rows plus the
-// gate row (index E), `wpe` warps per row split along d, one token tile of 8
-// tokens staged in shared memory (xs, >= 8 * d bf16) by one bulk copy.  Each
-// lane holds its CH 16-byte chunks of its row, requested before any wait.
-template <int CH>
-__device__ __forceinline__ void router_tile(const RouterArgs& a, uint4* xs, int* status) {
-  __shared__ float red[kRouterWarps][kRouterTokens];
-  __shared__ __align__(8) uint64_t xbar;
+// Fixed reduction tree of every router logit (and of the shared-expert gate
+// logit x . w_sg, which rides as row E): kRouterSplit partial sums per row,
+// partial p summing -- one fp32 fma chain per lane, in ascending i -- the
+// 16-byte chunks c = 32 p + lane + 32 kRouterSplit i of the row, then a warp
+// butterfly over the lanes; the row's value is the partials added in ascending
+// p.  A CTA spreads its rows x partials over its warps in any proportion (wpe
+// warps per row, kRouterSplit / wpe partials per warp), so the launch shape
+// may follow T while every token's arithmetic stays the same: the routing of a
+// token does not depend on the other tokens of the call.
+constexpr int kRouterSplit = 8;
+
+// Bytes of dynamic shared memory one router CTA stages: its rows, then the
+// 8-token tile.
+__host__ __device__ constexpr size_t router_smem_bytes(int d, int wpe) {
+  return ((size_t)(kRouterWarps / wpe) + kRouterTokens) * d * 2;
+}
+
+// Requests this CTA's router rows (rows [blockIdx.x * epc, +epc), index E =
+// the gate row) into `wsm` by bulk copy, completing on `bar`.  The router and
+// gate weights are inputs no kernel of this library writes, so this may run
+// before the dependency wait.
+__device__ __forceinline__ void router_rows_request(const RouterArgs& a, uint8_t* wsm,
+                                                    uint64_t* bar) {
+  const int epc = kRouterWarps / a.wpe;
+  const int rows = a.E + (a.w_sg ? 1 : 0);
+  const int e0 = blockIdx.x * epc;
+  const int n = min(epc, rows - e0);
+  const int nr = min(n, a.E - e0);  // routed rows among them
+  const uint32_t rb = (uint32_t)a.d * 2;
+  uint32_t bytes = (nr > 0 ? (uint32_t)nr * rb : 0u) + (n > nr ? rb : 0u);
+  mbar_arrive_expect_tx(bar, bytes);
+  const uint64_t pol = policy_evict_first();
+  if (nr > 0) bulk_g2s(wsm, a.wr + (size_t)e0 * a.d, nr * rb, bar, pol);
+  if (n > nr) bulk_g2s(wsm + (size_t)(nr > 0 ? nr : 0) * rb, a.w_sg, rb, bar, pol);
+}
+
+// One router CTA: rows [blockIdx.x * epc, +epc) for one token tile of 8
+// tokens.  smem: >= router_smem_bytes(d, wpe), 16-byte aligned.
+__device__ __forceinline__ void router_tile(const RouterArgs& a, uint8_t* smem, int* status) {
+  __shared__ float red[kRouterWarps][kRouterSplit][kRouterTokens];
+  __shared__ __align__(8) uint64_t bars[2];  // [0] router rows, [1] token tile
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int d = a.d, nch = d >> 3;
+  const int epc = kRouterWarps / a.wpe;
   const int rows = a.E + (a.w_sg ? 1 : 0);
   const int t0 = blockIdx.y * kRouterTokens;
   const int nt = min(kRouterTokens, a.T - t0);
-  const int epc = kRouterWarps / a.wpe;
-  const int e = blockIdx.x * epc + warp / a.wpe;
-  const int q = warp % a.wpe;
+  uint8_t* wsm = smem;
+  uint8_t* xsm = smem + (size_t)epc * d * 2;
 
-  // Router and gate weights are inputs that no kernel of this library writes:
-  // request them before waiting on the predecessor.
-  const uint16_t* rowp = (e < a.E) ? a.wr + (size_t)e * d : a.w_sg;
-  uint4 w[CH];
-#pragma unroll
-  for (int i = 0; i < CH; ++i) {
-    const int c = q * 32 + lane + i * a.wpe * 32;
-    w[i] = (e < rows && c < nch) ? __ldg(reinterpret_cast<const uint4*>(rowp) + c)
-                                 : make_uint4(0, 0, 0, 0);
-  }
   if (threadIdx.x == 0) {
-    mbar_init(&xbar, 1);
+    mbar_init(&bars[0], 1);
+    mbar_init(&bars[1], 1);
     fence_barrier_init();
+    router_rows_request(a, wsm, &bars[0]);
   }
   __syncthreads();
   pdl_wait();
-  // The token tile is contiguous: one bulk copy, completion on xbar.
+  // The token tile is contiguous: one bulk copy.
   if (threadIdx.x == 0) {
     const uint32_t bytes = (uint32_t)nt * d * 2;
-    mbar_arrive_expect_tx(&xbar, bytes);
-    bulk_g2s(xs, a.x + (size_t)t0 * d, bytes, &xbar, policy_evict_last());
+    mbar_arrive_expect_tx(&bars[1], bytes);
+    bulk_g2s(xsm, a.x + (size_t)t0 * d, bytes, &bars[1], policy_evict_last());
   }
-  mbar_wait(&xbar, 0, status);  // on a timeout the logits are garbage; the status says so
+  // On a timeout the logits are garbage; the status word says so.
+  mbar_wait(&bars[0], 0, status);
+  mbar_wait(&bars[1], 0, status);
 
-  float acc[kRouterTokens];
+  const int r = warp / a.wpe;                 // row of this CTA
+  const int G = kRouterSplit / a.wpe;         // partials of this warp
+  const int p0 = (warp % a.wpe) * G;
+  const bool live = blockIdx.x * epc + r < rows;
+  const uint32_t wrow = smem_u32(wsm) + (uint32_t)(r * d * 2);
+  const uint32_t xrow = smem_u32(xsm);
+  for (int g = 0; g < G && live; ++g) {
+    const int p = p0 + g;
+    float acc[kRouterTokens];
 #pragma unroll
-  for (int j = 0; j < kRouterTokens; ++j) {
-    acc[j] = 0.f;
-    if (j < nt) {
+    for (int j = 0; j < kRouterTokens; ++j) acc[j] = 0.f;
+    for (int c = 32 * p + lane; c < nch; c += 32 * kRouterSplit) {
+      uint4 wv;
+      asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+                   : "=r"(wv.x), "=r"(wv.y), "=r"(wv.z), "=r"(wv.w)
+                   : "r"(wrow + c * 16));
 #pragma unroll
-      for (int i = 0; i < CH; ++i) {
-        const int c = q * 32 + lane + i * a.wpe * 32;
-        if (c < nch) acc[j] = dot8_bf16(w[i], xs[j * nch + c], acc[j]);
+      for (int j = 0; j < kRouterTokens; ++j) {
+        if (j < nt) {
+          uint4 xv;
+          asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+                       : "=r"(xv.x), "=r"(xv.y), "=r"(xv.z), "=r"(xv.w)
+                       : "r"(xrow + (uint32_t)(j * d * 2 + c * 16)));
+          acc[j] = dot8_bf16(wv, xv, acc[j]);
+        }
       }
     }
-  }
 #pragma unroll
-  for (int j = 0; j < kRouterTokens; ++j) acc[j] = warp_sum(acc[j]);
-  if (lane == 0) {
+    for (int j = 0; j < kRouterTokens; ++j) acc[j] = warp_sum(acc[j]);
+    if (lane == 0) {
 #pragma unroll
-    for (int j = 0; j < kRouterTokens; ++j) red[warp][j] = acc[j];
+      for (int j = 0; j < kRouterTokens; ++j) red[r][p][j] = acc[j];
+    }
   }
   __syncthreads();
   if (threadIdx.x < epc * kRouterTokens) {
     const int g = threadIdx.x / kRouterTokens, j = threadIdx.x % kRouterTokens;
     const int eo = blockIdx.x * epc + g;
     if (eo < rows && j < nt) {
-      float s = 0.f;
-      for (int p = 0; p < a.wpe; ++p) s += red[g * a.wpe + p][j];
+      float v = 0.f;
+#pragma unroll
+      for (int p = 0; p < kRouterSplit; ++p) v += red[g][p][j];
       if (eo < a.E)
-        a.logits[(size_t)(t0 + j) * a.E + eo] = s;
+        a.logits[(size_t)(t0 + j) * a.E + eo] = v;
       else
-        a.sg[t0 + j] = s;
+        a.sg[t0 + j] = v;
     }
   }
 }
 
-template <int CH>
 __global__ void __launch_bounds__(kRouterThreads) router_logits_kernel(RouterArgs a, int* status) {
-  extern __shared__ __align__(16) uint4 xs[];
-  router_tile<CH>(a, xs, status);
+  extern __shared__ __align__(16) uint8_t rsm[];
+  router_tile(a, rsm, status);
   pdl_trigger();
 }
 
@@ -227,14 +270,19 @@ __device__ void warp_topk(const float* __restrict__ L, int E, int k, int renorma
 }
 
 // Top-k of token t, stored (lanes j < k) to the routing buffers (and, when
-// ids_smem, to shared memory at the same slot index).
+// ids_smem, to shared memory at the same slot index).  NV > 0: the logits per
+// lane are known at compile time (E <= 32 NV); 0: dispatch on E.
+template <int NV = 0>
 __device__ __forceinline__ void topk_token(const float* logits, int t, int E, int k,
                                            int renormalize, int32_t* ids, float* w,
                                            int32_t* ids_copy, float* w_copy,
                                            int32_t* ids_smem = nullptr) {
   int id;
   float wt;
-  warp_topk(logits + (size_t)t * E, E, k, renormalize, id, wt);
+  if (NV > 0)
+    warp_topk_nv<NV ? NV : 1>(logits + (size_t)t * E, E, k, renormalize, id, wt);
+  else
+    warp_topk(logits + (size_t)t * E, E, k, renormalize, id, wt);
   const int lane = threadIdx.x & 31;
   if (lane < k) {
     const size_t o = (size_t)t * k + lane;
@@ -738,11 +786,13 @@ struct RouteArgs {
 // tiles), 256 threads.  Dynamic shared memory: max(router tile, align step).
 // Every CTA arrives on its tile's counter exactly once, whatever happened
 // before, so the counters return to zero by the end of every launch.
-template <int CH>
-__global__ void __launch_bounds__(kRouterThreads) route_kernel(RouteArgs a) {
+// NV: logits per lane of the top-k (E <= 32 NV), so that each instantiation
+// holds only the registers its E needs (two CTAs per SM).
+template <int NV>
+__global__ void __launch_bounds__(kRouterThreads, NV >= 32 ? 1 : 2) route_kernel(RouteArgs a) {
   extern __shared__ __align__(16) int dsm[];
   __shared__ int s_last;
-  router_tile<CH>(a.r, reinterpret_cast<uint4*>(dsm), a.status);
+  router_tile(a.r, reinterpret_cast<uint8_t*>(dsm), a.status);
   pdl_trigger();
 
   // Arrival on this token tile; the last CTA to arrive selects its top-k.
@@ -761,8 +811,8 @@ __global__ void __launch_bounds__(kRouterThreads) route_kernel(RouteArgs a) {
   // its shared-memory slots (the router's x tile there is no longer needed).
   int* sids = dsm + align_smem_ints(a.r.E) - kAlignSmemSlots;
   if ((threadIdx.x >> 5) < kRouterTokens && t < a.r.T)
-    topk_token(a.r.logits, t, a.r.E, a.k, a.renormalize, a.ids, a.w, a.ids_copy, a.w_copy,
-               gridDim.y == 1 ? sids : nullptr);
+    topk_token<NV>(a.r.logits, t, a.r.E, a.k, a.renormalize, a.ids, a.w, a.ids_copy, a.w_copy,
+                   gridDim.y == 1 ? sids : nullptr);
 
   // Arrival of this tile; the last tile to finish runs the align and the plan
   // (with one token tile, this CTA is already the last).
@@ -786,20 +836,23 @@ __global__ void __launch_bounds__(kRouterThreads) route_kernel(RouteArgs a) {
   align_block_small(sids, a.r.T, a.k, a.r.E, a.B, a.o, a.pp, a.status, dsm);
 }
 
-// Router CTA shape: warps per expert row (wpe) and 16-byte chunks per lane.
-void router_shape(int T, int d, int rows, int sms, int* wpe_out, int* ch_out) {
+// Router CTA shape: warps per router row.  The arithmetic is the same for
+// every shape (kRouterSplit), so the choice only sets the parallelism: the
+// fewest CTAs that still cover every SM (each CTA stages the whole token tile,
+// so fewer CTAs move fewer bytes), within the shared memory a CTA may hold.
+int router_wpe(int T, int d, int rows, int sms) {
   const int ty = (int)ceil_div(T, kRouterTokens);
-  const int nch = d / 8;
-  int wpe = 8;
-  for (int cand = 1; cand <= 8; cand <<= 1) {
-    if (ceil_div(rows, kRouterWarps / cand) * ty >= sms) {
-      wpe = cand;
-      break;
-    }
+  for (int wpe = 1; wpe <= 8; wpe <<= 1) {
+    if (router_smem_bytes(d, wpe) > 200 * 1024) continue;
+    if (wpe == 8 || ceil_div(rows, kRouterWarps / wpe) * ty >= sms) return wpe;
   }
-  while (wpe < 8 && ceil_div(nch, wpe * 32) > 8) wpe <<= 1;  // at most 8 chunks per lane
-  *wpe_out = wpe;
-  *ch_out = (int)ceil_div(nch, wpe * 32);
+  return 8;
+}
+
+size_t route_fused_smem(int d, int E, int wpe) {
+  const size_t a = align_smem_ints(E) * sizeof(int);
+  const size_t r = router_smem_bytes(d, wpe);
+  return a > r ? a : r;
 }
 
 }  // namespace
@@ -814,13 +867,9 @@ cudaError_t launch_router_logits(const LaunchCfg& c, const uint16_t* x, const ui
   if (T == 0) return cudaSuccess;
   RouterArgs a{x, wr, w_sg, logits, sg, T, d, E, 0};
   const int rows = E + (w_sg ? 1 : 0);
-  int ch;
-  router_shape(T, d, rows, sms, &a.wpe, &ch);
-  const size_t smem = (size_t)kRouterTokens * d * 2;
-  const void* fn = ch <= 1 ? (const void*)router_logits_kernel<1>
-                 : ch <= 2 ? (const void*)router_logits_kernel<2>
-                 : ch <= 4 ? (const void*)router_logits_kernel<4>
-                           : (const void*)router_logits_kernel<8>;
+  a.wpe = router_wpe(T, d, rows, sms);
+  const size_t smem = router_smem_bytes(d, a.wpe);
+  const void* fn = (const void*)router_logits_kernel;
   cudaError_t e = ensure_smem(fn, (int)smem);
   if (e != cudaSuccess) return e;
   dim3 grid((unsigned)ceil_div(rows, kRouterWarps / a.wpe), (unsigned)ceil_div(T, kRouterTokens));
@@ -838,8 +887,7 @@ cudaError_t launch_route_fused(const LaunchCfg& c, const uint16_t* x, const uint
   RouteArgs a;
   a.r = RouterArgs{x, wr, w_sg, logits, sg, T, d, E, 0};
   const int rows = E + (w_sg ? 1 : 0);
-  int ch;
-  router_shape(T, d, rows, sms, &a.r.wpe, &ch);
+  a.r.wpe = router_wpe(T, d, rows, sms);
   a.k = k;
   a.renormalize = renormalize;
   a.B = B;
@@ -851,13 +899,14 @@ cudaError_t launch_route_fused(const LaunchCfg& c, const uint16_t* x, const uint
   a.pp = pp;
   a.status = status;
   a.counters = counters;
-  size_t smem = (size_t)kRouterTokens * d * 2;
-  const size_t asmem = align_smem_ints(E) * sizeof(int);
-  if (asmem > smem) smem = asmem;
-  const void* fn = ch <= 1 ? (const void*)route_kernel<1>
-                 : ch <= 2 ? (const void*)route_kernel<2>
-                 : ch <= 4 ? (const void*)route_kernel<4>
-                           : (const void*)route_kernel<8>;
+  const size_t smem = route_fused_smem(d, E, a.r.wpe);
+  const int nv = (E + 31) / 32;
+  const void* fn = nv <= 1 ? (const void*)route_kernel<1>
+                 : nv <= 2 ? (const void*)route_kernel<2>
+                 : nv <= 4 ? (const void*)route_kernel<4>
+                 : nv <= 8 ? (const void*)route_kernel<8>
+                 : nv <= 16 ? (const void*)route_kernel<16>
+                            : (const void*)route_kernel<32>;
   cudaError_t e = ensure_smem(fn, (int)smem);
   if (e != cudaSuccess) return e;
   dim3 grid((unsigned)ceil_div(rows, kRouterWarps / a.r.wpe),

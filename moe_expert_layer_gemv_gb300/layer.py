@@ -12,11 +12,11 @@ def _dev(t, device):
 class MoeLayer:
     """Holds one layer's device weights (from inputs.make_inputs) and workspace."""
 
-    def __init__(self, inp: dict, device="cuda"):
+    def __init__(self, inp: dict, device="cuda", flags=0):
         s = inp["shape"]
         self.shape = s
         self.device = torch.device(device)
-        self.dims = abi.dims_of(s)
+        self.dims = abi.dims_of(s, flags)
         self.router_w = _dev(inp["router_w"], device)
         self.gate_up = _dev(inp["gate_up"], device)
         self.down = _dev(inp["down"], device)
@@ -48,3 +48,20 @@ class MoeLayer:
 
     def device_status(self) -> int:
         return abi.moe_read_device_status(self.ws)
+
+    def layout(self) -> dict:
+        """The routing and aligned layout the last forward left in the
+        workspace (moe_workspace_views), copied to host numpy arrays."""
+        s = self.shape
+        v = abi.moe_workspace_views(self.dims)
+
+        def take(name, n, dtype=torch.int32):
+            off = v[name]
+            return self.ws[off:off + 4 * n].view(dtype).cpu().numpy()
+
+        npp = int(take("num_post_pad", 1)[0])
+        return {"topk_ids": take("topk_ids", s.T * s.k).reshape(s.T, s.k),
+                "topk_weights": take("topk_weights", s.T * s.k, torch.float32).reshape(s.T, s.k),
+                "num_post_pad": npp, "sorted_ids": take("sorted_ids", npp),
+                "block_expert_ids": take("block_expert_ids", npp // s.block),
+                "expert_offsets": take("expert_offsets", s.E + 1)}

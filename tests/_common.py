@@ -9,16 +9,35 @@ Parity criteria (the layer's stated pass bar):
   * output rel-L2 error <= 5e-3 and max-abs error <= 2e-2 * rms(out) against
     the fp64 oracle, for the bf16 output.
 """
+import functools
+
 import numpy as np
 import torch
 
 import oracle
 from moe_expert_layer_gemv_gb300 import inputs as I
 
+# Parity figures of every layer comparison in this session, printed by the
+# terminal summary (conftest.py): name, rel-L2, max-abs/rms beyond rounding,
+# literal max-abs/rms, near-tie tokens, tokens whose ids differ.
+PARITY_LOG = []
+
 NEAR_TIE = 1e-4
 REL_L2_TOL = 5e-3
 MAX_ABS_TOL = 2e-2  # times rms(oracle out)
 WEIGHT_RTOL = 2e-5  # fp32 softmax weights vs fp64
+
+
+@functools.lru_cache(maxsize=3)
+def _cached_inputs(name, seed, over):
+    return I.make_inputs(I.shape(name, **dict(over)), seed)
+
+
+def inputs(name, seed=0, **over):
+    """I.make_inputs(I.shape(name, **over), seed), the last few kept: drawing a
+    full-size layer's weights takes seconds.  Callers must not modify the
+    returned tensors (make a new dict to change one)."""
+    return _cached_inputs(name, seed, tuple(sorted(over.items())))
 
 
 def oracle_args(inp):
@@ -49,8 +68,9 @@ def bf16_half_ulp(x):
     return np.where(x != 0, np.ldexp(1.0, p - 9), 0.0)
 
 
-def compare_out(gpu_out, ref_out):
-    """Returns (rel_l2, max_abs / rms) and asserts the pass bar.
+def compare_out(gpu_out, ref_out, name=None):
+    """Returns (rel_l2, max_abs / rms beyond rounding, literal max_abs / rms)
+    and asserts the pass bar; `name` logs the figures for the summary.
 
     The output is bf16, so even the correctly rounded exact result is off by
     up to half a bf16 ulp, which at a 6-sigma element lying just above a power
@@ -67,9 +87,33 @@ def compare_out(gpu_out, ref_out):
     err = np.abs(g - r)
     mx = float((err - bf16_half_ulp(r)).max() / max(rms, 1e-300)) if g.size else 0.0
     literal = float(err.max() / max(rms, 1e-300)) if g.size else 0.0
+    if name is not None:
+        PARITY_LOG.append({"name": name, "rel": rel, "max": mx, "literal": literal})
     assert rel <= REL_L2_TOL, f"rel-L2 {rel:.3e} > {REL_L2_TOL}"
     assert mx <= MAX_ABS_TOL, f"max-abs/rms beyond bf16 rounding {mx:.3e} > {MAX_ABS_TOL} (raw {literal:.3e})"
-    return rel, mx
+    return rel, mx, literal
+
+
+def oracle_routing(inp):
+    """The oracle's own routing of the inputs: fp64 router logits, top-k ids,
+    weights and the k-th vs (k+1)-th logit margin of every token."""
+    s = inp["shape"]
+    L = oracle.router_logits(oracle.decode_bf16(I.bits(inp["x"])),
+                             oracle.decode_bf16(I.bits(inp["router_w"])))
+    ids, w, margin, _ = oracle.topk(L, s.k, s.renormalize)
+    return {"ids": ids, "w": w, "margin": margin, "logits": L}
+
+
+def check_layout(lay, ids, E, B):
+    """The aligned layout a layer call left in its workspace, bit for bit
+    against the oracle's moe_align_block_size of the call's own ids."""
+    ref = oracle.align(np.asarray(ids).reshape(-1), E, B)
+    assert np.array_equal(lay["topk_ids"], ids)
+    assert lay["num_post_pad"] == ref["num_post_pad"]
+    assert np.array_equal(lay["sorted_ids"], ref["sorted_ids"])
+    assert np.array_equal(lay["block_expert_ids"], ref["block_expert_ids"])
+    assert np.array_equal(lay["expert_offsets"], ref["expert_offsets"])
+    return ref
 
 
 def check_routing(gpu_ids, gpu_w, ref, logits64=None):

@@ -117,6 +117,57 @@ def test_stage_calls_host_side_rejections(lib):
     assert lib.moe_read_device_status(None, C.byref(code), None) == abi.MOE_ERR_INVALID_ARG
 
 
+def test_workspace_views_point_inside_the_workspace(lib):
+    for name in ("tiny", "verify_t8", "verify_t64", "int4_t32", "prefill_t4096"):
+        s = I.shape(name)
+        dims = abi.dims_of(s)
+        need = abi.moe_workspace_bytes(dims)
+        v = abi.moe_workspace_views(dims)
+        S = s.T * s.k
+        cap = S + s.E * (s.block - 1)
+        sizes = {"topk_ids": 4 * S, "topk_weights": 4 * S, "sorted_ids": 4 * cap,
+                 "block_expert_ids": 4 * (cap // s.block + 1), "num_post_pad": 4,
+                 "expert_offsets": 4 * (s.E + 1)}
+        spans = sorted((v[k], v[k] + n) for k, n in sizes.items())
+        for (a0, a1), (b0, _) in zip(spans, spans[1:]):
+            assert a1 <= b0  # disjoint
+        assert all(off % 256 == 0 for off in v.values())
+        assert spans[0][0] >= 256 and spans[-1][1] <= need  # past the header, inside
+    vv = abi.moe_workspace_views_t()
+    assert lib.moe_workspace_views(None, C.byref(vv)) == abi.MOE_ERR_INVALID_ARG
+    assert lib.moe_workspace_views(C.byref(abi.dims_of(I.shape("tiny"))), None) == \
+        abi.MOE_ERR_INVALID_ARG
+
+
+def test_flags_and_stall_hook_host_checks(lib):
+    dims = abi.dims_of(I.shape("verify_t8"), flags=abi.MOE_FLAG_BATCH_INVARIANT)
+    assert abi.moe_workspace_bytes(dims) > 0
+    with pytest.raises(abi.MoeError) as e:
+        abi.moe_workspace_bytes(abi.dims_of(I.shape("verify_t8"), flags=2))
+    assert e.value.status == abi.MOE_ERR_UNSUPPORTED
+    assert lib.moe_workspace_inject_stall(None, 1024, 100, None) == abi.MOE_ERR_WORKSPACE
+    assert lib.moe_workspace_inject_stall(FAKE + 16, 1024, 100, None) == abi.MOE_ERR_WORKSPACE
+    assert lib.moe_workspace_inject_stall(FAKE, 1024, 0, None) == abi.MOE_ERR_INVALID_ARG
+    assert lib.moe_workspace_inject_stall(FAKE, 1024, 2000000, None) == abi.MOE_ERR_INVALID_ARG
+
+
+def test_static_entry_point_host_checks_launch_nothing(lib):
+    dims = abi.dims_of(I.shape("verify_t8"))
+    ex = abi.moe_expert_weights_t(FAKE, None, FAKE, None)
+    sh = abi.moe_shared_weights_t(FAKE, FAKE, FAKE)
+    assert lib.moe_layer_forward_static(C.byref(dims), None, FAKE, C.byref(ex), C.byref(sh), FAKE,
+                                        None, None, None, None) == abi.MOE_ERR_INVALID_ARG
+    assert lib.moe_layer_forward_static(C.byref(dims), FAKE, FAKE, C.byref(ex), None, FAKE,
+                                        None, None, None, None) == abi.MOE_ERR_INVALID_ARG
+    big = abi.dims_of(I.shape("prefill_t4096"))
+    assert lib.moe_layer_forward_static(C.byref(big), FAKE, FAKE, C.byref(ex), C.byref(sh), FAKE,
+                                        None, None, None, None) == abi.MOE_ERR_WORKSPACE
+    zero = abi.dims_of(I.shape("verify_t8", T=0))
+    assert lib.moe_layer_forward_static(C.byref(zero), None, None, None, None, None, None, None,
+                                        None, None) == abi.MOE_OK
+    assert abi.moe_kernel_launch_count() == 0
+
+
 def test_launch_counter_starts_at_zero_without_launches(lib):
     assert abi.moe_kernel_launch_count() == 0
 
@@ -142,11 +193,18 @@ int main(void) {
   memset(&d, 0, sizeof d);
   d.T = 8; d.d = 2048; d.E = 256; d.top_k = 8; d.I = 512; d.I_shared = 512;
   d.renormalize = 1; d.block_size = 16; d.weight_format = MOE_WEIGHTS_BF16; d.group_size = 32;
+  d.flags = MOE_FLAG_BATCH_INVARIANT;
   if (moe_workspace_bytes(&d, &n) != MOE_OK || n == 0) return 1;
   d.top_k = 0;
   if (moe_workspace_bytes(&d, &n) == MOE_OK) return 2;
   if (moe_layer_forward(NULL, NULL, NULL, NULL, NULL, NULL, NULL, NULL, NULL, 0, NULL) == MOE_OK)
     return 3;
+  {
+    moe_workspace_views_t v;
+    d.top_k = 8;
+    if (moe_workspace_views(&d, &v) != MOE_OK || v.sorted_ids == 0 || v.expert_offsets == 0)
+      return 4;
+  }
   printf("%s|%s\n", moe_status_string(MOE_OK), moe_status_string(MOE_ERR_INVALID_ARG));
   return 0;
 }

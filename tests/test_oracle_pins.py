@@ -330,17 +330,21 @@ def test_layer_single_expert_is_dense_swiglu():
 
 
 def test_layer_closed_form_with_shared_expert():
-    bf = lambda vals: np.array([f32_bits_to_bf16(v) for v in vals], np.uint16)
-    x = bf([1.0, 0.0]).reshape(1, 2)
-    wr = bf([1.0, 0.0, 0.0, 0.0]).reshape(2, 2)            # logits [1, 0] -> expert 0
-    gu = bf([2, 0, 3, 0, 0, 0, 0, 0]).reshape(2, 2, 2)      # expert 0: g=2, u=3
-    dn = bf([1.0, 0.5, 0.0, 0.0]).reshape(2, 2, 1)          # y = [h, h/2]
-    sh = {"gate_up": bf([1, 0, 1, 0]).reshape(2, 2), "down": bf([1, 1]).reshape(2, 1),
-          "gate_w": bf([0, 0])}
-    res = oracle.layer(x, wr, {"format": oracle.BF16, "gate_up": gu, "down": dn}, sh,
-                       {"T": 1, "d": 2, "E": 2, "k": 1, "I": 1, "Is": 1, "renormalize": 1})
-    h = 2.0 / (1.0 + math.exp(-2.0)) * 3.0
-    hs = 1.0 / (1.0 + math.exp(-1.0))
+    """tests/golden/closed_form_layer.json: a hand-chosen one-token layer whose
+    output has a closed form in exp() (computed here, not stored)."""
+    import json
+    import os
+
+    g = json.load(open(os.path.join(os.path.dirname(__file__), "golden", "closed_form_layer.json")))
+    bf = lambda a: np.array([f32_bits_to_bf16(v) for v in np.ravel(a)], np.uint16).reshape(
+        np.shape(a))
+    dm = g["dims"]
+    sh = {"gate_up": bf(g["shared_gate_up"]), "down": bf(g["shared_down"]), "gate_w": bf(g["w_sg"])}
+    res = oracle.layer(bf(g["x"]), bf(g["router_w"]),
+                       {"format": oracle.BF16, "gate_up": bf(g["gate_up"]), "down": bf(g["down"])},
+                       sh, dm)
+    h = 2.0 / (1.0 + math.exp(-2.0)) * 3.0   # expert 0: g = 2, u = 3
+    hs = 1.0 / (1.0 + math.exp(-1.0))        # shared: g = u = 1, sigmoid gate at 0 = 1/2
     assert res["ids"].tolist() == [[0]]
     assert res["w"].tolist() == [[1.0]]
     np.testing.assert_allclose(res["out"][0], [h + 0.5 * hs, 0.5 * h + 0.5 * hs], rtol=1e-15)

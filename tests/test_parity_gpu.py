@@ -2,6 +2,9 @@
 oracle on the same seeded inputs: the whole layer on every workload shape,
 each stage on its own, and the edge cases (T=1, T=0, ties, k=E, one expert
 holding all tokens, several align block sizes, ragged tiles, bad ids)."""
+import dataclasses
+import time
+
 import numpy as np
 import pytest
 import torch
@@ -11,7 +14,8 @@ from moe_expert_layer_gemv_gb300 import abi, build
 from moe_expert_layer_gemv_gb300 import inputs as I
 from moe_expert_layer_gemv_gb300.layer import MoeLayer
 
-from _common import NEAR_TIE, WEIGHT_RTOL, bf16_to_f64, check_routing, compare_out, oracle_args
+from _common import (NEAR_TIE, PARITY_LOG, WEIGHT_RTOL, bf16_to_f64, check_layout, check_routing,
+                     compare_out, inputs, oracle_args, oracle_routing)
 
 pytestmark = pytest.mark.gpu
 
@@ -24,9 +28,9 @@ def _lib():
     abi.load()
 
 
-def run_layer(inp):
+def run_layer(inp, flags=0):
     s = inp["shape"]
-    layer = MoeLayer(inp, "cuda")
+    layer = MoeLayer(inp, "cuda", flags)
     x = inp["x"].cuda()
     ids = torch.empty((s.T, s.k), dtype=torch.int32, device="cuda")
     w = torch.empty((s.T, s.k), dtype=torch.float32, device="cuda")
@@ -40,21 +44,25 @@ def logits64(inp):
     return (inp["x"].to(torch.float64) @ inp["router_w"].to(torch.float64).T).numpy()
 
 
-def layer_parity(inp, tokens=None):
-    """Full-layer check.  tokens: None = all; else a sample (large T)."""
+def layer_parity(inp, name=None, flags=0):
+    """Full-layer check of every token: routing against the oracle's (ids
+    bit-exact off near-ties), the aligned layout the call left in its
+    workspace bit for bit against the oracle's align of the call's ids, and the
+    output against the oracle fed the call's ids (which covers near-ties)."""
     s = inp["shape"]
-    layer, out, ids, w = run_layer(inp)
-    args = oracle_args(inp)
-    tl = None if tokens is None else np.asarray(tokens, np.int32)
-    ref = oracle.layer(*args, tokens=tl)
-    sel = slice(None) if tl is None else tl
-    L64 = logits64(inp)[sel]
-    n_near, n_mism = check_routing(ids[sel], w[sel], ref, L64)
-    # outputs against the oracle fed the GPU's routing (covers near-ties)
-    ov = oracle.layer(*args, ids_override=ids, tokens=tl)
-    np.testing.assert_allclose(w[sel], ov["w"], rtol=WEIGHT_RTOL, atol=1e-7)
-    rel, mx = compare_out(bf16_to_f64(out)[sel], ov["out"])
-    return {"rel": rel, "max": mx, "near": n_near, "mism": n_mism, "layer": layer, "ids": ids}
+    layer, out, ids, w = run_layer(inp, flags)
+    ref = oracle_routing(inp)
+    n_near, n_mism = check_routing(ids, w, ref, ref["logits"])
+    lay = layer.layout()
+    check_layout(lay, ids, s.E, s.block)
+    assert np.array_equal(lay["topk_weights"], w)
+    ov = oracle.layer(*oracle_args(inp), ids_override=ids)
+    np.testing.assert_allclose(w, ov["w"], rtol=WEIGHT_RTOL, atol=1e-7)
+    name = name or f"{s.name} T={s.T} d={s.d} E={s.E} k={s.k} I={s.I} Is={s.Is} B={s.block}"
+    rel, mx, lit = compare_out(bf16_to_f64(out), ov["out"], name)
+    PARITY_LOG[-1].update(near=n_near, mism=n_mism)
+    return {"rel": rel, "max": mx, "literal": lit, "near": n_near, "mism": n_mism,
+            "layer": layer, "ids": ids, "out": out}
 
 
 @pytest.mark.parametrize("name,seed", [("tiny", 0), ("tiny", 1), ("tiny", 2),
@@ -62,23 +70,15 @@ def layer_parity(inp, tokens=None):
                                        ("verify_t64", 0), ("verify_t64_skew", 0),
                                        ("int4_t32", 0), ("int4_t32", 1)])
 def test_layer_parity_workloads(name, seed):
-    r = layer_parity(I.make_inputs(I.shape(name), seed))
-    print(f"{name} seed {seed}: rel-L2 {r['rel']:.2e} max/rms {r['max']:.2e} "
-          f"near-ties {r['near']} mismatched {r['mism']}")
+    layer_parity(inputs(name, seed), f"{name} seed {seed}")
 
 
-def test_layer_parity_prefill_sampled():
-    s = I.shape("prefill_t4096")
-    inp = I.make_inputs(s, 0)
-    rng = np.random.default_rng(0)
-    tokens = np.sort(rng.choice(s.T, size=48, replace=False))
-    tokens[0], tokens[-1] = 0, s.T - 1
-    r = layer_parity(inp, tokens)
-    # whole-layer property at full size: the align layout of the GPU's ids
-    ids = r["ids"]
-    ref = oracle.align(ids.reshape(-1), s.E, s.block)
-    assert ref["counts"].sum() == s.T * s.k
-    print(f"prefill sampled: rel-L2 {r['rel']:.2e} max/rms {r['max']:.2e}")
+def test_layer_parity_prefill_full():
+    """The T=4096 prefill layer on the tensor-core path, every token against
+    the oracle: all ~380 padded 128-row M blocks of the routed experts and all
+    32 M blocks of the shared expert hold checked rows, and the multi-CTA
+    align's layout is compared bit for bit."""
+    layer_parity(inputs("prefill_t4096", 0), "prefill_t4096 seed 0 (all tokens)")
 
 
 @pytest.mark.parametrize("over,seed", [
@@ -151,7 +151,7 @@ def _stage_tensors(s):
                                        ("prefill_t4096", {"T": 1000, "I": 16, "Is": 16})])
 def test_stage_route(name, over):
     s = I.shape(name, **over)
-    inp = I.make_inputs(s, 0)
+    inp = inputs(name, 0, **over)
     dims = abi.dims_of(s)
     ws = abi.alloc_workspace(dims)
     t = _stage_tensors(s)
@@ -248,7 +248,7 @@ def test_stage_expert_forward_from_oracle_routing(name):
 
 
 def test_repeat_calls_are_bitwise_deterministic():
-    inp = I.make_inputs(I.shape("verify_t64_skew"), 0)
+    inp = inputs("verify_t64_skew", 0)
     layer = MoeLayer(inp, "cuda")
     x = inp["x"].cuda()
     a = layer.forward(x).clone()
@@ -258,7 +258,7 @@ def test_repeat_calls_are_bitwise_deterministic():
 
 
 def test_timed_entry_point_matches_and_records_events():
-    inp = I.make_inputs(I.shape("verify_t8"), 0)
+    inp = inputs("verify_t8", 0)
     layer = MoeLayer(inp, "cuda")
     x = inp["x"].cuda()
     a = layer.forward(x).clone()
@@ -307,7 +307,7 @@ def test_layer_forward_replays_from_a_cuda_graph(name):
     """One layer call captured into a CUDA graph and replayed gives the eager
     call's output bit for bit, for new tokens copied into the captured x too."""
     s = I.shape(name)
-    layer = MoeLayer(I.make_inputs(s, 0), "cuda")
+    layer = MoeLayer(inputs(name, 0), "cuda")
     x = I.make_x(s, 100).cuda()
     out_g = layer.new_out()
     layer.forward(x, out_g)  # warm-up: one-time kernel attributes stay out of the capture
@@ -322,3 +322,77 @@ def test_layer_forward_replays_from_a_cuda_graph(name):
         torch.cuda.synchronize()
         assert torch.equal(out_g, ref)
     assert layer.device_status() == abi.MOE_OK
+
+
+# ----------------------------------------------------------------------------- batch invariance
+# "veloGB10", Kernel work: batch-invariant GEMMs, so that a verify pass gives
+# exactly what plain decode steps give.  Each token of a batched call must equal,
+# bit for bit, the same token run alone.
+
+
+def _single_token_rows(inp, flags=0):
+    s = inp["shape"]
+    one = dict(inp, shape=dataclasses.replace(s, T=1))
+    one["x"] = inp["x"][:1].clone()
+    layer = MoeLayer(one, "cuda", flags)
+    rows, ids = [], []
+    for t in range(s.T):
+        x = inp["x"][t:t + 1].cuda()
+        i1 = torch.empty((1, s.k), dtype=torch.int32, device="cuda")
+        rows.append(layer.forward(x, topk_ids=i1).clone())
+        ids.append(i1.clone())
+    torch.cuda.synchronize()
+    assert layer.device_status() == abi.MOE_OK
+    return torch.cat(rows), torch.cat(ids)
+
+
+@pytest.mark.parametrize("name,over", [("verify_t8", {}), ("verify_t64", {}),
+                                       ("verify_t64_skew", {}), ("int4_t32", {}),
+                                       # above the single-launch routing (unfused router)
+                                       ("verify_t8", {"T": 160, "d": 512, "E": 64, "I": 128,
+                                                      "Is": 128})])
+def test_batch_invariance_decode_path(name, over):
+    inp = inputs(name, 0, **over)
+    layer, out, ids, _ = run_layer(inp)
+    rows, ids1 = _single_token_rows(inp)
+    assert np.array_equal(ids1.cpu().numpy(), ids)
+    assert torch.equal(out, rows), "batched rows differ from single-token calls"
+
+
+def test_batch_invariance_flag_keeps_prefill_sizes_invariant():
+    """T >= 256 with tensor-core dims: only with MOE_FLAG_BATCH_INVARIANT do
+    the rows equal single-token calls; the flagged call still meets parity."""
+    s = I.shape("verify_t8", T=300, d=512, E=64, k=4, I=128, Is=128, block=128)
+    inp = I.make_inputs(s, 5)
+    f = abi.MOE_FLAG_BATCH_INVARIANT
+    r = layer_parity(inp, "T=300 tensor-core dims, batch-invariant flag", flags=f)
+    rows, ids1 = _single_token_rows(inp, flags=f)
+    assert np.array_equal(ids1.cpu().numpy(), r["ids"])
+    assert torch.equal(r["out"], rows)
+
+
+# ----------------------------------------------------------------------------- bounded waits
+
+
+def test_bounded_wait_times_out_and_the_workspace_recovers():
+    """The stall hook makes the gate_up kernel's producers issue nothing: its
+    consumers' bounded waits run out (no fault, nothing read out of bounds),
+    the call records MOE_ERR_TIMEOUT, and after moe_workspace_init the same
+    workspace gives the correct output again."""
+    inp = inputs("verify_t8", 0)
+    layer = MoeLayer(inp, "cuda")
+    x = inp["x"].cuda()
+    ref = layer.forward(x).clone()
+    torch.cuda.synchronize()
+    abi.moe_workspace_inject_stall(layer.ws, layer.ws.numel(), 2000)  # 2 ms
+    t0 = time.perf_counter()
+    layer.forward(x)
+    code = layer.device_status()  # synchronises
+    took = time.perf_counter() - t0
+    assert code == abi.MOE_ERR_TIMEOUT
+    assert took < 10.0
+    abi.moe_workspace_init(layer.ws, layer.ws.numel())
+    again = layer.forward(x)
+    torch.cuda.synchronize()
+    assert layer.device_status() == abi.MOE_OK
+    assert torch.equal(again, ref)

@@ -2,21 +2,22 @@
 device memory (no cudaMalloc allowed or available, so no workspace to pass): it
 runs the layer with scratch in a fixed array inside the library.
 
-Its output must match the workspace entry point, moe_layer_forward, within the
-parity tolerance used everywhere in this suite, on two calls in a row (the
-second call reuses the array the first one left behind).  This file is
-collected last on purpose."""
+It runs the very kernels moe_layer_forward runs, on the same inputs, so its
+output must equal that entry point's bit for bit, on two calls in a row (the
+second call reuses the array the first one left behind); it is also held to the
+parity bar against the fp64 oracle.  This file is collected last on purpose."""
 import ctypes as C
 
 import numpy as np
 import pytest
 import torch
 
+import oracle
 from moe_expert_layer_gemv_gb300 import abi, build
 from moe_expert_layer_gemv_gb300 import inputs as I
 from moe_expert_layer_gemv_gb300.layer import MoeLayer
 
-from _common import bf16_to_f64, compare_out
+from _common import bf16_to_f64, compare_out, oracle_args
 
 pytestmark = pytest.mark.gpu
 
@@ -32,7 +33,8 @@ def _lib():
 @pytest.mark.parametrize("name", ["verify_t8", "int4_t32"])
 def test_static_scratch_matches_workspace_entry_point(name):
     s = I.shape(name)
-    layer = MoeLayer(I.make_inputs(s, 0), "cuda")
+    inp0 = I.make_inputs(s, 0)
+    layer = MoeLayer(inp0, "cuda")
     lib = abi.load()
     status = torch.full((1,), -1, dtype=torch.int32, device="cuda")
     for seed in (11, 12):  # two calls in a row, different token batches
@@ -50,7 +52,26 @@ def test_static_scratch_matches_workspace_entry_point(name):
         assert rc == abi.MOE_OK, abi.moe_status_string(rc)
         assert int(status.item()) == abi.MOE_OK
         assert torch.equal(ids, ids_ref)
-        compare_out(bf16_to_f64(out), bf16_to_f64(ref))
+        assert torch.equal(out, ref)
+        inp = dict(inp0, x=x.cpu())
+        ov = oracle.layer(*oracle_args(inp), ids_override=ids.cpu().numpy())
+        compare_out(bf16_to_f64(out), ov["out"], f"{name} static scratch, batch {seed}")
+
+
+def test_static_scratch_checks_arguments_before_enqueueing_anything():
+    """Argument errors come back before any GPU work (no launch counted)."""
+    s = I.shape("verify_t8")
+    dims = abi.dims_of(s)
+    lib = abi.load()
+    ex = abi.moe_expert_weights_t(1 << 40, None, 1 << 40, None)
+    sh = abi.moe_shared_weights_t(1 << 40, 1 << 40, 1 << 40)
+    before = abi.moe_kernel_launch_count()
+    assert lib.moe_layer_forward_static(C.byref(dims), None, 1 << 40, C.byref(ex), C.byref(sh),
+                                        1 << 40, None, None, None, None) == abi.MOE_ERR_INVALID_ARG
+    assert lib.moe_layer_forward_static(C.byref(dims), (1 << 40) + 2, 1 << 40, C.byref(ex),
+                                        C.byref(sh), 1 << 40, None, None, None,
+                                        None) == abi.MOE_ERR_INVALID_ARG
+    assert abi.moe_kernel_launch_count() == before
 
 
 def test_static_scratch_rejects_dims_beyond_its_size():
