@@ -6,10 +6,14 @@
 // start while the stream's previous kernel finishes: it requests only the
 // router weights before its griddepcontrol.wait):
 //   1. routing: at decode sizes (T <= 128) one launch -- router GEMV over many
-//      CTAs, top-k by the last CTA of each token tile, align + work plan by the
-//      last tile; above that, router, top-k and align as three launches
+//      CTAs, top-k by the last CTA of each token tile; above that, router,
+//      top-k and align (+ the workspace plan) as three launches
 //   2. gate_up + SwiGLU                  (persistent, bulk-copy pipeline)
 //   3. down                              (persistent, bulk-copy pipeline)
+//   At decode sizes stages 2 and 3 build the align layout and their work plan
+//   from the routing ids in every CTA's shared memory (no serial plan step
+//   between the routing and the weight streams); the down stage also leaves
+//   the aligned layout in the workspace.
 //   4. combine + shared-expert gate      (one CTA per token and column block)
 // The shared expert rides in stages 2-3 as one more work expert, so its weight
 // stream overlaps the routed experts' ("veloGB10", Kernel work: shared-expert
@@ -185,15 +189,34 @@ moe_status_t check_weights(const moe_dims_t& dm, const moe_expert_weights_t* ex,
 struct ExpertPlan {
   GemvShape gu, dn;
   PlanParams pp;
-  bool tc;  // run the expert stages on the tensor cores
+  bool tc;         // run the expert stages on the tensor cores
+  bool smem_plan;  // the GEMV stages plan from the routing ids in shared memory
   int sms;
 };
 
+// Routing slots and tokens up to which the GEMV stages may plan in shared
+// memory (the token bitmasks of the plan hold up to 128 tokens per expert).
+constexpr int kSmemPlanMaxSlots = 2048;
+constexpr int kSmemPlanMaxT = 128;
+
+// smem_plan_ok: the caller leaves the routing ids in the workspace and does
+// not build a workspace plan, so the GEMV stages may plan for themselves.
 moe_status_t expert_plan(const moe_dims_t& dm, void* ws, const Layout& L, int sms,
-                         ExpertPlan* ep) {
+                         bool smem_plan_ok, ExpertPlan* ep) {
   const int fmt = dm.weight_format;
-  ep->gu = gate_up_shape(fmt, dm.d, dm.I, dm.I_shared, kGemvSmemBudget);
-  ep->dn = down_shape(fmt, dm.d, dm.I, dm.I_shared, kGemvSmemBudget);
+  const int S = dm.T * dm.top_k;
+  ep->smem_plan = false;
+  if (smem_plan_ok && !L.tc && S <= kSmemPlanMaxSlots && dm.T <= kSmemPlanMaxT) {
+    const int r = smem_plan_bytes(dm.E, S);
+    ep->gu = gate_up_shape(fmt, dm.d, dm.I, dm.I_shared, kGemvSmemBudget, r);
+    ep->dn = down_shape(fmt, dm.d, dm.I, dm.I_shared, kGemvSmemBudget, r);
+    ep->smem_plan = smem_plan_fits(ep->gu, dm.E, dm.T, dm.top_k) &&
+                    smem_plan_fits(ep->dn, dm.E, dm.T, dm.top_k);
+  }
+  if (!ep->smem_plan) {
+    ep->gu = gate_up_shape(fmt, dm.d, dm.I, dm.I_shared, kGemvSmemBudget, 0);
+    ep->dn = down_shape(fmt, dm.d, dm.I, dm.I_shared, kGemvSmemBudget, 0);
+  }
   if (ep->gu.n_stages < 2 || ep->dn.n_stages < 2) return MOE_ERR_UNSUPPORTED;
   PlanParams& pp = ep->pp;
   pp.work = at<WorkExpert>(ws, L.work);
@@ -250,11 +273,28 @@ moe_status_t record(void* const* events, int which, cudaStream_t st) {
   return MOE_OK;
 }
 
-// Stages 3-5 given a plan already in the workspace.
+// Stages 3-5 given a plan in the workspace, or (ep.smem_plan) the routing ids
+// in the workspace.
 moe_status_t run_experts(const moe_dims_t& dm, const void* x, const float* topk_w,
                          const float* sg, const int32_t* sorted_ids, const moe_expert_weights_t* ex,
                          const moe_shared_weights_t* sh, void* out, void* ws, const Layout& L,
                          const ExpertPlan& ep, cudaStream_t st, void* const* events) {
+  SmemPlanArgs sp_gu = {}, sp_dn = {};
+  if (ep.smem_plan) {
+    sp_gu.ids = at<int32_t>(ws, L.ids);
+    sp_gu.E = dm.E;
+    sp_gu.B = dm.block_size;
+    sp_dn = sp_gu;
+    sp_gu.base = ep.pp.base_gu;
+    sp_gu.base_s = ep.pp.base_gu_s;
+    sp_dn.base = ep.pp.base_dn;
+    sp_dn.base_s = ep.pp.base_dn_s;
+    // The down stage leaves the aligned layout in the workspace.
+    sp_dn.sorted_ids = at<int32_t>(ws, L.sorted);
+    sp_dn.block_ids = at<int32_t>(ws, L.blocks);
+    sp_dn.num_post_pad = at<int32_t>(ws, L.npp);
+    sp_dn.expert_offsets = at<int32_t>(ws, L.offs);
+  }
   const LaunchCfg next{st, true};
   int* status = at<int>(ws, L.header);
   const ExpertArgs a = expert_args(dm, ex, sh);
@@ -274,11 +314,11 @@ moe_status_t run_experts(const moe_dims_t& dm, const void* x, const float* topk_
       return MOE_ERR_CUDA;
   } else {
     if (launch_gate_up(next, a, ep.gu, static_cast<const uint16_t*>(x), sorted_ids, ep.pp.plan,
-                       ep.pp.work, ep.pp.cta_gu, h, hs, status, ep.pp.grid) != cudaSuccess)
+                       ep.pp.work, ep.pp.cta_gu, sp_gu, h, hs, status, ep.pp.grid) != cudaSuccess)
       return MOE_ERR_CUDA;
     if ((s = record(events, MOE_EV_GATE_UP, st)) != MOE_OK) return s;
-    if (launch_down(next, a, ep.dn, sorted_ids, ep.pp.plan, ep.pp.work, ep.pp.cta_dn, h, hs, y,
-                    ys, status, ep.pp.grid) != cudaSuccess)
+    if (launch_down(next, a, ep.dn, sorted_ids, ep.pp.plan, ep.pp.work, ep.pp.cta_dn, sp_dn, h, hs,
+                    y, ys, status, ep.pp.grid) != cudaSuccess)
       return MOE_ERR_CUDA;
   }
   if ((s = record(events, MOE_EV_DOWN, st)) != MOE_OK) return s;
@@ -317,8 +357,9 @@ moe_status_t layer_forward(const moe_dims_t* dims, const void* x, const void* ro
   if ((s = check_ws(dm, ws, ws_bytes, &L)) != MOE_OK) return s;
   DeviceInfo di;
   if (!device_info(&di)) return MOE_ERR_CUDA;
+  const bool fused = fused_route_supported(dm.T, dm.E, dm.top_k);
   ExpertPlan ep;
-  if ((s = expert_plan(dm, ws, L, di.sms, &ep)) != MOE_OK) return s;
+  if ((s = expert_plan(dm, ws, L, di.sms, fused, &ep)) != MOE_OK) return s;
 
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   const LaunchCfg next{st, true};
@@ -331,11 +372,11 @@ moe_status_t layer_forward(const moe_dims_t* dims, const void* x, const void* ro
   if ((s = record(events, MOE_EV_BEGIN, st)) != MOE_OK) return s;
   const uint16_t* w_sg = sh ? static_cast<const uint16_t*>(sh->gate_w) : nullptr;
   float* sg = at<float>(ws, L.sg);
-  if (fused_route_supported(dm.T, dm.E, dm.top_k)) {
+  if (fused) {
     if (launch_route_fused(next, static_cast<const uint16_t*>(x),
                            static_cast<const uint16_t*>(router_w), w_sg, logits, sg, dm.T, dm.d,
-                           dm.E, dm.top_k, dm.renormalize, ids, w, ids_out, w_out, dm.block_size,
-                           sorted, at<int32_t>(ws, L.blocks), at<int32_t>(ws, L.npp),
+                           dm.E, dm.top_k, dm.renormalize, ids, w, ids_out, w_out, !ep.smem_plan,
+                           dm.block_size, sorted, at<int32_t>(ws, L.blocks), at<int32_t>(ws, L.npp),
                            at<int32_t>(ws, L.offs), ep.pp, status, status + kRouteCounterBase,
                            di.sms) != cudaSuccess)
       return MOE_ERR_CUDA;
@@ -550,7 +591,7 @@ moe_status_t moe_expert_forward(const moe_dims_t* dims, const void* x, const flo
   DeviceInfo di;
   if (!device_info(&di)) return MOE_ERR_CUDA;
   ExpertPlan ep;
-  if ((s = expert_plan(dm, workspace, L, di.sms, &ep)) != MOE_OK) return s;
+  if ((s = expert_plan(dm, workspace, L, di.sms, false, &ep)) != MOE_OK) return s;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   if (launch_plan(LaunchCfg{st, true}, dm.T, dm.E, dm.top_k, dm.block_size, sorted_ids,
                   num_post_pad, expert_offsets, ep.pp, at<int>(workspace, L.header)) !=

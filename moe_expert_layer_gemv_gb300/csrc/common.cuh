@@ -164,6 +164,66 @@ __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t by
       : "memory");
 }
 
+// ------------------------------------------------------------------ block scan
+// Exclusive scan of V ints per thread over the CTA (blockDim a multiple of 32,
+// <= 1024).  scratch: >= 32 * V ints.  Every thread gets the totals.
+template <int V>
+__device__ __forceinline__ void block_scan(const int (&v)[V], int (&ex)[V], int (&tot)[V], int* scratch) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
+  int inc[V];
+#pragma unroll
+  for (int i = 0; i < V; ++i) {
+    inc[i] = v[i];
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int n = __shfl_up_sync(0xffffffffu, inc[i], o);
+      if (lane >= o) inc[i] += n;
+    }
+    if (lane == 31) scratch[i * 32 + warp] = inc[i];
+  }
+  __syncthreads();
+  if (warp == 0) {
+#pragma unroll
+    for (int i = 0; i < V; ++i) {
+      int s = lane < nw ? scratch[i * 32 + lane] : 0;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int n = __shfl_up_sync(0xffffffffu, s, o);
+        if (lane >= o) s += n;
+      }
+      scratch[i * 32 + lane] = s;
+    }
+  }
+  __syncthreads();
+#pragma unroll
+  for (int i = 0; i < V; ++i) {
+    ex[i] = (warp ? scratch[i * 32 + warp - 1] : 0) + inc[i] - v[i];
+    tot[i] = scratch[i * 32 + nw - 1];
+  }
+  __syncthreads();
+}
+
+// ---------------------------------------------------------------- unit split
+// First unit of the work expert whose estimated costs start at c0 (units from
+// u0; n tokens in groups of xt, `tiles` row tiles per group, cost base + tokens
+// per unit) at which the running cost reaches `target`.
+__device__ __forceinline__ int unit_at_cost(int target, int c0, int u0, int tiles, int n, int xt, int base) {
+  const int groups = (n + xt - 1) / xt;
+  const int nt_last = n - (groups - 1) * xt;
+  const int per_full = tiles * (base + xt);
+  const int r = target - c0;
+  int g, t;
+  if (groups > 1 && r < (groups - 1) * per_full) {
+    g = r / per_full;
+    t = (r - g * per_full) / (base + xt);
+  } else {
+    g = groups - 1;
+    t = (r - (groups - 1) * per_full) / (base + nt_last);
+    t = min(t, tiles - 1);
+  }
+  return u0 + g * tiles + t;
+}
+
 // ---------------------------------------------------------------- misc
 __host__ __device__ constexpr int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 __host__ __device__ constexpr int64_t round_up(int64_t a, int64_t b) { return ceil_div(a, b) * b; }

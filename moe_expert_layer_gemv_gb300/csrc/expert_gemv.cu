@@ -7,8 +7,11 @@
 //
 // Structure (both stages): a persistent grid of kCtasPerSm CTAs per SM.  Work
 // is cut into units = (work expert, token group, row tile); each CTA takes one
-// contiguous range of units (its first work expert is precomputed by the
-// plan), so consecutive units mostly share an expert and a token group.  The
+// contiguous range of units of about equal estimated cost, so consecutive
+// units mostly share an expert and a token group.  At decode sizes every CTA
+// derives the plan (align layout, work list, its range) from the routing ids
+// in its own shared memory (smem_plan); otherwise it reads the plan the align
+// step wrote to the workspace.  The
 // last warp of a CTA is the producer: one bulk copy (cp.async.bulk, the
 // non-tensor TMA) per weight block and per activation row lands a unit in a
 // shared-memory ring stage and completes the stage's mbarrier by transaction
@@ -42,11 +45,13 @@ struct GuArgs {
   const Plan* plan;
   const WorkExpert* work;
   const int32_t* cta;         // CTA unit ranges and first work experts (see PlanParams)
-  float* h;                   // [num_post_pad][I]
+  float* h;                   // [sorted positions][I]
   float* hs;                  // [T][Is]
   int* status;
   int T, d, I, Is, k;
   int rg, rgs, xt, stage_bytes, n_stages;
+  int stage_off;              // shared-memory offset of the stage ring
+  SmemPlanArgs sp;
 };
 
 struct DnArgs {
@@ -64,29 +69,249 @@ struct DnArgs {
   int* status;
   int T, d, I, Is, k;
   int rd, rds, xt, stage_bytes, n_stages;
+  int stage_off;
+  SmemPlanArgs sp;
 };
 
 // Walks the work experts along a CTA's contiguous unit range.  Units of one
 // work expert are numbered group-major: unit = grp * tiles + tile, so
-// consecutive units share a token group (same activation rows).
-template <bool kDown>
+// consecutive units share a token group (same activation rows).  The work
+// experts come from the workspace plan (work != nullptr) or from the CTA's
+// shared-memory plan (wex, wnt), where each expert's first unit and first
+// sorted position follow from the previous expert's.
 struct UnitCursor {
-  const WorkExpert* work;
+  const WorkExpert* work;  // workspace plan, or nullptr
+  const int16_t* wex;      // shared-memory plan: expert ids (-1 = the shared expert)
+  const int16_t* wnt;      //   and their token counts
   int n_work, tiles_r, tiles_s, xt;
+  bool down;
   int i, ubeg, uend, tiles, groups;
-  WorkExpert we;
-  __device__ __forceinline__ void load(int idx) {
-    i = idx;
-    we = work[idx];
-    tiles = we.expert < 0 ? tiles_s : tiles_r;
-    groups = (int)ceil_div(we.n_tok, xt);
-    ubeg = kDown ? we.unit_dn : we.unit_gu;
+  int expert, n_tok, pos;  // current work expert; pos: its first sorted position
+  __device__ __forceinline__ void set(int e, int n) {
+    expert = e;
+    n_tok = n;
+    tiles = e < 0 ? tiles_s : tiles_r;
+    groups = (n + xt - 1) / xt;
     uend = ubeg + tiles * groups;
   }
+  __device__ __forceinline__ void from_workspace(int idx) {
+    const WorkExpert we = work[idx];
+    ubeg = down ? we.unit_dn : we.unit_gu;
+    pos = we.pos;
+    set(we.expert, we.n_tok);
+  }
+  __device__ __forceinline__ void start(int idx, int ubeg0, int pos0) {
+    i = idx;
+    if (work) {
+      from_workspace(idx);
+    } else {
+      ubeg = ubeg0;
+      pos = pos0;
+      set(wex[idx], wnt[idx]);
+    }
+  }
+  __device__ __forceinline__ void advance() {
+    ++i;
+    if (work) {
+      from_workspace(i);
+    } else {
+      if (expert >= 0) pos += n_tok;
+      ubeg = uend;
+      set(wex[i], wnt[i]);
+    }
+  }
   __device__ __forceinline__ void seek(int u) {
-    while (u >= uend && i + 1 < n_work) load(i + 1);
+    while (u >= uend && i + 1 < n_work) advance();
   }
 };
+
+// This CTA's share of a stage: units [u_begin, u_end), starting in work
+// expert w0 (first unit ubeg0, first sorted position pos0), of n_work.
+struct CtaRange {
+  int u_begin, u_end, w0, ubeg0, pos0, n_work;
+};
+
+// Ints of shared-memory scratch smem_plan needs (it lives in the stage ring,
+// before the first copy is issued).
+__host__ __device__ constexpr int smem_plan_scratch_ints(int S, int E, int T) {
+  return S + E * ((T + 31) / 32) + 2 * E + 3 * (E + 2) + 32 * 5;
+}
+
+// floor(n / d) for 0 <= n < 2^22 and d >= 1, given inv = 1.0f / d: (n + 1/2)
+// / d lies at least 1/(2d) from an integer, and the two float roundings move
+// it by less than (n / d) 2^-23 < 1/(2d).
+__device__ __forceinline__ int div_small(int n, float inv) {
+  return (int)(((float)n + 0.5f) * inv);
+}
+
+// The most experts one thread of a plan-building CTA owns (E <= 1024 over the
+// 160 threads of the expert kernels).
+constexpr int kPlanRun = 8;
+
+// The plan of one expert stage, built in shared memory by all threads of the
+// CTA from the routing ids (decode sizes: T <= 128, E <= 1024): the align
+// step's counting sort by expert in arrival order, the work list (touched
+// experts in ascending id, then the shared expert) and this CTA's unit range
+// -- the split the workspace plan gives: CTA c starts where the running
+// estimated cost reaches c / grid of the stage's total.  Every CTA derives the
+// same plan from the same ids.
+// A token's k experts are distinct, so a slot's rank within its expert (its
+// arrival order) is the number of earlier TOKENS that chose the expert: each
+// expert keeps a bitmask over the tokens, set with one shared-memory atomicOr
+// per slot, and a rank is the popcount of the bits below the token.  Each
+// thread owns a run of at most kPlanRun experts; one block scan gives the
+// work indices, first units, costs and positions.  The steps are
+// latency-bound, so the code keeps the dependent chain short: counts cached
+// in registers, float-reciprocal divisions, four barriers.
+// Persistent results: wex, wnt ([n_work]) and sorted ([T*k]: each expert's
+// slots at its running position, no padding).  With sp.sorted_ids, the CTA
+// also writes its slice of the aligned layout (moe_align_block_size) to the
+// workspace: the experts [blockIdx.x * E / grid, (blockIdx.x + 1) * E / grid).
+__device__ CtaRange smem_plan(const SmemPlanArgs sp, int T, int k, bool shared_expert,
+                              int tiles_r, int tiles_s, int xt, int16_t* wex, int16_t* wnt,
+                              int32_t* sorted, int* scratch, int* status) {
+  __shared__ CtaRange s_range;
+  const int tid = threadIdx.x, nthr = blockDim.x;
+  const int S = T * k, E = sp.E, B = sp.B, W = (T + 31) >> 5;
+  const int base = sp.base, base_s = sp.base_s;
+  int32_t* const abi_sorted = sp.sorted_ids;
+  const float inv_k = 1.0f / (float)k, inv_xt = 1.0f / (float)xt, inv_b = 1.0f / (float)B;
+  // This CTA's slice of the aligned layout (E * grid < 2^31).
+  const int eb = (int)(blockIdx.x * (unsigned)E / gridDim.x);
+  const int ee = (int)((blockIdx.x + 1) * (unsigned)E / gridDim.x);
+  int* s_ids = scratch;                                     // [S]
+  uint32_t* mask = reinterpret_cast<uint32_t*>(s_ids + S);  // [E][W] tokens of each expert
+  int* p0e = reinterpret_cast<int*>(mask + E * W);          // [E] first sorted position
+  int* poe = p0e + E;                                       // [E] padded offset
+  int* u0 = poe + E;                                        // [E + 2] first unit of a work expert
+  int* c0 = u0 + E + 2;                                     // [E + 2] cost before a work expert
+  int* p0 = c0 + E + 2;                                     // [E + 2] its first sorted position
+  int* scan = p0 + E + 2;                                   // [32 * 5]
+  for (int s = tid; s < S; s += nthr) {
+    int e = __ldcg(sp.ids + s);
+    if (e < 0 || e >= E) {
+      record_status(status, kStatusDeviceCheck);
+      e = -1;
+    }
+    s_ids[s] = e;
+  }
+  for (int i = tid; i < E * W; i += nthr) mask[i] = 0u;
+  __syncthreads();
+  for (int s = tid; s < S; s += nthr) {
+    const int e = s_ids[s];
+    const int t = div_small(s, inv_k);
+    if (e >= 0) atomicOr(&mask[e * W + (t >> 5)], 1u << (t & 31));
+  }
+  __syncthreads();
+  // Thread-owned experts [e0, e0 + n): counts, then per expert padded rows,
+  // touched, units, cost, tokens.
+  const int run = (E + nthr - 1) / nthr;
+  const int e0 = min(E, tid * run), n = min(E, e0 + run) - e0;
+  int cnt[kPlanRun];
+  int loc[5] = {0, 0, 0, 0, 0};
+#pragma unroll
+  for (int i = 0; i < kPlanRun; ++i) {
+    int c = 0;
+    if (i < n)
+      for (int w = 0; w < W; ++w) c += __popc(mask[(e0 + i) * W + w]);
+    cnt[i] = c;
+    const int g = div_small(c + xt - 1, inv_xt);
+    loc[0] += div_small(c + B - 1, inv_b) * B;
+    loc[1] += c > 0 ? 1 : 0;
+    loc[2] += tiles_r * g;
+    loc[3] += tiles_r * (g * base + c);
+    loc[4] += c;
+  }
+  int ex[5], tot[5];
+  block_scan<5>(loc, ex, tot, scan);
+#pragma unroll
+  for (int i = 0; i < kPlanRun; ++i) {
+    const int c = cnt[i], e = e0 + i;
+    const int g = div_small(c + xt - 1, inv_xt);
+    const int P = div_small(c + B - 1, inv_b) * B;
+    if (c > 0) {
+      const int idx = ex[1];
+      wex[idx] = (int16_t)e;
+      wnt[idx] = (int16_t)c;
+      u0[idx] = ex[2];
+      c0[idx] = ex[3];
+      p0[idx] = ex[4];
+      p0e[e] = ex[4];
+      poe[e] = ex[0];
+      if (abi_sorted != nullptr && e >= eb && e < ee) {
+        for (int r = c; r < P; ++r) abi_sorted[ex[0] + r] = S;  // padding
+        for (int b = 0; b < P; b += B) sp.block_ids[div_small(ex[0] + b, inv_b)] = e;
+      }
+    }
+    if (abi_sorted != nullptr && i < n && e >= eb && e < ee) sp.expert_offsets[e] = ex[0];
+    ex[0] += P;
+    ex[1] += c > 0 ? 1 : 0;
+    ex[2] += tiles_r * g;
+    ex[3] += tiles_r * (g * base + c);
+    ex[4] += c;
+  }
+  int n_work = tot[1], units = tot[2], cost = tot[3];
+  if (shared_expert) {
+    const int sg = div_small(T + xt - 1, inv_xt);
+    if (tid == 0) {
+      wex[n_work] = -1;
+      wnt[n_work] = (int16_t)T;
+      u0[n_work] = units;
+      c0[n_work] = cost;
+      p0[n_work] = 0;
+    }
+    n_work += 1;
+    units += tiles_s * sg;
+    cost += tiles_s * (sg * base_s + T);
+  }
+  if (abi_sorted != nullptr && blockIdx.x == 0 && tid == 0) {
+    sp.expert_offsets[E] = tot[0];
+    *sp.num_post_pad = tot[0];
+  }
+  __syncthreads();
+  // Each slot at its expert's running position (arrival order: the earlier
+  // tokens of the expert come first); this CTA's slice of the aligned layout.
+  for (int s = tid; s < S; s += nthr) {
+    const int e = s_ids[s];
+    if (e < 0) continue;
+    const int t = div_small(s, inv_k);
+    const uint32_t* m = mask + e * W;
+    int r = __popc(m[t >> 5] & ((1u << (t & 31)) - 1u));
+    for (int w = 0; w < (t >> 5); ++w) r += __popc(m[w]);
+    sorted[p0e[e] + r] = s;
+    if (abi_sorted != nullptr && e >= eb && e < ee) abi_sorted[poe[e] + r] = s;
+  }
+  // This CTA's range: the start of CTA c and of CTA c + 1.
+  if (tid < 2) {
+    const int c = blockIdx.x + tid;
+    int u = 0, w = 0;
+    if (c >= (int)gridDim.x) {
+      u = units;
+    } else if (c > 0) {
+      const int target = min(cost, (int)((float)c * ((float)cost / (float)gridDim.x)));
+      int lo = 0, hi = n_work - 1;
+      while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (c0[mid] <= target) lo = mid; else hi = mid - 1;
+      }
+      w = lo;
+      const bool sh = shared_expert && lo == n_work - 1;
+      u = unit_at_cost(target, c0[lo], u0[lo], sh ? tiles_s : tiles_r, wnt[lo], xt,
+                       sh ? base_s : base);
+    }
+    if (tid == 0) {
+      s_range.u_begin = u;
+      s_range.w0 = w;
+      s_range.ubeg0 = u0[w];
+      s_range.pos0 = p0[w];
+      s_range.n_work = n_work;
+    } else {
+      s_range.u_end = u;
+    }
+  }
+  __syncthreads();
+  return s_range;
+}
 
 // ------------------------------------------------------------------ smem loads
 __device__ __forceinline__ uint4 lds128(uint32_t addr) {
@@ -394,12 +619,24 @@ __device__ __forceinline__ void prefetch_slice_l2(const uint8_t* p, size_t bytes
     bulk_prefetch_l2(p + b, (uint32_t)min((size_t)65536, b1 - b));
 }
 
+// Shared-memory layout of both expert kernels: barriers (kBarBytes), then
+// (shared-memory plan only) the persistent plan -- wex int16 [E + 1], wnt
+// int16 [E + 1], sorted int32 [T*k] -- then, at stage_off, the stage ring, whose
+// start also holds smem_plan's scratch until the first copy is issued.
+__device__ __forceinline__ void plan_arrays(uint8_t* smem, int E, int16_t*& wex, int16_t*& wnt,
+                                            int32_t*& sorted) {
+  const int wb = (int)round_up(2 * (E + 1), 16);
+  wex = reinterpret_cast<int16_t*>(smem + kBarBytes);
+  wnt = reinterpret_cast<int16_t*>(smem + kBarBytes + wb);
+  sorted = reinterpret_cast<int32_t*>(smem + kBarBytes + 2 * wb);
+}
+
 template <int kFmt>
 __global__ void __launch_bounds__(kThreads, kCtasPerSm) gate_up_kernel(const GuArgs a) {
   extern __shared__ __align__(128) uint8_t smem[];
   uint64_t* full = reinterpret_cast<uint64_t*>(smem);
   uint64_t* empty = full + kMaxStages;
-  uint8_t* stages = smem + kBarBytes;
+  uint8_t* stages = smem + a.stage_off;
   const uint32_t stages_sa = smem_u32(stages);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int NS = a.n_stages;
@@ -428,21 +665,40 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) gate_up_kernel(const GuA
   const int stall_us = a.status ? __ldcg(a.status + kStallWord) : 0;
   const uint64_t wait_ns = stall_us > 0 ? (uint64_t)stall_us * 1000u : kWaitLimitNs;
 
-  const Plan plan = *a.plan;
   const int d = a.d;
   const int xt = a.xt;
   // Routed row bytes (codes only, for int4) and int4 scale bytes per row.
   const int rowb = kFmt ? d / 2 : d * 2;
   const int srowb = kFmt ? d / 16 : 0;
-  const int u_begin = a.cta[blockIdx.x];
-  const int u_end = a.cta[blockIdx.x + 1];
-  UnitCursor<false> cur;
-  cur.work = a.work;
-  cur.n_work = plan.n_work;
+  UnitCursor cur;
   cur.tiles_r = (int)ceil_div(a.I, a.rg);
   cur.tiles_s = a.Is > 0 ? (int)ceil_div(a.Is, a.rgs) : 1;
   cur.xt = xt;
-  if (u_begin < u_end) cur.load(a.cta[gridDim.x + 1 + blockIdx.x]);
+  cur.down = false;
+  CtaRange rg;
+  const int32_t* sorted;  // sorted position -> slot (shared or global memory)
+  if (a.sp.ids != nullptr) {
+    int16_t *wex, *wnt;
+    int32_t* ss;
+    plan_arrays(smem, a.sp.E, wex, wnt, ss);
+    cur.work = nullptr;
+    cur.wex = wex;
+    cur.wnt = wnt;
+    rg = smem_plan(a.sp, a.T, a.k, a.Is > 0, cur.tiles_r, cur.tiles_s, xt, wex, wnt, ss,
+                   reinterpret_cast<int*>(stages), a.status);
+    sorted = ss;
+  } else {
+    cur.work = a.work;
+    rg.n_work = a.plan->n_work;
+    rg.u_begin = a.cta[blockIdx.x];
+    rg.u_end = a.cta[blockIdx.x + 1];
+    rg.w0 = a.cta[gridDim.x + 1 + blockIdx.x];
+    rg.ubeg0 = rg.pos0 = 0;
+    sorted = a.sorted_ids;
+  }
+  cur.n_work = rg.n_work;
+  const int u_begin = rg.u_begin, u_end = rg.u_end;
+  if (u_begin < u_end) cur.start(rg.w0, rg.ubeg0, rg.pos0);
 
   if (warp == kConsumerWarps) {
     // ------------------------------------------------------------ producer
@@ -455,16 +711,15 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) gate_up_kernel(const GuA
     for (int u = u_begin; u < u_end; ++u, ++j) {
       const int s = j % NS, use = j / NS;
       cur.seek(u);
-      const WorkExpert& we = cur.we;
       const int local = u - cur.ubeg;
       const int grp = local / cur.tiles, tile = local - grp * cur.tiles;
-      const bool shared = we.expert < 0;
+      const bool shared = cur.expert < 0;
       const int RG = shared ? a.rgs : a.rg;
       const int Iw = shared ? a.Is : a.I;
       const int r0 = tile * RG;
       const int nr = min(RG, Iw - r0);
       const int g0 = grp * xt;
-      const int nt = min(xt, we.n_tok - g0);
+      const int nt = min(xt, cur.n_tok - g0);
       if (use > 0 && !mbar_wait(&empty[s], (uint32_t)((use - 1) & 1), a.status)) {
         ok = false;
         break;
@@ -475,13 +730,13 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) gate_up_kernel(const GuA
       const uint32_t bytes = 2u * nr * (rb + sb) + (uint32_t)nt * d * 2;
       if (lane == 0) mbar_arrive_expect_tx(&full[s], bytes);
       __syncwarp();
-      const uint8_t* wbase = shared ? a.sgu : a.gu + (size_t)we.expert * 2 * a.I * rb;
+      const uint8_t* wbase = shared ? a.sgu : a.gu + (size_t)cur.expert * 2 * a.I * rb;
       if (lane == 0) bulk_g2s(st, wbase + (size_t)r0 * rb, nr * rb, &full[s], pol_w);
       if (lane == 1)
         bulk_g2s(st + RG * rb, wbase + (size_t)(Iw + r0) * rb, nr * rb, &full[s], pol_w);
       if (kFmt && !shared) {
         const uint8_t* sbase =
-            reinterpret_cast<const uint8_t*>(a.gu_scales) + (size_t)we.expert * 2 * a.I * sb;
+            reinterpret_cast<const uint8_t*>(a.gu_scales) + (size_t)cur.expert * 2 * a.I * sb;
         if (lane == 2)
           bulk_g2s(st + 2 * RG * rb, sbase + (size_t)r0 * sb, nr * sb, &full[s], pol_w);
         if (lane == 3)
@@ -497,7 +752,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) gate_up_kernel(const GuA
         if (lane >= 4 && lane < 4 + nt) {
           tok = g0 + lane - 4;
           if (!shared) {
-            const int slot = a.sorted_ids[we.pos + g0 + lane - 4];
+            const int slot = sorted[cur.pos + g0 + lane - 4];
             tok = slot / a.k;
             if (slot < 0 || tok >= a.T) {
               record_status(a.status, kStatusDeviceCheck);
@@ -519,16 +774,15 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) gate_up_kernel(const GuA
   for (int u = u_begin; u < u_end; ++u, ++j) {
     const int s = j % NS, use = j / NS;
     cur.seek(u);
-    const WorkExpert& we = cur.we;
     const int local = u - cur.ubeg;
     const int grp = local / cur.tiles, tile = local - grp * cur.tiles;
-    const bool shared = we.expert < 0;
+    const bool shared = cur.expert < 0;
     const int RG = shared ? a.rgs : a.rg;
     const int Iw = shared ? a.Is : a.I;
     const int r0 = tile * RG;
     const int nr = min(RG, Iw - r0);
     const int g0 = grp * xt;
-    const int nt = min(xt, we.n_tok - g0);
+    const int nt = min(xt, cur.n_tok - g0);
     const int rb = shared ? d * 2 : rowb;
     const int sb = shared ? 0 : srowb;
     // Warp -> (pair p, token subset tsub of nsub): tokens m = tsub + q * nsub.
@@ -542,7 +796,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) gate_up_kernel(const GuA
     const uint32_t xs = (uint32_t)(nsub * d * 2);
     const uint32_t xa = st + 2 * RG * (rb + sb) + tsub * d * 2;
     float* hout = shared ? a.hs + (size_t)(g0 + tsub) * a.Is + r0 + p
-                         : a.h + (size_t)(we.pos + g0 + tsub) * a.I + r0 + p;
+                         : a.h + (size_t)(cur.pos + g0 + tsub) * a.I + r0 + p;
     const size_t hstride = (size_t)nsub * (shared ? a.Is : a.I);
     const bool int4 = kFmt && !shared;
 #define MOE_GU_CASE(N)                                                   \
@@ -577,7 +831,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) down_kernel(const DnArgs
   extern __shared__ __align__(128) uint8_t smem[];
   uint64_t* full = reinterpret_cast<uint64_t*>(smem);
   uint64_t* empty = full + kMaxStages;
-  uint8_t* stages = smem + kBarBytes;
+  uint8_t* stages = smem + a.stage_off;
   const uint32_t stages_sa = smem_u32(stages);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int NS = a.n_stages;
@@ -590,27 +844,48 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) down_kernel(const DnArgs
     fence_barrier_init();
   }
   __syncthreads();
-  // Consumers need the predecessor's h; the producer first streams the weight
-  // rows of its first units, which do not depend on it.  The plan it reads was
-  // written by the align step, which completed before the gate_up stage began.
+
+  // The plan does not depend on the gate_up stage: its ids (or the workspace
+  // plan) were written by the routing kernels, which completed before the
+  // gate_up stage began.  So it is built (or read) before the dependency wait,
+  // and the producer then streams the weight rows of its first units, which do
+  // not depend on gate_up either; the consumers wait for h.
+  const int xt = a.xt;
+  const int rowb = kFmt ? a.I / 2 : a.I * 2;
+  const int srowb = kFmt ? a.I / 16 : 0;
+  UnitCursor cur;
+  cur.tiles_r = (int)ceil_div(a.d, a.rd);
+  cur.tiles_s = a.Is > 0 ? (int)ceil_div(a.d, a.rds) : 1;
+  cur.xt = xt;
+  cur.down = true;
+  CtaRange rg;
+  const int32_t* sorted;  // sorted position -> slot (shared or global memory)
+  if (a.sp.ids != nullptr) {
+    int16_t *wex, *wnt;
+    int32_t* ss;
+    plan_arrays(smem, a.sp.E, wex, wnt, ss);
+    cur.work = nullptr;
+    cur.wex = wex;
+    cur.wnt = wnt;
+    rg = smem_plan(a.sp, a.T, a.k, a.Is > 0, cur.tiles_r, cur.tiles_s, xt, wex, wnt, ss,
+                   reinterpret_cast<int*>(stages), a.status);
+    sorted = ss;
+  } else {
+    cur.work = a.work;
+    rg.n_work = a.plan->n_work;
+    rg.u_begin = a.cta[blockIdx.x];
+    rg.u_end = a.cta[blockIdx.x + 1];
+    rg.w0 = a.cta[gridDim.x + 1 + blockIdx.x];
+    rg.ubeg0 = rg.pos0 = 0;
+    sorted = a.sorted_ids;
+  }
+  cur.n_work = rg.n_work;
+  const int u_begin = rg.u_begin, u_end = rg.u_end;
+  if (u_begin < u_end) cur.start(rg.w0, rg.ubeg0, rg.pos0);
   if (warp != kConsumerWarps) {
     pdl_wait();
     pdl_trigger();
   }
-
-  const Plan plan = *a.plan;
-  const int xt = a.xt;
-  const int rowb = kFmt ? a.I / 2 : a.I * 2;
-  const int srowb = kFmt ? a.I / 16 : 0;
-  const int u_begin = a.cta[blockIdx.x];
-  const int u_end = a.cta[blockIdx.x + 1];
-  UnitCursor<true> cur;
-  cur.work = a.work;
-  cur.n_work = plan.n_work;
-  cur.tiles_r = (int)ceil_div(a.d, a.rd);
-  cur.tiles_s = a.Is > 0 ? (int)ceil_div(a.d, a.rds) : 1;
-  cur.xt = xt;
-  if (u_begin < u_end) cur.load(a.cta[gridDim.x + 1 + blockIdx.x]);
 
   if (warp == kConsumerWarps) {
     const uint64_t pol_w = policy_evict_first();
@@ -623,22 +898,21 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) down_kernel(const DnArgs
       if (pass == 1) {
         pdl_wait();
         pdl_trigger();
-        if (u_begin < u_end) cur.load(a.cta[gridDim.x + 1 + blockIdx.x]);
+        if (u_begin < u_end) cur.start(rg.w0, rg.ubeg0, rg.pos0);
       }
       j = 0;
       for (int u = u_begin; u < (pass == 0 ? u_begin + n_pre : u_end); ++u, ++j) {
         const int s = j % NS, use = j / NS;
         cur.seek(u);
-        const WorkExpert& we = cur.we;
         const int local = u - cur.ubeg;
         const int grp = local / cur.tiles, tile = local - grp * cur.tiles;
-        const bool shared = we.expert < 0;
+        const bool shared = cur.expert < 0;
         const int RD = shared ? a.rds : a.rd;
         const int Iw = shared ? a.Is : a.I;
         const int r0 = tile * RD;
         const int nr = min(RD, a.d - r0);
         const int g0 = grp * xt;
-        const int nt = min(xt, we.n_tok - g0);
+        const int nt = min(xt, cur.n_tok - g0);
         const bool pre = j < n_pre;  // weights already issued in pass 0
         if (pass == 1 && !pre && use > 0 &&
             !mbar_wait(&empty[s], (uint32_t)((use - 1) & 1), a.status)) {
@@ -653,17 +927,17 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) down_kernel(const DnArgs
           if (lane == 0) mbar_arrive_expect_tx(&full[s], bytes);
           __syncwarp();
           if (lane == 0) {
-            const uint8_t* wb = shared ? a.sdn : a.dn + (size_t)we.expert * a.d * rb;
+            const uint8_t* wb = shared ? a.sdn : a.dn + (size_t)cur.expert * a.d * rb;
             bulk_g2s(st, wb + (size_t)r0 * rb, nr * rb, &full[s], pol_w);
           }
           if (kFmt && !shared && lane == 1) {
             const uint8_t* sbase =
-                reinterpret_cast<const uint8_t*>(a.dn_scales) + (size_t)we.expert * a.d * sb;
+                reinterpret_cast<const uint8_t*>(a.dn_scales) + (size_t)cur.expert * a.d * sb;
             bulk_g2s(st + RD * rb, sbase + (size_t)r0 * sb, nr * sb, &full[s], pol_w);
           }
         }
         if (pass == 1 && lane == 2) {
-          const float* hsrc = shared ? a.hs + (size_t)g0 * Iw : a.h + (size_t)(we.pos + g0) * Iw;
+          const float* hsrc = shared ? a.hs + (size_t)g0 * Iw : a.h + (size_t)(cur.pos + g0) * Iw;
           bulk_g2s(st + RD * (rb + sb), hsrc, nt * Iw * 4, &full[s], pol_h);
         }
       }
@@ -678,20 +952,19 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) down_kernel(const DnArgs
   for (int u = u_begin; u < u_end; ++u, ++j) {
     const int s = j % NS, use = j / NS;
     cur.seek(u);
-    const WorkExpert& we = cur.we;
     const int local = u - cur.ubeg;
     const int grp = local / cur.tiles, tile = local - grp * cur.tiles;
-    const bool shared = we.expert < 0;
+    const bool shared = cur.expert < 0;
     const int RD = shared ? a.rds : a.rd;
     const int Iw = shared ? a.Is : a.I;
     const int r0 = tile * RD;
     const int nr = min(RD, a.d - r0);
     const int g0 = grp * xt;
-    const int nt = min(xt, we.n_tok - g0);
+    const int nt = min(xt, cur.n_tok - g0);
     if (cur.i != slot_i || grp != slot_g) {
       slot_i = cur.i;
       slot_g = grp;
-      slot_of_lane = (!shared && sl < nt) ? a.sorted_ids[we.pos + g0 + sl] : 0;
+      slot_of_lane = (!shared && sl < nt) ? sorted[cur.pos + g0 + sl] : 0;
     }
     const int rb = shared ? Iw * 2 : rowb;
     const int sb = shared ? 0 : srowb;
@@ -753,7 +1026,16 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) down_kernel(const DnArgs
 
 }  // namespace
 
-GemvShape gate_up_shape(int fmt, int d, int I, int Is, int smem_budget) {
+int smem_plan_bytes(int E, int S) {
+  return (int)round_up(2 * round_up(2 * (E + 1), 16) + round_up(4 * (int64_t)S, 16), 128);
+}
+
+bool smem_plan_fits(const GemvShape& g, int E, int T, int k) {
+  return g.n_stages >= 2 && (int64_t)smem_plan_scratch_ints(T * k, E, T) * 4 <=
+                                (int64_t)g.n_stages * g.stage_bytes;
+}
+
+GemvShape gate_up_shape(int fmt, int d, int I, int Is, int smem_budget, int reserve) {
   (void)I;
   GemvShape g;
   const int rowr = fmt ? d / 2 + d / 16 : d * 2;
@@ -768,12 +1050,13 @@ GemvShape gate_up_shape(int fmt, int d, int I, int Is, int smem_budget) {
   int w = 2 * g.rg * rowr;
   if (Is > 0 && 2 * g.rg_shared * rows > w) w = 2 * g.rg_shared * rows;
   g.stage_bytes = (int)round_up(w + g.xt * d * 2, 128);
-  g.n_stages = (smem_budget - kBarBytes) / g.stage_bytes;
+  g.stage_off = kBarBytes + reserve;
+  g.n_stages = (smem_budget - g.stage_off) / g.stage_bytes;
   if (g.n_stages > kMaxStages) g.n_stages = kMaxStages;
   return g;
 }
 
-GemvShape down_shape(int fmt, int d, int I, int Is, int smem_budget) {
+GemvShape down_shape(int fmt, int d, int I, int Is, int smem_budget, int reserve) {
   (void)d;
   GemvShape g;
   const int rowr = fmt ? I / 2 + I / 16 : I * 2;
@@ -789,16 +1072,19 @@ GemvShape down_shape(int fmt, int d, int I, int Is, int smem_budget) {
   int w = g.rg * rowr + g.xt * I * 4;
   if (Is > 0 && g.rg_shared * rows + g.xt * Is * 4 > w) w = g.rg_shared * rows + g.xt * Is * 4;
   g.stage_bytes = (int)round_up(w, 128);
-  g.n_stages = (smem_budget - kBarBytes) / g.stage_bytes;
+  g.stage_off = kBarBytes + reserve;
+  g.n_stages = (smem_budget - g.stage_off) / g.stage_bytes;
   if (g.n_stages > kMaxStages) g.n_stages = kMaxStages;
   return g;
 }
 
 cudaError_t launch_gate_up(const LaunchCfg& c, const ExpertArgs& e, const GemvShape& g,
                            const uint16_t* x, const int32_t* sorted_ids, const Plan* plan,
-                           const WorkExpert* work, const int32_t* cta, float* h, float* hs,
-                           int* status, int grid) {
+                           const WorkExpert* work, const int32_t* cta, const SmemPlanArgs& sp,
+                           float* h, float* hs, int* status, int grid) {
   GuArgs a;
+  a.sp = sp;
+  a.stage_off = g.stage_off;
   a.cta = cta;
   a.gu = static_cast<const uint8_t*>(e.gate_up);
   a.gu_scales = e.gate_up_scales;
@@ -821,7 +1107,7 @@ cudaError_t launch_gate_up(const LaunchCfg& c, const ExpertArgs& e, const GemvSh
   a.xt = g.xt;
   a.stage_bytes = g.stage_bytes;
   a.n_stages = g.n_stages;
-  const int smem = kBarBytes + g.stage_bytes * g.n_stages;
+  const int smem = g.stage_off + g.stage_bytes * g.n_stages;
   const void* fn = e.fmt ? (const void*)gate_up_kernel<1> : (const void*)gate_up_kernel<0>;
   cudaError_t err = ensure_smem(fn, smem);
   if (err != cudaSuccess) return err;
@@ -831,9 +1117,11 @@ cudaError_t launch_gate_up(const LaunchCfg& c, const ExpertArgs& e, const GemvSh
 
 cudaError_t launch_down(const LaunchCfg& c, const ExpertArgs& e, const GemvShape& g,
                         const int32_t* sorted_ids, const Plan* plan, const WorkExpert* work,
-                        const int32_t* cta, const float* h, const float* hs, float* y,
-                        float* ys, int* status, int grid) {
+                        const int32_t* cta, const SmemPlanArgs& sp, const float* h,
+                        const float* hs, float* y, float* ys, int* status, int grid) {
   DnArgs a;
+  a.sp = sp;
+  a.stage_off = g.stage_off;
   a.cta = cta;
   a.dn = static_cast<const uint8_t*>(e.down);
   a.dn_scales = e.down_scales;
@@ -856,7 +1144,7 @@ cudaError_t launch_down(const LaunchCfg& c, const ExpertArgs& e, const GemvShape
   a.xt = g.xt;
   a.stage_bytes = g.stage_bytes;
   a.n_stages = g.n_stages;
-  const int smem = kBarBytes + g.stage_bytes * g.n_stages;
+  const int smem = g.stage_off + g.stage_bytes * g.n_stages;
   const void* fn = e.fmt ? (const void*)down_kernel<1> : (const void*)down_kernel<0>;
   cudaError_t err = ensure_smem(fn, smem);
   if (err != cudaSuccess) return err;

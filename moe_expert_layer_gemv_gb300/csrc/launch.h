@@ -80,13 +80,15 @@ cudaError_t launch_router_logits(const LaunchCfg& c, const uint16_t* x, const ui
 // Whether launch_route_fused handles these dims.
 bool fused_route_supported(int T, int E, int k);
 
-// Router + top-k + align + plan in one launch (decode sizes).
+// Router + top-k in one launch (decode sizes); with `align`, also the align
+// and the workspace plan of the expert stages (by the last token tile).
 cudaError_t launch_route_fused(const LaunchCfg& c, const uint16_t* x, const uint16_t* wr,
                                const uint16_t* w_sg, float* logits, float* sg, int T, int d,
                                int E, int k, int renormalize, int32_t* ids, float* w,
-                               int32_t* ids_copy, float* w_copy, int B, int32_t* sorted_ids,
-                               int32_t* block_ids, int32_t* num_post_pad, int32_t* expert_offsets,
-                               const PlanParams& pp, int* status, int* counters, int sms);
+                               int32_t* ids_copy, float* w_copy, bool align, int B,
+                               int32_t* sorted_ids, int32_t* block_ids, int32_t* num_post_pad,
+                               int32_t* expert_offsets, const PlanParams& pp, int* status,
+                               int* counters, int sms);
 
 // Per token: softmax over E, top-k (ties -> lower id), (re)normalised weights.
 // With w_sg and sg also sg[t] = x[t] . w_sg (fp32, one warp per token).
@@ -118,7 +120,27 @@ struct GemvShape {
   int xt;        // tokens per unit
   int stage_bytes;
   int n_stages;
+  int stage_off; // shared-memory offset of the stage ring
 };
+
+// Source of a stage's plan.  ids == nullptr: the plan the align step wrote to
+// the workspace (Plan, WorkExpert list, per-CTA unit ranges).  Otherwise
+// (decode sizes) every CTA builds the plan in its own shared memory from the
+// routing ids; the down stage also writes the aligned layout to the workspace.
+struct SmemPlanArgs {
+  const int32_t* ids;         // [T*k] routing ids, or nullptr
+  int E, B;                   // experts, align block size
+  int base, base_s;           // unit cost bases of this stage: routed, shared expert
+  int32_t* sorted_ids;        // align outputs to write (down stage), or nullptr
+  int32_t* block_ids;
+  int32_t* num_post_pad;
+  int32_t* expert_offsets;
+};
+
+// Persistent shared memory of the shared-memory plan (E experts, S = T*k
+// slots), and whether its scratch fits a stage ring of shape g.
+int smem_plan_bytes(int E, int S);
+bool smem_plan_fits(const GemvShape& g, int E, int T, int k);
 
 struct ExpertArgs {
   int fmt;                  // 0 bf16, 1 int4 (routed experts)
@@ -133,13 +155,13 @@ struct ExpertArgs {
 
 cudaError_t launch_gate_up(const LaunchCfg& c, const ExpertArgs& a, const GemvShape& g,
                            const uint16_t* x, const int32_t* sorted_ids, const Plan* plan,
-                           const WorkExpert* work, const int32_t* cta, float* h, float* hs,
-                           int* status, int grid);
+                           const WorkExpert* work, const int32_t* cta, const SmemPlanArgs& sp,
+                           float* h, float* hs, int* status, int grid);
 
 cudaError_t launch_down(const LaunchCfg& c, const ExpertArgs& a, const GemvShape& g,
                         const int32_t* sorted_ids, const Plan* plan, const WorkExpert* work,
-                        const int32_t* cta, const float* h, const float* hs, float* y,
-                        float* ys, int* status, int grid);
+                        const int32_t* cta, const SmemPlanArgs& sp, const float* h,
+                        const float* hs, float* y, float* ys, int* status, int grid);
 
 // out[t] = sum_j w[t][j] y[t*k+j] + sigmoid(sg[t]) ys[t]   (bf16, RNE); sg[t] =
 // x[t] . w_sg, read from `sg` when given, else computed here.
@@ -163,8 +185,9 @@ cudaError_t launch_tc_router(const LaunchCfg& c, const uint16_t* x, const uint16
 int tc_tiles_per_mblock_gu(int I);
 int tc_tiles_per_mblock_dn(int d);
 
-// Host-side tile/stage choices for the two GEMV stages.
-GemvShape gate_up_shape(int fmt, int d, int I, int Is, int smem_budget);
-GemvShape down_shape(int fmt, int d, int I, int Is, int smem_budget);
+// Host-side tile/stage choices for the two GEMV stages; `reserve` bytes of
+// shared memory before the ring hold the shared-memory plan (0: none).
+GemvShape gate_up_shape(int fmt, int d, int I, int Is, int smem_budget, int reserve);
+GemvShape down_shape(int fmt, int d, int I, int Is, int smem_budget, int reserve);
 
 }  // namespace moe

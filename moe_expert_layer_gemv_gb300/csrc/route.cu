@@ -12,9 +12,11 @@
 //
 // At decode sizes the whole routing step is one launch (route_kernel): router
 // CTAs write logits; the last CTA of each token tile to finish (an integer
-// arrival counter) selects that tile's top-k; the last tile to finish runs the
-// align and builds the work plan ("veloGB10", Kernel work: the expert routing
-// folded into its neighbours).
+// arrival counter) selects that tile's top-k.  The align and the work plan are
+// then built by the expert stages themselves, in every CTA's shared memory
+// from the routing ids (expert_gemv.cu), or -- when their shared memory cannot
+// hold that plan -- by the last token tile of this kernel ("veloGB10", Kernel
+// work: the expert routing folded into its neighbours).
 #include <math.h>
 
 #include "launch.h"
@@ -317,45 +319,6 @@ __global__ void __launch_bounds__(256)
   }
 }
 
-// ------------------------------------------------------------------ block scan
-// Exclusive scan of V ints per thread over the CTA (blockDim a multiple of 32,
-// <= 1024).  scratch: >= 32 * V ints.  Every thread gets the totals.
-template <int V>
-__device__ void block_scan(const int (&v)[V], int (&ex)[V], int (&tot)[V], int* scratch) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
-  int inc[V];
-#pragma unroll
-  for (int i = 0; i < V; ++i) {
-    inc[i] = v[i];
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const int n = __shfl_up_sync(0xffffffffu, inc[i], o);
-      if (lane >= o) inc[i] += n;
-    }
-    if (lane == 31) scratch[i * 32 + warp] = inc[i];
-  }
-  __syncthreads();
-  if (warp == 0) {
-#pragma unroll
-    for (int i = 0; i < V; ++i) {
-      int s = lane < nw ? scratch[i * 32 + lane] : 0;
-#pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const int n = __shfl_up_sync(0xffffffffu, s, o);
-        if (lane >= o) s += n;
-      }
-      scratch[i * 32 + lane] = s;
-    }
-  }
-  __syncthreads();
-#pragma unroll
-  for (int i = 0; i < V; ++i) {
-    ex[i] = (warp ? scratch[i * 32 + warp - 1] : 0) + inc[i] - v[i];
-    tot[i] = scratch[i * 32 + nw - 1];
-  }
-  __syncthreads();
-}
-
 // Thread-owned runs of experts: thread i owns [i * run, min(E, (i + 1) * run)).
 __device__ __forceinline__ int expert_run(int E) { return (E + blockDim.x - 1) / blockDim.x; }
 
@@ -364,23 +327,6 @@ __device__ __forceinline__ int expert_run(int E) { return (E + blockDim.x - 1) /
 // `base` for streaming (and, int4, dequantising) the unit's weight rows plus
 // one per token of arithmetic.  The routed experts' base and the shared
 // expert's are separate (PlanParams::base_gu / base_gu_s, base_dn / base_dn_s).
-
-__device__ int unit_at_cost(int target, int c0, int u0, int tiles, int n, int xt, int base) {
-  const int groups = (n + xt - 1) / xt;
-  const int nt_last = n - (groups - 1) * xt;
-  const int per_full = tiles * (base + xt);
-  const int r = target - c0;
-  int g, t;
-  if (groups > 1 && r < (groups - 1) * per_full) {
-    g = r / per_full;
-    t = (r - g * per_full) / (base + xt);
-  } else {
-    g = groups - 1;
-    t = (r - (groups - 1) * per_full) / (base + nt_last);
-    t = min(t, tiles - 1);
-  }
-  return u0 + g * tiles + t;
-}
 
 // CTA c of one stage gets units [cta[c], cta[c+1]) and starts in work expert
 // cta[grid + 1 + c]: its share of the stage's estimated cost starts at
@@ -772,6 +718,7 @@ __global__ void __launch_bounds__(kAlignThreads)
 struct RouteArgs {
   RouterArgs r;
   int k, renormalize, B;
+  int align;             // 1: the last token tile also runs the align and the plan
   int32_t* ids;          // workspace routing [T][k]
   float* w;
   int32_t* ids_copy;     // caller copies (may be null)
@@ -812,7 +759,9 @@ __global__ void __launch_bounds__(kRouterThreads, NV >= 32 ? 1 : 2) route_kernel
   int* sids = dsm + align_smem_ints(a.r.E) - kAlignSmemSlots;
   if ((threadIdx.x >> 5) < kRouterTokens && t < a.r.T)
     topk_token<NV>(a.r.logits, t, a.r.E, a.k, a.renormalize, a.ids, a.w, a.ids_copy, a.w_copy,
-                   gridDim.y == 1 ? sids : nullptr);
+                   gridDim.y == 1 && a.align ? sids : nullptr);
+  // Without the align here, the expert stages plan from the ids themselves.
+  if (!a.align) return;
 
   // Arrival of this tile; the last tile to finish runs the align and the plan
   // (with one token tile, this CTA is already the last).
@@ -880,9 +829,10 @@ cudaError_t launch_router_logits(const LaunchCfg& c, const uint16_t* x, const ui
 cudaError_t launch_route_fused(const LaunchCfg& c, const uint16_t* x, const uint16_t* wr,
                                const uint16_t* w_sg, float* logits, float* sg, int T, int d,
                                int E, int k, int renormalize, int32_t* ids, float* w,
-                               int32_t* ids_copy, float* w_copy, int B, int32_t* sorted_ids,
-                               int32_t* block_ids, int32_t* num_post_pad, int32_t* expert_offsets,
-                               const PlanParams& pp, int* status, int* counters, int sms) {
+                               int32_t* ids_copy, float* w_copy, bool align, int B,
+                               int32_t* sorted_ids, int32_t* block_ids, int32_t* num_post_pad,
+                               int32_t* expert_offsets, const PlanParams& pp, int* status,
+                               int* counters, int sms) {
   if (T == 0) return cudaSuccess;
   RouteArgs a;
   a.r = RouterArgs{x, wr, w_sg, logits, sg, T, d, E, 0};
@@ -891,6 +841,7 @@ cudaError_t launch_route_fused(const LaunchCfg& c, const uint16_t* x, const uint
   a.k = k;
   a.renormalize = renormalize;
   a.B = B;
+  a.align = align ? 1 : 0;
   a.ids = ids;
   a.w = w;
   a.ids_copy = ids_copy;
@@ -899,7 +850,7 @@ cudaError_t launch_route_fused(const LaunchCfg& c, const uint16_t* x, const uint
   a.pp = pp;
   a.status = status;
   a.counters = counters;
-  const size_t smem = route_fused_smem(d, E, a.r.wpe);
+  const size_t smem = align ? route_fused_smem(d, E, a.r.wpe) : router_smem_bytes(d, a.r.wpe);
   const int nv = (E + 31) / 32;
   const void* fn = nv <= 1 ? (const void*)route_kernel<1>
                  : nv <= 2 ? (const void*)route_kernel<2>
