@@ -43,8 +43,8 @@ def parse():
     p.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     p.add_argument("--workload", default="verify_t8")
     p.add_argument("--also", default="tiny,verify_t64,verify_t64_skew,int4_t32,prefill_t4096",
-                   help="further workloads measured in the same run ('' = none); each gets "
-                        "its own entry under 'workloads' in the JSON line")
+                   help="further workloads measured in the same run ('none' = none); each "
+                        "gets its own entry under 'workloads' in the JSON line")
     p.add_argument("--copies", type=int, default=0, help="weight copies to rotate (0 = auto)")
     p.add_argument("--batches", type=int, default=8, help="token batches to rotate")
     p.add_argument("--cpu-seconds", type=float, default=10.0)
@@ -397,6 +397,56 @@ def measure(shape, args, dev, world, local, inp0, e2e):
     return res
 
 
+def measure_chain(shape, args, dev, inp0, n_layers=16):
+    """A decode step's MoE layers back to back: n_layers calls, each reading
+    the previous call's output, captured once into a CUDA graph (programmatic
+    dependent launch between every pair of kernels, inside and across layers)
+    and replayed; layers alternate between weight copies so that HBM, not L2,
+    serves the weights.  Each layer routes its own input (the previous
+    layer's output), so the bytes are counted from every layer's own routing.
+    Returns (per-layer microseconds: device time, events around the replays;
+    the algorithmic bytes per layer averaged over the chain)."""
+    import torch
+
+    from moe_expert_layer_gemv_gb300 import inputs as I
+    from moe_expert_layer_gemv_gb300.layer import MoeLayer
+
+    copies = [MoeLayer(inp0, dev) for _ in range(2)]
+    acts = [torch.empty((shape.T, shape.d), dtype=torch.bfloat16, device=dev)
+            for _ in range(n_layers + 1)]
+    ids = [torch.empty((shape.T, shape.k), dtype=torch.int32, device=dev)
+           for _ in range(n_layers)]
+    xs = [I.make_x(shape, seed=300 + b).to(dev) for b in range(4)]
+
+    def chain():
+        for i in range(n_layers):
+            copies[i % 2].forward(acts[i], acts[i + 1], topk_ids=ids[i])
+
+    acts[0].copy_(xs[0])
+    chain()
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        chain()
+    for i in range(max(3, args.warmup)):
+        acts[0].copy_(xs[i % 4])
+        g.replay()
+    torch.cuda.synchronize()
+    reps = max(5, args.steps // 4)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for i in range(reps):
+        acts[0].copy_(xs[i % 4])
+        g.replay()
+    e1.record()
+    torch.cuda.synchronize()
+    us = e0.elapsed_time(e1) * 1e3 / (reps * n_layers)
+    layer_bytes = algorithmic(shape, [t.cpu().numpy() for t in ids])["layer_bytes"]
+    del g, copies, acts, xs, ids
+    torch.cuda.empty_cache()
+    return us, layer_bytes
+
+
 def roofline_of(shape, m, peaks, peak_kind):
     """Dominant kernel (the gate_up stage) against its roofline, and the layer
     figures, from one measure() result."""
@@ -476,6 +526,7 @@ def main():
                                        f"{el1:.1f} s"}
 
     m = measure(shape, args, dev, world, local, inp0, e2e=True)
+    chain = measure_chain(shape, args, dev, inp0) if shape.T <= 128 else None
     del inp0
     ms, ms_e2e = ranks_max([m["ms"], m["ms_e2e"]], dev)
     peaks, peak_kind = measured_peaks()
@@ -484,7 +535,19 @@ def main():
 
     # The other workloads: same protocol (regions A and B), each its own entry.
     others = {}
-    for name in [w for w in args.also.split(",") if w and w != shape.name]:
+    if chain is not None:
+        chain_us, chain_bytes = chain
+        chain_us = ranks_max([chain_us], dev)[0]
+        others[f"{shape.name}_chain16_graph"] = {
+            "config": {**config_of(shape, world, m), "layers": 16,
+                       "note": "16 chained layer calls (each reads the previous output), one "
+                               "CUDA graph, two weight copies alternating; bytes from every "
+                               "layer's own routing of its input"},
+            "value": job_tokens_per_s(shape.T, world, chain_us * 1e-3), "unit": UNIT,
+            "layer_us": chain_us, "layer_bytes": chain_bytes,
+            "layer_hbm_gbs": chain_bytes / (chain_us * 1e-6) / 1e9,
+            "layer_roofline_frac": chain_bytes / (chain_us * 1e-6) / 1e9 / peaks["hbm_gbs"]}
+    for name in [w for w in args.also.split(",") if w not in ("", "none", shape.name)]:
         sh = I.shape(name)
         mo = measure(sh, args, dev, world, local, I.make_inputs(sh, seed=0), e2e=False)
         mo["ms"] = ranks_max([mo["ms"]], dev)[0]

@@ -370,6 +370,83 @@ __device__ __forceinline__ uint32_t word(const uint4& v, int k) {
 // Two bf16 (element 2j low, 2j + 1 high) as an fp32 pair.
 __device__ __forceinline__ uint64_t bf16x2_f2(uint32_t w) { return f2(w << 16, w & 0xffff0000u); }
 
+// ------------------------------------------------------------------ int4 on the tensor pipe
+// Shared-memory pitches of an int4 gate_up stage and of the token rows of an
+// int4 layer: 16 bytes beyond the row shift consecutive rows by four banks, so
+// that the eight rows one load instruction reads fall on distinct banks.
+__host__ __device__ constexpr int i4_code_pitch(int d) { return d / 2 + 16; }
+__host__ __device__ constexpr int i4_scale_pitch(int d) { return d / 16 + 16; }
+__host__ __device__ constexpr int x_pitch(int fmt, int d) { return fmt ? 2 * d + 16 : 2 * d; }
+// Bytes of the cross-warp partial sums of the int4 gate_up consumers: two
+// buffers x three warps x 32 lanes x 4 floats.
+constexpr int kI4RedBytes = 2 * 3 * 32 * 16;
+
+// Four exact bf16 pairs from one word of eight int4 codes (element j in nibble
+// j, stored as code + 8): pair i = (code i, code i + 4), low half first.  The
+// two nibbles land in the mantissa of 128.0 (bf16 0x4300, mantissa step 1) by
+// one shift and one and-or; one packed fma then takes 136 = 128 + 8 off both
+// halves, exactly.
+__device__ __forceinline__ void dequant_pairs(uint32_t v, uint32_t (&q)[4]) {
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const uint32_t biased = ((v >> (4 * i)) & 0x000F000Fu) | 0x43004300u;
+    asm("fma.rn.bf16x2 %0, %1, %2, %3;"
+        : "=r"(q[i])
+        : "r"(biased), "r"(0x3F803F80u), "r"(0xC308C308u));  // x * 1 - 136
+  }
+}
+
+// D = A B + C on the tensor pipe: 16x16 bf16 A (row-major fragment), 16x8 bf16
+// B (column fragment), fp32 accumulators.
+__device__ __forceinline__ void mma_16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
+                                          uint32_t a3, uint32_t b0, uint32_t b1,
+                                          const float (&c)[4]) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, "
+      "{%8, %9}, {%10, %11, %12, %13};"
+      : "=f"(d[0]), "=f"(d[1]), "=f"(d[2]), "=f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1), "f"(c[0]), "f"(c[1]), "f"(c[2]),
+        "f"(c[3]));
+}
+
+// One consumer warp's share of an int4 gate_up unit (8 gate rows + the 8 up
+// rows of the same intermediate columns, up to 8 tokens) on the tensor pipe:
+// the groups [gb, ge) of 32 codes along d.  The unit is one 16x8 product per
+// 16 codes: A = gate rows on tile rows 0..7, up rows on 8..15; B = the tokens'
+// activations; lane (g, t) = (lane / 4, lane % 4) holds, in acc, gate and up
+// row g for tokens 2t and 2t + 1 -- both halves of a SwiGLU.
+// Within a group of 32, thread t takes its code word t (codes 8t .. 8t + 7) and
+// the tile's k positions map onto them as (8t, 8t + 4), (8t + 1, 8t + 5) for the
+// first product and (8t + 2, 8t + 6), (8t + 3, 8t + 7) for the second; the
+// activations are permuted to match.  Each group's two products start from
+// zero and are scaled by the rows' bf16 scales into the fp32 accumulators: the
+// same regrouping (sum of code x activation, then x scale) as the scalar path.
+__device__ __forceinline__ void gu_int4_mma(uint32_t cg, uint32_t cu, uint32_t sgp, uint32_t sup,
+                                            uint32_t xr, bool has_x, int gb, int ge,
+                                            float (&acc)[4]) {
+  const float zero[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll 2
+  for (int gi = gb; gi < ge; ++gi) {
+    uint32_t vg, vu;
+    asm volatile("ld.shared.u32 %0, [%1];" : "=r"(vg) : "r"(cg + 16u * gi));
+    asm volatile("ld.shared.u32 %0, [%1];" : "=r"(vu) : "r"(cu + 16u * gi));
+    const float fg = lds_bf16(sgp + 2u * gi), fu = lds_bf16(sup + 2u * gi);
+    const uint4 xv = has_x ? lds128(xr + 64u * gi) : make_uint4(0u, 0u, 0u, 0u);
+    uint32_t qg[4], qu[4];
+    dequant_pairs(vg, qg);
+    dequant_pairs(vu, qu);
+    const uint32_t b10 = __byte_perm(xv.x, xv.z, 0x5410), b11 = __byte_perm(xv.x, xv.z, 0x7632);
+    const uint32_t b20 = __byte_perm(xv.y, xv.w, 0x5410), b21 = __byte_perm(xv.y, xv.w, 0x7632);
+    float p[4];
+    mma_16816(p, qg[0], qu[0], qg[1], qu[1], b10, b11, zero);
+    mma_16816(p, qg[2], qu[2], qg[3], qu[3], b20, b21, p);
+    acc[0] = fmaf(p[0], fg, acc[0]);
+    acc[1] = fmaf(p[1], fg, acc[1]);
+    acc[2] = fmaf(p[2], fu, acc[2]);
+    acc[3] = fmaf(p[3], fu, acc[3]);
+  }
+}
+
 // ------------------------------------------------------------------ gate_up math
 // One warp: gate row at wg, up row at wu (shared addresses), NT token rows at
 // xa + q * xs.  bf16 weights; 16-byte chunks strided over the lanes.  Returns
@@ -414,64 +491,13 @@ __device__ __forceinline__ void gu_rows_bf16(uint32_t wg, uint32_t wu, uint32_t 
   }
 }
 
-// int4 weights: 32 codes (16 bytes) form one scale group, with bf16 scales at
-// sg / su.  Lane l takes the 8-code words w = l, l + 32, ... of the rows, so
-// the lanes' x chunks and code words are consecutive in shared memory (no bank
-// conflicts).  Each word's codes are dequantised once and used for every token;
-// per token its 8 products go into an (even, odd) pair, and scale x pair sum
-// into the total.
+// One consumer warp's share of a bf16 gate_up unit: NT tokens; lane q writes
+// token q's h value at hout + q * hstride.
 template <int NT>
-__device__ __forceinline__ void gu_rows_int4(uint32_t wg, uint32_t wu, uint32_t sg, uint32_t su,
-                                             uint32_t xa, uint32_t xs, int nwords, int lane,
-                                             float* g, float* u) {
-  float ga[NT], ua[NT];
-#pragma unroll
-  for (int q = 0; q < NT; ++q) ga[q] = ua[q] = 0.f;
-#pragma unroll 2
-  for (int w = lane; w < nwords; w += 32) {
-    uint32_t cg, cu;
-    asm volatile("ld.shared.u32 %0, [%1];" : "=r"(cg) : "r"(wg + 4u * w));
-    asm volatile("ld.shared.u32 %0, [%1];" : "=r"(cu) : "r"(wu + 4u * w));
-    const float fg = lds_bf16(sg + 2u * (w >> 2)), fu = lds_bf16(su + 2u * (w >> 2));
-    uint64_t qg[4], qu[4];
-    dequant8(cg, qg);
-    dequant8(cu, qu);
-#pragma unroll
-    for (int q = 0; q < NT; ++q) {
-      const uint4 xv = lds128(xa + q * xs + 16u * w);
-      uint64_t pg = 0ull, pu = 0ull;
-      const uint64_t x0 = bf16x2_f2(xv.x), x1 = bf16x2_f2(xv.y);
-      const uint64_t x2 = bf16x2_f2(xv.z), x3 = bf16x2_f2(xv.w);
-      pg = ffma2(qg[0], x0, pg);
-      pu = ffma2(qu[0], x0, pu);
-      pg = ffma2(qg[1], x1, pg);
-      pu = ffma2(qu[1], x1, pu);
-      pg = ffma2(qg[2], x2, pg);
-      pu = ffma2(qu[2], x2, pu);
-      pg = ffma2(qg[3], x3, pg);
-      pu = ffma2(qu[3], x3, pu);
-      ga[q] = fmaf(fg, f2sum(pg), ga[q]);
-      ua[q] = fmaf(fu, f2sum(pu), ua[q]);
-    }
-  }
-#pragma unroll
-  for (int q = 0; q < NT; ++q) {
-    g[q] = warp_sum(ga[q]);
-    u[q] = warp_sum(ua[q]);
-  }
-}
-
-// One consumer warp's share of a gate_up unit: NT tokens; lane q writes token
-// q's h value at hout + q * hstride.
-template <int NT, bool kInt4>
-__device__ __forceinline__ void gu_warp(uint32_t wg, uint32_t wu, uint32_t sg, uint32_t su,
-                                        uint32_t xa, uint32_t xs, int d, int lane, float* hout,
-                                        size_t hstride) {
+__device__ __forceinline__ void gu_warp(uint32_t wg, uint32_t wu, uint32_t xa, uint32_t xs, int d,
+                                        int lane, float* hout, size_t hstride) {
   float g[NT], u[NT];
-  if (kInt4)
-    gu_rows_int4<NT>(wg, wu, sg, su, xa, xs, d / 8, lane, g, u);
-  else
-    gu_rows_bf16<NT>(wg, wu, xa, xs, d / 8, lane, g, u);
+  gu_rows_bf16<NT>(wg, wu, xa, xs, d / 8, lane, g, u);
   float gv = g[0], uv = u[0];
 #pragma unroll
   for (int q = 1; q < NT; ++q)
@@ -636,6 +662,8 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) gate_up_kernel(const GuA
   extern __shared__ __align__(128) uint8_t smem[];
   uint64_t* full = reinterpret_cast<uint64_t*>(smem);
   uint64_t* empty = full + kMaxStages;
+  uint64_t* red_full = empty + kMaxStages;  // [2] int4 partial-sum hand-off
+  uint64_t* red_empty = red_full + 2;       // [2]
   uint8_t* stages = smem + a.stage_off;
   const uint32_t stages_sa = smem_u32(stages);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -645,6 +673,10 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) gate_up_kernel(const GuA
     for (int s = 0; s < NS; ++s) {
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], kConsumerWarps);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&red_full[b], kConsumerWarps - 1);
+      mbar_init(&red_empty[b], 1);
     }
     fence_barrier_init();
   }
@@ -667,9 +699,11 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) gate_up_kernel(const GuA
 
   const int d = a.d;
   const int xt = a.xt;
-  // Routed row bytes (codes only, for int4) and int4 scale bytes per row.
+  // Routed row bytes (codes only, for int4) and int4 scale bytes per row; the
+  // token rows' pitch in a stage.
   const int rowb = kFmt ? d / 2 : d * 2;
   const int srowb = kFmt ? d / 16 : 0;
+  const int xp = x_pitch(kFmt, d);
   UnitCursor cur;
   cur.tiles_r = (int)ceil_div(a.I, a.rg);
   cur.tiles_s = a.Is > 0 ? (int)ceil_div(a.Is, a.rgs) : 1;
@@ -707,7 +741,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) gate_up_kernel(const GuA
     const uint64_t pol_x = policy_evict_last();
     int j = 0;
     bool ok = true;
-    int tok = 0, tok_i = -1, tok_g = -1;  // lane 4+m: token of member m of the cached group
+    int tok = 0, tok_i = -1, tok_g = -1;  // lane m: token of member m of the cached group
     for (int u = u_begin; u < u_end; ++u, ++j) {
       const int s = j % NS, use = j / NS;
       cur.seek(u);
@@ -731,28 +765,40 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) gate_up_kernel(const GuA
       if (lane == 0) mbar_arrive_expect_tx(&full[s], bytes);
       __syncwarp();
       const uint8_t* wbase = shared ? a.sgu : a.gu + (size_t)cur.expert * 2 * a.I * rb;
-      if (lane == 0) bulk_g2s(st, wbase + (size_t)r0 * rb, nr * rb, &full[s], pol_w);
-      if (lane == 1)
-        bulk_g2s(st + RG * rb, wbase + (size_t)(Iw + r0) * rb, nr * rb, &full[s], pol_w);
+      int xoff;
       if (kFmt && !shared) {
+        // One row per lane (RG == 8): gate codes, up codes, gate scales, up
+        // scales, each row at its padded pitch.
         const uint8_t* sbase =
             reinterpret_cast<const uint8_t*>(a.gu_scales) + (size_t)cur.expert * 2 * a.I * sb;
-        if (lane == 2)
-          bulk_g2s(st + 2 * RG * rb, sbase + (size_t)r0 * sb, nr * sb, &full[s], pol_w);
-        if (lane == 3)
-          bulk_g2s(st + 2 * RG * rb + RG * sb, sbase + (size_t)(Iw + r0) * sb, nr * sb, &full[s],
-                   pol_w);
+        const int cp = i4_code_pitch(d), sp = i4_scale_pitch(d);
+        const int part = lane >> 3, r = lane & 7;
+        const int row = (part & 1 ? Iw : 0) + r0 + r;
+        if (r < nr) {
+          if (part < 2)
+            bulk_g2s(st + (part * RG + r) * cp, wbase + (size_t)row * rb, rb, &full[s], pol_w);
+          else
+            bulk_g2s(st + 2 * RG * cp + ((part - 2) * RG + r) * sp, sbase + (size_t)row * sb, sb,
+                     &full[s], pol_w);
+        }
+        xoff = 2 * RG * (cp + sp);
+      } else {
+        if (lane == 0) bulk_g2s(st, wbase + (size_t)r0 * rb, nr * rb, &full[s], pol_w);
+        if (lane == 1)
+          bulk_g2s(st + RG * rb, wbase + (size_t)(Iw + r0) * rb, nr * rb, &full[s], pol_w);
+        xoff = 2 * RG * rb;
       }
       // Token rows of this group (looked up once per (work expert, group)),
-      // after the weight copies are under way: they come from L2.
+      // after the weight copies are under way: they come from L2.  Lane m
+      // holds member m's token.
       if (cur.i != tok_i || grp != tok_g) {
         tok_i = cur.i;
         tok_g = grp;
         tok = 0;
-        if (lane >= 4 && lane < 4 + nt) {
-          tok = g0 + lane - 4;
+        if (lane < nt) {
+          tok = g0 + lane;
           if (!shared) {
-            const int slot = sorted[cur.pos + g0 + lane - 4];
+            const int slot = sorted[cur.pos + g0 + lane];
             tok = slot / a.k;
             if (slot < 0 || tok >= a.T) {
               record_status(a.status, kStatusDeviceCheck);
@@ -761,9 +807,8 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) gate_up_kernel(const GuA
           }
         }
       }
-      const int xoff = 2 * RG * (rb + sb);
-      if (lane >= 4 && lane < 4 + nt)
-        bulk_g2s(st + xoff + (lane - 4) * d * 2, a.x + (size_t)tok * d, d * 2, &full[s], pol_x);
+      if (lane < nt)
+        bulk_g2s(st + xoff + lane * xp, a.x + (size_t)tok * d, d * 2, &full[s], pol_x);
     }
     if (!ok) drain_stages(full, j, NS, a.status);
     return;
@@ -771,6 +816,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) gate_up_kernel(const GuA
 
   // -------------------------------------------------------------- consumers
   int j = 0;
+  int nred = 0;  // int4 units reduced so far
   for (int u = u_begin; u < u_end; ++u, ++j) {
     const int s = j % NS, use = j / NS;
     cur.seek(u);
@@ -785,26 +831,67 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) gate_up_kernel(const GuA
     const int nt = min(xt, cur.n_tok - g0);
     const int rb = shared ? d * 2 : rowb;
     const int sb = shared ? 0 : srowb;
+    if (!mbar_wait(&full[s], (uint32_t)(use & 1), a.status, wait_ns)) break;
+    const uint32_t st = stages_sa + (uint32_t)(s * a.stage_bytes);
+    if (kFmt && !shared) {
+      // int4 routed unit on the tensor pipe: every consumer warp takes a
+      // quarter of the groups along d; warp 0 adds the other warps' partial
+      // sums and writes h.
+      const int g = lane >> 2, t = lane & 3;
+      const int cp = i4_code_pitch(d), sp = i4_scale_pitch(d);
+      const int ng = d / 32, per = ng / kConsumerWarps;
+      const int rr = min(g, nr - 1);  // rows past the tile's end: computed, not written
+      float acc[4] = {0.f, 0.f, 0.f, 0.f};
+      gu_int4_mma(st + rr * cp + 4 * t, st + (RG + rr) * cp + 4 * t,
+                  st + 2 * RG * cp + rr * sp, st + 2 * RG * cp + (RG + rr) * sp,
+                  st + 2 * RG * (cp + sp) + g * xp + 16 * t, g < nt, warp * per, (warp + 1) * per,
+                  acc);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&empty[s]);
+      // Hand-off of the partial sums through one of two buffers, each with a
+      // full barrier (the other warps wrote) and an empty one (warp 0 read).
+      const int buf = nred & 1;
+      const uint32_t ph = (uint32_t)(nred >> 1) & 1u;
+      ++nred;
+      float4* red = reinterpret_cast<float4*>(stages + (size_t)NS * a.stage_bytes) + buf * 96;
+      if (warp > 0) {
+        if (nred > 2 && !mbar_wait(&red_empty[buf], ph ^ 1u, a.status, wait_ns)) break;
+        red[(warp - 1) * 32 + lane] = make_float4(acc[0], acc[1], acc[2], acc[3]);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&red_full[buf]);
+        continue;
+      }
+      if (!mbar_wait(&red_full[buf], ph, a.status, wait_ns)) break;
+#pragma unroll
+      for (int w = 0; w < kConsumerWarps - 1; ++w) {
+        const float4 o = red[w * 32 + lane];
+        acc[0] += o.x;
+        acc[1] += o.y;
+        acc[2] += o.z;
+        acc[3] += o.w;
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&red_empty[buf]);
+      if (g < nr) {
+        float* hr = a.h + (size_t)(cur.pos + g0) * a.I + r0 + g;
+        if (2 * t < nt) hr[(size_t)(2 * t) * a.I] = silu(acc[0]) * acc[2];
+        if (2 * t + 1 < nt) hr[(size_t)(2 * t + 1) * a.I] = silu(acc[1]) * acc[3];
+      }
+      continue;
+    }
     // Warp -> (pair p, token subset tsub of nsub): tokens m = tsub + q * nsub.
     const int nsub = kConsumerWarps / RG;
     const int p = warp % RG, tsub = warp / RG;
     const int cnt = (p < nr && nt > tsub) ? (nt - tsub + nsub - 1) / nsub : 0;
-    if (!mbar_wait(&full[s], (uint32_t)(use & 1), a.status, wait_ns)) break;
-    const uint32_t st = stages_sa + (uint32_t)(s * a.stage_bytes);
     const uint32_t wg = st + p * rb, wu = st + RG * rb + p * rb;
-    const uint32_t sg = st + 2 * RG * rb + p * sb, su = sg + RG * sb;
-    const uint32_t xs = (uint32_t)(nsub * d * 2);
-    const uint32_t xa = st + 2 * RG * (rb + sb) + tsub * d * 2;
+    const uint32_t xs = (uint32_t)(nsub * xp);
+    const uint32_t xa = st + 2 * RG * rb + tsub * xp;
     float* hout = shared ? a.hs + (size_t)(g0 + tsub) * a.Is + r0 + p
                          : a.h + (size_t)(cur.pos + g0 + tsub) * a.I + r0 + p;
     const size_t hstride = (size_t)nsub * (shared ? a.Is : a.I);
-    const bool int4 = kFmt && !shared;
-#define MOE_GU_CASE(N)                                                   \
-  case N:                                                                \
-    if (int4)                                                            \
-      gu_warp<N, true>(wg, wu, sg, su, xa, xs, d, lane, hout, hstride);  \
-    else                                                                 \
-      gu_warp<N, false>(wg, wu, sg, su, xa, xs, d, lane, hout, hstride); \
+#define MOE_GU_CASE(N)                                  \
+  case N:                                               \
+    gu_warp<N>(wg, wu, xa, xs, d, lane, hout, hstride); \
     break;
     switch (cnt) {
       MOE_GU_CASE(1)
@@ -1038,6 +1125,24 @@ bool smem_plan_fits(const GemvShape& g, int E, int T, int k) {
 GemvShape gate_up_shape(int fmt, int d, int I, int Is, int smem_budget, int reserve) {
   (void)I;
   GemvShape g;
+  if (fmt) {
+    // int4 routed units: 8 gate + 8 up rows (one tensor-pipe tile, one row
+    // per producer lane) at padded pitches; shared-expert (bf16) units of up
+    // to four row pairs within 16 KB; the cross-warp partial sums after the
+    // ring.
+    g.rg = 8;
+    g.rg_shared = kConsumerWarps;
+    while (g.rg_shared > 1 && 2 * g.rg_shared * d * 2 > 16 * 1024) g.rg_shared /= 2;
+    g.xt = 16 * 1024 / (d * 2);
+    g.xt = g.xt < 1 ? 1 : (g.xt > kMaxXT ? kMaxXT : g.xt);
+    int w = 2 * g.rg * (i4_code_pitch(d) + i4_scale_pitch(d));
+    if (Is > 0 && 2 * g.rg_shared * d * 2 > w) w = 2 * g.rg_shared * d * 2;
+    g.stage_bytes = (int)round_up(w + g.xt * x_pitch(1, d), 128);
+    g.stage_off = kBarBytes + reserve;
+    g.n_stages = (smem_budget - g.stage_off - kI4RedBytes) / g.stage_bytes;
+    if (g.n_stages > kMaxStages) g.n_stages = kMaxStages;
+    return g;
+  }
   const int rowr = fmt ? d / 2 + d / 16 : d * 2;
   const int rows = d * 2;
   const int target = 32 * 1024;  // weight bytes per stage
@@ -1107,7 +1212,7 @@ cudaError_t launch_gate_up(const LaunchCfg& c, const ExpertArgs& e, const GemvSh
   a.xt = g.xt;
   a.stage_bytes = g.stage_bytes;
   a.n_stages = g.n_stages;
-  const int smem = g.stage_off + g.stage_bytes * g.n_stages;
+  const int smem = g.stage_off + g.stage_bytes * g.n_stages + (e.fmt ? kI4RedBytes : 0);
   const void* fn = e.fmt ? (const void*)gate_up_kernel<1> : (const void*)gate_up_kernel<0>;
   cudaError_t err = ensure_smem(fn, smem);
   if (err != cudaSuccess) return err;

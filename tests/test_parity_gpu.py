@@ -396,3 +396,50 @@ def test_bounded_wait_times_out_and_the_workspace_recovers():
     torch.cuda.synchronize()
     assert layer.device_status() == abi.MOE_OK
     assert torch.equal(again, ref)
+
+
+# ----------------------------------------------------------------------------- layer chains
+# A decode step runs the MoE layer of every transformer block in turn; the
+# pages' engines capture that step into CUDA graphs ("Qwen3.6-35B-A3B on NVIDIA
+# GB10", CUDA graphs; "Qwen3.8 Flash-Next - GB10 UltraFast", How it works:
+# piecewise graphs).  Here several layers, each reading the previous layer's
+# output, run back to back on one stream -- every launch with programmatic
+# dependent launch, so a layer's routing starts while the previous layer's
+# combine finishes -- once eagerly and once as one captured graph.
+
+
+@pytest.mark.parametrize("T", [1, 8])
+def test_multi_layer_chain_in_a_cuda_graph(T):
+    s = I.shape("verify_t8", T=T, d=512, E=32, k=4, I=128, Is=64)
+    n_layers = 4
+    layers = [MoeLayer(I.make_inputs(s, 20 + i), "cuda") for i in range(n_layers)]
+    acts = [torch.empty((T, s.d), dtype=torch.bfloat16, device="cuda") for _ in range(n_layers + 1)]
+
+    def chain():
+        for i, L in enumerate(layers):
+            L.forward(acts[i], acts[i + 1])
+
+    acts[0].copy_(I.make_x(s, 5).cuda())
+    chain()  # eager; also sets the kernels' one-time attributes before the capture
+    torch.cuda.synchronize()
+    eager = [a.clone() for a in acts]
+    # each layer against the oracle fed that layer's actual (bf16) input
+    for i in range(n_layers):
+        inp = dict(I.make_inputs(s, 20 + i), x=eager[i].cpu())
+        ids = layers[i].layout()["topk_ids"]
+        ov = oracle.layer(*oracle_args(inp), ids_override=ids)
+        compare_out(bf16_to_f64(eager[i + 1]), ov["out"], f"chain T={T} layer {i}")
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        chain()
+    for seed in (6, 7):
+        acts[0].copy_(I.make_x(s, seed).cuda())
+        g.replay()
+        torch.cuda.synchronize()
+        replayed = [a.clone() for a in acts]
+        chain()
+        torch.cuda.synchronize()
+        for a, b in zip(replayed[1:], acts[1:]):
+            assert torch.equal(a, b)
+    for L in layers:
+        assert L.device_status() == abi.MOE_OK
