@@ -263,6 +263,7 @@ ExpertArgs expert_args(const moe_dims_t& dm, const moe_expert_weights_t* ex,
   a.k = dm.top_k;
   a.I = dm.I;
   a.Is = sh ? dm.I_shared : 0;
+  a.h_rows = (int)((int64_t)dm.T * dm.top_k + (int64_t)dm.E * (dm.block_size - 1));
   return a;
 }
 

@@ -23,6 +23,10 @@
 // int4 weights are dequantised in registers: (nibble - 8) accumulated against
 // the activations per group of 32, times the group's bf16 scale (W4A16 routed
 // experts: "Qwen3.8 Flash-Next - GB10 UltraFast", How it works).
+#include <cuda_bf16.h>
+
+#include <cstring>
+
 #include "launch.h"
 
 namespace moe {
@@ -45,16 +49,18 @@ struct GuArgs {
   const Plan* plan;
   const WorkExpert* work;
   const int32_t* cta;         // CTA unit ranges and first work experts (see PlanParams)
-  float* h;                   // [sorted positions][I]
+  float* h;                   // [sorted positions][I]; int4 layers: two bf16 planes
   float* hs;                  // [T][Is]
   int* status;
   int T, d, I, Is, k;
   int rg, rgs, xt, stage_bytes, n_stages;
   int stage_off;              // shared-memory offset of the stage ring
+  int h_rows;                 // rows of each bf16 plane of h (int4 layers)
   SmemPlanArgs sp;
 };
 
 struct DnArgs {
+  CUtensorMap tm_codes;       // int4: codes as [E*d][I/2] bytes, box {128, 64}, 128-byte swizzle
   const uint8_t* dn;          // routed down: bf16 [E][d][I] or codes [E][d][I/2]
   const uint16_t* dn_scales;  // int4 scales [E][d][I/32]
   const uint8_t* sdn;         // shared down bf16 [d][Is]
@@ -70,6 +76,7 @@ struct DnArgs {
   int T, d, I, Is, k;
   int rd, rds, xt, stage_bytes, n_stages;
   int stage_off;
+  int h_rows;
   SmemPlanArgs sp;
 };
 
@@ -313,6 +320,17 @@ __device__ CtaRange smem_plan(const SmemPlanArgs sp, int T, int k, bool shared_e
   return s_range;
 }
 
+// Tiled 2D tensor copy of the box at (x, y) into shared memory, completion as
+// transaction bytes on `bar`.
+__device__ __forceinline__ void tma_box_2d(uint32_t dst, const CUtensorMap* map, int x, int y,
+                                           uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_u32(bar))
+      : "memory");
+}
+
 // ------------------------------------------------------------------ smem loads
 __device__ __forceinline__ uint4 lds128(uint32_t addr) {
   uint4 v;
@@ -347,24 +365,6 @@ __device__ __forceinline__ uint64_t ffma2(uint64_t a, uint64_t b, uint64_t c) {
 }
 __device__ __forceinline__ float f2sum(uint64_t v) {
   return __uint_as_float((uint32_t)v) + __uint_as_float((uint32_t)(v >> 32));
-}
-
-// The 8 codes of word v as exact float pairs (code - 8): element 2j is the low
-// nibble of byte j, 2j + 1 its high nibble; each is placed under the exponent
-// of 2^23 by one byte permute, then 2^23 + 8 comes off both halves at once.
-__device__ __forceinline__ void dequant8(uint32_t v, uint64_t (&q)[4]) {
-  const uint32_t lo = v & 0x0F0F0F0Fu, hi = (v >> 4) & 0x0F0F0F0Fu;
-  const uint32_t mag = 0x4B000000u;          // 2^23
-  const uint64_t off = f2(0x4B000008u, 0x4B000008u);  // 2^23 + 8 in both halves
-#pragma unroll
-  for (int j = 0; j < 4; ++j) {
-    const uint64_t e = f2(__byte_perm(lo, mag, 0x7540 + j), __byte_perm(hi, mag, 0x7540 + j));
-    asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(q[j]) : "l"(e), "l"(off));
-  }
-}
-
-__device__ __forceinline__ uint32_t word(const uint4& v, int k) {
-  return k == 0 ? v.x : (k == 1 ? v.y : (k == 2 ? v.z : v.w));
 }
 
 // Two bf16 (element 2j low, 2j + 1 high) as an fp32 pair.
@@ -447,6 +447,63 @@ __device__ __forceinline__ void gu_int4_mma(uint32_t cg, uint32_t cu, uint32_t s
   }
 }
 
+// int4 down stage: the unit's 64 code rows of W_down arrive as I / 256 tensor
+// boxes of 64 rows x 128 bytes with the 128-byte swizzle (16-byte chunk c of
+// row r stored at chunk c ^ (r % 8): the eight rows one load reads fall on
+// distinct banks), then the rows' scales densely, then the tokens' h rows.
+constexpr int kI4DnRows = 64;
+constexpr int kI4DnBox = kI4DnRows * 128;  // bytes of one code box
+__host__ __device__ constexpr int i4d_codes_bytes(int I) { return (I / 256) * kI4DnBox; }
+__host__ __device__ constexpr int i4d_h_pitch(int I) { return 2 * I + 16; }
+
+// Shared address of code word t of group gi of row r in a swizzled box set.
+__device__ __forceinline__ uint32_t i4d_code_addr(uint32_t codes, int r, int gi, int t) {
+  return codes + (uint32_t)((gi >> 3) * kI4DnBox + r * 128 + (((gi & 7) ^ (r & 7)) << 4) + 4 * t);
+}
+
+// One consumer warp's m16 tile of an int4 down unit: rows ra and rb (the
+// tile's rows g and g + 8 of lane (g, t)), all I / 32 groups, up to 8 tokens.
+// In an int4 layer h travels as two bf16 planes, hi = bf16(h) and lo = bf16(h
+// - hi), and each group takes one product on each (the pair carries h to about
+// 2^-17): the k positions map onto the codes as in gu_int4_mma.  acc: rows
+// ra, rb x tokens 2t, 2t + 1.
+__device__ __forceinline__ void dn_int4_mma(uint32_t codes, int ra, int rb, int t, uint32_t sa,
+                                            uint32_t sb, uint32_t hh, uint32_t hl, bool has_h,
+                                            int ng, float (&acc)[4]) {
+  const float zero[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll 2
+  for (int gi = 0; gi < ng; ++gi) {
+    uint32_t va, vb;
+    asm volatile("ld.shared.u32 %0, [%1];" : "=r"(va) : "r"(i4d_code_addr(codes, ra, gi, t)));
+    asm volatile("ld.shared.u32 %0, [%1];" : "=r"(vb) : "r"(i4d_code_addr(codes, rb, gi, t)));
+    const float fa = lds_bf16(sa + 2u * gi), fb = lds_bf16(sb + 2u * gi);
+    const uint4 H = has_h ? lds128(hh + 64u * gi) : make_uint4(0u, 0u, 0u, 0u);
+    const uint4 L = has_h ? lds128(hl + 64u * gi) : make_uint4(0u, 0u, 0u, 0u);
+    uint32_t qa[4], qb[4];
+    dequant_pairs(va, qa);
+    dequant_pairs(vb, qb);
+    float p[4];
+    mma_16816(p, qa[0], qb[0], qa[1], qb[1], __byte_perm(H.x, H.z, 0x5410),
+              __byte_perm(H.x, H.z, 0x7632), zero);
+    mma_16816(p, qa[2], qb[2], qa[3], qb[3], __byte_perm(H.y, H.w, 0x5410),
+              __byte_perm(H.y, H.w, 0x7632), p);
+    mma_16816(p, qa[0], qb[0], qa[1], qb[1], __byte_perm(L.x, L.z, 0x5410),
+              __byte_perm(L.x, L.z, 0x7632), p);
+    mma_16816(p, qa[2], qb[2], qa[3], qb[3], __byte_perm(L.y, L.w, 0x5410),
+              __byte_perm(L.y, L.w, 0x7632), p);
+    acc[0] = fmaf(p[0], fa, acc[0]);
+    acc[1] = fmaf(p[1], fa, acc[1]);
+    acc[2] = fmaf(p[2], fb, acc[2]);
+    acc[3] = fmaf(p[3], fb, acc[3]);
+  }
+}
+
+// bf16 of v, round to nearest even, as raw bits.
+__device__ __forceinline__ uint16_t bf16_bits(float v) {
+  const __nv_bfloat16 b = __float2bfloat16_rn(v);
+  return *reinterpret_cast<const uint16_t*>(&b);
+}
+
 // ------------------------------------------------------------------ gate_up math
 // One warp: gate row at wg, up row at wu (shared addresses), NT token rows at
 // xa + q * xs.  bf16 weights; 16-byte chunks strided over the lanes.  Returns
@@ -509,105 +566,55 @@ __device__ __forceinline__ void gu_warp(uint32_t wg, uint32_t wu, uint32_t xa, u
 }
 
 // ------------------------------------------------------------------ down math
-// Two weight rows (wa, wb) per 8-lane group, so every h chunk loaded from
+// Two bf16 weight rows (wa, wb) per 8-lane group, so every h chunk loaded from
 // shared memory serves both.  NT tokens' h rows (fp32) at ha + q * hsb.  On
 // return, lane sl of the group holds token sl's outputs for both rows.
-template <int NT, bool kInt4>
-__device__ __forceinline__ void dn_rows2(uint32_t wa, uint32_t wb, uint32_t sa, uint32_t sbb,
-                                         uint32_t ha, uint32_t hsb, int Iw, int sl, float& oa,
-                                         float& ob) {
+template <int NT>
+__device__ __forceinline__ void dn_rows2(uint32_t wa, uint32_t wb, uint32_t ha, uint32_t hsb,
+                                         int Iw, int sl, float& oa, float& ob) {
   float a0[NT], a1[NT], b0[NT], b1[NT];
+  // (even, odd) pairs with packed fmas: the sums of a0/a1 and b0/b1 in order.
+  uint64_t pa[NT], pb[NT];
 #pragma unroll
-  for (int q = 0; q < NT; ++q) a0[q] = a1[q] = b0[q] = b1[q] = 0.f;
-  if (!kInt4) {
-    // (even, odd) pairs with packed fmas: the sums of a0/a1 and b0/b1 in order.
-    uint64_t pa[NT], pb[NT];
-#pragma unroll
-    for (int q = 0; q < NT; ++q) pa[q] = pb[q] = 0ull;
+  for (int q = 0; q < NT; ++q) pa[q] = pb[q] = 0ull;
 #pragma unroll 2
-    for (int c = sl; c < Iw / 8; c += 8) {
-      const uint32_t off = (uint32_t)c * 16u;
-      const uint4 va = lds128(wa + off), vb = lds128(wb + off);
-      const uint64_t wa0 = bf16x2_f2(va.x), wa1 = bf16x2_f2(va.y), wa2 = bf16x2_f2(va.z),
-                     wa3 = bf16x2_f2(va.w);
-      const uint64_t wb0 = bf16x2_f2(vb.x), wb1 = bf16x2_f2(vb.y), wb2 = bf16x2_f2(vb.z),
-                     wb3 = bf16x2_f2(vb.w);
-#pragma unroll
-      for (int q = 0; q < NT; ++q) {
-        // Lanes sl >= 4 load the chunk's upper 16 bytes first (the lanes' h
-        // chunks are 32 bytes apart: this puts one load's lanes on distinct
-        // banks); the products are taken in the same order either way.
-        const uint32_t hb = ha + q * hsb + 2u * off;
-        const bool up = (sl >> 2) & 1;
-        const float4 first = lds128f(hb + (up ? 16u : 0u));
-        const float4 second = lds128f(hb + (up ? 0u : 16u));
-        const float4 hp = up ? second : first, hq = up ? first : second;
-        const uint64_t h0 = f2(__float_as_uint(hp.x), __float_as_uint(hp.y));
-        const uint64_t h1 = f2(__float_as_uint(hp.z), __float_as_uint(hp.w));
-        const uint64_t h2 = f2(__float_as_uint(hq.x), __float_as_uint(hq.y));
-        const uint64_t h3 = f2(__float_as_uint(hq.z), __float_as_uint(hq.w));
-        pa[q] = ffma2(wa0, h0, pa[q]);
-        pb[q] = ffma2(wb0, h0, pb[q]);
-        pa[q] = ffma2(wa1, h1, pa[q]);
-        pb[q] = ffma2(wb1, h1, pb[q]);
-        pa[q] = ffma2(wa2, h2, pa[q]);
-        pb[q] = ffma2(wb2, h2, pb[q]);
-        pa[q] = ffma2(wa3, h3, pa[q]);
-        pb[q] = ffma2(wb3, h3, pb[q]);
-      }
-    }
+  for (int c = sl; c < Iw / 8; c += 8) {
+    const uint32_t off = (uint32_t)c * 16u;
+    const uint4 va = lds128(wa + off), vb = lds128(wb + off);
+    const uint64_t wa0 = bf16x2_f2(va.x), wa1 = bf16x2_f2(va.y), wa2 = bf16x2_f2(va.z),
+                   wa3 = bf16x2_f2(va.w);
+    const uint64_t wb0 = bf16x2_f2(vb.x), wb1 = bf16x2_f2(vb.y), wb2 = bf16x2_f2(vb.z),
+                   wb3 = bf16x2_f2(vb.w);
 #pragma unroll
     for (int q = 0; q < NT; ++q) {
-      a0[q] = __uint_as_float((uint32_t)pa[q]);
-      a1[q] = __uint_as_float((uint32_t)(pa[q] >> 32));
-      b0[q] = __uint_as_float((uint32_t)pb[q]);
-      b1[q] = __uint_as_float((uint32_t)(pb[q] >> 32));
+      // Lanes sl >= 4 load the chunk's upper 16 bytes first (the lanes' h
+      // chunks are 32 bytes apart: this puts one load's lanes on distinct
+      // banks); the products are taken in the same order either way.
+      const uint32_t hb = ha + q * hsb + 2u * off;
+      const bool up = (sl >> 2) & 1;
+      const float4 first = lds128f(hb + (up ? 16u : 0u));
+      const float4 second = lds128f(hb + (up ? 0u : 16u));
+      const float4 hp = up ? second : first, hq = up ? first : second;
+      const uint64_t h0 = f2(__float_as_uint(hp.x), __float_as_uint(hp.y));
+      const uint64_t h1 = f2(__float_as_uint(hp.z), __float_as_uint(hp.w));
+      const uint64_t h2 = f2(__float_as_uint(hq.x), __float_as_uint(hq.y));
+      const uint64_t h3 = f2(__float_as_uint(hq.z), __float_as_uint(hq.w));
+      pa[q] = ffma2(wa0, h0, pa[q]);
+      pb[q] = ffma2(wb0, h0, pb[q]);
+      pa[q] = ffma2(wa1, h1, pa[q]);
+      pb[q] = ffma2(wb1, h1, pb[q]);
+      pa[q] = ffma2(wa2, h2, pa[q]);
+      pb[q] = ffma2(wb2, h2, pb[q]);
+      pa[q] = ffma2(wa3, h3, pa[q]);
+      pb[q] = ffma2(wb3, h3, pb[q]);
     }
-  } else {
-    // Codes dequantised once per group, h already fp32 pairs in shared memory.
-    // Lane sl's h chunks lie 128 bytes apart from its neighbours': it takes the
-    // group's words in the order (k + sl) mod 4 and, for sl >= 4, the upper 16
-    // bytes of each word first, so one load instruction's lanes hit distinct
-    // banks.
-    for (int c = sl; c < Iw / 32; c += 8) {
-      const uint32_t off = (uint32_t)c * 16u;
-      const uint4 va = lds128(wa + off), vb = lds128(wb + off);
-      const float fa = lds_bf16(sa + 2u * c), fb = lds_bf16(sbb + 2u * c);
-      const bool up = (sl >> 2) & 1;  // upper half first
-      uint64_t pa[NT], pb[NT];
+  }
 #pragma unroll
-      for (int q = 0; q < NT; ++q) pa[q] = pb[q] = 0ull;
-#pragma unroll
-      for (int k0 = 0; k0 < 4; ++k0) {
-        const int k = (k0 + sl) & 3;
-        uint64_t qa[4], qb[4];
-        dequant8(word(va, k), qa);
-        dequant8(word(vb, k), qb);
-        // Pairs in load order: 2, 3 then 0, 1 for the upper-first lanes.
-        const uint64_t qa0 = up ? qa[2] : qa[0], qa1 = up ? qa[3] : qa[1];
-        const uint64_t qa2 = up ? qa[0] : qa[2], qa3 = up ? qa[1] : qa[3];
-        const uint64_t qb0 = up ? qb[2] : qb[0], qb1 = up ? qb[3] : qb[1];
-        const uint64_t qb2 = up ? qb[0] : qb[2], qb3 = up ? qb[1] : qb[3];
-#pragma unroll
-        for (int q = 0; q < NT; ++q) {
-          const uint32_t hr = ha + q * hsb + 8u * off + 32u * (uint32_t)k;
-          const uint4 h0 = lds128(hr + (up ? 16u : 0u)), h1 = lds128(hr + (up ? 0u : 16u));
-          pa[q] = ffma2(qa0, f2(h0.x, h0.y), pa[q]);
-          pb[q] = ffma2(qb0, f2(h0.x, h0.y), pb[q]);
-          pa[q] = ffma2(qa1, f2(h0.z, h0.w), pa[q]);
-          pb[q] = ffma2(qb1, f2(h0.z, h0.w), pb[q]);
-          pa[q] = ffma2(qa2, f2(h1.x, h1.y), pa[q]);
-          pb[q] = ffma2(qb2, f2(h1.x, h1.y), pb[q]);
-          pa[q] = ffma2(qa3, f2(h1.z, h1.w), pa[q]);
-          pb[q] = ffma2(qb3, f2(h1.z, h1.w), pb[q]);
-        }
-      }
-#pragma unroll
-      for (int q = 0; q < NT; ++q) {
-        a0[q] = fmaf(fa, f2sum(pa[q]), a0[q]);
-        b0[q] = fmaf(fb, f2sum(pb[q]), b0[q]);
-      }
-    }
+  for (int q = 0; q < NT; ++q) {
+    a0[q] = __uint_as_float((uint32_t)pa[q]);
+    a1[q] = __uint_as_float((uint32_t)(pa[q] >> 32));
+    b0[q] = __uint_as_float((uint32_t)pb[q]);
+    b1[q] = __uint_as_float((uint32_t)(pb[q] >> 32));
   }
   oa = ob = 0.f;
 #pragma unroll
@@ -873,9 +880,18 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) gate_up_kernel(const GuA
       __syncwarp();
       if (lane == 0) mbar_arrive(&red_empty[buf]);
       if (g < nr) {
-        float* hr = a.h + (size_t)(cur.pos + g0) * a.I + r0 + g;
-        if (2 * t < nt) hr[(size_t)(2 * t) * a.I] = silu(acc[0]) * acc[2];
-        if (2 * t + 1 < nt) hr[(size_t)(2 * t + 1) * a.I] = silu(acc[1]) * acc[3];
+        // h as two bf16 planes: hi = bf16(h), lo = bf16(h - hi).
+        uint16_t* hh = reinterpret_cast<uint16_t*>(a.h) + (size_t)(cur.pos + g0) * a.I + r0 + g;
+        uint16_t* hl = hh + (size_t)a.h_rows * a.I;
+#pragma unroll
+        for (int c = 0; c < 2; ++c) {
+          if (2 * t + c < nt) {
+            const float v = silu(acc[c]) * acc[2 + c];
+            const uint16_t hi = bf16_bits(v);
+            hh[(size_t)(2 * t + c) * a.I] = hi;
+            hl[(size_t)(2 * t + c) * a.I] = bf16_bits(v - __uint_as_float((uint32_t)hi << 16));
+          }
+        }
       }
       continue;
     }
@@ -914,11 +930,15 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) gate_up_kernel(const GuA
 // --------------------------------------------------------------------------- down
 // Consumers: 8 lanes per pair of weight rows, 16 row pairs per pass of the CTA.
 template <int kFmt>
-__global__ void __launch_bounds__(kThreads, kCtasPerSm) down_kernel(const DnArgs a) {
+__global__ void __launch_bounds__(kThreads, kCtasPerSm)
+    down_kernel(const __grid_constant__ DnArgs a) {
   extern __shared__ __align__(128) uint8_t smem[];
   uint64_t* full = reinterpret_cast<uint64_t*>(smem);
   uint64_t* empty = full + kMaxStages;
-  uint8_t* stages = smem + a.stage_off;
+  // int4: the ring starts on a 1024-byte boundary (the swizzled code boxes).
+  const uint32_t ring_pad =
+      kFmt ? ((1024u - ((smem_u32(smem) + (uint32_t)a.stage_off) & 1023u)) & 1023u) : 0u;
+  uint8_t* stages = smem + a.stage_off + ring_pad;
   const uint32_t stages_sa = smem_u32(stages);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int NS = a.n_stages;
@@ -1009,23 +1029,47 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) down_kernel(const DnArgs
         uint8_t* st = stages + (size_t)s * a.stage_bytes;
         const int rb = shared ? Iw * 2 : rowb;
         const int sb = shared ? 0 : srowb;
+        const bool i4 = kFmt && !shared;
         if (pass == 0 || !pre) {
-          const uint32_t bytes = (uint32_t)nr * (rb + sb) + (uint32_t)nt * Iw * 4;
+          // (int4 boxes always move 64 rows: the byte count says so.)
+          const uint32_t bytes = (i4 ? (uint32_t)i4d_codes_bytes(Iw) : (uint32_t)nr * rb) +
+                                 (uint32_t)nr * sb + (uint32_t)nt * Iw * 4;
           if (lane == 0) mbar_arrive_expect_tx(&full[s], bytes);
           __syncwarp();
-          if (lane == 0) {
-            const uint8_t* wb = shared ? a.sdn : a.dn + (size_t)cur.expert * a.d * rb;
-            bulk_g2s(st, wb + (size_t)r0 * rb, nr * rb, &full[s], pol_w);
-          }
-          if (kFmt && !shared && lane == 1) {
-            const uint8_t* sbase =
-                reinterpret_cast<const uint8_t*>(a.dn_scales) + (size_t)cur.expert * a.d * sb;
-            bulk_g2s(st + RD * rb, sbase + (size_t)r0 * sb, nr * sb, &full[s], pol_w);
+          const uint8_t* wb = shared ? a.sdn : a.dn + (size_t)cur.expert * a.d * rb;
+          if (i4) {
+            // The code rows as I / 256 swizzled boxes (64 rows each, whatever
+            // nr), the scales as one block.
+            if (lane < Iw / 256)
+              tma_box_2d(smem_u32(st) + lane * kI4DnBox, &a.tm_codes, lane * 128,
+                         cur.expert * a.d + r0, &full[s]);
+            if (lane == 31) {
+              const uint8_t* sbase =
+                  reinterpret_cast<const uint8_t*>(a.dn_scales) + (size_t)cur.expert * a.d * sb;
+              bulk_g2s(st + i4d_codes_bytes(Iw), sbase + (size_t)r0 * sb, nr * sb, &full[s],
+                       pol_w);
+            }
+          } else {
+            if (lane == 0) bulk_g2s(st, wb + (size_t)r0 * rb, nr * rb, &full[s], pol_w);
           }
         }
-        if (pass == 1 && lane == 2) {
-          const float* hsrc = shared ? a.hs + (size_t)g0 * Iw : a.h + (size_t)(cur.pos + g0) * Iw;
-          bulk_g2s(st + RD * (rb + sb), hsrc, nt * Iw * 4, &full[s], pol_h);
+        if (pass == 1) {
+          if (i4) {
+            // The tokens' h rows, both bf16 planes.
+            const int hp = i4d_h_pitch(Iw);
+            const uint32_t hoff = i4d_codes_bytes(Iw) + RD * sb;
+            const uint16_t* h16 = reinterpret_cast<const uint16_t*>(a.h);
+            if (lane < 2 * nt) {
+              const int m = lane % nt, plane = lane / nt;
+              const uint16_t* src =
+                  h16 + (size_t)plane * a.h_rows * Iw + (size_t)(cur.pos + g0 + m) * Iw;
+              bulk_g2s(st + hoff + (plane * xt + m) * hp, src, Iw * 2, &full[s], pol_h);
+            }
+          } else if (lane == 2) {
+            const float* hsrc =
+                shared ? a.hs + (size_t)g0 * Iw : a.h + (size_t)(cur.pos + g0) * Iw;
+            bulk_g2s(st + RD * (rb + sb), hsrc, nt * Iw * 4, &full[s], pol_h);
+          }
         }
       }
     }
@@ -1057,9 +1101,39 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) down_kernel(const DnArgs
     const int sb = shared ? 0 : srowb;
     if (!mbar_wait(&full[s], (uint32_t)(use & 1), a.status)) break;
     const uint32_t st = stages_sa + (uint32_t)(s * a.stage_bytes);
-    const uint32_t ha = st + RD * (rb + sb);
+    if (kFmt && !shared) {
+      // int4 routed unit on the tensor pipe: warp w takes rows [16 w, 16 w + 16)
+      // of each pass of 16 kConsumerWarps rows.
+      const int g = lane >> 2, t = lane & 3;
+      const int hp = i4d_h_pitch(Iw);
+      const uint32_t sc = st + i4d_codes_bytes(Iw);
+      const uint32_t hoff = sc + RD * sb + g * hp + 16 * t;
+      const int s0 = 2 * t < nt ? sorted[cur.pos + g0 + 2 * t] : 0;
+      const int s1 = 2 * t + 1 < nt ? sorted[cur.pos + g0 + 2 * t + 1] : 0;
+      for (int rb0 = warp * 16; rb0 < nr; rb0 += 16 * kConsumerWarps) {
+        const int ra = min(rb0 + g, nr - 1), rbb = min(rb0 + g + 8, nr - 1);
+        float acc[4] = {0.f, 0.f, 0.f, 0.f};
+        dn_int4_mma(st, ra, rbb, t, sc + ra * sb, sc + rbb * sb, hoff, hoff + xt * hp, g < nt,
+                    Iw / 32, acc);
+#pragma unroll
+        for (int c = 0; c < 2; ++c) {
+          const int slot = c ? s1 : s0;
+          if (2 * t + c >= nt) continue;
+          if (slot < 0 || slot >= a.T * a.k) {
+            record_status(a.status, kStatusDeviceCheck);
+            continue;
+          }
+          float* yr = a.y + (size_t)slot * a.d + r0 + rb0;
+          if (rb0 + g < nr) yr[g] = acc[c];
+          if (rb0 + g + 8 < nr) yr[g + 8] = acc[2 + c];
+        }
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&empty[s]);
+      continue;
+    }
+    const uint32_t ha = st + RD * rb;
     const uint32_t hsb = (uint32_t)Iw * 4u;
-    const bool int4 = kFmt && !shared;
 
     // 8-lane group grp8 (0..15) takes rows grp8 and grp8 + 16 of each 32-row block.
     const int grp8 = warp * 4 + sub;
@@ -1067,14 +1141,10 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) down_kernel(const DnArgs
       const int ra = rb0 + grp8, rbr = rb0 + grp8 + 16;
       const int ca = min(ra, nr - 1), cb = min(rbr, nr - 1);  // clamp: recompute, not written
       const uint32_t wa = st + ca * rb, wb = st + cb * rb;
-      const uint32_t sa = st + RD * rb + ca * sb, sbb = st + RD * rb + cb * sb;
       float oa = 0.f, ob = 0.f;
-#define MOE_DN_CASE(N)                                                 \
-  case N:                                                              \
-    if (int4)                                                          \
-      dn_rows2<N, true>(wa, wb, sa, sbb, ha, hsb, Iw, sl, oa, ob);     \
-    else                                                               \
-      dn_rows2<N, false>(wa, wb, sa, sbb, ha, hsb, Iw, sl, oa, ob);    \
+#define MOE_DN_CASE(N)                                     \
+  case N:                                                  \
+    dn_rows2<N>(wa, wb, ha, hsb, Iw, sl, oa, ob);          \
     break;
       switch (nt) {
         MOE_DN_CASE(1)
@@ -1164,6 +1234,24 @@ GemvShape gate_up_shape(int fmt, int d, int I, int Is, int smem_budget, int rese
 GemvShape down_shape(int fmt, int d, int I, int Is, int smem_budget, int reserve) {
   (void)d;
   GemvShape g;
+  if (fmt) {
+    // int4 routed units: 64 rows (four m16 tiles, one per consumer warp) at
+    // padded pitches and the tokens' h rows as two bf16 planes; shared-expert
+    // (bf16) units of up to 16 rows within 16 KB with fp32 h rows.
+    g.rg = kI4DnRows;
+    g.rg_shared = 16;
+    while (Is > 0 && g.rg_shared > 4 && g.rg_shared * Is * 2 > 16 * 1024) g.rg_shared /= 2;
+    const int imax = Is > I ? Is : I;
+    g.xt = 16 * 1024 / (imax * 4);
+    g.xt = g.xt < 1 ? 1 : (g.xt > kMaxXT ? kMaxXT : g.xt);
+    const int wr = i4d_codes_bytes(I) + g.rg * (I / 16) + 2 * g.xt * i4d_h_pitch(I);
+    const int ws = Is > 0 ? g.rg_shared * Is * 2 + g.xt * Is * 4 : 0;
+    g.stage_bytes = (int)round_up(wr > ws ? wr : ws, 1024);
+    g.stage_off = kBarBytes + reserve;
+    g.n_stages = (smem_budget - g.stage_off - 1024) / g.stage_bytes;
+    if (g.n_stages > kMaxStages) g.n_stages = kMaxStages;
+    return g;
+  }
   const int rowr = fmt ? I / 2 + I / 16 : I * 2;
   const int rows = Is * 2;
   const int target = 32 * 1024;
@@ -1190,6 +1278,7 @@ cudaError_t launch_gate_up(const LaunchCfg& c, const ExpertArgs& e, const GemvSh
   GuArgs a;
   a.sp = sp;
   a.stage_off = g.stage_off;
+  a.h_rows = e.h_rows;
   a.cta = cta;
   a.gu = static_cast<const uint8_t*>(e.gate_up);
   a.gu_scales = e.gate_up_scales;
@@ -1225,8 +1314,14 @@ cudaError_t launch_down(const LaunchCfg& c, const ExpertArgs& e, const GemvShape
                         const int32_t* cta, const SmemPlanArgs& sp, const float* h,
                         const float* hs, float* y, float* ys, int* status, int grid) {
   DnArgs a;
+  memset(&a, 0, sizeof(a));
+  if (e.fmt && !encode_map_2d(&a.tm_codes, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, e.down,
+                              (uint64_t)e.E * e.d, (uint64_t)e.I / 2, 128, kI4DnRows,
+                              CU_TENSOR_MAP_SWIZZLE_128B))
+    return cudaErrorInvalidValue;
   a.sp = sp;
   a.stage_off = g.stage_off;
+  a.h_rows = e.h_rows;
   a.cta = cta;
   a.dn = static_cast<const uint8_t*>(e.down);
   a.dn_scales = e.down_scales;
@@ -1249,7 +1344,7 @@ cudaError_t launch_down(const LaunchCfg& c, const ExpertArgs& e, const GemvShape
   a.xt = g.xt;
   a.stage_bytes = g.stage_bytes;
   a.n_stages = g.n_stages;
-  const int smem = g.stage_off + g.stage_bytes * g.n_stages;
+  const int smem = g.stage_off + g.stage_bytes * g.n_stages + (e.fmt ? 1024 : 0);
   const void* fn = e.fmt ? (const void*)down_kernel<1> : (const void*)down_kernel<0>;
   cudaError_t err = ensure_smem(fn, smem);
   if (err != cudaSuccess) return err;

@@ -577,6 +577,24 @@ bool make_map(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols, ui
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+}  // namespace
+
+bool encode_map_2d(CUtensorMap* m, CUtensorMapDataType type, int elem_bytes, const void* base,
+                   uint64_t rows, uint64_t cols, uint32_t box_cols, uint32_t box_rows,
+                   CUtensorMapSwizzle swizzle) {
+  PFN_cuTensorMapEncodeTiled_v12000 fn = encode_fn();
+  if (fn == nullptr) return false;
+  cuuint64_t dims[2] = {cols, rows};
+  cuuint64_t strides[1] = {cols * (cuuint64_t)elem_bytes};
+  cuuint32_t box[2] = {box_cols, box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  return fn(m, type, 2, const_cast<void*>(base), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+namespace {
+
 constexpr int kTcBNExpert = 256;  // N tile of the expert GEMMs
 constexpr int kTcBNRouter = 64;   // N tile of the router GEMM (E / 64 tiles per M block)
 

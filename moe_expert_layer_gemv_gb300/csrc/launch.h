@@ -3,6 +3,7 @@
 // kernel on `stream` and returns the cudaError_t of the launch.
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -151,6 +152,7 @@ struct ExpertArgs {
   const uint16_t* s_gate_up;  // shared (bf16), may be null
   const uint16_t* s_down;
   int T, d, E, k, I, Is;
+  int h_rows;               // rows of the h buffer (int4 layers: of each of its two bf16 planes)
 };
 
 cudaError_t launch_gate_up(const LaunchCfg& c, const ExpertArgs& a, const GemvShape& g,
@@ -168,6 +170,12 @@ cudaError_t launch_down(const LaunchCfg& c, const ExpertArgs& a, const GemvShape
 cudaError_t launch_combine(const LaunchCfg& c, int T, int d, int k, const float* w,
                            const float* y, const float* ys, const float* sg, const uint16_t* x,
                            const uint16_t* w_sg, uint16_t* out);
+
+// A 2D tensor map over [rows][cols] elements of `elem_bytes` (row-major),
+// box {box_cols, box_rows}, the given swizzle; reads past the end return zeros.
+bool encode_map_2d(CUtensorMap* m, CUtensorMapDataType type, int elem_bytes, const void* base,
+                   uint64_t rows, uint64_t cols, uint32_t box_cols, uint32_t box_rows,
+                   CUtensorMapSwizzle swizzle);
 
 // Tensor-core grouped GEMMs (prefill): whether the dims qualify, and one
 // stage's launch (down = false: gate_up + SwiGLU into h; true: down into y/ys).
