@@ -40,6 +40,8 @@ constexpr int kBarBytes = 256;     // barrier area at the start of shared memory
 constexpr int kMaxStages = 8;
 
 struct GuArgs {
+  CUtensorMap tm_codes;       // int4: codes as {128-byte chunk, row of [E*2I], chunk of d/256},
+                              // box {128, 8, d/256}, 128-byte swizzle
   const uint8_t* gu;          // routed gate_up: bf16 [E][2I][d] or codes [E][2I][d/2]
   const uint16_t* gu_scales;  // int4 scales [E][2I][d/32]
   const uint8_t* sgu;         // shared gate_up bf16 [2Is][d] (may be null)
@@ -331,6 +333,16 @@ __device__ __forceinline__ void tma_box_2d(uint32_t dst, const CUtensorMap* map,
       : "memory");
 }
 
+// Tiled 3D tensor copy of the box at (x, y, z).
+__device__ __forceinline__ void tma_box_3d(uint32_t dst, const CUtensorMap* map, int x, int y,
+                                           int z, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(smem_u32(bar))
+      : "memory");
+}
+
 // ------------------------------------------------------------------ smem loads
 __device__ __forceinline__ uint4 lds128(uint32_t addr) {
   uint4 v;
@@ -371,11 +383,9 @@ __device__ __forceinline__ float f2sum(uint64_t v) {
 __device__ __forceinline__ uint64_t bf16x2_f2(uint32_t w) { return f2(w << 16, w & 0xffff0000u); }
 
 // ------------------------------------------------------------------ int4 on the tensor pipe
-// Shared-memory pitches of an int4 gate_up stage and of the token rows of an
-// int4 layer: 16 bytes beyond the row shift consecutive rows by four banks, so
-// that the eight rows one load instruction reads fall on distinct banks.
-__host__ __device__ constexpr int i4_code_pitch(int d) { return d / 2 + 16; }
-__host__ __device__ constexpr int i4_scale_pitch(int d) { return d / 16 + 16; }
+// Token rows of an int4 layer sit at a pitch 16 bytes beyond the row: that
+// shifts consecutive rows by four banks, so the eight rows one load reads fall
+// on distinct banks.
 __host__ __device__ constexpr int x_pitch(int fmt, int d) { return fmt ? 2 * d + 16 : 2 * d; }
 // Bytes of the cross-warp partial sums of the int4 gate_up consumers: two
 // buffers x three warps x 32 lanes x 4 floats.
@@ -409,41 +419,61 @@ __device__ __forceinline__ void mma_16816(float (&d)[4], uint32_t a0, uint32_t a
         "f"(c[3]));
 }
 
-// One consumer warp's share of an int4 gate_up unit (8 gate rows + the 8 up
-// rows of the same intermediate columns, up to 8 tokens) on the tensor pipe:
-// the groups [gb, ge) of 32 codes along d.  The unit is one 16x8 product per
-// 16 codes: A = gate rows on tile rows 0..7, up rows on 8..15; B = the tokens'
-// activations; lane (g, t) = (lane / 4, lane % 4) holds, in acc, gate and up
-// row g for tokens 2t and 2t + 1 -- both halves of a SwiGLU.
+// int4 gate_up stage: the unit's 8 gate code rows arrive as one tensor box of
+// d / 256 chunks x 8 rows x 128 bytes (chunk-major) with the 128-byte swizzle,
+// the 8 up rows as a second, then the 16 rows' scales densely (gate, up), then
+// the tokens' x rows.  Chunk c of a row holds groups 8c .. 8c + 7 of 32 codes,
+// 16 bytes each; group 8c + i of row r sits in slot i ^ r of the row's 128
+// bytes.
+__host__ __device__ constexpr int i4g_box_bytes(int d) { return 4 * d; }
+__host__ __device__ constexpr int i4g_weight_bytes(int d) { return 8 * d + d; }
+
+// One consumer warp's share of an int4 gate_up unit on the tensor pipe: the
+// 8-group chunks c = c0, c0 + cstep, ... of d.  The unit is one 16x8 product
+// per 16 codes: A = gate rows on tile rows 0..7, up rows on 8..15; B = the
+// tokens' activations; lane (g, t) = (lane / 4, lane % 4) holds, in acc, gate
+// and up row g for tokens 2t and 2t + 1 -- both halves of a SwiGLU.
 // Within a group of 32, thread t takes its code word t (codes 8t .. 8t + 7) and
 // the tile's k positions map onto them as (8t, 8t + 4), (8t + 1, 8t + 5) for the
 // first product and (8t + 2, 8t + 6), (8t + 3, 8t + 7) for the second; the
 // activations are permuted to match.  Each group's two products start from
 // zero and are scaled by the rows' bf16 scales into the fp32 accumulators: the
 // same regrouping (sum of code x activation, then x scale) as the scalar path.
-__device__ __forceinline__ void gu_int4_mma(uint32_t cg, uint32_t cu, uint32_t sgp, uint32_t sup,
-                                            uint32_t xr, bool has_x, int gb, int ge,
-                                            float (&acc)[4]) {
+// codes: the stage; sg, su: row g's scales; xr: token g's row at thread t's
+// 16 bytes.
+__device__ __forceinline__ void gu_int4_mma(uint32_t codes, int d, int g, int t, uint32_t sg,
+                                            uint32_t su, uint32_t xr, bool has_x, int c0,
+                                            int cstep, float (&acc)[4]) {
   const float zero[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll 2
-  for (int gi = gb; gi < ge; ++gi) {
-    uint32_t vg, vu;
-    asm volatile("ld.shared.u32 %0, [%1];" : "=r"(vg) : "r"(cg + 16u * gi));
-    asm volatile("ld.shared.u32 %0, [%1];" : "=r"(vu) : "r"(cu + 16u * gi));
-    const float fg = lds_bf16(sgp + 2u * gi), fu = lds_bf16(sup + 2u * gi);
-    const uint4 xv = has_x ? lds128(xr + 64u * gi) : make_uint4(0u, 0u, 0u, 0u);
-    uint32_t qg[4], qu[4];
-    dequant_pairs(vg, qg);
-    dequant_pairs(vu, qu);
-    const uint32_t b10 = __byte_perm(xv.x, xv.z, 0x5410), b11 = __byte_perm(xv.x, xv.z, 0x7632);
-    const uint32_t b20 = __byte_perm(xv.y, xv.w, 0x5410), b21 = __byte_perm(xv.y, xv.w, 0x7632);
-    float p[4];
-    mma_16816(p, qg[0], qu[0], qg[1], qu[1], b10, b11, zero);
-    mma_16816(p, qg[2], qu[2], qg[3], qu[3], b20, b21, p);
-    acc[0] = fmaf(p[0], fg, acc[0]);
-    acc[1] = fmaf(p[1], fg, acc[1]);
-    acc[2] = fmaf(p[2], fu, acc[2]);
-    acc[3] = fmaf(p[3], fu, acc[3]);
+  const int nc = d / 256;
+  const uint32_t up = (uint32_t)i4g_box_bytes(d);
+  for (int c = c0; c < nc; c += cstep) {
+    const uint4 sgv = lds128(sg + 16u * c), suv = lds128(su + 16u * c);
+    const uint32_t crow = codes + (uint32_t)(c * 1024 + g * 128 + 4 * t);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const uint32_t ca = crow + (uint32_t)((i ^ g) << 4);
+      uint32_t vg, vu;
+      asm volatile("ld.shared.u32 %0, [%1];" : "=r"(vg) : "r"(ca));
+      asm volatile("ld.shared.u32 %0, [%1];" : "=r"(vu) : "r"(ca + up));
+      const uint32_t wg = (i < 2 ? sgv.x : i < 4 ? sgv.y : i < 6 ? sgv.z : sgv.w);
+      const uint32_t wu = (i < 2 ? suv.x : i < 4 ? suv.y : i < 6 ? suv.z : suv.w);
+      const float fg = __uint_as_float(i & 1 ? wg & 0xffff0000u : wg << 16);
+      const float fu = __uint_as_float(i & 1 ? wu & 0xffff0000u : wu << 16);
+      const uint4 xv = has_x ? lds128(xr + 64u * (8 * c + i)) : make_uint4(0u, 0u, 0u, 0u);
+      uint32_t qg[4], qu[4];
+      dequant_pairs(vg, qg);
+      dequant_pairs(vu, qu);
+      const uint32_t b10 = __byte_perm(xv.x, xv.z, 0x5410), b11 = __byte_perm(xv.x, xv.z, 0x7632);
+      const uint32_t b20 = __byte_perm(xv.y, xv.w, 0x5410), b21 = __byte_perm(xv.y, xv.w, 0x7632);
+      float p[4];
+      mma_16816(p, qg[0], qu[0], qg[1], qu[1], b10, b11, zero);
+      mma_16816(p, qg[2], qu[2], qg[3], qu[3], b20, b21, p);
+      acc[0] = fmaf(p[0], fg, acc[0]);
+      acc[1] = fmaf(p[1], fg, acc[1]);
+      acc[2] = fmaf(p[2], fu, acc[2]);
+      acc[3] = fmaf(p[3], fu, acc[3]);
+    }
   }
 }
 
@@ -665,13 +695,17 @@ __device__ __forceinline__ void plan_arrays(uint8_t* smem, int E, int16_t*& wex,
 }
 
 template <int kFmt>
-__global__ void __launch_bounds__(kThreads, kCtasPerSm) gate_up_kernel(const GuArgs a) {
+__global__ void __launch_bounds__(kThreads, kCtasPerSm)
+    gate_up_kernel(const __grid_constant__ GuArgs a) {
   extern __shared__ __align__(128) uint8_t smem[];
   uint64_t* full = reinterpret_cast<uint64_t*>(smem);
   uint64_t* empty = full + kMaxStages;
   uint64_t* red_full = empty + kMaxStages;  // [2] int4 partial-sum hand-off
   uint64_t* red_empty = red_full + 2;       // [2]
-  uint8_t* stages = smem + a.stage_off;
+  // int4: the ring starts on a 1024-byte boundary (the swizzled code boxes).
+  const uint32_t ring_pad =
+      kFmt ? ((1024u - ((smem_u32(smem) + (uint32_t)a.stage_off) & 1023u)) & 1023u) : 0u;
+  uint8_t* stages = smem + a.stage_off + ring_pad;
   const uint32_t stages_sa = smem_u32(stages);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int NS = a.n_stages;
@@ -768,27 +802,27 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) gate_up_kernel(const GuA
       uint8_t* st = stages + (size_t)s * a.stage_bytes;
       const int rb = shared ? d * 2 : rowb;
       const int sb = shared ? 0 : srowb;
-      const uint32_t bytes = 2u * nr * (rb + sb) + (uint32_t)nt * d * 2;
+      // (int4 boxes always move 8 rows: the byte count says so.)
+      const uint32_t bytes = (kFmt && !shared ? (uint32_t)i4g_weight_bytes(d)
+                                              : 2u * nr * (rb + sb)) +
+                             (uint32_t)nt * d * 2;
       if (lane == 0) mbar_arrive_expect_tx(&full[s], bytes);
       __syncwarp();
       const uint8_t* wbase = shared ? a.sgu : a.gu + (size_t)cur.expert * 2 * a.I * rb;
       int xoff;
       if (kFmt && !shared) {
-        // One row per lane (RG == 8): gate codes, up codes, gate scales, up
-        // scales, each row at its padded pitch.
-        const uint8_t* sbase =
-            reinterpret_cast<const uint8_t*>(a.gu_scales) + (size_t)cur.expert * 2 * a.I * sb;
-        const int cp = i4_code_pitch(d), sp = i4_scale_pitch(d);
-        const int part = lane >> 3, r = lane & 7;
-        const int row = (part & 1 ? Iw : 0) + r0 + r;
-        if (r < nr) {
-          if (part < 2)
-            bulk_g2s(st + (part * RG + r) * cp, wbase + (size_t)row * rb, rb, &full[s], pol_w);
-          else
-            bulk_g2s(st + 2 * RG * cp + ((part - 2) * RG + r) * sp, sbase + (size_t)row * sb, sb,
-                     &full[s], pol_w);
+        // Gate and up codes as one tensor box each (RG == 8), their scales
+        // as one block each.
+        if (lane < 2)
+          tma_box_3d(smem_u32(st) + lane * i4g_box_bytes(d), &a.tm_codes, 0,
+                     cur.expert * 2 * a.I + lane * Iw + r0, 0, &full[s]);
+        else if (lane < 4) {
+          const uint8_t* sbase = reinterpret_cast<const uint8_t*>(a.gu_scales) +
+                                 ((size_t)cur.expert * 2 * a.I + (lane - 2) * Iw + r0) * sb;
+          bulk_g2s(st + 2 * i4g_box_bytes(d) + (lane - 2) * RG * sb, sbase, RG * sb, &full[s],
+                   pol_w);
         }
-        xoff = 2 * RG * (cp + sp);
+        xoff = i4g_weight_bytes(d);
       } else {
         if (lane == 0) bulk_g2s(st, wbase + (size_t)r0 * rb, nr * rb, &full[s], pol_w);
         if (lane == 1)
@@ -841,18 +875,14 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) gate_up_kernel(const GuA
     if (!mbar_wait(&full[s], (uint32_t)(use & 1), a.status, wait_ns)) break;
     const uint32_t st = stages_sa + (uint32_t)(s * a.stage_bytes);
     if (kFmt && !shared) {
-      // int4 routed unit on the tensor pipe: every consumer warp takes a
-      // quarter of the groups along d; warp 0 adds the other warps' partial
-      // sums and writes h.
+      // int4 routed unit on the tensor pipe: consumer warp w takes the
+      // 8-group chunks w, w + 4, ... along d; warp 0 adds the other warps'
+      // partial sums and writes h.
       const int g = lane >> 2, t = lane & 3;
-      const int cp = i4_code_pitch(d), sp = i4_scale_pitch(d);
-      const int ng = d / 32, per = ng / kConsumerWarps;
-      const int rr = min(g, nr - 1);  // rows past the tile's end: computed, not written
+      const uint32_t sc = st + 2 * i4g_box_bytes(d);
       float acc[4] = {0.f, 0.f, 0.f, 0.f};
-      gu_int4_mma(st + rr * cp + 4 * t, st + (RG + rr) * cp + 4 * t,
-                  st + 2 * RG * cp + rr * sp, st + 2 * RG * cp + (RG + rr) * sp,
-                  st + 2 * RG * (cp + sp) + g * xp + 16 * t, g < nt, warp * per, (warp + 1) * per,
-                  acc);
+      gu_int4_mma(st, d, g, t, sc + g * (d / 16), sc + (RG + g) * (d / 16),
+                  st + i4g_weight_bytes(d) + g * xp + 16 * t, g < nt, warp, kConsumerWarps, acc);
       __syncwarp();
       if (lane == 0) mbar_arrive(&empty[s]);
       // Hand-off of the partial sums through one of two buffers, each with a
@@ -1205,11 +1235,11 @@ GemvShape gate_up_shape(int fmt, int d, int I, int Is, int smem_budget, int rese
     while (g.rg_shared > 1 && 2 * g.rg_shared * d * 2 > 16 * 1024) g.rg_shared /= 2;
     g.xt = 16 * 1024 / (d * 2);
     g.xt = g.xt < 1 ? 1 : (g.xt > kMaxXT ? kMaxXT : g.xt);
-    int w = 2 * g.rg * (i4_code_pitch(d) + i4_scale_pitch(d));
+    int w = i4g_weight_bytes(d);
     if (Is > 0 && 2 * g.rg_shared * d * 2 > w) w = 2 * g.rg_shared * d * 2;
-    g.stage_bytes = (int)round_up(w + g.xt * x_pitch(1, d), 128);
+    g.stage_bytes = (int)round_up(w + g.xt * x_pitch(1, d), 1024);
     g.stage_off = kBarBytes + reserve;
-    g.n_stages = (smem_budget - g.stage_off - kI4RedBytes) / g.stage_bytes;
+    g.n_stages = (smem_budget - g.stage_off - kI4RedBytes - 1024) / g.stage_bytes;
     if (g.n_stages > kMaxStages) g.n_stages = kMaxStages;
     return g;
   }
@@ -1276,6 +1306,15 @@ cudaError_t launch_gate_up(const LaunchCfg& c, const ExpertArgs& e, const GemvSh
                            const WorkExpert* work, const int32_t* cta, const SmemPlanArgs& sp,
                            float* h, float* hs, int* status, int grid) {
   GuArgs a;
+  memset(&a, 0, sizeof(a));
+  if (e.fmt) {
+    const uint64_t dims[3] = {128, (uint64_t)e.E * 2 * e.I, (uint64_t)e.d / 256};
+    const uint64_t strides[2] = {(uint64_t)e.d / 2, 128};
+    const uint32_t box[3] = {128, 8, (uint32_t)e.d / 256};
+    if (!encode_map(&a.tm_codes, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, e.gate_up, dims, strides, box,
+                    CU_TENSOR_MAP_SWIZZLE_128B))
+      return cudaErrorInvalidValue;
+  }
   a.sp = sp;
   a.stage_off = g.stage_off;
   a.h_rows = e.h_rows;
@@ -1301,7 +1340,7 @@ cudaError_t launch_gate_up(const LaunchCfg& c, const ExpertArgs& e, const GemvSh
   a.xt = g.xt;
   a.stage_bytes = g.stage_bytes;
   a.n_stages = g.n_stages;
-  const int smem = g.stage_off + g.stage_bytes * g.n_stages + (e.fmt ? kI4RedBytes : 0);
+  const int smem = g.stage_off + g.stage_bytes * g.n_stages + (e.fmt ? kI4RedBytes + 1024 : 0);
   const void* fn = e.fmt ? (const void*)gate_up_kernel<1> : (const void*)gate_up_kernel<0>;
   cudaError_t err = ensure_smem(fn, smem);
   if (err != cudaSuccess) return err;

@@ -171,6 +171,13 @@ cudaError_t launch_combine(const LaunchCfg& c, int T, int d, int k, const float*
                            const float* y, const float* ys, const float* sg, const uint16_t* x,
                            const uint16_t* w_sg, uint16_t* out);
 
+// A tiled tensor map of rank 2 or 3: dims and box innermost first, strides in
+// bytes of dimensions 1.. (any order: a dimension may step by less than the
+// one before it), reads past the end return zeros.
+bool encode_map(CUtensorMap* m, CUtensorMapDataType type, int rank, const void* base,
+                const uint64_t* dims, const uint64_t* strides, const uint32_t* box,
+                CUtensorMapSwizzle swizzle);
+
 // A 2D tensor map over [rows][cols] elements of `elem_bytes` (row-major),
 // box {box_cols, box_rows}, the given swizzle; reads past the end return zeros.
 bool encode_map_2d(CUtensorMap* m, CUtensorMapDataType type, int elem_bytes, const void* base,
