@@ -231,10 +231,13 @@ moe_status_t expert_plan(const moe_dims_t& dm, void* ws, const Layout& L, int sm
   // timing the decode layers).  A bf16 gate_up unit streams its weight rows
   // from HBM in about the time of four tokens' arithmetic on them.  A bf16
   // down unit is worth about three: each of its tokens re-reads an h row from
-  // shared memory per row pair.  Beside the dequant-bound int4 experts, down
-  // units of both kinds balance best at eight.
-  pp.base_gu = 4;
-  pp.base_dn = fmt ? 8 : 3;
+  // shared memory per row pair.  An int4 routed unit runs on the tensor pipe,
+  // where up to eight tokens cost what one does: its cost is a constant, about
+  // that of a three-token shared-expert gate_up unit (16 + 16 rows against 4
+  // row pairs) and of two four-token shared down units (128 rows against 8).
+  pp.tok_w = fmt ? 0 : 1;
+  pp.base_gu = fmt ? 7 : 4;
+  pp.base_dn = fmt ? 16 : 3;
   pp.base_gu_s = 4;
   pp.base_dn_s = fmt ? 8 : 3;
   ep->sms = sms;
@@ -290,6 +293,7 @@ moe_status_t run_experts(const moe_dims_t& dm, const void* x, const float* topk_
     sp_gu.base_s = ep.pp.base_gu_s;
     sp_dn.base = ep.pp.base_dn;
     sp_dn.base_s = ep.pp.base_dn_s;
+    sp_gu.tok_w = sp_dn.tok_w = ep.pp.tok_w;
     // The down stage leaves the aligned layout in the workspace.
     sp_dn.sorted_ids = at<int32_t>(ws, L.sorted);
     sp_dn.block_ids = at<int32_t>(ws, L.blocks);

@@ -205,20 +205,21 @@ __device__ __forceinline__ void block_scan(const int (&v)[V], int (&ex)[V], int 
 
 // ---------------------------------------------------------------- unit split
 // First unit of the work expert whose estimated costs start at c0 (units from
-// u0; n tokens in groups of xt, `tiles` row tiles per group, cost base + tokens
-// per unit) at which the running cost reaches `target`.
-__device__ __forceinline__ int unit_at_cost(int target, int c0, int u0, int tiles, int n, int xt, int base) {
+// u0; n tokens in groups of xt, `tiles` row tiles per group, cost base + tw x
+// tokens per unit, base >= 1) at which the running cost reaches `target`.
+__device__ __forceinline__ int unit_at_cost(int target, int c0, int u0, int tiles, int n, int xt,
+                                            int base, int tw) {
   const int groups = (n + xt - 1) / xt;
   const int nt_last = n - (groups - 1) * xt;
-  const int per_full = tiles * (base + xt);
+  const int per_full = tiles * (base + tw * xt);
   const int r = target - c0;
   int g, t;
   if (groups > 1 && r < (groups - 1) * per_full) {
     g = r / per_full;
-    t = (r - g * per_full) / (base + xt);
+    t = (r - g * per_full) / (base + tw * xt);
   } else {
     g = groups - 1;
-    t = (r - (groups - 1) * per_full) / (base + nt_last);
+    t = (r - (groups - 1) * per_full) / (base + tw * nt_last);
     t = min(t, tiles - 1);
   }
   return u0 + g * tiles + t;

@@ -182,7 +182,7 @@ __device__ CtaRange smem_plan(const SmemPlanArgs sp, int T, int k, bool shared_e
   __shared__ CtaRange s_range;
   const int tid = threadIdx.x, nthr = blockDim.x;
   const int S = T * k, E = sp.E, B = sp.B, W = (T + 31) >> 5;
-  const int base = sp.base, base_s = sp.base_s;
+  const int base = sp.base, base_s = sp.base_s, tw = sp.tok_w;
   int32_t* const abi_sorted = sp.sorted_ids;
   const float inv_k = 1.0f / (float)k, inv_xt = 1.0f / (float)xt, inv_b = 1.0f / (float)B;
   // This CTA's slice of the aligned layout (E * grid < 2^31).
@@ -228,7 +228,7 @@ __device__ CtaRange smem_plan(const SmemPlanArgs sp, int T, int k, bool shared_e
     loc[0] += div_small(c + B - 1, inv_b) * B;
     loc[1] += c > 0 ? 1 : 0;
     loc[2] += tiles_r * g;
-    loc[3] += tiles_r * (g * base + c);
+    loc[3] += tiles_r * (g * base + tw * c);
     loc[4] += c;
   }
   int ex[5], tot[5];
@@ -256,7 +256,7 @@ __device__ CtaRange smem_plan(const SmemPlanArgs sp, int T, int k, bool shared_e
     ex[0] += P;
     ex[1] += c > 0 ? 1 : 0;
     ex[2] += tiles_r * g;
-    ex[3] += tiles_r * (g * base + c);
+    ex[3] += tiles_r * (g * base + tw * c);
     ex[4] += c;
   }
   int n_work = tot[1], units = tot[2], cost = tot[3];
@@ -306,7 +306,7 @@ __device__ CtaRange smem_plan(const SmemPlanArgs sp, int T, int k, bool shared_e
       w = lo;
       const bool sh = shared_expert && lo == n_work - 1;
       u = unit_at_cost(target, c0[lo], u0[lo], sh ? tiles_s : tiles_r, wnt[lo], xt,
-                       sh ? base_s : base);
+                       sh ? base_s : base, sh ? 1 : tw);
     }
     if (tid == 0) {
       s_range.u_begin = u;
@@ -419,37 +419,38 @@ __device__ __forceinline__ void mma_16816(float (&d)[4], uint32_t a0, uint32_t a
         "f"(c[3]));
 }
 
-// int4 gate_up stage: the unit's 8 gate code rows arrive as one tensor box of
-// d / 256 chunks x 8 rows x 128 bytes (chunk-major) with the 128-byte swizzle,
-// the 8 up rows as a second, then the 16 rows' scales densely (gate, up), then
-// the tokens' x rows.  Chunk c of a row holds groups 8c .. 8c + 7 of 32 codes,
-// 16 bytes each; group 8c + i of row r sits in slot i ^ r of the row's 128
-// bytes.
-__host__ __device__ constexpr int i4g_box_bytes(int d) { return 4 * d; }
-__host__ __device__ constexpr int i4g_weight_bytes(int d) { return 8 * d + d; }
+// int4 gate_up stage of RG rows (8 or 16): the unit's RG gate code rows arrive
+// as one tensor box of d / 256 chunks x RG rows x 128 bytes (chunk-major) with
+// the 128-byte swizzle, the RG up rows as a second, then their scales densely
+// (gate, up), then the tokens' x rows.  Chunk c of a row holds groups 8c ..
+// 8c + 7 of 32 codes, 16 bytes each; group 8c + i of row r sits in slot
+// i ^ (r % 8) of the row's 128 bytes.
+__host__ __device__ constexpr int i4g_box_bytes(int d, int rg) { return rg * d / 2; }
+__host__ __device__ constexpr int i4g_weight_bytes(int d, int rg) { return rg * (d + d / 8); }
 
-// One consumer warp's share of an int4 gate_up unit on the tensor pipe: the
-// 8-group chunks c = c0, c0 + cstep, ... of d.  The unit is one 16x8 product
-// per 16 codes: A = gate rows on tile rows 0..7, up rows on 8..15; B = the
-// tokens' activations; lane (g, t) = (lane / 4, lane % 4) holds, in acc, gate
-// and up row g for tokens 2t and 2t + 1 -- both halves of a SwiGLU.
+// One consumer warp's share of an int4 gate_up unit on the tensor pipe: rows
+// r8 .. r8 + 7 of the unit's gate and up rows, over the 8-group chunks c = c0,
+// c0 + cstep, ... of d.  The share is one 16x8 product per 16 codes: A = the
+// gate rows on tile rows 0..7, the up rows on 8..15; B = the tokens'
+// activations; lane (g, t) = (lane / 4, lane % 4) holds, in acc, gate and up
+// row r8 + g for tokens 2t and 2t + 1 -- both halves of a SwiGLU.
 // Within a group of 32, thread t takes its code word t (codes 8t .. 8t + 7) and
 // the tile's k positions map onto them as (8t, 8t + 4), (8t + 1, 8t + 5) for the
 // first product and (8t + 2, 8t + 6), (8t + 3, 8t + 7) for the second; the
 // activations are permuted to match.  Each group's two products start from
 // zero and are scaled by the rows' bf16 scales into the fp32 accumulators: the
 // same regrouping (sum of code x activation, then x scale) as the scalar path.
-// codes: the stage; sg, su: row g's scales; xr: token g's row at thread t's
-// 16 bytes.
-__device__ __forceinline__ void gu_int4_mma(uint32_t codes, int d, int g, int t, uint32_t sg,
-                                            uint32_t su, uint32_t xr, bool has_x, int c0,
-                                            int cstep, float (&acc)[4]) {
+// codes: the stage (RG rows per box); sg, su: the gate and up scales of row
+// r8 + g; xr: token g's row at thread t's 16 bytes.
+__device__ __forceinline__ void gu_int4_mma(uint32_t codes, int d, int RG, int r8, int g, int t,
+                                            uint32_t sg, uint32_t su, uint32_t xr, bool has_x,
+                                            int c0, int cstep, float (&acc)[4]) {
   const float zero[4] = {0.f, 0.f, 0.f, 0.f};
   const int nc = d / 256;
-  const uint32_t up = (uint32_t)i4g_box_bytes(d);
+  const uint32_t up = (uint32_t)i4g_box_bytes(d, RG);
   for (int c = c0; c < nc; c += cstep) {
     const uint4 sgv = lds128(sg + 16u * c), suv = lds128(su + 16u * c);
-    const uint32_t crow = codes + (uint32_t)(c * 1024 + g * 128 + 4 * t);
+    const uint32_t crow = codes + (uint32_t)((c * RG + r8 + g) * 128 + 4 * t);
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
       const uint32_t ca = crow + (uint32_t)((i ^ g) << 4);
@@ -477,11 +478,11 @@ __device__ __forceinline__ void gu_int4_mma(uint32_t codes, int d, int g, int t,
   }
 }
 
-// int4 down stage: the unit's 64 code rows of W_down arrive as I / 256 tensor
-// boxes of 64 rows x 128 bytes with the 128-byte swizzle (16-byte chunk c of
+// int4 down stage: the unit's 128 code rows of W_down arrive as I / 256 tensor
+// boxes of 128 rows x 128 bytes with the 128-byte swizzle (16-byte chunk c of
 // row r stored at chunk c ^ (r % 8): the eight rows one load reads fall on
 // distinct banks), then the rows' scales densely, then the tokens' h rows.
-constexpr int kI4DnRows = 64;
+constexpr int kI4DnRows = 128;
 constexpr int kI4DnBox = kI4DnRows * 128;  // bytes of one code box
 __host__ __device__ constexpr int i4d_codes_bytes(int I) { return (I / 256) * kI4DnBox; }
 __host__ __device__ constexpr int i4d_h_pitch(int I) { return 2 * I + 16; }
@@ -716,8 +717,10 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
       mbar_init(&empty[s], kConsumerWarps);
     }
     for (int b = 0; b < 2; ++b) {
-      mbar_init(&red_full[b], kConsumerWarps - 1);
-      mbar_init(&red_empty[b], 1);
+      // int4: warps tp + ntile j (j >= 1) hand their partial sums to warp tp.
+      const int ntile = a.rg / 8;
+      mbar_init(&red_full[b], kConsumerWarps - ntile);
+      mbar_init(&red_empty[b], ntile);
     }
     fence_barrier_init();
   }
@@ -803,7 +806,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
       const int rb = shared ? d * 2 : rowb;
       const int sb = shared ? 0 : srowb;
       // (int4 boxes always move 8 rows: the byte count says so.)
-      const uint32_t bytes = (kFmt && !shared ? (uint32_t)i4g_weight_bytes(d)
+      const uint32_t bytes = (kFmt && !shared ? (uint32_t)i4g_weight_bytes(d, RG)
                                               : 2u * nr * (rb + sb)) +
                              (uint32_t)nt * d * 2;
       if (lane == 0) mbar_arrive_expect_tx(&full[s], bytes);
@@ -811,18 +814,18 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
       const uint8_t* wbase = shared ? a.sgu : a.gu + (size_t)cur.expert * 2 * a.I * rb;
       int xoff;
       if (kFmt && !shared) {
-        // Gate and up codes as one tensor box each (RG == 8), their scales
-        // as one block each.
+        // Gate and up codes as one tensor box each (RG rows: I is a multiple
+        // of 256, so every unit is whole), their scales as one block each.
         if (lane < 2)
-          tma_box_3d(smem_u32(st) + lane * i4g_box_bytes(d), &a.tm_codes, 0,
+          tma_box_3d(smem_u32(st) + lane * i4g_box_bytes(d, RG), &a.tm_codes, 0,
                      cur.expert * 2 * a.I + lane * Iw + r0, 0, &full[s]);
         else if (lane < 4) {
           const uint8_t* sbase = reinterpret_cast<const uint8_t*>(a.gu_scales) +
                                  ((size_t)cur.expert * 2 * a.I + (lane - 2) * Iw + r0) * sb;
-          bulk_g2s(st + 2 * i4g_box_bytes(d) + (lane - 2) * RG * sb, sbase, RG * sb, &full[s],
-                   pol_w);
+          bulk_g2s(st + 2 * i4g_box_bytes(d, RG) + (lane - 2) * RG * sb, sbase, RG * sb,
+                   &full[s], pol_w);
         }
-        xoff = i4g_weight_bytes(d);
+        xoff = i4g_weight_bytes(d, RG);
       } else {
         if (lane == 0) bulk_g2s(st, wbase + (size_t)r0 * rb, nr * rb, &full[s], pol_w);
         if (lane == 1)
@@ -875,33 +878,37 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
     if (!mbar_wait(&full[s], (uint32_t)(use & 1), a.status, wait_ns)) break;
     const uint32_t st = stages_sa + (uint32_t)(s * a.stage_bytes);
     if (kFmt && !shared) {
-      // int4 routed unit on the tensor pipe: consumer warp w takes the
-      // 8-group chunks w, w + 4, ... along d; warp 0 adds the other warps'
-      // partial sums and writes h.
+      // int4 routed unit on the tensor pipe: RG / 8 tiles of 8 gate + 8 up
+      // rows; consumer warp w takes tile tp = w % ntile over the 8-group
+      // chunks w / ntile, w / ntile + kConsumerWarps / ntile, ... along d.
+      // Warp tp adds the partial sums of the tile's other warps and writes h.
       const int g = lane >> 2, t = lane & 3;
-      const uint32_t sc = st + 2 * i4g_box_bytes(d);
+      const int ntile = RG / 8, tp = warp % ntile, r8 = 8 * tp;
+      const uint32_t sc = st + 2 * i4g_box_bytes(d, RG);
       float acc[4] = {0.f, 0.f, 0.f, 0.f};
-      gu_int4_mma(st, d, g, t, sc + g * (d / 16), sc + (RG + g) * (d / 16),
-                  st + i4g_weight_bytes(d) + g * xp + 16 * t, g < nt, warp, kConsumerWarps, acc);
+      gu_int4_mma(st, d, RG, r8, g, t, sc + (r8 + g) * sb, sc + (RG + r8 + g) * sb,
+                  st + i4g_weight_bytes(d, RG) + g * xp + 16 * t, g < nt, warp / ntile,
+                  kConsumerWarps / ntile, acc);
       __syncwarp();
       if (lane == 0) mbar_arrive(&empty[s]);
       // Hand-off of the partial sums through one of two buffers, each with a
-      // full barrier (the other warps wrote) and an empty one (warp 0 read).
+      // full barrier (the writing warps arrived) and an empty one (the tiles'
+      // first warps read).
       const int buf = nred & 1;
       const uint32_t ph = (uint32_t)(nred >> 1) & 1u;
       ++nred;
-      float4* red = reinterpret_cast<float4*>(stages + (size_t)NS * a.stage_bytes) + buf * 96;
-      if (warp > 0) {
+      float4* red = reinterpret_cast<float4*>(stages + (size_t)NS * a.stage_bytes) +
+                    buf * (kConsumerWarps - 1) * 32;
+      if (warp >= ntile) {
         if (nred > 2 && !mbar_wait(&red_empty[buf], ph ^ 1u, a.status, wait_ns)) break;
-        red[(warp - 1) * 32 + lane] = make_float4(acc[0], acc[1], acc[2], acc[3]);
+        red[(warp - ntile) * 32 + lane] = make_float4(acc[0], acc[1], acc[2], acc[3]);
         __syncwarp();
         if (lane == 0) mbar_arrive(&red_full[buf]);
         continue;
       }
       if (!mbar_wait(&red_full[buf], ph, a.status, wait_ns)) break;
-#pragma unroll
-      for (int w = 0; w < kConsumerWarps - 1; ++w) {
-        const float4 o = red[w * 32 + lane];
+      for (int w = warp + ntile; w < kConsumerWarps; w += ntile) {
+        const float4 o = red[(w - ntile) * 32 + lane];
         acc[0] += o.x;
         acc[1] += o.y;
         acc[2] += o.z;
@@ -909,9 +916,10 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(&red_empty[buf]);
-      if (g < nr) {
+      if (r8 + g < nr) {
         // h as two bf16 planes: hi = bf16(h), lo = bf16(h - hi).
-        uint16_t* hh = reinterpret_cast<uint16_t*>(a.h) + (size_t)(cur.pos + g0) * a.I + r0 + g;
+        uint16_t* hh =
+            reinterpret_cast<uint16_t*>(a.h) + (size_t)(cur.pos + g0) * a.I + r0 + r8 + g;
         uint16_t* hl = hh + (size_t)a.h_rows * a.I;
 #pragma unroll
         for (int c = 0; c < 2; ++c) {
@@ -1061,14 +1069,14 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
         const int sb = shared ? 0 : srowb;
         const bool i4 = kFmt && !shared;
         if (pass == 0 || !pre) {
-          // (int4 boxes always move 64 rows: the byte count says so.)
+          // (int4 boxes always move whole 128-row boxes: the byte count says so.)
           const uint32_t bytes = (i4 ? (uint32_t)i4d_codes_bytes(Iw) : (uint32_t)nr * rb) +
                                  (uint32_t)nr * sb + (uint32_t)nt * Iw * 4;
           if (lane == 0) mbar_arrive_expect_tx(&full[s], bytes);
           __syncwarp();
           const uint8_t* wb = shared ? a.sdn : a.dn + (size_t)cur.expert * a.d * rb;
           if (i4) {
-            // The code rows as I / 256 swizzled boxes (64 rows each, whatever
+            // The code rows as I / 256 swizzled boxes (128 rows each, whatever
             // nr), the scales as one block.
             if (lane < Iw / 256)
               tma_box_2d(smem_u32(st) + lane * kI4DnBox, &a.tm_codes, lane * 128,
@@ -1226,20 +1234,29 @@ GemvShape gate_up_shape(int fmt, int d, int I, int Is, int smem_budget, int rese
   (void)I;
   GemvShape g;
   if (fmt) {
-    // int4 routed units: 8 gate + 8 up rows (one tensor-pipe tile, one row
-    // per producer lane) at padded pitches; shared-expert (bf16) units of up
-    // to four row pairs within 16 KB; the cross-warp partial sums after the
-    // ring.
-    g.rg = 8;
-    g.rg_shared = kConsumerWarps;
-    while (g.rg_shared > 1 && 2 * g.rg_shared * d * 2 > 16 * 1024) g.rg_shared /= 2;
-    g.xt = 16 * 1024 / (d * 2);
-    g.xt = g.xt < 1 ? 1 : (g.xt > kMaxXT ? kMaxXT : g.xt);
-    int w = i4g_weight_bytes(d);
-    if (Is > 0 && 2 * g.rg_shared * d * 2 > w) w = 2 * g.rg_shared * d * 2;
-    g.stage_bytes = (int)round_up(w + g.xt * x_pitch(1, d), 1024);
+    // int4 routed units of 16 gate + 16 up rows (two tensor-pipe tiles), or 8
+    // + 8 where d leaves no room for two such stages; shared-expert (bf16)
+    // units of up to four row pairs within the routed unit's weight bytes;
+    // as many tokens per unit as keep two stages (at most 16 KB of them); the
+    // cross-warp partial sums after the ring (and up to 1 KB of alignment).
+    const int avail = smem_budget - kBarBytes - reserve - kI4RedBytes - 1024;
+    const int xp = x_pitch(1, d);
+    int xcap = 16 * 1024 / (d * 2);
+    xcap = xcap < 1 ? 1 : (xcap > kMaxXT ? kMaxXT : xcap);
+    for (int rg = 16; rg >= 8; rg /= 2) {
+      g.rg = rg;
+      const int wr = i4g_weight_bytes(d, rg);
+      g.rg_shared = kConsumerWarps;
+      while (g.rg_shared > 1 && 2 * g.rg_shared * d * 2 > (wr > 16384 ? wr : 16384))
+        g.rg_shared /= 2;
+      const int w = Is > 0 && 2 * g.rg_shared * d * 2 > wr ? 2 * g.rg_shared * d * 2 : wr;
+      g.xt = xcap;
+      while (g.xt > 1 && 2 * (int)round_up(w + g.xt * xp, 1024) > avail) --g.xt;
+      g.stage_bytes = (int)round_up(w + g.xt * xp, 1024);
+      if (2 * g.stage_bytes <= avail) break;
+    }
     g.stage_off = kBarBytes + reserve;
-    g.n_stages = (smem_budget - g.stage_off - kI4RedBytes - 1024) / g.stage_bytes;
+    g.n_stages = avail / g.stage_bytes;
     if (g.n_stages > kMaxStages) g.n_stages = kMaxStages;
     return g;
   }
@@ -1265,8 +1282,8 @@ GemvShape down_shape(int fmt, int d, int I, int Is, int smem_budget, int reserve
   (void)d;
   GemvShape g;
   if (fmt) {
-    // int4 routed units: 64 rows (four m16 tiles, one per consumer warp) at
-    // padded pitches and the tokens' h rows as two bf16 planes; shared-expert
+    // int4 routed units: 128 rows (eight m16 tiles, two per consumer warp) as
+    // swizzled tensor boxes and the tokens' h rows as two bf16 planes; shared-expert
     // (bf16) units of up to 16 rows within 16 KB with fp32 h rows.
     g.rg = kI4DnRows;
     g.rg_shared = 16;
@@ -1310,7 +1327,7 @@ cudaError_t launch_gate_up(const LaunchCfg& c, const ExpertArgs& e, const GemvSh
   if (e.fmt) {
     const uint64_t dims[3] = {128, (uint64_t)e.E * 2 * e.I, (uint64_t)e.d / 256};
     const uint64_t strides[2] = {(uint64_t)e.d / 2, 128};
-    const uint32_t box[3] = {128, 8, (uint32_t)e.d / 256};
+    const uint32_t box[3] = {128, (uint32_t)g.rg, (uint32_t)e.d / 256};
     if (!encode_map(&a.tm_codes, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, e.gate_up, dims, strides, box,
                     CU_TENSOR_MAP_SWIZZLE_128B))
       return cudaErrorInvalidValue;

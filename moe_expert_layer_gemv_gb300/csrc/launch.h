@@ -42,6 +42,9 @@ struct PlanParams {
   int base_dn;           // same for down
   int base_gu_s;         // same for the shared expert's (bf16) units
   int base_dn_s;
+  int tok_w;             // cost of a token in a routed unit (0: the tensor-pipe int4
+                         // units, whose arithmetic does not grow with their tokens);
+                         // a shared-expert unit's tokens cost 1 each
   int tc_nb_gu;          // tensor-core path: N blocks per expert (0 = no tensor-core plan)
   int tc_nb_dn;
   int grid;              // CTAs of the persistent expert kernels (<= kMaxGrid)
@@ -132,6 +135,7 @@ struct SmemPlanArgs {
   const int32_t* ids;         // [T*k] routing ids, or nullptr
   int E, B;                   // experts, align block size
   int base, base_s;           // unit cost bases of this stage: routed, shared expert
+  int tok_w;                  // cost of a token in a routed unit (shared-expert units: 1)
   int32_t* sorted_ids;        // align outputs to write (down stage), or nullptr
   int32_t* block_ids;
   int32_t* num_post_pad;

@@ -325,7 +325,7 @@ __device__ __forceinline__ int expert_run(int E) { return (E + blockDim.x - 1) /
 // ------------------------------------------------------------------ plan
 // Estimated cost of a unit with nt tokens, in token-equivalents: a fixed part
 // `base` for streaming (and, int4, dequantising) the unit's weight rows plus
-// one per token of arithmetic.  The routed experts' base and the shared
+// tok_w per token of arithmetic (1 for the shared expert's units).  The routed experts' base and the shared
 // expert's are separate (PlanParams::base_gu / base_gu_s, base_dn / base_dn_s).
 
 // CTA c of one stage gets units [cta[c], cta[c+1]) and starts in work expert
@@ -333,7 +333,7 @@ __device__ __forceinline__ int expert_run(int E) { return (E + blockDim.x - 1) /
 // c * total / grid (taken in fp32: monotone in c, exact enough for balancing).
 __device__ void split_one(int c, int n_work, const int* s_cost, const int* s_unit, const int* s_n,
                           const int* s_tiles, int total_cost, int total_units, int xt, int base,
-                          int base_s, bool has_shared, int grid, int32_t* cta) {
+                          int base_s, int tw, bool has_shared, int grid, int32_t* cta) {
   if (c == grid || n_work == 0) {
     cta[c] = c == grid ? total_units : 0;
     if (c < grid) cta[grid + 1 + c] = 0;
@@ -345,8 +345,9 @@ __device__ void split_one(int c, int n_work, const int* s_cost, const int* s_uni
     const int mid = (lo + hi + 1) >> 1;
     if (s_cost[mid] <= target) lo = mid; else hi = mid - 1;
   }
+  const bool sh = has_shared && lo == n_work - 1;
   cta[c] = c == 0 ? 0 : unit_at_cost(target, s_cost[lo], s_unit[lo], s_tiles[lo], s_n[lo], xt,
-                                      has_shared && lo == n_work - 1 ? base_s : base);
+                                      sh ? base_s : base, sh ? 1 : tw);
   cta[grid + 1 + c] = lo;
 }
 
@@ -363,8 +364,8 @@ __device__ __forceinline__ void expert_vals(int c, int B, const PlanParams& pp, 
   v[1] = t ? 1 : 0;
   v[2] = t ? pp.tiles_gu * ggu : 0;
   v[3] = t ? pp.tiles_dn * gdn : 0;
-  v[4] = t ? pp.tiles_gu * (ggu * pp.base_gu + c) : 0;
-  v[5] = t ? pp.tiles_dn * (gdn * pp.base_dn + c) : 0;
+  v[4] = t ? pp.tiles_gu * (ggu * pp.base_gu + pp.tok_w * c) : 0;
+  v[5] = t ? pp.tiles_dn * (gdn * pp.base_dn + pp.tok_w * c) : 0;
   v[6] = mb * pp.tc_nb_gu;
   v[7] = mb * pp.tc_nb_dn;
 }
@@ -497,10 +498,10 @@ __device__ void split_stages(const PlanTotals& pt, int E, const PlanParams& pp, 
   for (int i = threadIdx.x; pp.tc_nb_gu == 0 && i < 2 * per; i += blockDim.x) {
     if (i < per)
       split_one(i, pt.n_work, tmp + 2 * W, tmp, tmp + 4 * W, tmp + 5 * W, pt.cost_gu, pt.units_gu,
-                pp.xt_gu, pp.base_gu, pp.base_gu_s, pt.has_shared, pp.grid, pp.cta_gu);
+                pp.xt_gu, pp.base_gu, pp.base_gu_s, pp.tok_w, pt.has_shared, pp.grid, pp.cta_gu);
     else
       split_one(i - per, pt.n_work, tmp + 3 * W, tmp + W, tmp + 4 * W, tmp + 6 * W, pt.cost_dn,
-                pt.units_dn, pp.xt_dn, pp.base_dn, pp.base_dn_s, pt.has_shared, pp.grid,
+                pt.units_dn, pp.xt_dn, pp.base_dn, pp.base_dn_s, pp.tok_w, pt.has_shared, pp.grid,
                 pp.cta_dn);
   }
   if (threadIdx.x == 0) {
