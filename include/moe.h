@@ -146,11 +146,13 @@ const char* moe_status_string(moe_status_t status);
  * 0 and the status says why). */
 moe_status_t moe_workspace_bytes(const moe_dims_t* dims, size_t* bytes);
 
-/* Zero a workspace's control words on `stream`: the device status word and the
+/* Zero a workspace's control words on `stream`: the device status word, the
  * arrival counters of the routing and align kernels (each launch returns its
- * counters to zero).  Call once after allocating the workspace, and again if a
- * call left MOE_ERR_TIMEOUT in the status word (its launches may have stopped
- * short of resetting a counter).  Also disarms moe_workspace_inject_stall. */
+ * counters to zero) and the work tickets of the two expert GEMV stages (each
+ * stage zeroes the other's).  Call once after allocating the workspace, and
+ * again if a call left MOE_ERR_TIMEOUT in the status word or failed part-way
+ * with MOE_ERR_CUDA (its launches may have stopped short of resetting a
+ * counter).  Also disarms moe_workspace_inject_stall. */
 moe_status_t moe_workspace_init(void* workspace, size_t workspace_bytes, void* stream);
 
 /* Byte offsets, from the start of a workspace sized for the same dims, of the

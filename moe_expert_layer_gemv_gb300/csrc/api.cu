@@ -236,6 +236,25 @@ moe_status_t expert_plan(const moe_dims_t& dm, void* ws, const Layout& L, int sm
   // that of a three-token shared-expert gate_up unit (16 + 16 rows against 4
   // row pairs) and of two four-token shared down units (128 rows against 8).
   pp.tok_w = fmt ? 0 : 1;
+  // Dynamic tails (kStaticShare) pay on long stages only: a stage's end
+  // spread is about a tenth of its length, while a tail costs a ticket round
+  // trip at the end of every CTA -- and, for gate_up, the down stage's head
+  // start (down CTAs plan and start their first weight copies in the SM slots
+  // of gate_up CTAs that finish early, about 5 us, lost when every gate_up CTA
+  // is kept busy to the end).  So a stage gets a tail when the weight stream
+  // of its at most min(E, T k) touched experts reaches 150 MB (down) or 300 MB
+  // (gate_up): about 25 and 50 us at the measured HBM rate (timed on the
+  // decode layers: verify_t8's down at 134 MB loses with one, int4_t32's at
+  // 189 MB gains).
+  {
+    const double touched = (double)(dm.E < S ? dm.E : S);
+    const double gu_bytes =
+        touched * (fmt ? 2.0 * dm.I * (dm.d / 2.0 + dm.d / 16.0) : 4.0 * dm.I * dm.d);
+    const double dn_bytes =
+        touched * (fmt ? (double)dm.d * (dm.I / 2.0 + dm.I / 16.0) : 2.0 * dm.d * dm.I);
+    pp.tail_gu = gu_bytes >= 300e6 ? 1 : 0;
+    pp.tail_dn = dn_bytes >= 150e6 ? 1 : 0;
+  }
   pp.base_gu = fmt ? 7 : 4;
   pp.base_dn = fmt ? 16 : 3;
   pp.base_gu_s = 4;
@@ -294,6 +313,8 @@ moe_status_t run_experts(const moe_dims_t& dm, const void* x, const float* topk_
     sp_dn.base = ep.pp.base_dn;
     sp_dn.base_s = ep.pp.base_dn_s;
     sp_gu.tok_w = sp_dn.tok_w = ep.pp.tok_w;
+    sp_gu.tail = ep.pp.tail_gu;
+    sp_dn.tail = ep.pp.tail_dn;
     // The down stage leaves the aligned layout in the workspace.
     sp_dn.sorted_ids = at<int32_t>(ws, L.sorted);
     sp_dn.block_ids = at<int32_t>(ws, L.blocks);
@@ -319,11 +340,12 @@ moe_status_t run_experts(const moe_dims_t& dm, const void* x, const float* topk_
       return MOE_ERR_CUDA;
   } else {
     if (launch_gate_up(next, a, ep.gu, static_cast<const uint16_t*>(x), sorted_ids, ep.pp.plan,
-                       ep.pp.work, ep.pp.cta_gu, sp_gu, h, hs, status, ep.pp.grid) != cudaSuccess)
+                       ep.pp.work, ep.pp.cta_gu, sp_gu, h, hs, status, ep.pp.grid,
+                       ep.pp.tail_gu != 0) != cudaSuccess)
       return MOE_ERR_CUDA;
     if ((s = record(events, MOE_EV_GATE_UP, st)) != MOE_OK) return s;
     if (launch_down(next, a, ep.dn, sorted_ids, ep.pp.plan, ep.pp.work, ep.pp.cta_dn, sp_dn, h, hs,
-                    y, ys, status, ep.pp.grid) != cudaSuccess)
+                    y, ys, status, ep.pp.grid, ep.pp.tail_dn != 0) != cudaSuccess)
       return MOE_ERR_CUDA;
   }
   if ((s = record(events, MOE_EV_DOWN, st)) != MOE_OK) return s;

@@ -204,6 +204,20 @@ __device__ __forceinline__ void block_scan(const int (&v)[V], int (&ex)[V], int 
 }
 
 // ---------------------------------------------------------------- unit split
+// Share of a GEMV stage's estimated cost that the CTAs split among themselves
+// statically when the stage has a dynamic tail; the units past it go, one at a
+// time, to whichever producer asks first (an atomic ticket), so that a CTA
+// whose units ran slower than their estimate takes fewer of them.
+constexpr float kStaticShare = 0.85f;
+
+// The cost split of one stage: CTA c starts where the running cost reaches
+// c * share * cost / grid; with a tail (share < 1) the tail starts at the cost
+// share * cost, without one (share 1) the last CTA ends at the last unit.
+__device__ __forceinline__ int split_target(int c, int grid, int cost, bool tail) {
+  const int fcost = tail ? (int)(kStaticShare * (float)cost) : cost;
+  return min(fcost, (int)((float)c * ((float)fcost / (float)grid)));
+}
+
 // First unit of the work expert whose estimated costs start at c0 (units from
 // u0; n tokens in groups of xt, `tiles` row tiles per group, cost base + tw x
 // tokens per unit, base >= 1) at which the running cost reaches `target`.

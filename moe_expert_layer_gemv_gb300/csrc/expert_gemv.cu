@@ -54,6 +54,8 @@ struct GuArgs {
   float* h;                   // [sorted positions][I]; int4 layers: two bf16 planes
   float* hs;                  // [T][Is]
   int* status;
+  int* dyn;                   // the stage's dynamic-tail ticket counter (DynTail)
+  int* dyn_other;             // the down stage's, zeroed here
   int T, d, I, Is, k;
   int rg, rgs, xt, stage_bytes, n_stages;
   int stage_off;              // shared-memory offset of the stage ring
@@ -75,6 +77,8 @@ struct DnArgs {
   float* y;                   // [T*k][d]
   float* ys;                  // [T][d]
   int* status;
+  int* dyn;                   // the stage's dynamic-tail ticket counter (DynTail)
+  int* dyn_other;             // the gate_up stage's, zeroed here
   int T, d, I, Is, k;
   int rd, rds, xt, stage_bytes, n_stages;
   int stage_off;
@@ -135,10 +139,53 @@ struct UnitCursor {
 };
 
 // This CTA's share of a stage: units [u_begin, u_end), starting in work
-// expert w0 (first unit ubeg0, first sorted position pos0), of n_work.
+// expert w0 (first unit ubeg0, first sorted position pos0), of n_work; then
+// the stage's dynamic tail [u_dyn, u_total), starting in work expert w_dyn
+// (first unit ubeg_dyn, first sorted position pos_dyn).
 struct CtaRange {
   int u_begin, u_end, w0, ubeg0, pos0, n_work;
+  int u_dyn, u_total, w_dyn, ubeg_dyn, pos_dyn;
 };
+
+// The producer's side of a stage's dynamic tail: ticket i of *ctr is unit
+// u_dyn + i.  A ticket is fetched ahead of its use (the first two units
+// before, the others one), so the atomic's round trip overlaps the copies of
+// the units before it.  The counter starts a launch at zero: the other GEMV
+// stage of the layer zeroes it, after its dependency wait, in between (gate_up
+// zeroes down's, down zeroes gate_up's; every kernel of the layer waits for
+// its predecessor to complete before it completes).
+struct DynTail {
+  int* ctr;
+  int u_dyn, u_total;
+  int ticket;  // lane 0: the fetched ticket
+  __device__ __forceinline__ void fetch(int lane) {
+    if (lane == 0) ticket = atomicAdd(ctr, 1);
+  }
+  __device__ __forceinline__ int take() const {
+    return u_dyn + __shfl_sync(0xffffffffu, ticket, 0);
+  }
+};
+
+// Shared-memory word of each stage holding the unit the producer put there,
+// for the units of the dynamic tail (-1: no more units).
+constexpr int kStageUnitOff = 192;  // inside the barrier area, after the barriers
+
+// The producer's last stage (its j-th): no unit, so that the consumers, which
+// learn the tail's units from the stages, stop.  Clears ok if the wait for the
+// slot gives up.
+__device__ __forceinline__ void end_of_units(uint64_t* full, uint64_t* empty, int* s_unit, int j,
+                                             int NS, int lane, int* status, bool& ok) {
+  const int s = j % NS, use = j / NS;
+  if (use > 0 && !mbar_wait(&empty[s], (uint32_t)((use - 1) & 1), status)) {
+    ok = false;
+    return;
+  }
+  if (lane == 0) {
+    s_unit[s] = -1;
+    mbar_arrive(&full[s]);
+  }
+  __syncwarp();
+}
 
 // Ints of shared-memory scratch smem_plan needs (it lives in the stage ring,
 // before the first copy is issued).
@@ -176,10 +223,10 @@ constexpr int kPlanRun = 8;
 // slots at its running position, no padding).  With sp.sorted_ids, the CTA
 // also writes its slice of the aligned layout (moe_align_block_size) to the
 // workspace: the experts [blockIdx.x * E / grid, (blockIdx.x + 1) * E / grid).
-__device__ CtaRange smem_plan(const SmemPlanArgs sp, int T, int k, bool shared_expert,
+// The CTA's range is left in `range` (shared memory).
+__device__ void smem_plan(CtaRange& range, const SmemPlanArgs sp, int T, int k, bool shared_expert,
                               int tiles_r, int tiles_s, int xt, int16_t* wex, int16_t* wnt,
                               int32_t* sorted, int* scratch, int* status) {
-  __shared__ CtaRange s_range;
   const int tid = threadIdx.x, nthr = blockDim.x;
   const int S = T * k, E = sp.E, B = sp.B, W = (T + 31) >> 5;
   const int base = sp.base, base_s = sp.base_s, tw = sp.tok_w;
@@ -290,14 +337,16 @@ __device__ CtaRange smem_plan(const SmemPlanArgs sp, int T, int k, bool shared_e
     sorted[p0e[e] + r] = s;
     if (abi_sorted != nullptr && e >= eb && e < ee) abi_sorted[poe[e] + r] = s;
   }
-  // This CTA's range: the start of CTA c and of CTA c + 1.
-  if (tid < 2) {
-    const int c = blockIdx.x + tid;
+  // This CTA's range: the start of CTA c and of CTA c + 1, and the start of
+  // the dynamic tail (CTA grid).
+  if (tid < 3) {
+    const int c = tid < 2 ? (int)blockIdx.x + tid : (int)gridDim.x;
     int u = 0, w = 0;
-    if (c >= (int)gridDim.x) {
+    if (c == (int)gridDim.x && !sp.tail) {
       u = units;
-    } else if (c > 0) {
-      const int target = min(cost, (int)((float)c * ((float)cost / (float)gridDim.x)));
+      w = n_work > 0 ? n_work - 1 : 0;
+    } else if (c > 0 && n_work > 0) {
+      const int target = split_target(c, gridDim.x, cost, sp.tail != 0);
       int lo = 0, hi = n_work - 1;
       while (lo < hi) {
         const int mid = (lo + hi + 1) >> 1;
@@ -309,17 +358,22 @@ __device__ CtaRange smem_plan(const SmemPlanArgs sp, int T, int k, bool shared_e
                        sh ? base_s : base, sh ? 1 : tw);
     }
     if (tid == 0) {
-      s_range.u_begin = u;
-      s_range.w0 = w;
-      s_range.ubeg0 = u0[w];
-      s_range.pos0 = p0[w];
-      s_range.n_work = n_work;
+      range.u_begin = u;
+      range.w0 = w;
+      range.ubeg0 = u0[w];
+      range.pos0 = p0[w];
+      range.n_work = n_work;
+    } else if (tid == 1) {
+      range.u_end = u;
     } else {
-      s_range.u_end = u;
+      range.u_dyn = u;
+      range.u_total = units;
+      range.w_dyn = w;
+      range.ubeg_dyn = u0[w];
+      range.pos_dyn = p0[w];
     }
   }
   __syncthreads();
-  return s_range;
 }
 
 // Tiled 2D tensor copy of the box at (x, y) into shared memory, completion as
@@ -695,7 +749,7 @@ __device__ __forceinline__ void plan_arrays(uint8_t* smem, int E, int16_t*& wex,
   sorted = reinterpret_cast<int32_t*>(smem + kBarBytes + 2 * wb);
 }
 
-template <int kFmt>
+template <int kFmt, bool kTail>
 __global__ void __launch_bounds__(kThreads, kCtasPerSm)
     gate_up_kernel(const __grid_constant__ GuArgs a) {
   extern __shared__ __align__(128) uint8_t smem[];
@@ -735,6 +789,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
   __syncthreads();
   pdl_wait();
   pdl_trigger();
+  if (blockIdx.x == 0 && threadIdx.x == 0) *a.dyn_other = 0;
 
   // The stall test hook (moe_workspace_inject_stall): the producer issues
   // nothing and the consumers' waits give up after the armed limit.
@@ -753,7 +808,9 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
   cur.tiles_s = a.Is > 0 ? (int)ceil_div(a.Is, a.rgs) : 1;
   cur.xt = xt;
   cur.down = false;
-  CtaRange rg;
+  // This CTA's range, in shared memory (read where needed, not held in
+  // registers across the unit loops).
+  __shared__ CtaRange rg;
   const int32_t* sorted;  // sorted position -> slot (shared or global memory)
   if (a.sp.ids != nullptr) {
     int16_t *wex, *wnt;
@@ -762,31 +819,59 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
     cur.work = nullptr;
     cur.wex = wex;
     cur.wnt = wnt;
-    rg = smem_plan(a.sp, a.T, a.k, a.Is > 0, cur.tiles_r, cur.tiles_s, xt, wex, wnt, ss,
+    smem_plan(rg, a.sp, a.T, a.k, a.Is > 0, cur.tiles_r, cur.tiles_s, xt, wex, wnt, ss,
                    reinterpret_cast<int*>(stages), a.status);
     sorted = ss;
   } else {
     cur.work = a.work;
-    rg.n_work = a.plan->n_work;
-    rg.u_begin = a.cta[blockIdx.x];
-    rg.u_end = a.cta[blockIdx.x + 1];
-    rg.w0 = a.cta[gridDim.x + 1 + blockIdx.x];
-    rg.ubeg0 = rg.pos0 = 0;
+    if (threadIdx.x == 0) {
+      rg.n_work = a.plan->n_work;
+      rg.u_begin = a.cta[blockIdx.x];
+      rg.u_end = a.cta[blockIdx.x + 1];
+      rg.w0 = a.cta[gridDim.x + 1 + blockIdx.x];
+      rg.ubeg0 = rg.pos0 = 0;
+      rg.u_dyn = a.cta[gridDim.x];
+      rg.w_dyn = a.cta[2 * gridDim.x + 1];
+      rg.ubeg_dyn = rg.pos_dyn = 0;
+      rg.u_total = a.plan->units_gu;
+    }
+    __syncthreads();
     sorted = a.sorted_ids;
   }
   cur.n_work = rg.n_work;
   const int u_begin = rg.u_begin, u_end = rg.u_end;
   if (u_begin < u_end) cur.start(rg.w0, rg.ubeg0, rg.pos0);
 
+  const int n_static = u_end - u_begin;
+  // The stage has a dynamic tail (kTail instances only: without one the
+  // kernel is the plain static split).
+  const bool tail = kTail && rg.u_dyn < rg.u_total;
+  int* const s_unit = reinterpret_cast<int*>(smem + kStageUnitOff);
+
   if (warp == kConsumerWarps) {
     // ------------------------------------------------------------ producer
+    DynTail dt{a.dyn, rg.u_dyn, rg.u_total, 0};
     if (stall_us > 0) return;  // nothing issued, nothing in flight
     const uint64_t pol_w = policy_evict_first();
     const uint64_t pol_x = policy_evict_last();
     int j = 0;
     bool ok = true;
     int tok = 0, tok_i = -1, tok_g = -1;  // lane m: token of member m of the cached group
-    for (int u = u_begin; u < u_end; ++u, ++j) {
+    // This CTA's static units, then tickets of the dynamic tail until they run
+    // out; the first ticket is fetched with the last static unit but one.
+    if (tail && n_static == 0) dt.fetch(lane);
+    for (;; ++j) {
+      int u;
+      if (j < n_static) {
+        u = u_begin + j;
+        if (tail && j == max(n_static - 2, 0)) dt.fetch(lane);
+      } else {
+        if (!tail) break;
+        u = dt.take();
+        if (u >= dt.u_total) break;
+        if (j == n_static) cur.start(rg.w_dyn, rg.ubeg_dyn, rg.pos_dyn);
+        dt.fetch(lane);
+      }
       const int s = j % NS, use = j / NS;
       cur.seek(u);
       const int local = u - cur.ubeg;
@@ -809,7 +894,10 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
       const uint32_t bytes = (kFmt && !shared ? (uint32_t)i4g_weight_bytes(d, RG)
                                               : 2u * nr * (rb + sb)) +
                              (uint32_t)nt * d * 2;
-      if (lane == 0) mbar_arrive_expect_tx(&full[s], bytes);
+      if (lane == 0) {
+        if (j >= n_static) s_unit[s] = u;
+        mbar_arrive_expect_tx(&full[s], bytes);
+      }
       __syncwarp();
       const uint8_t* wbase = shared ? a.sgu : a.gu + (size_t)cur.expert * 2 * a.I * rb;
       int xoff;
@@ -854,15 +942,26 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
       if (lane < nt)
         bulk_g2s(st + xoff + lane * xp, a.x + (size_t)tok * d, d * 2, &full[s], pol_x);
     }
+    if (ok && tail) end_of_units(full, empty, s_unit, j, NS, lane, a.status, ok);
     if (!ok) drain_stages(full, j, NS, a.status);
     return;
   }
 
   // -------------------------------------------------------------- consumers
-  int j = 0;
   int nred = 0;  // int4 units reduced so far
-  for (int u = u_begin; u < u_end; ++u, ++j) {
+  for (int j = 0;; ++j) {
     const int s = j % NS, use = j / NS;
+    int u;
+    if (j < n_static) {
+      u = u_begin + j;
+    } else {
+      // A unit of the dynamic tail, or none: the producer's word in the stage.
+      if (!tail) break;
+      if (!mbar_wait(&full[s], (uint32_t)(use & 1), a.status, wait_ns)) break;
+      u = *reinterpret_cast<volatile int*>(s_unit + s);
+      if (u < 0) break;
+      if (j == n_static) cur.start(rg.w_dyn, rg.ubeg_dyn, rg.pos_dyn);
+    }
     cur.seek(u);
     const int local = u - cur.ubeg;
     const int grp = local / cur.tiles, tile = local - grp * cur.tiles;
@@ -875,7 +974,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
     const int nt = min(xt, cur.n_tok - g0);
     const int rb = shared ? d * 2 : rowb;
     const int sb = shared ? 0 : srowb;
-    if (!mbar_wait(&full[s], (uint32_t)(use & 1), a.status, wait_ns)) break;
+    if (j < n_static && !mbar_wait(&full[s], (uint32_t)(use & 1), a.status, wait_ns)) break;
     const uint32_t st = stages_sa + (uint32_t)(s * a.stage_bytes);
     if (kFmt && !shared) {
       // int4 routed unit on the tensor pipe: RG / 8 tiles of 8 gate + 8 up
@@ -967,7 +1066,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
 
 // --------------------------------------------------------------------------- down
 // Consumers: 8 lanes per pair of weight rows, 16 row pairs per pass of the CTA.
-template <int kFmt>
+template <int kFmt, bool kTail>
 __global__ void __launch_bounds__(kThreads, kCtasPerSm)
     down_kernel(const __grid_constant__ DnArgs a) {
   extern __shared__ __align__(128) uint8_t smem[];
@@ -1003,7 +1102,9 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
   cur.tiles_s = a.Is > 0 ? (int)ceil_div(a.d, a.rds) : 1;
   cur.xt = xt;
   cur.down = true;
-  CtaRange rg;
+  // This CTA's range, in shared memory (read where needed, not held in
+  // registers across the unit loops).
+  __shared__ CtaRange rg;
   const int32_t* sorted;  // sorted position -> slot (shared or global memory)
   if (a.sp.ids != nullptr) {
     int16_t *wex, *wnt;
@@ -1012,16 +1113,23 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
     cur.work = nullptr;
     cur.wex = wex;
     cur.wnt = wnt;
-    rg = smem_plan(a.sp, a.T, a.k, a.Is > 0, cur.tiles_r, cur.tiles_s, xt, wex, wnt, ss,
+    smem_plan(rg, a.sp, a.T, a.k, a.Is > 0, cur.tiles_r, cur.tiles_s, xt, wex, wnt, ss,
                    reinterpret_cast<int*>(stages), a.status);
     sorted = ss;
   } else {
     cur.work = a.work;
-    rg.n_work = a.plan->n_work;
-    rg.u_begin = a.cta[blockIdx.x];
-    rg.u_end = a.cta[blockIdx.x + 1];
-    rg.w0 = a.cta[gridDim.x + 1 + blockIdx.x];
-    rg.ubeg0 = rg.pos0 = 0;
+    if (threadIdx.x == 0) {
+      rg.n_work = a.plan->n_work;
+      rg.u_begin = a.cta[blockIdx.x];
+      rg.u_end = a.cta[blockIdx.x + 1];
+      rg.w0 = a.cta[gridDim.x + 1 + blockIdx.x];
+      rg.ubeg0 = rg.pos0 = 0;
+      rg.u_dyn = a.cta[gridDim.x];
+      rg.w_dyn = a.cta[2 * gridDim.x + 1];
+      rg.ubeg_dyn = rg.pos_dyn = 0;
+      rg.u_total = a.plan->units_dn;
+    }
+    __syncthreads();
     sorted = a.sorted_ids;
   }
   cur.n_work = rg.n_work;
@@ -1032,21 +1140,43 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
     pdl_trigger();
   }
 
+  const int n_static = u_end - u_begin;
+  // The stage has a dynamic tail (kTail instances only: without one the
+  // kernel is the plain static split).
+  const bool tail = kTail && rg.u_dyn < rg.u_total;
+  int* const s_unit = reinterpret_cast<int*>(smem + kStageUnitOff);
+
   if (warp == kConsumerWarps) {
     const uint64_t pol_w = policy_evict_first();
     const uint64_t pol_h = policy_evict_last();  // h rows are re-read by every row tile
+    DynTail dt{a.dyn, rg.u_dyn, rg.u_total, 0};
     int j = 0;
     bool ok = true;
-    const int n_pre = min(NS, u_end - u_begin);  // units whose weights go before the wait
+    const int n_pre = min(NS, n_static);  // units whose weights go before the wait
     for (int pass = 0; pass < 2 && ok; ++pass) {
-      // pass 0: weight rows of the first n_pre units; pass 1: everything else.
+      // pass 0: weight rows of the first n_pre units; pass 1: everything else:
+      // this CTA's static units, then tickets of the dynamic tail until they
+      // run out (the first fetched with the last static unit).
       if (pass == 1) {
         pdl_wait();
         pdl_trigger();
+        if (blockIdx.x == 0 && lane == 0) *a.dyn_other = 0;
         if (u_begin < u_end) cur.start(rg.w0, rg.ubeg0, rg.pos0);
+        if (tail && n_static == 0) dt.fetch(lane);
       }
-      j = 0;
-      for (int u = u_begin; u < (pass == 0 ? u_begin + n_pre : u_end); ++u, ++j) {
+      for (j = 0;; ++j) {
+        int u;
+        if (j < n_static) {
+          if (pass == 0 && j >= n_pre) break;
+          u = u_begin + j;
+          if (tail && pass == 1 && j == max(n_static - 2, 0)) dt.fetch(lane);
+        } else {
+          if (pass == 0 || !tail) break;
+          u = dt.take();
+          if (u >= dt.u_total) break;
+          if (j == n_static) cur.start(rg.w_dyn, rg.ubeg_dyn, rg.pos_dyn);
+          dt.fetch(lane);
+        }
         const int s = j % NS, use = j / NS;
         cur.seek(u);
         const int local = u - cur.ubeg;
@@ -1072,7 +1202,10 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
           // (int4 boxes always move whole 128-row boxes: the byte count says so.)
           const uint32_t bytes = (i4 ? (uint32_t)i4d_codes_bytes(Iw) : (uint32_t)nr * rb) +
                                  (uint32_t)nr * sb + (uint32_t)nt * Iw * 4;
-          if (lane == 0) mbar_arrive_expect_tx(&full[s], bytes);
+          if (lane == 0) {
+            if (j >= n_static) s_unit[s] = u;
+            mbar_arrive_expect_tx(&full[s], bytes);
+          }
           __syncwarp();
           const uint8_t* wb = shared ? a.sdn : a.dn + (size_t)cur.expert * a.d * rb;
           if (i4) {
@@ -1111,15 +1244,26 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
         }
       }
     }
+    if (ok && tail) end_of_units(full, empty, s_unit, j, NS, lane, a.status, ok);
     if (!ok) drain_stages(full, j, NS, a.status);
     return;
   }
 
   const int sub = lane >> 3, sl = lane & 7;  // row within the warp's quad, lane in row
-  int j = 0;
   int slot_of_lane = 0, slot_i = -1, slot_g = -1;  // slot id of token sl of the cached group
-  for (int u = u_begin; u < u_end; ++u, ++j) {
+  for (int j = 0;; ++j) {
     const int s = j % NS, use = j / NS;
+    int u;
+    if (j < n_static) {
+      u = u_begin + j;
+    } else {
+      // A unit of the dynamic tail, or none: the producer's word in the stage.
+      if (!tail) break;
+      if (!mbar_wait(&full[s], (uint32_t)(use & 1), a.status)) break;
+      u = *reinterpret_cast<volatile int*>(s_unit + s);
+      if (u < 0) break;
+      if (j == n_static) cur.start(rg.w_dyn, rg.ubeg_dyn, rg.pos_dyn);
+    }
     cur.seek(u);
     const int local = u - cur.ubeg;
     const int grp = local / cur.tiles, tile = local - grp * cur.tiles;
@@ -1137,7 +1281,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
     }
     const int rb = shared ? Iw * 2 : rowb;
     const int sb = shared ? 0 : srowb;
-    if (!mbar_wait(&full[s], (uint32_t)(use & 1), a.status)) break;
+    if (j < n_static && !mbar_wait(&full[s], (uint32_t)(use & 1), a.status)) break;
     const uint32_t st = stages_sa + (uint32_t)(s * a.stage_bytes);
     if (kFmt && !shared) {
       // int4 routed unit on the tensor pipe: warp w takes rows [16 w, 16 w + 16)
@@ -1321,7 +1465,7 @@ GemvShape down_shape(int fmt, int d, int I, int Is, int smem_budget, int reserve
 cudaError_t launch_gate_up(const LaunchCfg& c, const ExpertArgs& e, const GemvShape& g,
                            const uint16_t* x, const int32_t* sorted_ids, const Plan* plan,
                            const WorkExpert* work, const int32_t* cta, const SmemPlanArgs& sp,
-                           float* h, float* hs, int* status, int grid) {
+                           float* h, float* hs, int* status, int grid, bool tail) {
   GuArgs a;
   memset(&a, 0, sizeof(a));
   if (e.fmt) {
@@ -1347,6 +1491,8 @@ cudaError_t launch_gate_up(const LaunchCfg& c, const ExpertArgs& e, const GemvSh
   a.h = h;
   a.hs = hs;
   a.status = status;
+  a.dyn = status + kDynCounterBase;
+  a.dyn_other = status + kDynCounterBase + 1;
   a.T = e.T;
   a.d = e.d;
   a.I = e.I;
@@ -1358,7 +1504,10 @@ cudaError_t launch_gate_up(const LaunchCfg& c, const ExpertArgs& e, const GemvSh
   a.stage_bytes = g.stage_bytes;
   a.n_stages = g.n_stages;
   const int smem = g.stage_off + g.stage_bytes * g.n_stages + (e.fmt ? kI4RedBytes + 1024 : 0);
-  const void* fn = e.fmt ? (const void*)gate_up_kernel<1> : (const void*)gate_up_kernel<0>;
+  const void* fn = e.fmt ? (tail ? (const void*)gate_up_kernel<1, true>
+                                 : (const void*)gate_up_kernel<1, false>)
+                          : (tail ? (const void*)gate_up_kernel<0, true>
+                                  : (const void*)gate_up_kernel<0, false>);
   cudaError_t err = ensure_smem(fn, smem);
   if (err != cudaSuccess) return err;
   void* args[] = {&a};
@@ -1368,7 +1517,7 @@ cudaError_t launch_gate_up(const LaunchCfg& c, const ExpertArgs& e, const GemvSh
 cudaError_t launch_down(const LaunchCfg& c, const ExpertArgs& e, const GemvShape& g,
                         const int32_t* sorted_ids, const Plan* plan, const WorkExpert* work,
                         const int32_t* cta, const SmemPlanArgs& sp, const float* h,
-                        const float* hs, float* y, float* ys, int* status, int grid) {
+                        const float* hs, float* y, float* ys, int* status, int grid, bool tail) {
   DnArgs a;
   memset(&a, 0, sizeof(a));
   if (e.fmt && !encode_map_2d(&a.tm_codes, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, e.down,
@@ -1390,6 +1539,8 @@ cudaError_t launch_down(const LaunchCfg& c, const ExpertArgs& e, const GemvShape
   a.y = y;
   a.ys = ys;
   a.status = status;
+  a.dyn = status + kDynCounterBase + 1;
+  a.dyn_other = status + kDynCounterBase;
   a.T = e.T;
   a.d = e.d;
   a.I = e.I;
@@ -1401,7 +1552,10 @@ cudaError_t launch_down(const LaunchCfg& c, const ExpertArgs& e, const GemvShape
   a.stage_bytes = g.stage_bytes;
   a.n_stages = g.n_stages;
   const int smem = g.stage_off + g.stage_bytes * g.n_stages + (e.fmt ? 1024 : 0);
-  const void* fn = e.fmt ? (const void*)down_kernel<1> : (const void*)down_kernel<0>;
+  const void* fn = e.fmt ? (tail ? (const void*)down_kernel<1, true>
+                                 : (const void*)down_kernel<1, false>)
+                          : (tail ? (const void*)down_kernel<0, true>
+                                  : (const void*)down_kernel<0, false>);
   cudaError_t err = ensure_smem(fn, smem);
   if (err != cudaSuccess) return err;
   void* args[] = {&a};

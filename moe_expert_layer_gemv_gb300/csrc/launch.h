@@ -42,6 +42,7 @@ struct PlanParams {
   int base_dn;           // same for down
   int base_gu_s;         // same for the shared expert's (bf16) units
   int base_dn_s;
+  int tail_gu, tail_dn;  // 1: the stage ends with a dynamic tail (kStaticShare)
   int tok_w;             // cost of a token in a routed unit (0: the tensor-pipe int4
                          // units, whose arithmetic does not grow with their tokens);
                          // a shared-expert unit's tokens cost 1 each
@@ -60,6 +61,10 @@ constexpr int kFusedRouteMaxT = 128;
 // Workspace-header ints used as arrival counters by route_kernel (the status
 // word is int 0): [kRouteCounterBase] tiles done, then one per token tile.
 constexpr int kRouteCounterBase = 16;
+// Workspace-header ints of the GEMV stages' dynamic tails: [kDynCounterBase]
+// the gate_up stage's next ticket, [+ 1] the down stage's.  Each stage zeroes
+// the other's (zero after moe_workspace_init).
+constexpr int kDynCounterBase = 48;
 // Workspace-header int counting the finished CTAs of the multi-CTA align.
 constexpr int kAlignCounter = 60;
 // Workspace-header int holding the stall test hook (moe_workspace_inject_stall):
@@ -136,6 +141,7 @@ struct SmemPlanArgs {
   int E, B;                   // experts, align block size
   int base, base_s;           // unit cost bases of this stage: routed, shared expert
   int tok_w;                  // cost of a token in a routed unit (shared-expert units: 1)
+  int tail;                   // 1: the stage ends with a dynamic tail (kStaticShare)
   int32_t* sorted_ids;        // align outputs to write (down stage), or nullptr
   int32_t* block_ids;
   int32_t* num_post_pad;
@@ -162,12 +168,12 @@ struct ExpertArgs {
 cudaError_t launch_gate_up(const LaunchCfg& c, const ExpertArgs& a, const GemvShape& g,
                            const uint16_t* x, const int32_t* sorted_ids, const Plan* plan,
                            const WorkExpert* work, const int32_t* cta, const SmemPlanArgs& sp,
-                           float* h, float* hs, int* status, int grid);
+                           float* h, float* hs, int* status, int grid, bool tail);
 
 cudaError_t launch_down(const LaunchCfg& c, const ExpertArgs& a, const GemvShape& g,
                         const int32_t* sorted_ids, const Plan* plan, const WorkExpert* work,
                         const int32_t* cta, const SmemPlanArgs& sp, const float* h,
-                        const float* hs, float* y, float* ys, int* status, int grid);
+                        const float* hs, float* y, float* ys, int* status, int grid, bool tail);
 
 // out[t] = sum_j w[t][j] y[t*k+j] + sigmoid(sg[t]) ys[t]   (bf16, RNE); sg[t] =
 // x[t] . w_sg, read from `sg` when given, else computed here.

@@ -330,16 +330,24 @@ __device__ __forceinline__ int expert_run(int E) { return (E + blockDim.x - 1) /
 
 // CTA c of one stage gets units [cta[c], cta[c+1]) and starts in work expert
 // cta[grid + 1 + c]: its share of the stage's estimated cost starts at
-// c * total / grid (taken in fp32: monotone in c, exact enough for balancing).
+// split_target(c) (taken in fp32: monotone in c, exact enough for balancing).
+// cta[grid] is where the dynamic tail starts, in work expert cta[2 grid + 1]
+// (without a tail: the total of units).
 __device__ void split_one(int c, int n_work, const int* s_cost, const int* s_unit, const int* s_n,
-                          const int* s_tiles, int total_cost, int total_units, int xt, int base,
-                          int base_s, int tw, bool has_shared, int grid, int32_t* cta) {
-  if (c == grid || n_work == 0) {
-    cta[c] = c == grid ? total_units : 0;
-    if (c < grid) cta[grid + 1 + c] = 0;
+                          const int* s_tiles, int total_cost, int xt, int base,
+                          int base_s, int tw, bool has_shared, bool tail, int total_units,
+                          int grid, int32_t* cta) {
+  if (n_work == 0) {
+    cta[c] = 0;
+    cta[grid + 1 + c] = 0;
     return;
   }
-  const int target = min(total_cost, (int)((float)c * ((float)total_cost / (float)grid)));
+  if (c == grid && !tail) {
+    cta[c] = total_units;
+    cta[2 * grid + 1] = n_work - 1;
+    return;
+  }
+  const int target = split_target(c, grid, total_cost, tail);
   int lo = 0, hi = n_work - 1;
   while (lo < hi) {
     const int mid = (lo + hi + 1) >> 1;
@@ -497,12 +505,13 @@ __device__ void split_stages(const PlanTotals& pt, int E, const PlanParams& pp, 
   // The tensor-core kernels walk the plan by tiles, not by these ranges.
   for (int i = threadIdx.x; pp.tc_nb_gu == 0 && i < 2 * per; i += blockDim.x) {
     if (i < per)
-      split_one(i, pt.n_work, tmp + 2 * W, tmp, tmp + 4 * W, tmp + 5 * W, pt.cost_gu, pt.units_gu,
-                pp.xt_gu, pp.base_gu, pp.base_gu_s, pp.tok_w, pt.has_shared, pp.grid, pp.cta_gu);
+      split_one(i, pt.n_work, tmp + 2 * W, tmp, tmp + 4 * W, tmp + 5 * W, pt.cost_gu, pp.xt_gu,
+                pp.base_gu, pp.base_gu_s, pp.tok_w, pt.has_shared, pp.tail_gu != 0, pt.units_gu,
+                pp.grid, pp.cta_gu);
     else
       split_one(i - per, pt.n_work, tmp + 3 * W, tmp + W, tmp + 4 * W, tmp + 6 * W, pt.cost_dn,
-                pt.units_dn, pp.xt_dn, pp.base_dn, pp.base_dn_s, pp.tok_w, pt.has_shared, pp.grid,
-                pp.cta_dn);
+                pp.xt_dn, pp.base_dn, pp.base_dn_s, pp.tok_w, pt.has_shared, pp.tail_dn != 0,
+                pt.units_dn, pp.grid, pp.cta_dn);
   }
   if (threadIdx.x == 0) {
     Plan p;
