@@ -204,6 +204,178 @@ __device__ __forceinline__ int div_small(int n, float inv) {
 // 160 threads of the expert kernels).
 constexpr int kPlanRun = 8;
 
+// smem_plan for S = T k <= 64 slots, on one warp (lane = threadIdx.x < 32):
+// the same work list, sorted positions and aligned-layout slice.  Keys
+// (expert << 12 | slot) of the 64 positions i = lane + 32 r sit two per lane
+// and go through a bitonic sort network (in-lane at distance 32, shuffles
+// below); invalid ids sort last and count nowhere.  A run of one expert starts
+// where the expert changes; its work index is the number of run starts below
+// it, its first sorted position is its index in the sorted keys.  Results in
+// shared memory: wex, wnt, u0, c0, p0 per work expert, poe (padded offset) per
+// routed work expert, sorted; n_work / units / cost returned in every lane.
+__device__ __forceinline__ void warp_plan(const SmemPlanArgs& sp, int S, int E, int B, int T,
+                                          int xt, int tiles_r, int tiles_s, int base, int base_s,
+                                          int tw, bool shared_expert, int eb, int ee,
+                                          int16_t* wex, int16_t* wnt, int32_t* sorted, int* poe,
+                                          int* u0, int* c0, int* p0, int& n_work, int& units,
+                                          int& cost, int* status) {
+  constexpr unsigned kAll = 0xffffffffu;
+  constexpr int kNone = 0x7fffffff;
+  const int lane = threadIdx.x & 31;
+  const float inv_xt = 1.0f / (float)xt, inv_b = 1.0f / (float)B;
+  int key[2];
+#pragma unroll
+  for (int r = 0; r < 2; ++r) {
+    const int slot = lane + 32 * r;
+    int v = kNone;
+    if (slot < S) {
+      const int e = __ldcg(sp.ids + slot);
+      if (e < 0 || e >= E)
+        record_status(status, kStatusDeviceCheck);
+      else
+        v = (e << 12) | slot;
+    }
+    key[r] = v;
+  }
+  // Bitonic network over i = lane + 32 r: blocks of `size` alternate
+  // ascending / descending until the last (size 64) sorts all ascending.
+#pragma unroll
+  for (int size = 2; size <= 64; size <<= 1) {
+#pragma unroll
+    for (int stride = size >> 1; stride > 0; stride >>= 1) {
+      if (stride == 32) {
+        const int lo = min(key[0], key[1]), hi = max(key[0], key[1]);
+        key[0] = lo;
+        key[1] = hi;
+      } else {
+#pragma unroll
+        for (int r = 0; r < 2; ++r) {
+          const int i = lane + 32 * r;
+          const int other = __shfl_xor_sync(kAll, key[r], stride);
+          const bool up = (i & size) == 0, lower = (i & stride) == 0;
+          key[r] = lower == up ? min(key[r], other) : max(key[r], other);
+        }
+      }
+    }
+  }
+  int ex[2], sl[2];
+  bool val[2], head[2];
+#pragma unroll
+  for (int r = 0; r < 2; ++r) {
+    val[r] = key[r] != kNone;
+    ex[r] = key[r] >> 12;
+    sl[r] = key[r] & 4095;
+  }
+  int prev0 = __shfl_up_sync(kAll, ex[0], 1), prev1 = __shfl_up_sync(kAll, ex[1], 1);
+  const int last0 = __shfl_sync(kAll, ex[0], 31);
+  if (lane == 0) {
+    prev0 = -1;
+    prev1 = last0;
+  }
+  head[0] = val[0] && ex[0] != prev0;
+  head[1] = val[1] && ex[1] != prev1;
+  const uint64_t H = (uint64_t)__ballot_sync(kAll, head[1]) << 32 | __ballot_sync(kAll, head[0]);
+  const int nvalid = __popc(__ballot_sync(kAll, val[0])) + __popc(__ballot_sync(kAll, val[1]));
+  const int nw = __popcll(H);
+  // Per run start: rows after padding, units, cost; exclusive scans in i order.
+  int q[2][3];
+#pragma unroll
+  for (int r = 0; r < 2; ++r) {
+    const int i = lane + 32 * r;
+    q[r][0] = q[r][1] = q[r][2] = 0;
+    if (head[r]) {
+      const uint64_t above = i == 63 ? 0ull : H >> (i + 1);
+      const int c = above ? __ffsll((long long)above) : nvalid - i;
+      const int g = div_small(c + xt - 1, inv_xt);
+      q[r][0] = div_small(c + B - 1, inv_b) * B;
+      q[r][1] = tiles_r * g;
+      q[r][2] = tiles_r * (g * base + tw * c);
+    }
+  }
+  int xs[2][3], tot[3];
+#pragma unroll
+  for (int j = 0; j < 3; ++j) {
+    int inc0 = q[0][j], inc1 = q[1][j];
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int n0 = __shfl_up_sync(kAll, inc0, o), n1 = __shfl_up_sync(kAll, inc1, o);
+      if (lane >= o) {
+        inc0 += n0;
+        inc1 += n1;
+      }
+    }
+    const int t0 = __shfl_sync(kAll, inc0, 31);
+    xs[0][j] = inc0 - q[0][j];
+    xs[1][j] = t0 + inc1 - q[1][j];
+    tot[j] = t0 + __shfl_sync(kAll, inc1, 31);
+  }
+#pragma unroll
+  for (int r = 0; r < 2; ++r) {
+    const int i = lane + 32 * r;
+    if (val[r]) sorted[i] = sl[r];
+    if (head[r]) {
+      const uint64_t above = i == 63 ? 0ull : H >> (i + 1);
+      const int c = above ? __ffsll((long long)above) : nvalid - i;
+      const int idx = __popcll(H & ((1ull << i) - 1ull));
+      wex[idx] = (int16_t)ex[r];
+      wnt[idx] = (int16_t)c;
+      u0[idx] = xs[r][1];
+      c0[idx] = xs[r][2];
+      p0[idx] = i;
+      poe[idx] = xs[r][0];
+    }
+  }
+  n_work = nw;
+  units = tot[1];
+  cost = tot[2];
+  if (shared_expert) {
+    const int sg = div_small(T + xt - 1, inv_xt);
+    if (lane == 0) {
+      wex[nw] = -1;
+      wnt[nw] = (int16_t)T;
+      u0[nw] = units;
+      c0[nw] = cost;
+      p0[nw] = 0;
+    }
+    n_work += 1;
+    units += tiles_s * sg;
+    cost += tiles_s * (sg * base_s + T);
+  }
+  __syncwarp();
+  int32_t* const abi_sorted = sp.sorted_ids;
+  if (abi_sorted == nullptr) return;
+  // This CTA's slice [eb, ee) of the aligned layout.
+#pragma unroll
+  for (int r = 0; r < 2; ++r) {
+    const int i = lane + 32 * r;
+    if (val[r] && ex[r] >= eb && ex[r] < ee) {
+      const uint64_t at_or_below = i == 63 ? ~0ull : (2ull << i) - 1ull;
+      const int idx = __popcll(H & at_or_below) - 1;
+      abi_sorted[poe[idx] + (i - p0[idx])] = sl[r];
+    }
+  }
+  for (int e = eb + lane; e < ee; e += 32) {
+    // Padded offset of expert e: that of the first touched expert >= e.
+    int lo = 0, hi = nw;
+    while (lo < hi) {
+      const int mid = (lo + hi) >> 1;
+      if (wex[mid] < e) lo = mid + 1; else hi = mid;
+    }
+    const int off = lo < nw ? poe[lo] : tot[0];
+    sp.expert_offsets[e] = off;
+    if (lo < nw && wex[lo] == e) {
+      const int c = wnt[lo];
+      const int P = div_small(c + B - 1, inv_b) * B;
+      for (int rr = c; rr < P; ++rr) abi_sorted[off + rr] = S;  // padding
+      for (int b = 0; b < P; b += B) sp.block_ids[div_small(off + b, inv_b)] = e;
+    }
+  }
+  if (blockIdx.x == 0 && lane == 0) {
+    sp.expert_offsets[E] = tot[0];
+    *sp.num_post_pad = tot[0];
+  }
+}
+
 // The plan of one expert stage, built in shared memory by all threads of the
 // CTA from the routing ids (decode sizes: T <= 128, E <= 1024): the align
 // step's counting sort by expert in arrival order, the work list (touched
@@ -243,99 +415,111 @@ __device__ void smem_plan(CtaRange& range, const SmemPlanArgs sp, int T, int k, 
   int* c0 = u0 + E + 2;                                     // [E + 2] cost before a work expert
   int* p0 = c0 + E + 2;                                     // [E + 2] its first sorted position
   int* scan = p0 + E + 2;                                   // [32 * 5]
-  for (int s = tid; s < S; s += nthr) {
-    int e = __ldcg(sp.ids + s);
-    if (e < 0 || e >= E) {
-      record_status(status, kStatusDeviceCheck);
-      e = -1;
-    }
-    s_ids[s] = e;
-  }
-  for (int i = tid; i < E * W; i += nthr) mask[i] = 0u;
-  __syncthreads();
-  for (int s = tid; s < S; s += nthr) {
-    const int e = s_ids[s];
-    const int t = div_small(s, inv_k);
-    if (e >= 0) atomicOr(&mask[e * W + (t >> 5)], 1u << (t & 31));
-  }
-  __syncthreads();
-  // Thread-owned experts [e0, e0 + n): counts, then per expert padded rows,
-  // touched, units, cost, tokens.
-  const int run = (E + nthr - 1) / nthr;
-  const int e0 = min(E, tid * run), n = min(E, e0 + run) - e0;
-  int cnt[kPlanRun];
-  int loc[5] = {0, 0, 0, 0, 0};
-#pragma unroll
-  for (int i = 0; i < kPlanRun; ++i) {
-    int c = 0;
-    if (i < n)
-      for (int w = 0; w < W; ++w) c += __popc(mask[(e0 + i) * W + w]);
-    cnt[i] = c;
-    const int g = div_small(c + xt - 1, inv_xt);
-    loc[0] += div_small(c + B - 1, inv_b) * B;
-    loc[1] += c > 0 ? 1 : 0;
-    loc[2] += tiles_r * g;
-    loc[3] += tiles_r * (g * base + tw * c);
-    loc[4] += c;
-  }
-  int ex[5], tot[5];
-  block_scan<5>(loc, ex, tot, scan);
-#pragma unroll
-  for (int i = 0; i < kPlanRun; ++i) {
-    const int c = cnt[i], e = e0 + i;
-    const int g = div_small(c + xt - 1, inv_xt);
-    const int P = div_small(c + B - 1, inv_b) * B;
-    if (c > 0) {
-      const int idx = ex[1];
-      wex[idx] = (int16_t)e;
-      wnt[idx] = (int16_t)c;
-      u0[idx] = ex[2];
-      c0[idx] = ex[3];
-      p0[idx] = ex[4];
-      p0e[e] = ex[4];
-      poe[e] = ex[0];
-      if (abi_sorted != nullptr && e >= eb && e < ee) {
-        for (int r = c; r < P; ++r) abi_sorted[ex[0] + r] = S;  // padding
-        for (int b = 0; b < P; b += B) sp.block_ids[div_small(ex[0] + b, inv_b)] = e;
+  int n_work = 0, units = 0, cost = 0;  // warp 0 (tid < 3) reads them below
+  if (S <= 64) {
+    // Up to 64 slots: one warp sorts the (expert, slot) keys -- slot order
+    // within an expert is arrival order -- finds the runs by ballot and sums
+    // their rows, units and costs with warp scans; no block barrier.
+    if (tid < 32) warp_plan(sp, S, E, B, T, xt, tiles_r, tiles_s, base, base_s, tw, shared_expert,
+                            eb, ee, wex, wnt, sorted, poe, u0, c0, p0, n_work, units, cost,
+                            status);
+  } else {
+    for (int s = tid; s < S; s += nthr) {
+      int e = __ldcg(sp.ids + s);
+      if (e < 0 || e >= E) {
+        record_status(status, kStatusDeviceCheck);
+        e = -1;
       }
+      s_ids[s] = e;
     }
-    if (abi_sorted != nullptr && i < n && e >= eb && e < ee) sp.expert_offsets[e] = ex[0];
-    ex[0] += P;
-    ex[1] += c > 0 ? 1 : 0;
-    ex[2] += tiles_r * g;
-    ex[3] += tiles_r * (g * base + tw * c);
-    ex[4] += c;
-  }
-  int n_work = tot[1], units = tot[2], cost = tot[3];
-  if (shared_expert) {
-    const int sg = div_small(T + xt - 1, inv_xt);
-    if (tid == 0) {
-      wex[n_work] = -1;
-      wnt[n_work] = (int16_t)T;
-      u0[n_work] = units;
-      c0[n_work] = cost;
-      p0[n_work] = 0;
+    for (int i = tid; i < E * W; i += nthr) mask[i] = 0u;
+    __syncthreads();
+    for (int s = tid; s < S; s += nthr) {
+      const int e = s_ids[s];
+      const int t = div_small(s, inv_k);
+      if (e >= 0) atomicOr(&mask[e * W + (t >> 5)], 1u << (t & 31));
     }
-    n_work += 1;
-    units += tiles_s * sg;
-    cost += tiles_s * (sg * base_s + T);
-  }
-  if (abi_sorted != nullptr && blockIdx.x == 0 && tid == 0) {
-    sp.expert_offsets[E] = tot[0];
-    *sp.num_post_pad = tot[0];
-  }
-  __syncthreads();
-  // Each slot at its expert's running position (arrival order: the earlier
-  // tokens of the expert come first); this CTA's slice of the aligned layout.
-  for (int s = tid; s < S; s += nthr) {
-    const int e = s_ids[s];
-    if (e < 0) continue;
-    const int t = div_small(s, inv_k);
-    const uint32_t* m = mask + e * W;
-    int r = __popc(m[t >> 5] & ((1u << (t & 31)) - 1u));
-    for (int w = 0; w < (t >> 5); ++w) r += __popc(m[w]);
-    sorted[p0e[e] + r] = s;
-    if (abi_sorted != nullptr && e >= eb && e < ee) abi_sorted[poe[e] + r] = s;
+    __syncthreads();
+    // Thread-owned experts [e0, e0 + n): counts, then per expert padded rows,
+    // touched, units, cost, tokens.
+    const int run = (E + nthr - 1) / nthr;
+    const int e0 = min(E, tid * run), n = min(E, e0 + run) - e0;
+    int cnt[kPlanRun];
+    int loc[5] = {0, 0, 0, 0, 0};
+  #pragma unroll
+    for (int i = 0; i < kPlanRun; ++i) {
+      int c = 0;
+      if (i < n)
+        for (int w = 0; w < W; ++w) c += __popc(mask[(e0 + i) * W + w]);
+      cnt[i] = c;
+      const int g = div_small(c + xt - 1, inv_xt);
+      loc[0] += div_small(c + B - 1, inv_b) * B;
+      loc[1] += c > 0 ? 1 : 0;
+      loc[2] += tiles_r * g;
+      loc[3] += tiles_r * (g * base + tw * c);
+      loc[4] += c;
+    }
+    int ex[5], tot[5];
+    block_scan<5>(loc, ex, tot, scan);
+  #pragma unroll
+    for (int i = 0; i < kPlanRun; ++i) {
+      const int c = cnt[i], e = e0 + i;
+      const int g = div_small(c + xt - 1, inv_xt);
+      const int P = div_small(c + B - 1, inv_b) * B;
+      if (c > 0) {
+        const int idx = ex[1];
+        wex[idx] = (int16_t)e;
+        wnt[idx] = (int16_t)c;
+        u0[idx] = ex[2];
+        c0[idx] = ex[3];
+        p0[idx] = ex[4];
+        p0e[e] = ex[4];
+        poe[e] = ex[0];
+        if (abi_sorted != nullptr && e >= eb && e < ee) {
+          for (int r = c; r < P; ++r) abi_sorted[ex[0] + r] = S;  // padding
+          for (int b = 0; b < P; b += B) sp.block_ids[div_small(ex[0] + b, inv_b)] = e;
+        }
+      }
+      if (abi_sorted != nullptr && i < n && e >= eb && e < ee) sp.expert_offsets[e] = ex[0];
+      ex[0] += P;
+      ex[1] += c > 0 ? 1 : 0;
+      ex[2] += tiles_r * g;
+      ex[3] += tiles_r * (g * base + tw * c);
+      ex[4] += c;
+    }
+    n_work = tot[1];
+    units = tot[2];
+    cost = tot[3];
+    if (shared_expert) {
+      const int sg = div_small(T + xt - 1, inv_xt);
+      if (tid == 0) {
+        wex[n_work] = -1;
+        wnt[n_work] = (int16_t)T;
+        u0[n_work] = units;
+        c0[n_work] = cost;
+        p0[n_work] = 0;
+      }
+      n_work += 1;
+      units += tiles_s * sg;
+      cost += tiles_s * (sg * base_s + T);
+    }
+    if (abi_sorted != nullptr && blockIdx.x == 0 && tid == 0) {
+      sp.expert_offsets[E] = tot[0];
+      *sp.num_post_pad = tot[0];
+    }
+    __syncthreads();
+    // Each slot at its expert's running position (arrival order: the earlier
+    // tokens of the expert come first); this CTA's slice of the aligned layout.
+    for (int s = tid; s < S; s += nthr) {
+      const int e = s_ids[s];
+      if (e < 0) continue;
+      const int t = div_small(s, inv_k);
+      const uint32_t* m = mask + e * W;
+      int r = __popc(m[t >> 5] & ((1u << (t & 31)) - 1u));
+      for (int w = 0; w < (t >> 5); ++w) r += __popc(m[w]);
+      sorted[p0e[e] + r] = s;
+      if (abi_sorted != nullptr && e >= eb && e < ee) abi_sorted[poe[e] + r] = s;
+    }
   }
   // This CTA's range: the start of CTA c and of CTA c + 1, and the start of
   // the dynamic tail (CTA grid).
