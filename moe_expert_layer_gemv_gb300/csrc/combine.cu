@@ -57,31 +57,51 @@ __global__ void __launch_bounds__(kThreads)
     float acc[8];
 #pragma unroll
     for (int q = 0; q < 8; ++q) acc[q] = 0.f;
-#pragma unroll 4
-    for (int j = 0; j < k; ++j) {
-      const float wj = wt[j];
-      const float4* yr = reinterpret_cast<const float4*>(y + ((size_t)t * k + j) * d + c);
-      const float4 a = yr[0], b = yr[1];
-      acc[0] = fmaf(wj, a.x, acc[0]);
-      acc[1] = fmaf(wj, a.y, acc[1]);
-      acc[2] = fmaf(wj, a.z, acc[2]);
-      acc[3] = fmaf(wj, a.w, acc[3]);
-      acc[4] = fmaf(wj, b.x, acc[4]);
-      acc[5] = fmaf(wj, b.y, acc[5]);
-      acc[6] = fmaf(wj, b.z, acc[6]);
-      acc[7] = fmaf(wj, b.w, acc[7]);
-    }
+    // The shared row and up to eight expert rows are requested before the
+    // first product (one round trip to L2 per eight slots), then summed in
+    // ascending j and the shared term last.
+    float4 sa = make_float4(0.f, 0.f, 0.f, 0.f), sb = sa;
     if (ys != nullptr) {
       const float4* sr = reinterpret_cast<const float4*>(ys + (size_t)t * d + c);
-      const float4 a = sr[0], b = sr[1];
-      acc[0] = fmaf(gate, a.x, acc[0]);
-      acc[1] = fmaf(gate, a.y, acc[1]);
-      acc[2] = fmaf(gate, a.z, acc[2]);
-      acc[3] = fmaf(gate, a.w, acc[3]);
-      acc[4] = fmaf(gate, b.x, acc[4]);
-      acc[5] = fmaf(gate, b.y, acc[5]);
-      acc[6] = fmaf(gate, b.z, acc[6]);
-      acc[7] = fmaf(gate, b.w, acc[7]);
+      sa = sr[0];
+      sb = sr[1];
+    }
+    for (int j0 = 0; j0 < k; j0 += 8) {
+      float4 ya[8], yb[8];
+      float wj[8];
+#pragma unroll
+      for (int q = 0; q < 8; ++q) {
+        if (j0 + q < k) {
+          const float4* yr =
+              reinterpret_cast<const float4*>(y + ((size_t)t * k + j0 + q) * d + c);
+          ya[q] = yr[0];
+          yb[q] = yr[1];
+          wj[q] = wt[j0 + q];
+        }
+      }
+#pragma unroll
+      for (int q = 0; q < 8; ++q) {
+        if (j0 + q < k) {
+          acc[0] = fmaf(wj[q], ya[q].x, acc[0]);
+          acc[1] = fmaf(wj[q], ya[q].y, acc[1]);
+          acc[2] = fmaf(wj[q], ya[q].z, acc[2]);
+          acc[3] = fmaf(wj[q], ya[q].w, acc[3]);
+          acc[4] = fmaf(wj[q], yb[q].x, acc[4]);
+          acc[5] = fmaf(wj[q], yb[q].y, acc[5]);
+          acc[6] = fmaf(wj[q], yb[q].z, acc[6]);
+          acc[7] = fmaf(wj[q], yb[q].w, acc[7]);
+        }
+      }
+    }
+    if (ys != nullptr) {
+      acc[0] = fmaf(gate, sa.x, acc[0]);
+      acc[1] = fmaf(gate, sa.y, acc[1]);
+      acc[2] = fmaf(gate, sa.z, acc[2]);
+      acc[3] = fmaf(gate, sa.w, acc[3]);
+      acc[4] = fmaf(gate, sb.x, acc[4]);
+      acc[5] = fmaf(gate, sb.y, acc[5]);
+      acc[6] = fmaf(gate, sb.z, acc[6]);
+      acc[7] = fmaf(gate, sb.w, acc[7]);
     }
     uint4 o;
     uint32_t* ow = reinterpret_cast<uint32_t*>(&o);

@@ -210,12 +210,21 @@ __device__ __forceinline__ void block_scan(const int (&v)[V], int (&ex)[V], int 
 // whose units ran slower than their estimate takes fewer of them.
 constexpr float kStaticShare = 0.85f;
 
+// The down stage's CTAs are launched in index order as the gate_up stage's
+// CTAs retire, so a later index starts later (by up to the gate_up stage's
+// end spread): without a dynamic tail to absorb that, its static share of the
+// cost falls linearly across the grid, from (1 + kDownSkew) to (1 - kDownSkew)
+// times the average (timed on the decode layers).
+constexpr float kDownSkew = 0.15f;
+
 // The cost split of one stage: CTA c starts where the running cost reaches
-// c * share * cost / grid; with a tail (share < 1) the tail starts at the cost
-// share * cost, without one (share 1) the last CTA ends at the last unit.
-__device__ __forceinline__ int split_target(int c, int grid, int cost, bool tail) {
+// G(c / grid) * share * cost, G(x) = (1 + s) x - s x^2 (s = skew; G(x) = x
+// without one); with a tail (share < 1) the tail starts at the cost share *
+// cost, without one (share 1) the last CTA ends at the last unit.
+__device__ __forceinline__ int split_target(int c, int grid, int cost, bool tail, float skew) {
   const int fcost = tail ? (int)(kStaticShare * (float)cost) : cost;
-  return min(fcost, (int)((float)c * ((float)fcost / (float)grid)));
+  const float x = (float)c / (float)grid;
+  return min(fcost, (int)(((1.0f + skew) * x - skew * x * x) * (float)fcost));
 }
 
 // First unit of the work expert whose estimated costs start at c0 (units from

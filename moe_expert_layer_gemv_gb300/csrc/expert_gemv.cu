@@ -530,7 +530,9 @@ __device__ void smem_plan(CtaRange& range, const SmemPlanArgs sp, int T, int k, 
       u = units;
       w = n_work > 0 ? n_work - 1 : 0;
     } else if (c > 0 && n_work > 0) {
-      const int target = split_target(c, gridDim.x, cost, sp.tail != 0);
+      const int target =
+          split_target(c, gridDim.x, cost, sp.tail != 0,
+                       sp.sorted_ids != nullptr && !sp.tail ? kDownSkew : 0.f);
       int lo = 0, hi = n_work - 1;
       while (lo < hi) {
         const int mid = (lo + hi + 1) >> 1;

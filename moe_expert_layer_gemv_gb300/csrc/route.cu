@@ -336,7 +336,7 @@ __device__ __forceinline__ int expert_run(int E) { return (E + blockDim.x - 1) /
 __device__ void split_one(int c, int n_work, const int* s_cost, const int* s_unit, const int* s_n,
                           const int* s_tiles, int total_cost, int xt, int base,
                           int base_s, int tw, bool has_shared, bool tail, int total_units,
-                          int grid, int32_t* cta) {
+                          int grid, float skew, int32_t* cta) {
   if (n_work == 0) {
     cta[c] = 0;
     cta[grid + 1 + c] = 0;
@@ -347,7 +347,7 @@ __device__ void split_one(int c, int n_work, const int* s_cost, const int* s_uni
     cta[2 * grid + 1] = n_work - 1;
     return;
   }
-  const int target = split_target(c, grid, total_cost, tail);
+  const int target = split_target(c, grid, total_cost, tail, skew);
   int lo = 0, hi = n_work - 1;
   while (lo < hi) {
     const int mid = (lo + hi + 1) >> 1;
@@ -507,11 +507,11 @@ __device__ void split_stages(const PlanTotals& pt, int E, const PlanParams& pp, 
     if (i < per)
       split_one(i, pt.n_work, tmp + 2 * W, tmp, tmp + 4 * W, tmp + 5 * W, pt.cost_gu, pp.xt_gu,
                 pp.base_gu, pp.base_gu_s, pp.tok_w, pt.has_shared, pp.tail_gu != 0, pt.units_gu,
-                pp.grid, pp.cta_gu);
+                pp.grid, 0.f, pp.cta_gu);
     else
       split_one(i - per, pt.n_work, tmp + 3 * W, tmp + W, tmp + 4 * W, tmp + 6 * W, pt.cost_dn,
                 pp.xt_dn, pp.base_dn, pp.base_dn_s, pp.tok_w, pt.has_shared, pp.tail_dn != 0,
-                pt.units_dn, pp.grid, pp.cta_dn);
+                pt.units_dn, pp.grid, pp.tail_dn ? 0.f : kDownSkew, pp.cta_dn);
   }
   if (threadIdx.x == 0) {
     Plan p;
