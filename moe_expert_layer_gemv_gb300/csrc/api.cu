@@ -236,6 +236,10 @@ moe_status_t expert_plan(const moe_dims_t& dm, void* ws, const Layout& L, int sm
   // that of a three-token shared-expert gate_up unit (16 + 16 rows against 4
   // row pairs) and of two four-token shared down units (128 rows against 8).
   pp.tok_w = fmt ? 0 : 1;
+  // int4 layers number their units tile-major: the re-reads of a weight tile
+  // by an expert's further token groups come from L2 (timed: the bf16
+  // layers, whose units cost more per token, do better group-major).
+  pp.tile_major = fmt ? 1 : 0;
   // Dynamic tails (kStaticShare) pay on long stages only: a stage's end
   // spread is about a tenth of its length, while a tail costs a ticket round
   // trip at the end of every CTA -- and, for gate_up, the down stage's head
@@ -313,6 +317,7 @@ moe_status_t run_experts(const moe_dims_t& dm, const void* x, const float* topk_
     sp_dn.base = ep.pp.base_dn;
     sp_dn.base_s = ep.pp.base_dn_s;
     sp_gu.tok_w = sp_dn.tok_w = ep.pp.tok_w;
+    sp_gu.tile_major = sp_dn.tile_major = ep.pp.tile_major;
     sp_gu.tail = ep.pp.tail_gu;
     sp_dn.tail = ep.pp.tail_dn;
     // The down stage leaves the aligned layout in the workspace.

@@ -228,22 +228,30 @@ __device__ __forceinline__ int split_target(int c, int grid, int cost, bool tail
 }
 
 // First unit of the work expert whose estimated costs start at c0 (units from
-// u0; n tokens in groups of xt, `tiles` row tiles per group, cost base + tw x
-// tokens per unit, base >= 1) at which the running cost reaches `target`.
+// u0; n tokens in groups of xt, all full but the last; a unit costs base + tw
+// x its tokens, base >= 1) at which the running cost reaches `target`.  Units
+// are numbered group-major (unit = grp * tiles + tile) or, with tile_major,
+// tile-major (unit = tile * groups + grp).
 __device__ __forceinline__ int unit_at_cost(int target, int c0, int u0, int tiles, int n, int xt,
-                                            int base, int tw) {
+                                            int base, int tw, bool tile_major) {
   const int groups = (n + xt - 1) / xt;
   const int nt_last = n - (groups - 1) * xt;
-  const int per_full = tiles * (base + tw * xt);
+  const int full = base + tw * xt;  // cost of a full group's unit
   const int r = target - c0;
+  if (tile_major) {
+    const int per_tile = (groups - 1) * full + base + tw * nt_last;
+    const int t = min(r / per_tile, tiles - 1);
+    const int g = min((r - t * per_tile) / full, groups - 1);
+    return u0 + t * groups + g;
+  }
+  const int per_full = tiles * full;
   int g, t;
   if (groups > 1 && r < (groups - 1) * per_full) {
     g = r / per_full;
-    t = (r - g * per_full) / (base + tw * xt);
+    t = (r - g * per_full) / full;
   } else {
     g = groups - 1;
-    t = (r - (groups - 1) * per_full) / (base + tw * nt_last);
-    t = min(t, tiles - 1);
+    t = min((r - (groups - 1) * per_full) / (base + tw * nt_last), tiles - 1);
   }
   return u0 + g * tiles + t;
 }

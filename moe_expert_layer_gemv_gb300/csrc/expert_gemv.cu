@@ -87,8 +87,11 @@ struct DnArgs {
 };
 
 // Walks the work experts along a CTA's contiguous unit range.  Units of one
-// work expert are numbered group-major: unit = grp * tiles + tile, so
-// consecutive units share a token group (same activation rows).  The work
+// work expert are numbered group-major (unit = grp * tiles + tile: consecutive
+// units share a token group, its activation rows) or, in int4 layers,
+// tile-major (unit = tile * groups + grp: an expert with more tokens than a
+// unit takes streams each weight tile once from HBM, and its next token groups
+// read the tile back from L2 right after).  The work
 // experts come from the workspace plan (work != nullptr) or from the CTA's
 // shared-memory plan (wex, wnt), where each expert's first unit and first
 // sorted position follow from the previous expert's.
@@ -98,6 +101,7 @@ struct UnitCursor {
   const int16_t* wnt;      //   and their token counts
   int n_work, tiles_r, tiles_s, xt;
   bool down;
+  bool tile_major;
   int i, ubeg, uend, tiles, groups;
   int expert, n_tok, pos;  // current work expert; pos: its first sorted position
   __device__ __forceinline__ void set(int e, int n) {
@@ -541,7 +545,7 @@ __device__ void smem_plan(CtaRange& range, const SmemPlanArgs sp, int T, int k, 
       w = lo;
       const bool sh = shared_expert && lo == n_work - 1;
       u = unit_at_cost(target, c0[lo], u0[lo], sh ? tiles_s : tiles_r, wnt[lo], xt,
-                       sh ? base_s : base, sh ? 1 : tw);
+                       sh ? base_s : base, sh ? 1 : tw, sp.tile_major != 0);
     }
     if (tid == 0) {
       range.u_begin = u;
@@ -563,23 +567,24 @@ __device__ void smem_plan(CtaRange& range, const SmemPlanArgs sp, int T, int k, 
 }
 
 // Tiled 2D tensor copy of the box at (x, y) into shared memory, completion as
-// transaction bytes on `bar`.
+// transaction bytes on `bar`, with an L2 cache policy.
 __device__ __forceinline__ void tma_box_2d(uint32_t dst, const CUtensorMap* map, int x, int y,
-                                           uint64_t* bar) {
+                                           uint64_t* bar, uint64_t policy) {
   asm volatile(
       "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-      " [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_u32(bar))
+      ".L2::cache_hint [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_u32(bar)), "l"(policy)
       : "memory");
 }
 
 // Tiled 3D tensor copy of the box at (x, y, z).
 __device__ __forceinline__ void tma_box_3d(uint32_t dst, const CUtensorMap* map, int x, int y,
-                                           int z, uint64_t* bar) {
+                                           int z, uint64_t* bar, uint64_t policy) {
   asm volatile(
       "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-      " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(dst),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(smem_u32(bar))
+      ".L2::cache_hint [%0], [%1, {%2, %3, %4}], [%5], %6;" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(smem_u32(bar)),
+      "l"(policy)
       : "memory");
 }
 
@@ -994,6 +999,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
   cur.tiles_s = a.Is > 0 ? (int)ceil_div(a.Is, a.rgs) : 1;
   cur.xt = xt;
   cur.down = false;
+  cur.tile_major = kFmt != 0;
   // This CTA's range, in shared memory (read where needed, not held in
   // registers across the unit loops).
   __shared__ CtaRange rg;
@@ -1061,7 +1067,9 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
       const int s = j % NS, use = j / NS;
       cur.seek(u);
       const int local = u - cur.ubeg;
-      const int grp = local / cur.tiles, tile = local - grp * cur.tiles;
+      const bool tm = cur.tile_major;
+      const int grp = tm ? local % cur.groups : local / cur.tiles;
+      const int tile = tm ? local / cur.groups : local - grp * cur.tiles;
       const bool shared = cur.expert < 0;
       const int RG = shared ? a.rgs : a.rg;
       const int Iw = shared ? a.Is : a.I;
@@ -1086,24 +1094,27 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
       }
       __syncwarp();
       const uint8_t* wbase = shared ? a.sgu : a.gu + (size_t)cur.expert * 2 * a.I * rb;
+      // A weight tile that the expert's next token group reads again (the
+      // next unit) stays in L2; its last read may go first.
+      const uint64_t pol_t = tm && grp + 1 < cur.groups ? pol_x : pol_w;
       int xoff;
       if (kFmt && !shared) {
         // Gate and up codes as one tensor box each (RG rows: I is a multiple
         // of 256, so every unit is whole), their scales as one block each.
         if (lane < 2)
           tma_box_3d(smem_u32(st) + lane * i4g_box_bytes(d, RG), &a.tm_codes, 0,
-                     cur.expert * 2 * a.I + lane * Iw + r0, 0, &full[s]);
+                     cur.expert * 2 * a.I + lane * Iw + r0, 0, &full[s], pol_t);
         else if (lane < 4) {
           const uint8_t* sbase = reinterpret_cast<const uint8_t*>(a.gu_scales) +
                                  ((size_t)cur.expert * 2 * a.I + (lane - 2) * Iw + r0) * sb;
           bulk_g2s(st + 2 * i4g_box_bytes(d, RG) + (lane - 2) * RG * sb, sbase, RG * sb,
-                   &full[s], pol_w);
+                   &full[s], pol_t);
         }
         xoff = i4g_weight_bytes(d, RG);
       } else {
-        if (lane == 0) bulk_g2s(st, wbase + (size_t)r0 * rb, nr * rb, &full[s], pol_w);
+        if (lane == 0) bulk_g2s(st, wbase + (size_t)r0 * rb, nr * rb, &full[s], pol_t);
         if (lane == 1)
-          bulk_g2s(st + RG * rb, wbase + (size_t)(Iw + r0) * rb, nr * rb, &full[s], pol_w);
+          bulk_g2s(st + RG * rb, wbase + (size_t)(Iw + r0) * rb, nr * rb, &full[s], pol_t);
         xoff = 2 * RG * rb;
       }
       // Token rows of this group (looked up once per (work expert, group)),
@@ -1150,7 +1161,9 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
     }
     cur.seek(u);
     const int local = u - cur.ubeg;
-    const int grp = local / cur.tiles, tile = local - grp * cur.tiles;
+    const bool tm = cur.tile_major;
+    const int grp = tm ? local % cur.groups : local / cur.tiles;
+    const int tile = tm ? local / cur.groups : local - grp * cur.tiles;
     const bool shared = cur.expert < 0;
     const int RG = shared ? a.rgs : a.rg;
     const int Iw = shared ? a.Is : a.I;
@@ -1288,6 +1301,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
   cur.tiles_s = a.Is > 0 ? (int)ceil_div(a.d, a.rds) : 1;
   cur.xt = xt;
   cur.down = true;
+  cur.tile_major = kFmt != 0;
   // This CTA's range, in shared memory (read where needed, not held in
   // registers across the unit loops).
   __shared__ CtaRange rg;
@@ -1366,7 +1380,9 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
         const int s = j % NS, use = j / NS;
         cur.seek(u);
         const int local = u - cur.ubeg;
-        const int grp = local / cur.tiles, tile = local - grp * cur.tiles;
+        const bool tm = cur.tile_major;
+        const int grp = tm ? local % cur.groups : local / cur.tiles;
+        const int tile = tm ? local / cur.groups : local - grp * cur.tiles;
         const bool shared = cur.expert < 0;
         const int RD = shared ? a.rds : a.rd;
         const int Iw = shared ? a.Is : a.I;
@@ -1394,20 +1410,23 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
           }
           __syncwarp();
           const uint8_t* wb = shared ? a.sdn : a.dn + (size_t)cur.expert * a.d * rb;
+          // A weight tile that the expert's next token group reads again (the
+          // next unit) stays in L2; its last read may go first.
+          const uint64_t pol_t = tm && grp + 1 < cur.groups ? pol_h : pol_w;
           if (i4) {
             // The code rows as I / 256 swizzled boxes (128 rows each, whatever
             // nr), the scales as one block.
             if (lane < Iw / 256)
               tma_box_2d(smem_u32(st) + lane * kI4DnBox, &a.tm_codes, lane * 128,
-                         cur.expert * a.d + r0, &full[s]);
+                         cur.expert * a.d + r0, &full[s], pol_t);
             if (lane == 31) {
               const uint8_t* sbase =
                   reinterpret_cast<const uint8_t*>(a.dn_scales) + (size_t)cur.expert * a.d * sb;
               bulk_g2s(st + i4d_codes_bytes(Iw), sbase + (size_t)r0 * sb, nr * sb, &full[s],
-                       pol_w);
+                       pol_t);
             }
           } else {
-            if (lane == 0) bulk_g2s(st, wb + (size_t)r0 * rb, nr * rb, &full[s], pol_w);
+            if (lane == 0) bulk_g2s(st, wb + (size_t)r0 * rb, nr * rb, &full[s], pol_t);
           }
         }
         if (pass == 1) {
@@ -1452,7 +1471,9 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
     }
     cur.seek(u);
     const int local = u - cur.ubeg;
-    const int grp = local / cur.tiles, tile = local - grp * cur.tiles;
+    const bool tm = cur.tile_major;
+    const int grp = tm ? local % cur.groups : local / cur.tiles;
+    const int tile = tm ? local / cur.groups : local - grp * cur.tiles;
     const bool shared = cur.expert < 0;
     const int RD = shared ? a.rds : a.rd;
     const int Iw = shared ? a.Is : a.I;

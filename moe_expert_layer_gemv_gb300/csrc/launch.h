@@ -43,6 +43,7 @@ struct PlanParams {
   int base_gu_s;         // same for the shared expert's (bf16) units
   int base_dn_s;
   int tail_gu, tail_dn;  // 1: the stage ends with a dynamic tail (kStaticShare)
+  int tile_major;        // 1: units numbered tile-major (the int4 layers)
   int tok_w;             // cost of a token in a routed unit (0: the tensor-pipe int4
                          // units, whose arithmetic does not grow with their tokens);
                          // a shared-expert unit's tokens cost 1 each
@@ -141,6 +142,7 @@ struct SmemPlanArgs {
   int E, B;                   // experts, align block size
   int base, base_s;           // unit cost bases of this stage: routed, shared expert
   int tok_w;                  // cost of a token in a routed unit (shared-expert units: 1)
+  int tile_major;             // 1: units numbered tile-major (unit_at_cost)
   int tail;                   // 1: the stage ends with a dynamic tail (kStaticShare)
   int32_t* sorted_ids;        // align outputs to write (down stage), or nullptr
   int32_t* block_ids;

@@ -335,8 +335,8 @@ __device__ __forceinline__ int expert_run(int E) { return (E + blockDim.x - 1) /
 // (without a tail: the total of units).
 __device__ void split_one(int c, int n_work, const int* s_cost, const int* s_unit, const int* s_n,
                           const int* s_tiles, int total_cost, int xt, int base,
-                          int base_s, int tw, bool has_shared, bool tail, int total_units,
-                          int grid, float skew, int32_t* cta) {
+                          int base_s, int tw, bool tile_major, bool has_shared, bool tail,
+                          int total_units, int grid, float skew, int32_t* cta) {
   if (n_work == 0) {
     cta[c] = 0;
     cta[grid + 1 + c] = 0;
@@ -355,7 +355,7 @@ __device__ void split_one(int c, int n_work, const int* s_cost, const int* s_uni
   }
   const bool sh = has_shared && lo == n_work - 1;
   cta[c] = c == 0 ? 0 : unit_at_cost(target, s_cost[lo], s_unit[lo], s_tiles[lo], s_n[lo], xt,
-                                      sh ? base_s : base, sh ? 1 : tw);
+                                      sh ? base_s : base, sh ? 1 : tw, tile_major);
   cta[grid + 1 + c] = lo;
 }
 
@@ -506,11 +506,13 @@ __device__ void split_stages(const PlanTotals& pt, int E, const PlanParams& pp, 
   for (int i = threadIdx.x; pp.tc_nb_gu == 0 && i < 2 * per; i += blockDim.x) {
     if (i < per)
       split_one(i, pt.n_work, tmp + 2 * W, tmp, tmp + 4 * W, tmp + 5 * W, pt.cost_gu, pp.xt_gu,
-                pp.base_gu, pp.base_gu_s, pp.tok_w, pt.has_shared, pp.tail_gu != 0, pt.units_gu,
+                pp.base_gu, pp.base_gu_s, pp.tok_w, pp.tile_major != 0, pt.has_shared,
+                pp.tail_gu != 0, pt.units_gu,
                 pp.grid, 0.f, pp.cta_gu);
     else
       split_one(i - per, pt.n_work, tmp + 3 * W, tmp + W, tmp + 4 * W, tmp + 6 * W, pt.cost_dn,
-                pp.xt_dn, pp.base_dn, pp.base_dn_s, pp.tok_w, pt.has_shared, pp.tail_dn != 0,
+                pp.xt_dn, pp.base_dn, pp.base_dn_s, pp.tok_w, pp.tile_major != 0, pt.has_shared,
+                pp.tail_dn != 0,
                 pt.units_dn, pp.grid, pp.tail_dn ? 0.f : kDownSkew, pp.cta_dn);
   }
   if (threadIdx.x == 0) {
