@@ -14,7 +14,8 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libmoe_gb300.so")
-SOURCES = ["api.cu", "route.cu", "expert_gemv.cu", "grouped_tc.cu", "combine.cu", "noalloc.cu"]
+SOURCES = ["api.cu", "route.cu", "expert_gemv.cu", "grouped_tc.cu", "tensor_map.cu", "combine.cu",
+           "noalloc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC,-O2",
          "-Xptxas", "-v", f"-I{os.path.join(ROOT, 'include')}", f"-I{CSRC}"]
