@@ -281,9 +281,10 @@ def run_reference(args, shape):
 def measure(shape, args, dev, world, local, inp0, e2e):
     """Time one workload on this rank's GPU.
 
-    Region A: `steps` layer calls with inputs resident in HBM, as up to 5
-    rounds with an event at each boundary (a round set whose per-round times
-    vary by more than 3 % is run once more).  Region B: the same steps through
+    Region A: `steps` layer calls with inputs resident in HBM between two
+    events (the value), then the same calls as up to 5 rounds with an event at
+    each boundary to check their spread (when the rounds vary by more than 3 %,
+    region A is run once more).  Region B: the same steps through
     moe_layer_forward_timed, events at the stage boundaries (an event between
     two kernels also stops the second from starting early, so stage times
     include each stage's launch; region A has none of that).  Region C (e2e):
@@ -319,21 +320,39 @@ def measure(shape, args, dev, world, local, inp0, e2e):
         b = i % len(xs)
         layers[i % ncopy].forward(xs[b], outs[b], stream=stream)
 
-    for i in range(args.warmup):
-        step(i)
-    torch.cuda.synchronize()
-
     steps = args.steps
     clocks = ClockSampler(local) if e2e else None
     if clocks:
         clocks.start()
         time.sleep(0.3)
+    # The warm-up runs right before the timed region (no idle GPU in between).
+    for i in range(args.warmup):
+        step(i)
+    torch.cuda.synchronize()
     if world > 1:
         dist.barrier()
 
     def region_a():
+        # The timed region: exactly `steps` layer calls between two events, so
+        # that nothing in the stream breaks the programmatic launch chain from
+        # one layer to the next.
         torch.cuda.synchronize()
+        if world > 1:
+            dist.barrier()
         n0 = abi.moe_kernel_launch_count()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for i in range(steps):
+            step(i)
+        e1.record()
+        torch.cuda.synchronize()
+        if world > 1:
+            dist.barrier()
+        ms_a = e0.elapsed_time(e1) / steps
+        n_launch = abi.moe_kernel_launch_count() - n0
+        # Spread check, not part of the value: the same calls again as up to
+        # five rounds with an event at each boundary (each boundary event also
+        # ends one launch chain, so rounds read a little slower than the value).
         nr = min(5, steps)
         cut = [round(r * steps / nr) for r in range(nr + 1)]
         ev = [torch.cuda.Event(enable_timing=True) for _ in range(nr + 1)]
@@ -343,11 +362,9 @@ def measure(shape, args, dev, world, local, inp0, e2e):
                 step(i)
             ev[r + 1].record()
         torch.cuda.synchronize()
-        if world > 1:
-            dist.barrier()
         per = [ev[r].elapsed_time(ev[r + 1]) / (cut[r + 1] - cut[r]) for r in range(nr)]
         cv = statistics.pstdev(per) / statistics.mean(per)
-        return (ev[0].elapsed_time(ev[nr]) / steps, abi.moe_kernel_launch_count() - n0,
+        return (ms_a, n_launch,
                 {"n": nr, "us_per_step": [round(v * 1e3, 2) for v in per],
                  "median_us": statistics.median(per) * 1e3, "cv": cv})
 
