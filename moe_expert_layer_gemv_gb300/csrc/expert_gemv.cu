@@ -737,12 +737,19 @@ __device__ __forceinline__ uint32_t i4d_code_addr(uint32_t codes, int r, int gi,
   return codes + (uint32_t)((gi >> 3) * kI4DnBox + r * 128 + (((gi & 7) ^ (r & 7)) << 4) + 4 * t);
 }
 
+// Column of element c of an int4 layer's h row: each 8-element block is
+// stored in the order 0, 4, 1, 5, 2, 6, 3, 7 -- the k pairs (i, i + 4) of the
+// nibble pairing -- so that one 16-byte load is the four B registers of a
+// group's two down products, with no permute.
+__device__ __forceinline__ int i4h_col(int c) { return (c & ~7) | ((c & 3) << 1) | ((c >> 2) & 1); }
+
 // One consumer warp's m16 tile of an int4 down unit: rows ra and rb (the
 // tile's rows g and g + 8 of lane (g, t)), all I / 32 groups, up to 8 tokens.
 // In an int4 layer h travels as two bf16 planes, hi = bf16(h) and lo = bf16(h
 // - hi), and each group takes one product on each (the pair carries h to about
-// 2^-17): the k positions map onto the codes as in gu_int4_mma.  acc: rows
-// ra, rb x tokens 2t, 2t + 1.
+// 2^-17): the k positions map onto the codes as in gu_int4_mma, and the h
+// rows are stored in that order (i4h_col).  acc: rows ra, rb x tokens 2t,
+// 2t + 1.
 __device__ __forceinline__ void dn_int4_mma(uint32_t codes, int ra, int rb, int t, uint32_t sa,
                                             uint32_t sb, uint32_t hh, uint32_t hl, bool has_h,
                                             int ng, float (&acc)[4]) {
@@ -759,14 +766,10 @@ __device__ __forceinline__ void dn_int4_mma(uint32_t codes, int ra, int rb, int 
     dequant_pairs(va, qa);
     dequant_pairs(vb, qb);
     float p[4];
-    mma_16816(p, qa[0], qb[0], qa[1], qb[1], __byte_perm(H.x, H.z, 0x5410),
-              __byte_perm(H.x, H.z, 0x7632), zero);
-    mma_16816(p, qa[2], qb[2], qa[3], qb[3], __byte_perm(H.y, H.w, 0x5410),
-              __byte_perm(H.y, H.w, 0x7632), p);
-    mma_16816(p, qa[0], qb[0], qa[1], qb[1], __byte_perm(L.x, L.z, 0x5410),
-              __byte_perm(L.x, L.z, 0x7632), p);
-    mma_16816(p, qa[2], qb[2], qa[3], qb[3], __byte_perm(L.y, L.w, 0x5410),
-              __byte_perm(L.y, L.w, 0x7632), p);
+    mma_16816(p, qa[0], qb[0], qa[1], qb[1], H.x, H.y, zero);
+    mma_16816(p, qa[2], qb[2], qa[3], qb[3], H.z, H.w, p);
+    mma_16816(p, qa[0], qb[0], qa[1], qb[1], L.x, L.y, p);
+    mma_16816(p, qa[2], qb[2], qa[3], qb[3], L.z, L.w, p);
     acc[0] = fmaf(p[0], fa, acc[0]);
     acc[1] = fmaf(p[1], fa, acc[1]);
     acc[2] = fmaf(p[2], fb, acc[2]);
@@ -1215,9 +1218,10 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
       __syncwarp();
       if (lane == 0) mbar_arrive(&red_empty[buf]);
       if (r8 + g < nr) {
-        // h as two bf16 planes: hi = bf16(h), lo = bf16(h - hi).
-        uint16_t* hh =
-            reinterpret_cast<uint16_t*>(a.h) + (size_t)(cur.pos + g0) * a.I + r0 + r8 + g;
+        // h as two bf16 planes: hi = bf16(h), lo = bf16(h - hi), each row in
+        // the down products' k order (i4h_col).
+        uint16_t* hh = reinterpret_cast<uint16_t*>(a.h) + (size_t)(cur.pos + g0) * a.I +
+                       i4h_col(r0 + r8 + g);
         uint16_t* hl = hh + (size_t)a.h_rows * a.I;
 #pragma unroll
         for (int c = 0; c < 2; ++c) {
