@@ -87,6 +87,10 @@ def test_layer_parity_prefill_full():
     ({"T": 33, "d": 1032, "E": 70, "k": 5, "I": 200, "Is": 56, "block": 64}, 5),
     ({"T": 17, "d": 512, "E": 8, "k": 8, "I": 64, "Is": 0}, 6),      # k == E
     ({"T": 130, "d": 256, "E": 32, "k": 4, "I": 72, "Is": 40, "block": 128}, 7),  # T > fused top-k
+    # rows so short that the expert stages' rings cannot hold the shared-memory
+    # plan of 2048 slots over 512 experts: the routing kernel's last token tile
+    # (of 16) runs the align and the workspace plan
+    ({"T": 128, "d": 64, "E": 512, "k": 16, "I": 16, "Is": 16}, 8),
 ])
 def test_layer_parity_ragged_and_edges(over, seed):
     layer_parity(I.make_inputs(I.shape("verify_t8", **over), seed))
