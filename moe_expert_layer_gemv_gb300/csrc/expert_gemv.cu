@@ -7,22 +7,24 @@
 //
 // Structure (both stages): a persistent grid of kCtasPerSm CTAs per SM.  Work
 // is cut into units = (work expert, token group, row tile); each CTA takes one
-// contiguous range of units of about equal estimated cost, so consecutive
-// units mostly share an expert and a token group.  At decode sizes every CTA
+// contiguous range of units of about equal estimated cost (and, on long
+// stages, units of the dynamic tail one at a time).  At decode sizes every CTA
 // derives the plan (align layout, work list, its range) from the routing ids
-// in its own shared memory (smem_plan); otherwise it reads the plan the align
-// step wrote to the workspace.  The
-// last warp of a CTA is the producer: one bulk copy (cp.async.bulk, the
-// non-tensor TMA) per weight block and per activation row lands a unit in a
-// shared-memory ring stage and completes the stage's mbarrier by transaction
-// bytes.  The other warps consume: fp32 dot products out of shared memory with
-// several independent accumulators per output, warp-shuffle reductions, the
-// SwiGLU (gate_up) or the per-slot output write (down), then release the stage.
-// The number of tokens a consumer warp handles in a unit is a template
-// parameter, so the inner loops carry no per-token branches.
-// int4 weights are dequantised in registers: (nibble - 8) accumulated against
-// the activations per group of 32, times the group's bf16 scale (W4A16 routed
-// experts: "Qwen3.8 Flash-Next - GB10 UltraFast", How it works).
+// in its own shared memory (smem_plan; one warp for up to 64 slots);
+// otherwise it reads the plan the align step wrote to the workspace.  The last
+// warp of a CTA is the producer: bulk copies (bf16 weight blocks, activation
+// rows) and tiled tensor copies (int4 code boxes, 128-byte swizzle) land a unit
+// in a shared-memory ring stage and complete the stage's mbarrier by
+// transaction bytes.  The other warps consume, then release the stage:
+// - bf16: fp32 dot products out of shared memory (packed fp32 fma, several
+//   accumulators per output, warp-shuffle reductions), the token count a
+//   template parameter so the inner loops carry no per-token branches;
+// - int4: the codes dequantised in registers (two nibbles per bf16 pair, one
+//   packed fma) and multiplied on the tensor pipe (mma.sync m16n8k16, bf16,
+//   fp32 accumulation), each group's products scaled by its bf16 scale (W4A16
+//   routed experts, group size 32: "Qwen3.8 Flash-Next - GB10 UltraFast", How
+//   it works; Manual).
+// Then the SwiGLU (gate_up) or the per-slot output write (down).
 #include <cuda_bf16.h>
 
 #include <cstring>
@@ -683,8 +685,9 @@ __host__ __device__ constexpr int i4g_weight_bytes(int d, int rg) { return rg * 
 // the tile's k positions map onto them as (8t, 8t + 4), (8t + 1, 8t + 5) for the
 // first product and (8t + 2, 8t + 6), (8t + 3, 8t + 7) for the second; the
 // activations are permuted to match.  Each group's two products start from
-// zero and are scaled by the rows' bf16 scales into the fp32 accumulators: the
-// same regrouping (sum of code x activation, then x scale) as the scalar path.
+// zero and are scaled by the rows' bf16 scales into the fp32 accumulators: per
+// group, the sum of code x activation, then x scale (the definition regrouped,
+// exact up to rounding order).
 // codes: the stage (RG rows per box); sg, su: the gate and up scales of row
 // r8 + g; xr: token g's row at thread t's 16 bytes.
 __device__ __forceinline__ void gu_int4_mma(uint32_t codes, int d, int RG, int r8, int g, int t,
