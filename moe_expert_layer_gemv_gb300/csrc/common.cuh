@@ -256,6 +256,19 @@ __device__ __forceinline__ int unit_at_cost(int target, int c0, int u0, int tile
   return u0 + g * tiles + t;
 }
 
+// Atomic add at GPU scope with acquire-release semantics: the releasing side of
+// an arrival counter (stores ordered before it -- by this thread, or by the
+// CTA through a preceding barrier -- are published with it) and the acquiring
+// side for the last arrival.
+__device__ __forceinline__ int atom_add_acq_rel_gpu(int* p, int v) {
+  int old;
+  asm volatile("atom.acq_rel.gpu.global.add.s32 %0, [%1], %2;"
+               : "=r"(old)
+               : "l"(p), "r"(v)
+               : "memory");
+  return old;
+}
+
 // ---------------------------------------------------------------- misc
 __host__ __device__ constexpr int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 __host__ __device__ constexpr int64_t round_up(int64_t a, int64_t b) { return ceil_div(a, b) * b; }

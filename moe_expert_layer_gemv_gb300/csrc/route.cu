@@ -755,16 +755,17 @@ __global__ void __launch_bounds__(kRouterThreads, NV >= 32 ? 1 : 2) route_kernel
   pdl_trigger();
 
   // Arrival on this token tile; the last CTA to arrive selects its top-k.
-  __threadfence();
+  // The barrier orders the CTA's logit stores before thread 0's arrival, whose
+  // release publishes them; the last arrival's acquire, passed on by the
+  // second barrier, makes every CTA's logits of the tile visible here.
   __syncthreads();
   if (threadIdx.x == 0) {
-    const int old = atomicAdd(&a.counters[1 + blockIdx.y], 1);
+    const int old = atom_add_acq_rel_gpu(&a.counters[1 + blockIdx.y], 1);
     s_last = old == (int)gridDim.x - 1;
     if (s_last) a.counters[1 + blockIdx.y] = 0;  // ready for the next call
   }
   __syncthreads();
   if (!s_last) return;
-  __threadfence();
   const int t = blockIdx.y * kRouterTokens + (threadIdx.x >> 5);
   // With one token tile this CTA runs the align too: the ids go straight to
   // its shared-memory slots (the router's x tile there is no longer needed).
