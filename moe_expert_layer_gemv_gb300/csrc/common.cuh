@@ -221,7 +221,8 @@ constexpr float kDownSkew = 0.15f;
 // G(c / grid) * share * cost, G(x) = (1 + s) x - s x^2 (s = skew; G(x) = x
 // without one); with a tail (share < 1) the tail starts at the cost share *
 // cost, without one (share 1) the last CTA ends at the last unit.
-__device__ __forceinline__ int split_target(int c, int grid, int cost, bool tail, float skew) {
+__host__ __device__ __forceinline__ int split_target(int c, int grid, int cost, bool tail,
+                                                   float skew) {
   const int fcost = tail ? (int)(kStaticShare * (float)cost) : cost;
   const float x = (float)c / (float)grid;
   return min(fcost, (int)(((1.0f + skew) * x - skew * x * x) * (float)fcost));
@@ -232,8 +233,8 @@ __device__ __forceinline__ int split_target(int c, int grid, int cost, bool tail
 // x its tokens, base >= 1) at which the running cost reaches `target`.  Units
 // are numbered group-major (unit = grp * tiles + tile) or, with tile_major,
 // tile-major (unit = tile * groups + grp).
-__device__ __forceinline__ int unit_at_cost(int target, int c0, int u0, int tiles, int n, int xt,
-                                            int base, int tw, bool tile_major) {
+__host__ __device__ __forceinline__ int unit_at_cost(int target, int c0, int u0, int tiles, int n,
+                                                     int xt, int base, int tw, bool tile_major) {
   const int groups = (n + xt - 1) / xt;
   const int nt_last = n - (groups - 1) * xt;
   const int full = base + tw * xt;  // cost of a full group's unit
