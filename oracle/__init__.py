@@ -34,14 +34,15 @@ class Dims(C.Structure):
 
 class Experts(C.Structure):
     _fields_ = [("format", C.c_int32), ("group", C.c_int32), ("gate_up", C.c_void_p),
-                ("gate_up_scales", C.c_void_p), ("down", C.c_void_p), ("down_scales", C.c_void_p)]
+                ("gate_up_scales", C.c_void_p), ("down", C.c_void_p), ("down_scales", C.c_void_p),
+                ("gate_up_global", C.c_void_p), ("down_global", C.c_void_p)]
 
 
 class Shared(C.Structure):
     _fields_ = [("gate_up", C.c_void_p), ("down", C.c_void_p), ("gate_w", C.c_void_p)]
 
 
-BF16, INT4, F64 = 0, 1, 2
+BF16, INT4, F64, FP8, NVFP4 = 0, 1, 2, 3, 4
 
 _P = C.c_void_p
 
@@ -52,6 +53,12 @@ def _declare(L):
     L.moe_oracle_decode_bf16.argtypes = [C.c_size_t, _P, _P]
     L.moe_oracle_decode_bf16.restype = None
     L.moe_oracle_dequant_int4.argtypes = [C.c_int32, C.c_int32, C.c_int32, _P, _P, _P]
+    L.moe_oracle_e4m3_to_f64.argtypes = [C.c_uint8]
+    L.moe_oracle_e4m3_to_f64.restype = C.c_double
+    L.moe_oracle_e2m1_to_f64.argtypes = [C.c_uint8]
+    L.moe_oracle_e2m1_to_f64.restype = C.c_double
+    L.moe_oracle_dequant_fp8.argtypes = [C.c_int32, C.c_int32, C.c_int32, _P, _P, _P]
+    L.moe_oracle_dequant_nvfp4.argtypes = [C.c_int32, C.c_int32, C.c_int32, _P, _P, C.c_float, _P]
     L.moe_oracle_router_logits.argtypes = [C.c_int32, C.c_int32, C.c_int32, _P, _P, _P]
     L.moe_oracle_router_logits.restype = None
     L.moe_oracle_topk.argtypes = [C.c_int32, C.c_int32, C.c_int32, C.c_int32, _P, _P, _P, _P, _P]
@@ -93,6 +100,37 @@ def dequant_int4(codes, scales, cols: int, group: int) -> np.ndarray:
     rc = lib().moe_oracle_dequant_int4(rows, cols, group, _ptr(codes), _ptr(scales), _ptr(out))
     if rc:
         raise ValueError(f"moe_oracle_dequant_int4 failed ({rc})")
+    return out.reshape(codes.shape[:-1] + (cols,))
+
+
+def e4m3_to_f64(b: int) -> float:
+    return float(lib().moe_oracle_e4m3_to_f64(int(b)))
+
+
+def e2m1_to_f64(code: int) -> float:
+    return float(lib().moe_oracle_e2m1_to_f64(int(code)))
+
+
+def dequant_fp8(codes, scales, cols: int, group: int) -> np.ndarray:
+    codes = _c(codes, np.uint8)
+    scales = _c(scales, np.uint16)
+    rows = codes.size // cols
+    out = np.empty((rows, cols), np.float64)
+    rc = lib().moe_oracle_dequant_fp8(rows, cols, group, _ptr(codes), _ptr(scales), _ptr(out))
+    if rc:
+        raise ValueError(f"moe_oracle_dequant_fp8 failed ({rc})")
+    return out.reshape(codes.shape[:-1] + (cols,))
+
+
+def dequant_nvfp4(codes, scales, global_scale: float, cols: int, group: int) -> np.ndarray:
+    codes = _c(codes, np.uint8)
+    scales = _c(scales, np.uint8)
+    rows = codes.size // (cols // 2)
+    out = np.empty((rows, cols), np.float64)
+    rc = lib().moe_oracle_dequant_nvfp4(rows, cols, group, _ptr(codes), _ptr(scales),
+                                        float(global_scale), _ptr(out))
+    if rc:
+        raise ValueError(f"moe_oracle_dequant_nvfp4 failed ({rc})")
     return out.reshape(codes.shape[:-1] + (cols,))
 
 
@@ -185,24 +223,30 @@ def layer(x_bits, router_bits, experts: dict, shared, dims: dict, ids_override=N
     """Full layer.
 
     x_bits uint16[T,d]; router_bits uint16[E,d].
-    experts: {"format": BF16|INT4|F64, "group": g, "gate_up": arr, "down": arr,
-              "gate_up_scales": arr|None, "down_scales": arr|None}
+    experts: {"format": BF16|INT4|F64|FP8|NVFP4, "group": g, "gate_up": arr, "down": arr,
+              "gate_up_scales": arr|None, "down_scales": arr|None,
+              "gate_up_global": f32[E]|None, "down_global": f32[E]|None (NVFP4)}
     shared:  None or {"gate_up": uint16[2Is,d], "down": uint16[d,Is], "gate_w": uint16[d]}
     dims:    {"T","d","E","k","I","Is","renormalize"}
     Returns {"out": f64[n,d], "ids", "w", "margin", "sg"} for the listed tokens.
     """
     fmt = experts.get("format", BF16)
-    dt = {BF16: np.uint16, INT4: np.uint8, F64: np.float64}[fmt]
+    dt = {BF16: np.uint16, INT4: np.uint8, F64: np.float64, FP8: np.uint8, NVFP4: np.uint8}[fmt]
+    st = np.uint8 if fmt == NVFP4 else np.uint16  # E4M3 block scales, else bf16
     gu = _c(experts["gate_up"], dt)
     dn = _c(experts["down"], dt)
-    gus = None if experts.get("gate_up_scales") is None else _c(experts["gate_up_scales"], np.uint16)
-    dns = None if experts.get("down_scales") is None else _c(experts["down_scales"], np.uint16)
-    ex = Experts(fmt, int(experts.get("group", 0)), _ptr(gu), _ptr(gus), _ptr(dn), _ptr(dns))
+    gus = None if experts.get("gate_up_scales") is None else _c(experts["gate_up_scales"], st)
+    dns = None if experts.get("down_scales") is None else _c(experts["down_scales"], st)
+    gug = None if experts.get("gate_up_global") is None else _c(experts["gate_up_global"],
+                                                                np.float32)
+    dng = None if experts.get("down_global") is None else _c(experts["down_global"], np.float32)
+    ex = Experts(fmt, int(experts.get("group", 0)), _ptr(gu), _ptr(gus), _ptr(dn), _ptr(dns),
+                 _ptr(gug), _ptr(dng))
     x_bits = _c(x_bits, np.uint16)
     router_bits = _c(router_bits, np.uint16)
     dm = Dims(dims["T"], dims["d"], dims["E"], dims["k"], dims["I"],
               dims.get("Is", 0) if shared is not None else 0, int(dims.get("renormalize", 1)))
-    keep = [gu, dn, gus, dns]
+    keep = [gu, dn, gus, dns, gug, dng]
     sh_ptr = None
     if shared is not None:
         sgu = _c(shared["gate_up"], np.uint16)

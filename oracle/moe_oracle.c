@@ -48,6 +48,71 @@ int moe_oracle_dequant_int4(int32_t rows, int32_t cols, int32_t group,
   return 0;
 }
 
+/* One FP8 E4M3 byte: sign bit, 4 exponent bits with bias 7, 3 mantissa bits;
+ * exponent 0 holds the subnormals m * 2^-9; S.1111.111 is NaN; there is no
+ * infinity (the OCP 8-bit floating-point format E4M3). */
+double moe_oracle_e4m3_to_f64(uint8_t b) {
+  const int sign = b >> 7, e = (b >> 3) & 15, m = b & 7;
+  double v;
+  if (e == 15 && m == 7) return NAN;
+  if (e == 0)
+    v = ldexp((double)m, -9);
+  else
+    v = ldexp(1.0 + (double)m / 8.0, e - 7);
+  return sign ? -v : v;
+}
+
+/* One FP4 E2M1 code (low 4 bits): sign bit, 2 exponent bits with bias 1, 1
+ * mantissa bit; exponent 0 holds the subnormal m * 0.5; no NaN or infinity:
+ * magnitudes 0, 0.5, 1, 1.5, 2, 3, 4, 6. */
+double moe_oracle_e2m1_to_f64(uint8_t code) {
+  const int sign = (code >> 3) & 1, e = (code >> 1) & 3, m = code & 1;
+  double v;
+  if (e == 0)
+    v = 0.5 * (double)m;
+  else
+    v = ldexp(1.0 + (double)m / 2.0, e - 1);
+  return sign ? -v : v;
+}
+
+/* One FP8 element: byte c of the row (E4M3) times the bf16 scale of its group
+ * of `group` consecutive elements along the row. */
+static double fp8_elem(const uint8_t* codes, const uint16_t* scales, size_t row, int32_t cols,
+                       int32_t group, int32_t c) {
+  double s = moe_oracle_bf16_to_f64(scales[row * (size_t)(cols / group) + (size_t)(c / group)]);
+  return moe_oracle_e4m3_to_f64(codes[row * (size_t)cols + (size_t)c]) * s;
+}
+
+/* One NVFP4 element: E2M1 code in byte c/2 of the row (low nibble for even c,
+ * high for odd), times the E4M3 scale of its block of `group` consecutive
+ * elements, times the matrix's fp32 scale. */
+static double nvfp4_elem(const uint8_t* codes, const uint8_t* scales, double global, size_t row,
+                         int32_t cols, int32_t group, int32_t c) {
+  uint8_t byte = codes[row * (size_t)(cols / 2) + (size_t)(c / 2)];
+  uint8_t code = (c & 1) ? (uint8_t)(byte >> 4) : (uint8_t)(byte & 15);
+  double s = moe_oracle_e4m3_to_f64(scales[row * (size_t)(cols / group) + (size_t)(c / group)]);
+  return moe_oracle_e2m1_to_f64(code) * s * global;
+}
+
+int moe_oracle_dequant_fp8(int32_t rows, int32_t cols, int32_t group, const uint8_t* codes,
+                           const uint16_t* scales, double* out) {
+  if (rows < 0 || cols <= 0 || group <= 0 || cols % group) return -1;
+  for (int32_t r = 0; r < rows; ++r)
+    for (int32_t c = 0; c < cols; ++c)
+      out[(size_t)r * cols + c] = fp8_elem(codes, scales, (size_t)r, cols, group, c);
+  return 0;
+}
+
+int moe_oracle_dequant_nvfp4(int32_t rows, int32_t cols, int32_t group, const uint8_t* codes,
+                             const uint8_t* scales, float global, double* out) {
+  if (rows < 0 || cols <= 0 || cols % 2 || group <= 0 || cols % group) return -1;
+  for (int32_t r = 0; r < rows; ++r)
+    for (int32_t c = 0; c < cols; ++c)
+      out[(size_t)r * cols + c] =
+          nvfp4_elem(codes, scales, (double)global, (size_t)r, cols, group, c);
+  return 0;
+}
+
 void moe_oracle_router_logits(int32_t T, int32_t d, int32_t E, const double* x,
                               const double* wr, double* logits) {
   for (int32_t t = 0; t < T; ++t)
@@ -202,8 +267,9 @@ void moe_oracle_combine(int32_t T, int32_t k, int32_t d, const double* w,
     }
 }
 
-/* Row `row` of a routed weight matrix with `cols` columns, decoded to double. */
-static void expert_row(const moe_oracle_experts* ex, int which, size_t row,
+/* Row `row` (of expert e) of a routed weight matrix with `cols` columns,
+ * decoded to double. */
+static void expert_row(const moe_oracle_experts* ex, int which, int32_t e, size_t row,
                        int32_t cols, double* dst) {
   const void* base = which ? ex->down : ex->gate_up;
   const void* sc = which ? ex->down_scales : ex->gate_up_scales;
@@ -213,6 +279,14 @@ static void expert_row(const moe_oracle_experts* ex, int which, size_t row,
     for (int32_t c = 0; c < cols; ++c)
       dst[c] = int4_elem((const uint8_t*)base, (const uint16_t*)sc, row, cols,
                          ex->group, c);
+  } else if (ex->format == MOE_ORACLE_FP8) {
+    for (int32_t c = 0; c < cols; ++c)
+      dst[c] = fp8_elem((const uint8_t*)base, (const uint16_t*)sc, row, cols, ex->group, c);
+  } else if (ex->format == MOE_ORACLE_NVFP4) {
+    const double global = (double)(which ? ex->down_global : ex->gate_up_global)[e];
+    for (int32_t c = 0; c < cols; ++c)
+      dst[c] = nvfp4_elem((const uint8_t*)base, (const uint8_t*)sc, global, row, cols,
+                          ex->group, c);
   } else {
     memcpy(dst, (const double*)base + row * cols, sizeof(double) * (size_t)cols);
   }
@@ -222,9 +296,9 @@ static void expert_row(const moe_oracle_experts* ex, int which, size_t row,
 static void expert_dense(const moe_oracle_experts* ex, int32_t e, int32_t d,
                          int32_t I, double* wgu, double* wd) {
   for (int32_t r = 0; r < 2 * I; ++r)
-    expert_row(ex, 0, (size_t)e * 2 * I + r, d, wgu + (size_t)r * d);
+    expert_row(ex, 0, e, (size_t)e * 2 * I + r, d, wgu + (size_t)r * d);
   for (int32_t r = 0; r < d; ++r)
-    expert_row(ex, 1, (size_t)e * d + r, I, wd + (size_t)r * I);
+    expert_row(ex, 1, e, (size_t)e * d + r, I, wd + (size_t)r * I);
 }
 
 int moe_oracle_max_threads(void) {
@@ -243,8 +317,11 @@ int moe_oracle_layer(const moe_oracle_dims* dm, const uint16_t* x,
                      double* margin_out, double* sg_out, int32_t nthreads) {
   const int32_t T = dm->T, d = dm->d, E = dm->E, k = dm->k, I = dm->I, Is = dm->Is;
   if (T < 0 || d <= 0 || E <= 0 || k <= 0 || k > E || I <= 0 || Is < 0) return -1;
-  if (ex->format == MOE_ORACLE_INT4 &&
+  if ((ex->format == MOE_ORACLE_INT4 || ex->format == MOE_ORACLE_NVFP4) &&
       (ex->group <= 0 || d % ex->group || I % ex->group || d % 2 || I % 2)) return -1;
+  if (ex->format == MOE_ORACLE_FP8 && (ex->group <= 0 || d % ex->group || I % ex->group))
+    return -1;
+  if (ex->format == MOE_ORACLE_NVFP4 && (!ex->gate_up_global || !ex->down_global)) return -1;
   if (!token_list) n = T;
   if (n < 0) return -1;
   const int use_shared = (sh != NULL && Is > 0);

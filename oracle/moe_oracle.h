@@ -25,9 +25,16 @@
  *   int4    = symmetric 4-bit codes, one bf16 scale per group of 32 along the
  *             reduction dim (W4A16 routed experts: Flash-Next, "How it works";
  *             group size 32: Flash-Next, "Manual")
+ *   fp8     = E4M3 codes, one bf16 scale per group along the reduction dim
+ *   nvfp4   = E2M1 codes, one E4M3 scale per block of 16 along the reduction
+ *             dim and one fp32 scale per expert matrix (the "NVFP4/FP8
+ *             families" of veloGB10's README; the block layouts are not on the
+ *             pages: these are the plainest readings, the int4 grouping for
+ *             fp8 and the usual 16-element blocks with an FP8 block scale and a
+ *             per-tensor scale for NVFP4)
  *
- * Every floating-point step is done in IEEE double.  bf16 and int4 inputs are
- * decoded exactly.  There is no blocking, fusion or reordering beyond the plain
+ * Every floating-point step is done in IEEE double.  bf16, int4, E4M3 and
+ * E2M1 inputs are decoded exactly.  There is no blocking, fusion or reordering beyond the plain
  * definition: dot products run in ascending index order.
  *
  * Parity pins (each function is checked against something other than itself by
@@ -35,7 +42,9 @@
  * the softmax/renormalisation special cases, a stable library sort for the
  * align layout, a torch fp64 dense SwiGLU for the expert, a dense-mixture
  * restatement and an identity expert for the combine, an independent numpy
- * dequantisation for int4.
+ * dequantisation for int4, torch's float8_e4m3fn on all 256 E4M3 codes, the
+ * E2M1 value table, and the layer in each quantised format against the same
+ * layer on independently dequantised fp64 weights.
  */
 #ifndef MOE_ORACLE_H
 #define MOE_ORACLE_H
@@ -55,7 +64,13 @@ typedef struct {
 } moe_oracle_dims;
 
 /* Routed-expert weight storage formats. */
-enum { MOE_ORACLE_BF16 = 0, MOE_ORACLE_INT4 = 1, MOE_ORACLE_F64 = 2 };
+enum {
+  MOE_ORACLE_BF16 = 0,
+  MOE_ORACLE_INT4 = 1,
+  MOE_ORACLE_F64 = 2,
+  MOE_ORACLE_FP8 = 3,
+  MOE_ORACLE_NVFP4 = 4
+};
 
 /* Routed expert weights.
  *   BF16: gate_up uint16 bf16 bits [E][2I][d], down [E][d][I]; scales NULL.
@@ -63,7 +78,15 @@ enum { MOE_ORACLE_BF16 = 0, MOE_ORACLE_INT4 = 1, MOE_ORACLE_F64 = 2 };
  *         byte, even element in the low nibble, stored offset-binary u = q+8.
  *         gate_up_scales bf16 [E][2I][d/group], down_scales bf16 [E][d][I/group].
  *         Element value = (u - 8) * scale.
- *   F64 : gate_up double [E][2I][d], down double [E][d][I] (test hook). */
+ *   F64 : gate_up double [E][2I][d], down double [E][d][I] (test hook).
+ *   FP8 : gate_up uint8 E4M3 [E][2I][d], down uint8 [E][d][I];
+ *         gate_up_scales bf16 [E][2I][d/group], down_scales bf16 [E][d][I/group].
+ *         Element value = e4m3(code) * scale.
+ *   NVFP4: gate_up uint8 [E][2I][d/2], down uint8 [E][d][I/2]: two E2M1 codes
+ *         per byte, even element in the low nibble; gate_up_scales uint8 E4M3
+ *         [E][2I][d/group], down_scales [E][d][I/group]; gate_up_global,
+ *         down_global fp32 [E].  Element value = e2m1(code) * e4m3(scale) *
+ *         global[expert]. */
 typedef struct {
   int32_t format;
   int32_t group;
@@ -71,6 +94,8 @@ typedef struct {
   const void* gate_up_scales;
   const void* down;
   const void* down_scales;
+  const float* gate_up_global; /* NVFP4 only, else NULL */
+  const float* down_global;
 } moe_oracle_experts;
 
 /* Shared expert, bf16 bits: gate_up [2Is][d], down [d][Is], gate_w [d]. */
@@ -90,6 +115,16 @@ void moe_oracle_decode_bf16(size_t n, const uint16_t* in, double* out);
 int moe_oracle_dequant_int4(int32_t rows, int32_t cols, int32_t group,
                             const uint8_t* codes, const uint16_t* scales,
                             double* out);
+/* Exact E4M3 byte -> double (NaN for S.1111.111). */
+double moe_oracle_e4m3_to_f64(uint8_t b);
+/* Exact E2M1 code (low 4 bits) -> double. */
+double moe_oracle_e2m1_to_f64(uint8_t code);
+/* Dequantise an FP8 matrix [rows][cols] (layout as above) to double. */
+int moe_oracle_dequant_fp8(int32_t rows, int32_t cols, int32_t group, const uint8_t* codes,
+                           const uint16_t* scales, double* out);
+/* Dequantise an NVFP4 matrix [rows][cols] with matrix scale `global`. */
+int moe_oracle_dequant_nvfp4(int32_t rows, int32_t cols, int32_t group, const uint8_t* codes,
+                             const uint8_t* scales, float global, double* out);
 
 /* logits[t][e] = sum_i x[t][i] * wr[e][i], ascending i, fp64. */
 void moe_oracle_router_logits(int32_t T, int32_t d, int32_t E, const double* x,

@@ -405,3 +405,135 @@ def test_margin_is_kth_minus_next_logit():
     L = inp["x"].to(torch.float64) @ inp["router_w"].to(torch.float64).T
     srt = torch.sort(L, dim=1, descending=True).values
     np.testing.assert_allclose(res["margin"], (srt[:, 1] - srt[:, 2]).numpy(), rtol=1e-12)
+
+
+# ----------------------------------------------------------------------------- fp8 / nvfp4
+# Block-scaled weight formats ("veloGB10": the NVFP4/FP8 weight families it
+# serves).  The element decodes are pinned against torch's float8_e4m3fn and
+# against the E2M1 value table of the format's definition; the layer in each
+# format against the same layer on independently dequantised fp64 weights.
+
+E2M1_MAGNITUDES = [0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0]
+
+
+def test_e4m3_decode_matches_torch_on_every_code():
+    codes = torch.arange(256, dtype=torch.uint8)
+    ref = codes.view(torch.float8_e4m3fn).to(torch.float64).tolist()
+    got = [oracle.e4m3_to_f64(b) for b in range(256)]
+    for b in range(256):
+        if math.isnan(ref[b]):
+            assert math.isnan(got[b]) and (b & 0x7F) == 0x7F, hex(b)
+        else:
+            assert got[b] == ref[b] and math.copysign(1, got[b]) == math.copysign(1, ref[b]), hex(b)
+    # the format's landmarks: smallest subnormal, smallest normal, one, largest
+    assert got[0x01] == 2.0 ** -9 and got[0x08] == 2.0 ** -6
+    assert got[0x38] == 1.0 and got[0x7E] == 448.0
+
+
+def test_e2m1_decode_is_the_format_table():
+    got = [oracle.e2m1_to_f64(c) for c in range(16)]
+    assert got[:8] == E2M1_MAGNITUDES
+    assert got[8:] == [-m for m in E2M1_MAGNITUDES]
+    assert math.copysign(1, got[8]) == -1.0  # code 8 is -0
+
+
+def _fp8_codes(rng, shape):
+    """Random E4M3 bytes without the two NaN patterns."""
+    c = rng.integers(0, 254, size=shape, dtype=np.int64)
+    c = np.where(c >= 0x7F, c + 1, c)  # skip 0x7F
+    return np.where(c >= 0xFF, 0xFE, c).astype(np.uint8)
+
+
+def _bf16_scales(rng, shape):
+    return I.bits(torch.from_numpy(np.abs(rng.normal(0.0, 0.01, size=shape)).astype(np.float32))
+                  .to(torch.bfloat16))
+
+
+def _e4m3_scales(rng, shape):
+    """Positive E4M3 block scales (exponent field 1..14)."""
+    e = rng.integers(1, 15, size=shape)
+    m = rng.integers(0, 8, size=shape)
+    return ((e << 3) | m).astype(np.uint8)
+
+
+def _deq_fp8(codes, scales_bits, group):
+    v = torch.from_numpy(codes).view(torch.float8_e4m3fn).to(torch.float64).numpy()
+    sc = torch.from_numpy(scales_bits.astype(np.int16)).view(torch.bfloat16).to(torch.float64)
+    return v * np.repeat(sc.numpy(), group, axis=-1)
+
+
+def _deq_nvfp4(codes, scales, glob, group, cols):
+    table = np.array(E2M1_MAGNITUDES + [-m for m in E2M1_MAGNITUDES])
+    lo = table[codes & 15]
+    hi = table[codes >> 4]
+    v = np.stack([lo, hi], -1).reshape(codes.shape[:-1] + (cols,))
+    sc = torch.from_numpy(scales).view(torch.float8_e4m3fn).to(torch.float64).numpy()
+    return v * np.repeat(sc, group, axis=-1) * glob.astype(np.float64).reshape(
+        (-1,) + (1,) * (codes.ndim - 1))
+
+
+def test_fp8_dequant_matches_independent_decode():
+    rng = np.random.default_rng(11)
+    codes = _fp8_codes(rng, (5, 96))
+    scales = _bf16_scales(rng, (5, 3))
+    got = oracle.dequant_fp8(codes, scales, cols=96, group=32)
+    assert np.array_equal(got, _deq_fp8(codes, scales, 32))
+
+
+def test_nvfp4_dequant_matches_independent_decode():
+    rng = np.random.default_rng(12)
+    codes = rng.integers(0, 256, size=(4, 32), dtype=np.int64).astype(np.uint8)  # 64 elements/row
+    scales = _e4m3_scales(rng, (4, 4))
+    glob = np.float32(0.0625)
+    got = oracle.dequant_nvfp4(codes, scales, glob, cols=64, group=16)
+    ref = _deq_nvfp4(codes[None], scales[None], np.array([glob]), 16, 64)[0]
+    assert np.array_equal(got, ref)
+    # hand example: byte 0x2F -> low nibble 0xF = -6, high 0x2 = 1.0; scale 0x38 = 1.0
+    one = oracle.dequant_nvfp4(np.array([[0x2F]], np.uint8), np.array([[0x38]], np.uint8),
+                               np.float32(2.0), cols=2, group=2)
+    assert one.tolist() == [[-12.0, 2.0]]
+
+
+def _quant_layer_inputs(seed):
+    s = I.shape("verify_t8", T=4, d=128, E=6, k=3, I=64, Is=32)
+    return s, I.make_inputs(s, seed=seed)
+
+
+def test_layer_fp8_equals_dequantised_f64():
+    s, inp = _quant_layer_inputs(13)
+    x, wr, _, sh, dims = _oracle_args(inp)
+    rng = np.random.default_rng(13)
+    g = 32
+    gu = _fp8_codes(rng, (s.E, 2 * s.I, s.d))
+    dn = _fp8_codes(rng, (s.E, s.d, s.I))
+    gus = _bf16_scales(rng, (s.E, 2 * s.I, s.d // g))
+    dns = _bf16_scales(rng, (s.E, s.d, s.I // g))
+    q = oracle.layer(x, wr, {"format": oracle.FP8, "group": g, "gate_up": gu, "down": dn,
+                             "gate_up_scales": gus, "down_scales": dns}, sh, dims)
+    f = oracle.layer(x, wr, {"format": oracle.F64, "gate_up": _deq_fp8(gu, gus, g),
+                             "down": _deq_fp8(dn, dns, g)}, sh, dims)
+    assert np.array_equal(q["ids"], f["ids"])
+    assert np.array_equal(q["out"], f["out"])
+
+
+def test_layer_nvfp4_equals_dequantised_f64():
+    s, inp = _quant_layer_inputs(14)
+    x, wr, _, sh, dims = _oracle_args(inp)
+    rng = np.random.default_rng(14)
+    g = 16
+    gu = rng.integers(0, 256, size=(s.E, 2 * s.I, s.d // 2), dtype=np.int64).astype(np.uint8)
+    dn = rng.integers(0, 256, size=(s.E, s.d, s.I // 2), dtype=np.int64).astype(np.uint8)
+    gus = _e4m3_scales(rng, (s.E, 2 * s.I, s.d // g))
+    dns = _e4m3_scales(rng, (s.E, s.d, s.I // g))
+    gug = (2.0 ** rng.integers(-12, -6, size=s.E)).astype(np.float32)
+    dng = (2.0 ** rng.integers(-12, -6, size=s.E)).astype(np.float32)
+    ex = {"format": oracle.NVFP4, "group": g, "gate_up": gu, "down": dn, "gate_up_scales": gus,
+          "down_scales": dns, "gate_up_global": gug, "down_global": dng}
+    q = oracle.layer(x, wr, ex, sh, dims)
+    f = oracle.layer(x, wr, {"format": oracle.F64, "gate_up": _deq_nvfp4(gu, gus, gug, g, s.d),
+                             "down": _deq_nvfp4(dn, dns, dng, g, s.I)}, sh, dims)
+    assert np.array_equal(q["ids"], f["ids"])
+    assert np.array_equal(q["out"], f["out"])
+    # the per-expert scale is required
+    with pytest.raises(ValueError):
+        oracle.layer(x, wr, dict(ex, gate_up_global=None), sh, dims)
