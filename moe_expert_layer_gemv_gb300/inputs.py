@@ -22,6 +22,18 @@ suites; none is used here -- these synthetic tensors stand in for them):
   bf16 scale per group (512 routed experts, top-10, plus a shared expert:
   "veloGB10", The model; W4A16 routed experts: "Qwen3.8 Flash-Next - GB10
   UltraFast", How it works)
+
+Two more routed-weight formats are drawn for the oracle's FP8 / NVFP4 paths
+(the "NVFP4/FP8 families" of "veloGB10", README), by ``fmt`` on any shape:
+
+* ``fp8``    E4M3 codes uint8 [E,2I,d] / [E,d,I]: normals of std
+  FP8_VALUE_STD clamped to the format's +-448 and rounded by torch's
+  float8_e4m3fn cast (never NaN), with |N(0, FP8_SCALE_STD)| bf16 scales per
+  group of ``group`` along the reduction dim.
+* ``nvfp4``  E2M1 codes, two per byte (even element in the low nibble), each
+  nibble uniform over the 16 codes; E4M3 block scales per 16 elements drawn
+  as uniform [1, 4) rounded by the float8_e4m3fn cast; one fp32 scale per
+  expert matrix, 2^-8 times a uniform [0.5, 1) draw rounded to bf16 precision.
 """
 from dataclasses import dataclass, field, replace
 
@@ -29,6 +41,9 @@ import torch
 
 WEIGHT_STD = 0.02
 INT4_SCALE_STD = 0.003
+FP8_VALUE_STD = 64.0
+FP8_SCALE_STD = 0.0003
+E4M3_MAX = 448.0
 SKEW_HOT = 16
 SKEW_FACTOR = 4.0
 
@@ -43,8 +58,8 @@ class LayerShape:
     Is: int = 0                 # shared-expert intermediate; 0 = none
     renormalize: bool = True
     block: int = 16             # moe_align_block_size block B
-    fmt: str = "bf16"           # "bf16" | "int4"
-    group: int = 32             # int4 group length along the reduction dim
+    fmt: str = "bf16"           # "bf16" | "int4" | "fp8" | "nvfp4"
+    group: int = 32             # scale group length along the reduction dim (nvfp4: 16)
     skew: bool = False
     name: str = field(default="", compare=False)
 
@@ -89,12 +104,33 @@ def _int4_draw(g, rows_shape, cols, group):
     return _int4_pack(q), scales
 
 
+def _fp8_draw(g, rows_shape, cols, group):
+    v = torch.randn(tuple(rows_shape) + (cols,), generator=g, dtype=torch.float32) * FP8_VALUE_STD
+    codes = v.clamp(-E4M3_MAX, E4M3_MAX).to(torch.float8_e4m3fn).view(torch.uint8)
+    scales = (torch.randn(tuple(rows_shape) + (cols // group,), generator=g,
+                          dtype=torch.float32).abs() * FP8_SCALE_STD).to(torch.bfloat16)
+    return codes.contiguous(), scales
+
+
+def _nvfp4_draw(g, rows_shape, cols, group, n_experts):
+    nib = torch.randint(0, 16, tuple(rows_shape) + (cols,), generator=g, dtype=torch.int16)
+    codes = (nib[..., 0::2] | (nib[..., 1::2] << 4)).to(torch.uint8).contiguous()
+    bs = 1.0 + 3.0 * torch.rand(tuple(rows_shape) + (cols // group,), generator=g,
+                                dtype=torch.float32)
+    scales = bs.to(torch.float8_e4m3fn).view(torch.uint8).contiguous()
+    glob = ((0.5 + 0.5 * torch.rand((n_experts,), generator=g, dtype=torch.float32))
+            .to(torch.bfloat16).to(torch.float32) * 2.0 ** -8)
+    return codes, scales, glob
+
+
 def make_inputs(s: LayerShape, seed: int = 0) -> dict:
     """Draw one layer's inputs on the CPU.  Returns torch CPU tensors:
     x bf16[T,d], router_w bf16[E,d], gate_up / down (bf16 [E,2I,d] / [E,d,I], or
     int4 codes uint8 [E,2I,d/2] / [E,d,I/2] with bf16 scales [E,2I,d/g] /
-    [E,d,I/g]), and when Is > 0: w_sg bf16[d], shared_gate_up bf16[2Is,d],
-    shared_down bf16[d,Is]."""
+    [E,d,I/g], or fp8 codes uint8 [E,2I,d] / [E,d,I] with bf16 scales, or
+    nvfp4 codes uint8 [E,2I,d/2] / [E,d,I/2] with E4M3 scales uint8 [E,2I,d/g]
+    / [E,d,I/g] and fp32 gate_up_global / down_global [E]), and when Is > 0:
+    w_sg bf16[d], shared_gate_up bf16[2Is,d], shared_down bf16[d,Is]."""
     g = torch.Generator(device="cpu")
     g.manual_seed(seed)
     out = {"shape": s, "seed": seed}
@@ -115,6 +151,14 @@ def make_inputs(s: LayerShape, seed: int = 0) -> dict:
     elif s.fmt == "int4":
         out["gate_up"], out["gate_up_scales"] = _int4_draw(g, (s.E, 2 * s.I), s.d, s.group)
         out["down"], out["down_scales"] = _int4_draw(g, (s.E, s.d), s.I, s.group)
+    elif s.fmt == "fp8":
+        out["gate_up"], out["gate_up_scales"] = _fp8_draw(g, (s.E, 2 * s.I), s.d, s.group)
+        out["down"], out["down_scales"] = _fp8_draw(g, (s.E, s.d), s.I, s.group)
+    elif s.fmt == "nvfp4":
+        (out["gate_up"], out["gate_up_scales"],
+         out["gate_up_global"]) = _nvfp4_draw(g, (s.E, 2 * s.I), s.d, s.group, s.E)
+        (out["down"], out["down_scales"],
+         out["down_global"]) = _nvfp4_draw(g, (s.E, s.d), s.I, s.group, s.E)
     else:
         raise ValueError(f"unknown weight format {s.fmt!r}")
     if s.Is > 0:

@@ -94,3 +94,46 @@ def test_bits_round_trip():
     t = torch.tensor([1.0, -2.5, 0.0, float("inf")], dtype=torch.bfloat16)
     b = I.bits(t)
     assert b.dtype == np.uint16 and b.tolist() == [0x3F80, 0xC020, 0x0000, 0x7F80]
+
+
+def test_fp8_codes_scales_and_ranges():
+    s = I.shape("int4_t32", T=4, d=256, E=4, k=2, I=64, Is=32, fmt="fp8", group=32)
+    a = I.make_inputs(s, seed=2)
+    gu, dn = a["gate_up"], a["down"]
+    assert gu.shape == (s.E, 2 * s.I, s.d) and gu.dtype == torch.uint8
+    assert dn.shape == (s.E, s.d, s.I) and dn.dtype == torch.uint8
+    assert a["gate_up_scales"].shape == (s.E, 2 * s.I, s.d // 32)
+    assert a["down_scales"].shape == (s.E, s.d, s.I // 32)
+    for c in (gu, dn):
+        assert not bool(((c & 0x7F) == 0x7F).any())  # no NaN pattern
+        v = c.view(torch.float8_e4m3fn).to(torch.float32)
+        assert float(v.abs().max()) <= I.E4M3_MAX
+        assert abs(float(v.std()) / I.FP8_VALUE_STD - 1.0) < 0.05
+    sc = a["gate_up_scales"].to(torch.float32)
+    assert float(sc.min()) >= 0.0 and abs(float(sc.mean()) / (I.FP8_SCALE_STD * math.sqrt(2 / math.pi)) - 1) < 0.1
+
+
+def test_nvfp4_codes_scales_globals():
+    s = I.shape("int4_t32", T=4, d=256, E=4, k=2, I=64, Is=32, fmt="nvfp4", group=16)
+    a = I.make_inputs(s, seed=3)
+    assert a["gate_up"].shape == (s.E, 2 * s.I, s.d // 2)
+    assert a["down"].shape == (s.E, s.d, s.I // 2)
+    assert a["gate_up_scales"].shape == (s.E, 2 * s.I, s.d // 16)
+    assert a["down_scales"].shape == (s.E, s.d, s.I // 16)
+    nib = torch.cat([a["gate_up"] & 15, a["gate_up"] >> 4]).to(torch.int64)
+    counts = torch.bincount(nib.flatten(), minlength=16).to(torch.float64)
+    assert float(counts.min()) > 0.9 * float(counts.mean())  # all 16 codes, near uniform
+    for sc in (a["gate_up_scales"], a["down_scales"]):
+        v = sc.view(torch.float8_e4m3fn).to(torch.float32)
+        assert float(v.min()) >= 1.0 and float(v.max()) <= 4.0
+    for gl in (a["gate_up_global"], a["down_global"]):
+        assert gl.shape == (s.E,) and gl.dtype == torch.float32
+        assert float(gl.min()) >= 2.0 ** -9 and float(gl.max()) <= 2.0 ** -8
+
+
+def test_quantised_formats_are_deterministic():
+    for fmt, g in (("fp8", 32), ("nvfp4", 16)):
+        s = I.shape("int4_t32", T=2, d=256, E=3, k=2, I=64, Is=0, fmt=fmt, group=g)
+        a, b, c = I.make_inputs(s, 5), I.make_inputs(s, 5), I.make_inputs(s, 6)
+        assert torch.equal(a["gate_up"], b["gate_up"]) and torch.equal(a["down_scales"], b["down_scales"])
+        assert not torch.equal(a["gate_up"], c["gate_up"])

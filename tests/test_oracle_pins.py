@@ -259,11 +259,15 @@ def test_combine_shared_gate_zero_is_half():
 
 def _oracle_args(inp):
     s = inp["shape"]
-    fmt = oracle.BF16 if s.fmt == "bf16" else oracle.INT4
+    fmt = {"bf16": oracle.BF16, "int4": oracle.INT4, "fp8": oracle.FP8, "nvfp4": oracle.NVFP4}[s.fmt]
     conv = (lambda t: I.bits(t)) if s.fmt == "bf16" else (lambda t: t.numpy())
+    sconv = (lambda t: t.numpy()) if s.fmt == "nvfp4" else I.bits  # E4M3 bytes, else bf16 bits
     ex = {"format": fmt, "group": s.group, "gate_up": conv(inp["gate_up"]), "down": conv(inp["down"]),
-          "gate_up_scales": None if inp["gate_up_scales"] is None else I.bits(inp["gate_up_scales"]),
-          "down_scales": None if inp["down_scales"] is None else I.bits(inp["down_scales"])}
+          "gate_up_scales": None if inp["gate_up_scales"] is None else sconv(inp["gate_up_scales"]),
+          "down_scales": None if inp["down_scales"] is None else sconv(inp["down_scales"])}
+    if s.fmt == "nvfp4":
+        ex["gate_up_global"] = inp["gate_up_global"].numpy()
+        ex["down_global"] = inp["down_global"].numpy()
     sh = None
     if s.Is > 0:
         sh = {"gate_up": I.bits(inp["shared_gate_up"]), "down": I.bits(inp["shared_down"]),
@@ -537,3 +541,23 @@ def test_layer_nvfp4_equals_dequantised_f64():
     # the per-expert scale is required
     with pytest.raises(ValueError):
         oracle.layer(x, wr, dict(ex, gate_up_global=None), sh, dims)
+
+
+@pytest.mark.parametrize("fmt,group", [("fp8", 32), ("nvfp4", 16)])
+def test_layer_on_drawn_quantised_weights_equals_dequantised_f64(fmt, group):
+    """The same pin on the input recipe's own FP8 / NVFP4 draws."""
+    s = I.shape("int4_t32", T=5, d=256, E=6, k=3, I=64, Is=32, fmt=fmt, group=group)
+    inp = I.make_inputs(s, seed=15)
+    x, wr, ex, sh, dims = _oracle_args(inp)
+    q = oracle.layer(x, wr, ex, sh, dims)
+    if fmt == "fp8":
+        f64 = {"gate_up": _deq_fp8(ex["gate_up"], ex["gate_up_scales"], group),
+               "down": _deq_fp8(ex["down"], ex["down_scales"], group)}
+    else:
+        f64 = {"gate_up": _deq_nvfp4(ex["gate_up"], ex["gate_up_scales"], ex["gate_up_global"],
+                                     group, s.d),
+               "down": _deq_nvfp4(ex["down"], ex["down_scales"], ex["down_global"], group, s.I)}
+    f = oracle.layer(x, wr, dict(f64, format=oracle.F64), sh, dims)
+    assert np.array_equal(q["ids"], f["ids"])
+    assert np.array_equal(q["out"], f["out"])
+    assert np.isfinite(q["out"]).all()
